@@ -1,0 +1,257 @@
+"""CPU oracle for the gated delta rule (TEST INFRASTRUCTURE ONLY).
+
+The plain token-serial double-precision definition of the recurrence lives in
+``gdn_oracle.c``; this module loads it through ctypes and converts arrays.
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+import it.  It shares no code with the CUDA library and the library never
+calls it.
+
+Inputs may be numpy arrays or CPU torch tensors of any float dtype; they are
+converted exactly to float64 (fp16 and fp32 embed exactly).  Outputs come back
+as float64 numpy arrays, unrounded; ``round_to`` rounds once (round to
+nearest even) to an activation dtype.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+RULES = {"linear": 0, "gated": 1, "delta": 2, "gated_delta": 3, "gdn2": 4}
+ERR_BAD_SLOT = 1
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int32)
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
+        ("hq", ctypes.c_int32), ("hv", ctypes.c_int32),
+        ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
+        ("rule", ctypes.c_int32),
+        ("l2norm_q", ctypes.c_int32), ("l2norm_k", ctypes.c_int32),
+        ("beta_sigmoid", ctypes.c_int32), ("decay_per_key", ctypes.c_int32),
+        ("raw_gate", ctypes.c_int32), ("num_state_rows", ctypes.c_int32),
+        ("threads", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+        ("q", _dp), ("k", _dp), ("v", _dp),
+        ("decay", _dp), ("gate_bias", _dp), ("gate_scale", _dp), ("beta", _dp),
+        ("cu_seqlens", _ip), ("slot_ids", _ip),
+        ("initial_state", _dp), ("final_state", _dp), ("o", _dp),
+        ("error_word", _ip),
+    ]
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        lib.oracle_gdn.argtypes = [ctypes.POINTER(_Problem)]
+        lib.oracle_gdn.restype = ctypes.c_int
+        lib.oracle_gate.argtypes = [ctypes.c_int64, ctypes.c_int32, _dp, _dp, _dp, _dp, _dp, _dp]
+        lib.oracle_gate.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor (CPU)
+        x = x.detach().cpu()
+        if str(x.dtype) in ("torch.float16", "torch.bfloat16", "torch.float32", "torch.float64"):
+            x = x.double()
+        x = x.numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i32(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a, typ):
+    return None if a is None else a.ctypes.data_as(typ)
+
+
+def gate(a, dt_bias, decay_scale, b=None, want_beta=False):
+    """decay = decay_scale * softplus(a + dt_bias); beta = sigmoid(b).
+
+    "com.microsoft.LinearAttentionGate", Description.  The last axis of ``a``
+    is the head axis; leading axes are folded.
+    """
+    lib = _load()
+    a64 = _f64(a)
+    shape = a64.shape
+    h = shape[-1]
+    n = int(a64.size // h)
+    bias = _f64(dt_bias).reshape(-1)
+    dscale = _f64(decay_scale).reshape(-1)
+    b64 = _f64(b) if b is not None else None
+    decay = np.empty(shape, np.float64)
+    beta = np.empty(shape, np.float64) if want_beta else None
+    rc = lib.oracle_gate(n, h, _ptr(a64, _dp), _ptr(bias, _dp), _ptr(dscale, _dp),
+                         _ptr(b64, _dp), _ptr(decay, _dp), _ptr(beta, _dp))
+    if rc != 0:
+        raise ValueError("oracle_gate rejected its arguments")
+    return (decay, beta) if want_beta else decay
+
+
+def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
+        gate_scale=None, cu_seqlens=None, batch=None, slot_ids=None,
+        initial_state=None, final_state=None, num_state_rows=None, scale=0.0,
+        l2norm_q=False, l2norm_k=False, beta_sigmoid=False, decay_per_key=False,
+        threads=1):
+    """Runs the recurrence token by token in float64.
+
+    q, k: [T, Hq, dk]; v: [T, Hv, dv] (rank-4 callers flatten [B, S] to T and
+    pass batch=B).  Returns (o [T, Hv, dv], final_state [rows, Hv, dv, dk],
+    error_word).  ``final_state`` (if given) is the buffer the update lands in
+    (copied, so the caller's array is not modified); rows that no request
+    names keep its values.  Output tokens outside every request are NaN.
+    """
+    lib = _load()
+    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    T, hq, dk = q64.shape
+    hv, dv = v64.shape[1], v64.shape[2]
+    cu = _i32(cu_seqlens)
+    slots = _i32(slot_ids)
+    if batch is None:
+        batch = (len(cu) - 1) if cu is not None else 1
+    init = _f64(initial_state)
+    if num_state_rows is None:
+        if final_state is not None:
+            num_state_rows = int(np.asarray(final_state.shape)[0])
+        elif init is not None:
+            num_state_rows = init.shape[0]
+        else:
+            num_state_rows = batch
+    if final_state is not None:
+        fin = _f64(final_state).copy()
+    elif init is not None:
+        fin = init.copy()
+    else:
+        fin = np.zeros((num_state_rows, hv, dv, dk), np.float64)
+    o = np.full((T, hv, dv), np.nan, np.float64)
+    err = np.zeros(1, np.int32)
+    dec = _f64(decay)
+    bet = _f64(beta)
+    gb = _f64(gate_bias)
+    gs = _f64(gate_scale)
+    raw = gb is not None or gs is not None
+    prob = _Problem(
+        batch=batch, total_tokens=T, hq=hq, hv=hv, dk=dk, dv=dv, rule=RULES[rule],
+        l2norm_q=int(l2norm_q), l2norm_k=int(l2norm_k), beta_sigmoid=int(beta_sigmoid),
+        decay_per_key=int(decay_per_key), raw_gate=int(raw), num_state_rows=num_state_rows,
+        threads=int(threads), scale=float(scale),
+        q=_ptr(q64, _dp), k=_ptr(k64, _dp), v=_ptr(v64, _dp),
+        decay=_ptr(dec, _dp), gate_bias=_ptr(gb, _dp), gate_scale=_ptr(gs, _dp),
+        beta=_ptr(bet, _dp), cu_seqlens=_ptr(cu, _ip), slot_ids=_ptr(slots, _ip),
+        initial_state=_ptr(init, _dp), final_state=_ptr(fin, _dp), o=_ptr(o, _dp),
+        error_word=_ptr(err, _ip),
+    )
+    rc = lib.oracle_gdn(ctypes.byref(prob))
+    if rc != 0:
+        raise ValueError("oracle_gdn rejected its arguments (rc=%d)" % rc)
+    return o, fin, int(err[0])
+
+
+def torch_index(idx):
+    import torch
+    return torch.as_tensor(np.asarray(idx, dtype=np.int64))
+
+
+def round_to(x, dtype):
+    """Rounds float64 results once to an activation dtype ('f16' or 'f32')."""
+    np_dtype = {"f16": np.float16, "f32": np.float32}[dtype]
+    return np.asarray(x).astype(np_dtype).astype(np.float64)
+
+
+def lib_path():
+    return _build.LIB
+
+
+__all__ = ["gate", "gdn", "run_problem", "round_to", "RULES", "ERR_BAD_SLOT", "lib_path"]
+os.environ.setdefault("OMP_WAIT_POLICY", "PASSIVE")
+
+
+def run_problem(p, threads=1, requests=None):
+    """Runs the oracle on a problem dict (the layout ``workloads.make`` draws).
+
+    ``requests`` optionally restricts the run to a subset of request indices
+    (their tokens and state rows only); the other outputs stay NaN and the
+    other state rows keep their initial values.
+    """
+    q, k, v = p["q"], p["k"], p["v"]
+    T = p["total_tokens"]
+    q = q.reshape(T, p["hq"], p["dk"])
+    k = k.reshape(T, p["hq"], p["dk"])
+    v = v.reshape(T, p["hv"], p["dv"])
+    cu = p.get("cu_seqlens")
+    slots = p.get("slot_ids")
+    batch = p["batch"]
+    if cu is None:
+        L = T // batch
+        cu_np = np.arange(batch + 1, dtype=np.int64) * L
+    else:
+        cu_np = np.asarray(cu.numpy() if hasattr(cu, "numpy") else cu, dtype=np.int64)
+    if requests is not None:
+        # Sub-problem: the chosen requests keep their own token ranges; their
+        # state rows are gathered into a compact slab (row j = request j), so
+        # the returned final state has one row per chosen request.
+        req = list(requests)
+        sub_cu = np.zeros(len(req) + 1, dtype=np.int64)
+        rows = []
+        T_, idx = 0, []
+        for j, b in enumerate(req):
+            t0 = min(max(int(cu_np[b]), 0), T)
+            t1 = max(min(max(int(cu_np[b + 1]), 0), T), t0)
+            idx.extend(range(t0, t1))
+            T_ += t1 - t0
+            sub_cu[j + 1] = T_
+            rows.append(int(slots[b]) if slots is not None else b)
+        idx = np.asarray(idx, dtype=np.int64)
+
+        def take(x):
+            if x is None:
+                return None
+            if hasattr(x, "detach"):
+                x = x.reshape((T,) + tuple(x.shape[1:]))
+                return _f64(x[torch_index(idx)])
+            xn = _f64(x)
+            return xn.reshape((T,) + xn.shape[1:])[idx]
+
+        init = p.get("initial_state")
+        init_sub = None
+        if init is not None:
+            init_sub = _f64(init[torch_index(np.asarray(rows))] if hasattr(init, "detach")
+                            else np.asarray(init)[rows])
+        o_s, fin, err = gdn(take(q), take(k), take(v), rule=p["rule"], decay=take(p.get("decay")),
+                            beta=take(p.get("beta")), gate_bias=p.get("gate_bias"),
+                            gate_scale=p.get("gate_scale"), cu_seqlens=sub_cu, batch=len(req),
+                            slot_ids=None, initial_state=init_sub, num_state_rows=len(req),
+                            scale=p.get("scale", 0.0),
+                            l2norm_q=p.get("l2norm_q", False), l2norm_k=p.get("l2norm_k", False),
+                            beta_sigmoid=p.get("beta_sigmoid", False),
+                            decay_per_key=p.get("decay_per_key", False), threads=threads)
+        o = np.full((T, p["hv"], p["dv"]), np.nan)
+        if len(idx):
+            o[idx] = o_s
+        return o, fin, err
+    return gdn(q, k, v, rule=p["rule"], decay=p.get("decay"), beta=p.get("beta"),
+               gate_bias=p.get("gate_bias"), gate_scale=p.get("gate_scale"),
+               cu_seqlens=cu if cu is not None else None, batch=batch, slot_ids=slots,
+               initial_state=p.get("initial_state"),
+               num_state_rows=p.get("num_slots") or batch, scale=p.get("scale", 0.0),
+               l2norm_q=p.get("l2norm_q", False), l2norm_k=p.get("l2norm_k", False),
+               beta_sigmoid=p.get("beta_sigmoid", False),
+               decay_per_key=p.get("decay_per_key", False), threads=threads)
