@@ -1,0 +1,493 @@
+"""Benchmark of the gated delta rule library on one node.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+                    [--workload decode-L1|decode-L4|ragged-prefill|long-prefill-<rule>|gdn2]
+                    [--no-extra]
+
+A step is one call of the library on one batch of the workload (the decode
+workload: 256 requests of L tokens, Hq=16, Hv=32, dk=dv=128, fp16
+activations, an fp32 state slab [1024, 32, 128, 128] updated in place at
+permuted slot ids, raw gate and beta through the fused arm).  Inputs are
+seeded synthetic draws (workloads.py) resident in HBM.  Timing: W untimed
+warm-up steps, then K steps between a barrier + synchronize on both sides,
+CUDA events on the launching stream; the touched state (512 MiB) exceeds
+the 129 MB L2 every step, so no extra flush is needed.  Rank 0 prints one
+JSON line.  With N > 1 each rank runs its own independent batch (weak
+scaling: the work partitions over requests; no collective on the data path).
+
+--impl reference times the CPU oracle (the only other implementation there
+is) on the host cores on bounded samples of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "tokens/s per GDN layer (decode, prefill) and % of HBM / tensor-core roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILES = os.path.join(ROOT, "profiles")
+ESZ = {torch.float16: 2, torch.float32: 4, torch.int32: 4}
+CHUNK = 64
+
+
+# ------------------------------------------------------------------ workloads
+def make_workload(name, seed_offset=0):
+    if name.startswith("decode-L"):
+        L = int(name[len("decode-L"):])
+        return workloads.decode(L, seed=2 + seed_offset), "recurrent"
+    if name == "ragged-prefill":
+        return workloads.ragged_prefill(seed=3 + seed_offset), "chunked"
+    if name.startswith("long-prefill-"):
+        return workloads.long_prefill(name[len("long-prefill-"):], seed=4 + seed_offset), "chunked"
+    if name == "gdn2":
+        return workloads.gdn2(seed=5 + seed_offset), "chunked"
+    raise SystemExit("unknown workload " + name)
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * ESZ.get(t.dtype, t.element_size())
+
+
+def algorithmic_bytes(p):
+    """Each input read once, each output written once, the touched state rows
+    read (if an initial state is given) and written once."""
+    b = sum(_nbytes(p.get(k)) for k in ("q", "k", "v", "decay", "gate_bias", "gate_scale", "beta",
+                                         "cu_seqlens", "slot_ids"))
+    b += _nbytes(p["v"])  # o, same shape and dtype as v
+    tile = p["batch"] * p["hv"] * p["dv"] * p["dk"] * 4
+    b += tile * (2 if p.get("initial_state") is not None else 1)
+    return b
+
+
+def algorithmic_flops(p, C=CHUNK):
+    """Dense tile counts of the chunked form per (token, value head):
+    6 dk dv + 2C(3dk + 2dv) with retrieval, 4 dk dv + 2C(dk + dv) without."""
+    dk, dv = p["dk"], p["dv"]
+    if p["rule"] in ("delta", "gated_delta", "gdn2"):
+        per = 6 * dk * dv + 2 * C * (3 * dk + 2 * dv)
+    else:
+        per = 4 * dk * dv + 2 * C * (dk + dv)
+    return per * p["total_tokens"] * p["hv"]
+
+
+def tokens(p):
+    return sum(t1 - t0 for t0, t1 in workloads.token_ranges(p))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.lines = []
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        self.cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                    "-lms", "100"] + sel
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ device runs
+def to_dev(p, dev):
+    d = dict(p)
+    for k in ("q", "k", "v", "decay", "gate_bias", "gate_scale", "beta", "cu_seqlens", "slot_ids",
+              "initial_state"):
+        if p.get(k) is not None:
+            d[k] = p[k].to(dev).contiguous()
+    return d
+
+
+def build_problem(api, p, d, o, fin):
+    q, k, v = d["q"], d["k"], d["v"]
+    if p.get("seq_len"):
+        B, S = p["batch"], p["seq_len"]
+        q = q.view(B, S, p["hq"], p["dk"])
+        k = k.view(B, S, p["hq"], p["dk"])
+        v = v.view(B, S, p["hv"], p["dv"])
+        o = o.view(B, S, p["hv"], p["dv"])
+    init = fin if p.get("slot_ids") is not None else d.get("initial_state")
+    return api.make_problem(q=q, k=k, v=v, o=o, final_state=fin, rule=p["rule"],
+                            decay=d.get("decay"), beta=d.get("beta"), gate_bias=d.get("gate_bias"),
+                            gate_scale=d.get("gate_scale"), cu_seqlens=d.get("cu_seqlens"),
+                            slot_ids=d.get("slot_ids"), initial_state=init, batch=p["batch"],
+                            scale=p.get("scale", 0.0), l2norm_q=p.get("l2norm_q", False),
+                            l2norm_k=p.get("l2norm_k", False),
+                            beta_sigmoid=p.get("beta_sigmoid", False),
+                            decay_per_key=p.get("decay_per_key", False))
+
+
+def launch(api, prob, path, stream):
+    if path == "recurrent":
+        api.gdn_recurrent_step(prob, stream=stream)
+    else:
+        api.gdn_chunked_prefill(prob, chunk_size=CHUNK, workspace=prob._ws_buf, stream=stream)
+
+
+def prepare(api, p, path, dev):
+    d = to_dev(p, dev)
+    o = torch.empty_like(d["v"])
+    rows = p.get("num_slots") or p["batch"]
+    if p.get("slot_ids") is not None:
+        fin = d["initial_state"]  # the slab, updated in place
+    else:
+        fin = torch.empty(rows, p["hv"], p["dv"], p["dk"], dtype=torch.float32, device=dev)
+    prob = build_problem(api, p, d, o, fin)
+    prob._ws_buf = None
+    if path == "chunked":
+        n = api.gdn_chunked_prefill_workspace_size(prob, CHUNK)
+        prob._ws_buf = torch.empty(max(n, 1), dtype=torch.uint8, device=dev) if n else None
+    return d, o, fin, prob
+
+
+def time_device(api, prob, path, steps, warmup, stream, barrier):
+    for _ in range(warmup):
+        launch(api, prob, path, stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        launch(api, prob, path, stream)
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return total_ms, per_launch
+
+
+def time_e2e(api, p, d, prob, path, steps, warmup, stream, dev):
+    """Every step: pinned host -> device copies of the step's inputs, the call,
+    and a device -> host copy of the output."""
+    names = [k for k in ("q", "k", "v", "decay", "beta", "cu_seqlens", "slot_ids")
+             if p.get(k) is not None]
+    host = {k: p[k].contiguous().pin_memory() for k in names}
+    o_host = torch.empty(p["v"].shape, dtype=p["v"].dtype).pin_memory()
+    o_dev = prob._keep[3]
+    h2d = sum(_nbytes(host[k]) for k in names)
+    d2h = _nbytes(o_host)
+
+    def one():
+        with torch.cuda.stream(stream):
+            for k in names:
+                d[k].copy_(host[k], non_blocking=True)
+            launch(api, prob, path, stream)
+            o_host.copy_(o_dev.view(o_host.shape), non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        one()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+def kernel_source_digest(path):
+    f = os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc",
+                     "recurrent.cu" if path == "recurrent" else "chunked.cu")
+    with open(f, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload, path):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; None otherwise."""
+    f = os.path.join(PROFILES, "traffic.json")
+    try:
+        with open(f) as fh:
+            data = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    ent = data.get(workload)
+    if not ent or ent.get("source_sha256_16") != kernel_source_digest(path):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as fh:
+            pk = json.load(fh)
+        return pk["hbm_gbs"], pk["bf16_tflops"], pk.get("bf16_tflops_sustained"), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_rate(p, budget_s, threads, max_requests=None):
+    """Oracle tokens/s on a bounded sample of the workload's requests (all
+    value heads of each sampled request).  Grows the sample until one timed
+    pass takes >= budget_s seconds (or covers every request)."""
+    import oracle
+    ranges = workloads.token_ranges(p)
+    order = [b for b in range(p["batch"]) if ranges[b][1] > ranges[b][0]]
+    n = 1
+    while True:
+        sample = order[:n]
+        t = time.perf_counter()
+        oracle.run_problem(p, requests=sample, threads=threads)
+        dt = time.perf_counter() - t
+        toks = sum(ranges[b][1] - ranges[b][0] for b in sample)
+        if dt >= budget_s or n >= len(order) or (max_requests and n >= max_requests):
+            return toks / dt, sample, toks, dt
+        n = min(len(order), max(n + 1, int(n * max(2.0, 1.2 * budget_s / max(dt, 1e-3)))))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    p, path = make_workload(args.workload)
+    cores = cpu_cores()
+    import oracle
+    ranges = workloads.token_ranges(p)
+    order = [b for b in range(p["batch"]) if ranges[b][1] > ranges[b][0]]
+    # size one step: enough requests for ~0.05 s, capped so K + W steps stay in minutes
+    _, sample, toks, dt = oracle_rate(p, 0.05, cores)
+    per_step_s = dt
+    budget = 150.0
+    if (args.steps + args.warmup) * per_step_s > budget and len(sample) > 1:
+        keep = max(1, int(len(sample) * budget / ((args.steps + args.warmup) * per_step_s)))
+        sample = sample[:keep]
+    toks = sum(ranges[b][1] - ranges[b][0] for b in sample)
+    for _ in range(args.warmup):
+        oracle.run_problem(p, requests=sample, threads=cores)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.run_problem(p, requests=sample, threads=cores)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = toks * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(p, args, note="oracle on %d of %d requests per step" %
+                                  (len(sample), p["batch"])),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d requests x %d value heads (%d tokens) per step" %
+                                   (len(sample), p["hv"], toks)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(p, args, note=None):
+    cfg = {"workload": args.workload, "batch": p["batch"], "total_tokens": p["total_tokens"],
+           "seq_len": p.get("seq_len") or None, "Hq": p["hq"], "Hv": p["hv"], "dk": p["dk"],
+           "dv": p["dv"], "rule": p["rule"], "act_dtype": p["act_dtype"],
+           "state": "fp32 V-major", "parallelism": "replicas" if args.gpus > 1 else "single-gpu",
+           "l2_policy": "inputs larger than L2 (touched state > 129 MB)"}
+    if p.get("num_slots") and p.get("slot_ids") is not None:
+        cfg["slab_rows"] = p["num_slots"]
+    if note:
+        cfg["note"] = note
+    return cfg
+
+
+def extra_workloads(api, dev, stream, names, steps=20, warmup=5):
+    """Device throughput of the other workloads (one pass each), for context."""
+    out = {}
+    hbm, tc, tc_s, _ = peaks()
+    for name in names:
+        p, path = make_workload(name)
+        try:
+            d, o, fin, prob = prepare(api, p, path, dev)
+        except Exception as e:  # an unsupported configuration is reported, not hidden
+            out[name] = {"error": str(e)[:200]}
+            continue
+        total, per = time_device(api, prob, path, steps, warmup, stream, lambda: None)
+        ms = total / steps
+        toks = tokens(p)
+        ab = algorithmic_bytes(p)
+        ent = {"tokens_per_s": toks / (ms * 1e-3), "ms_per_call": ms,
+               "hbm_frac_of_measured": ab / (ms * 1e-3) / 1e9 / hbm,
+               "algorithmic_bytes": ab, "path": path}
+        if path == "chunked":
+            af = algorithmic_flops(p)
+            ent["tensor_frac_of_measured"] = af / (ms * 1e-3) / 1e12 / tc
+            ent["algorithmic_flops"] = af
+        out[name] = ent
+        del d, o, fin, prob
+        torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--workload", default="decode-L1")
+    ap.add_argument("--no-extra", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "gdn" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import gated_delta_rule_gate_gb300 as pkg
+    from gated_delta_rule_gate_gb300 import api
+    pkg.load()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    p, path = make_workload(args.workload, seed_offset=100 * rank)
+    d, o, fin, prob = prepare(api, p, path, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    total_ms, per_launch = time_device(api, prob, path, args.steps, args.warmup, stream, barrier)
+    clk = clocks.stop()
+
+    toks = tokens(p)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = toks * world / (ms * 1e-3)
+
+    e2e_ms, h2d, d2h = time_e2e(api, p, d, prob, path, max(1, min(args.steps, 50)), 3, stream, dev)
+    e2e_steps = max(1, min(args.steps, 50))
+    e2e_val = toks * world / (e2e_ms / e2e_steps * 1e-3)
+
+    hbm, tc, tc_s, src = peaks()
+    kern_ms = statistics.fmean(per_launch)
+    ab = algorithmic_bytes(p)
+    achieved = ab / (kern_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": ncu_traffic(args.workload, path),
+            "kernel": "recurrent_fast_kernel<128>" if path == "recurrent" else "chunked_prefill_kernel",
+            "algorithmic_bytes_per_launch": ab, "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)"}
+    if path == "chunked":
+        af = algorithmic_flops(p)
+        roof["tensor_achieved_tflops"] = af / (kern_ms * 1e-3) / 1e12
+        roof["tensor_frac"] = roof["tensor_achieved_tflops"] / tc
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (fp16 activations)",
+        "data": "synthetic (seeded, workloads.py)", "config": workload_config(p, args),
+        "roofline": roof, "clocks": clk,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        cores = cpu_cores()
+        rate, sample, stoks, sdt = oracle_rate(p, 3.0, cores)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": "%d of %d requests, all %d value heads (%d tokens, %.1f s)"
+                                          % (len(sample), p["batch"], p["hv"], stoks, sdt)}
+        if not args.no_extra and world == 1:
+            names = [n for n in ("decode-L1", "decode-L4", "ragged-prefill", "long-prefill-linear",
+                                 "long-prefill-gated", "long-prefill-delta",
+                                 "long-prefill-gated_delta", "gdn2") if n != args.workload]
+            del d, o, fin, prob
+            torch.cuda.empty_cache()
+            line["other_workloads"] = extra_workloads(api, dev, stream, names)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

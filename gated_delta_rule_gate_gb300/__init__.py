@@ -1,0 +1,10 @@
+"""Gated delta rule recurrence on GB300 (sm_103a): a C-ABI CUDA library
+(libgdn.so, declared in include/gdn.h) and a thin torch binding.
+
+Entry points (same names as the C ABI):
+    gdn_gate, gdn_recurrent_step, gdn_chunked_prefill,
+    gdn_chunked_prefill_workspace_size, gdn_status_string
+"""
+from ._native import GdnError, library_path, load  # noqa: F401
+from .api import (gdn_chunked_prefill, gdn_chunked_prefill_workspace_size,  # noqa: F401
+                  gdn_gate, gdn_recurrent_step, gdn_status_string, make_problem)

@@ -1,0 +1,37 @@
+// launch.h -- host-side launchers of the CUDA kernels (internal to libgdn).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace gdn {
+
+struct GateLaunch {
+    int64_t n;
+    int heads;
+    int f16;
+    const void *a;
+    const float *dt_bias;
+    const float *decay_scale;
+    const void *b;
+    void *decay_out;
+    void *beta_out;
+};
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+cudaError_t launch_gate(const GateLaunch &g, cudaStream_t stream);
+cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream);
+
+// Chunked prefill.  `why` receives a static reason string when the problem
+// falls outside what the kernel supports (the launcher then returns
+// cudaErrorNotSupported without launching).
+size_t chunked_workspace_bytes(const Problem &p, int chunk);
+bool chunked_supported(const Problem &p, int chunk, const char **why);
+cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,231 @@
+/*
+ * gdn.h -- C ABI of the gated delta rule library (libgdn.so, sm_103a).
+ *
+ * The operation (value-major storage; S is dv x dk fp32 per value head):
+ *
+ *   per token t of a request, for each value head h (query/key head
+ *   qh = h * Hq / Hv):
+ *     alpha = exp(g_t)                      (scalar, or a dk-vector per key)
+ *     S     = S * Diag(alpha)               (decay; rules gated, gated_delta, gdn2)
+ *     u     = S kappa                       (retrieval; rules delta, gated_delta, gdn2)
+ *     d     = beta_t (v_t - u)              (delta, gated_delta)
+ *     d     = v_t - u                       (gdn2; kappa = b_t .* k_t)
+ *     d     = v_t                           (linear, gated)
+ *     S     = S + d k_t^T
+ *     o_t   = scale * S q_t
+ *
+ * Sources: "com.microsoft.GatedDeltaNet" README (Description, Inputs,
+ * Outputs, Attributes); "com.microsoft.LinearAttentionGate" (Description);
+ * "aclnnRecurrentGatedDeltaRule" (Formula; two-phase workspace query);
+ * "gatedDeltaUpdate" (CLIKA runtime: slot_ids slab, raw-gate arm, per-key
+ * gate); ONNX issue "Spec gap: LinearAttention (opset 27) cannot represent
+ * Gated DeltaNet-2 channel-wise erase gate" (proposal A).
+ *
+ * Conventions for every entry point:
+ *  - Every tensor pointer is DEVICE memory owned by the caller, row-major and
+ *    contiguous in the layout stated, aligned at least to its element size.
+ *    The library allocates no device memory and keeps no pointer after the
+ *    call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and runs asynchronously: no entry point synchronises.  Inputs
+ *    must stay valid and outputs must not be read until the stream reaches
+ *    the work.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    non-OK status means nothing was enqueued and no output was touched.
+ *    gdn_last_error_message() then describes the first failed check.
+ *  - All entry points are thread-safe (the message is thread-local).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *gdn_stream;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID = 1,     /* the arguments break the op contract */
+    GDN_ERR_UNSUPPORTED = 2, /* a valid request this library declines (typed) */
+    GDN_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned */
+    GDN_ERR_CUDA = 4         /* a CUDA launch or runtime call failed */
+} gdn_status;
+
+typedef enum gdn_dtype {
+    GDN_DTYPE_F32 = 0,
+    GDN_DTYPE_F16 = 1,
+    GDN_DTYPE_BF16 = 2 /* named so it can be declined: GDN_ERR_UNSUPPORTED */
+} gdn_dtype;
+
+/* "com.microsoft.GatedDeltaNet", Attributes, update_rule; GDN2 is proposal
+ * (A) of the ONNX "Spec gap ... Gated DeltaNet-2" issue. */
+typedef enum gdn_rule {
+    GDN_RULE_LINEAR = 0,      /* no decay, no retrieval: S += v k^T */
+    GDN_RULE_GATED = 1,       /* decay only */
+    GDN_RULE_DELTA = 2,       /* retrieval only */
+    GDN_RULE_GATED_DELTA = 3, /* both (the default of the op) */
+    GDN_RULE_GDN2 = 4         /* decay, then erase with kappa = b .* k, write k v^T */
+} gdn_rule;
+
+/* Flags (gdn_problem.flags). */
+#define GDN_FLAG_L2NORM_Q 0x1u      /* q <- q / sqrt(sum q^2 + 1e-12) first (qk_l2_norm) */
+#define GDN_FLAG_L2NORM_K 0x2u      /* same for k */
+#define GDN_FLAG_BETA_SIGMOID 0x4u  /* beta <- sigmoid(beta) in fp32 (beta_activation) */
+#define GDN_FLAG_DECAY_PER_KEY 0x8u /* decay is [.., Hv, dk]: one log-decay per key channel */
+
+/* Bits OR-ed into *error_word by the device (never reset by the library). */
+#define GDN_DEVERR_BAD_SLOT 0x1 /* a slot id outside [0, num_state_rows): request skipped */
+
+/*
+ * One call of the recurrence over a batch of requests.
+ *
+ * Token layout.  Rank-3 packed form (seq_len == 0): q, k are
+ * [total_tokens, Hq, dk], v and o are [total_tokens, Hv, dv].  Request b owns
+ * tokens [clamp(cu_seqlens[b]), clamp(cu_seqlens[b+1])), each clamped to
+ * [0, total_tokens]; a decreasing pair gives an empty request (GatedDeltaNet
+ * Inputs table, cu_seqlens).  cu_seqlens NULL means uniform packing:
+ * total_tokens / batch tokens each (total_tokens must divide).  Output tokens
+ * that no request covers are not written.
+ * Rank-4 form (seq_len > 0): q, k are [batch, seq_len, Hq, dk] (the same
+ * memory layout), total_tokens must equal batch * seq_len, and cu_seqlens must
+ * be NULL (the op allows cu_seqlens with the rank-3 spelling only).
+ *
+ * Heads.  num_heads_v is a positive multiple of num_heads_q; value head h
+ * reads query/key head h * Hq / Hv.
+ *
+ * Gate (decay).  Present exactly for rules GATED, GATED_DELTA and GDN2.
+ *  - gate_bias == gate_scale == NULL: `decay` is the log-space decay g.
+ *  - both non-NULL (raw-gate arm, gatedDeltaUpdate): `decay` is the raw gate
+ *    projection and g = gate_scale[h] * softplus(decay + gate_bias) is formed
+ *    in fp32 inside the kernel.  gate_bias is [Hv] (or [Hv, dk] with
+ *    GDN_FLAG_DECAY_PER_KEY), gate_scale is [Hv] (the folded -exp(A_log)).
+ *  - exactly one of them non-NULL: GDN_ERR_INVALID.
+ *  decay is [total_tokens, Hv], or [total_tokens, Hv, dk] with
+ *  GDN_FLAG_DECAY_PER_KEY; decay_dtype is F32 or act_dtype.
+ *
+ * Beta.  Present exactly for rules DELTA, GATED_DELTA (shape [total_tokens,
+ * Hv]) and GDN2 (the erase gate b, [total_tokens, Hv, dk]); beta_dtype is F32
+ * or act_dtype; GDN_FLAG_BETA_SIGMOID applies the logistic sigmoid first.
+ * For GDN2 the write gate w is folded into v by the caller.
+ *
+ * State.  initial_state and final_state are fp32, value-major
+ * [num_state_rows, Hv, dv, dk].  Request b reads and writes row
+ * slot_ids[b] if slot_ids is non-NULL (the slab of gatedDeltaUpdate), else
+ * row b.  initial_state NULL means a zero state.  final_state may equal
+ * initial_state (in-place update); otherwise the two must not overlap.  Rows
+ * no request names are not touched.  A request with no tokens copies its
+ * incoming state through.  Slot ids must be distinct (caller's contract); a
+ * slot id outside [0, num_state_rows) makes every CTA of that request skip it
+ * and OR GDN_DEVERR_BAD_SLOT into *error_word (if error_word is non-NULL).
+ *
+ * scale == 0 selects 1/sqrt(dk).  state_update_capacity must be 0 (compact
+ * transition capture is not part of this library).
+ */
+typedef struct gdn_problem {
+    int32_t batch;          /* B: number of requests (0: nothing to do) */
+    int32_t total_tokens;   /* T */
+    int32_t seq_len;        /* 0: rank-3 packed; > 0: rank-4 uniform */
+    int32_t num_heads_q;    /* Hq */
+    int32_t num_heads_v;    /* Hv */
+    int32_t head_dim_k;     /* dk */
+    int32_t head_dim_v;     /* dv */
+    int32_t num_state_rows; /* rows of the state tensors; 0 means batch */
+    int32_t act_dtype;      /* gdn_dtype of q, k, v, o: F32 or F16 */
+    int32_t decay_dtype;    /* gdn_dtype of decay: F32 or act_dtype */
+    int32_t beta_dtype;     /* gdn_dtype of beta: F32 or act_dtype */
+    int32_t rule;           /* gdn_rule */
+    uint32_t flags;         /* GDN_FLAG_* */
+    float scale;            /* 0: 1/sqrt(dk) */
+    int32_t state_update_capacity; /* must be 0 */
+    const void *q;
+    const void *k;
+    const void *v;
+    void *o;
+    const void *decay;
+    const float *gate_bias;
+    const float *gate_scale;
+    const void *beta;
+    const int32_t *cu_seqlens; /* [batch + 1] or NULL */
+    const int32_t *slot_ids;   /* [batch] or NULL */
+    const float *initial_state;
+    float *final_state;
+    int32_t *error_word; /* optional device int32 */
+} gdn_problem;
+
+/*
+ * gdn_gate -- "com.microsoft.LinearAttentionGate", Description:
+ *   decay = decay_scale * softplus(a + dt_bias)   and, if beta_out != NULL,
+ *   beta  = sigmoid(b).
+ * a (and b) are [n, heads]: any leading axes folded into n, heads last.
+ * dt_bias and decay_scale are fp32 [heads].  a, b, decay_out and beta_out
+ * share `dtype` (F32 or F16).  Arithmetic is fp32, rounded once on store.
+ * beta_out requires b (GDN_ERR_INVALID otherwise); b without beta_out is
+ * accepted and unused.  n == 0 is a no-op.
+ */
+typedef struct gdn_gate_args {
+    int64_t n;
+    int32_t heads;
+    int32_t dtype;
+    const void *a;
+    const float *dt_bias;
+    const float *decay_scale;
+    const void *b;
+    void *decay_out;
+    void *beta_out;
+} gdn_gate_args;
+
+gdn_status gdn_gate(const gdn_gate_args *args, gdn_stream stream);
+
+/*
+ * gdn_recurrent_step -- token-serial recurrence ("aclnnRecurrentGatedDeltaRule":
+ * the variable-step-size form, designed for L_i <= 8 tokens per request, the
+ * decode / multi-token-prediction step).  Any request length is accepted;
+ * time grows linearly with the longest request.  Supports every rule, both
+ * gate arms, per-key decay, GDN2, 1 <= dk, dv <= 256 (larger:
+ * GDN_ERR_UNSUPPORTED).  fp32 arithmetic throughout; the state tile of each
+ * (request, value head) crosses HBM once each way.
+ */
+gdn_status gdn_recurrent_step(const gdn_problem *p, gdn_stream stream);
+
+/*
+ * gdn_chunked_prefill_workspace_size -- bytes of device workspace that
+ * gdn_chunked_prefill needs for this problem and chunk size (the first phase
+ * of the two-phase style of "aclnnRecurrentGatedDeltaRule").  Returns 0 when
+ * no workspace is needed, and (size_t)-1 when the problem is rejected (the
+ * reason is then in gdn_last_error_message()).
+ */
+size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_size);
+
+/*
+ * gdn_chunked_prefill -- the same result as gdn_recurrent_step, computed
+ * chunk-parallel: within a chunk the delta rule becomes a unit-lower-
+ * triangular system solved once per chunk, and the intra-chunk attention and
+ * the state carry-in/carry-out become dense fp16 tensor-core products with
+ * fp32 accumulation; the state itself stays fp32 across chunks.
+ * ("com.microsoft.GatedDeltaNet", Attributes, chunk_size: any value is
+ * accepted and none changes the result beyond rounding; <= 0 selects 64.)
+ * Extra constraints (GDN_ERR_UNSUPPORTED otherwise): dk and dv multiples of
+ * 16 with dk <= 256, dv <= 256.  fp32 activations are rounded to fp16 for the
+ * products.  `workspace` must hold gdn_chunked_prefill_workspace_size() bytes
+ * (NULL allowed when that is 0), 256-byte aligned; GDN_ERR_WORKSPACE
+ * otherwise.
+ */
+gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *workspace,
+                               size_t workspace_bytes, gdn_stream stream);
+
+/* Static description of a status code ("ok", "invalid argument", ...). */
+const char *gdn_status_string(gdn_status status);
+
+/* Detail of the most recent non-OK status returned on this thread ("" if none). */
+const char *gdn_last_error_message(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* GDN_H_ */
