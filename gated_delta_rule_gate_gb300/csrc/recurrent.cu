@@ -24,48 +24,52 @@
 //    lane c holds columns c + 32 i, full-warp reductions.
 #include "common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace gdn {
 
 constexpr int kTB = 8;           // tokens staged per step
-constexpr int kFastRows = 32;    // value rows per CTA, fast path
+constexpr int kFastRows = 32;    // value rows per state slice, fast path
 constexpr int kGenericRows = 8;  // value rows per CTA, generic path (one per warp)
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;    // compute threads per CTA (both paths)
+constexpr int kStages = 4;       // state slices in flight per CTA, fast path
 
 struct Stage {
     float *k, *q, *a, *x, *v, *alpha, *beta, *kq;
-    int dkp;
+    int dkp, vrows;
 };
 
-__device__ __forceinline__ Stage carve(float *smem, int dkp, int rows) {
+__device__ __forceinline__ Stage carve(float *smem, int dkp, int vrows) {
     Stage s;
     s.dkp = dkp;
+    s.vrows = vrows;
     s.k = smem;
     s.q = s.k + kTB * dkp;
     s.a = s.q + kTB * dkp;
     s.x = s.a + kTB * dkp;
     s.v = s.x + kTB * dkp;
-    s.alpha = s.v + kTB * rows;
+    s.alpha = s.v + kTB * vrows;
     s.beta = s.alpha + kTB;
     s.kq = s.beta + kTB;
     return s;
 }
 
-static size_t stage_bytes(int dkp, int rows) {
-    return sizeof(float) * ((size_t)4 * kTB * dkp + (size_t)kTB * rows + 3 * kTB);
+__host__ __device__ constexpr size_t stage_bytes(int dkp, int vrows) {
+    return sizeof(float) * ((size_t)4 * kTB * dkp + (size_t)kTB * vrows + 3 * kTB);
 }
 
-// Stages tokens [tb, tb + nt) of (request's head h / key head qh) and the v
-// entries of rows [r0, r0 + rows).  All warps of the CTA take part.
+// Stages tokens [tb, tb + nt) of value head h (key head qh) and the v entries
+// of rows [r0, r0 + s.vrows).  Threads [0, nthreads) of the CTA take part.
 __device__ void stage_tokens(const Problem &p, const Stage &s, int h, int qh, int tb, int nt,
-                             int r0, int rows) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+                             int r0, int tid, int nthreads) {
+    const int lane = tid & 31, warp = tid >> 5, nw = nthreads >> 5;
     const bool has_decay = rule_has_decay(p.rule);
     const bool perkey = (p.flags & kPerKey) != 0;
     const bool gdn2 = p.rule == kGdn2;
     const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
     const bool sig = (p.flags & kBetaSigmoid) != 0;
-    for (int idx = threadIdx.x; idx < nt * rows; idx += blockDim.x) {
+    const int rows = s.vrows;
+    for (int idx = tid; idx < nt * rows; idx += nthreads) {
         const int tt = idx / rows, r = idx % rows;
         const int i = r0 + r;
         s.v[tt * rows + r] = i < p.dv ? ld_any(p.v, ((size_t)(tb + tt) * p.Hv + h) * p.dv + i, p.act_f16) : 0.f;
@@ -142,94 +146,376 @@ __device__ __forceinline__ float dot4(const float4 &a, const float4 &b) {
 }
 __device__ __forceinline__ float4 ld_f4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
-template <int DK>
-__global__ void __launch_bounds__(kThreads) recurrent_fast_kernel(Problem p, int slices) {
-    constexpr int NV = DK / 32;  // float4s per lane per row
-    extern __shared__ __align__(16) float smem[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int cg = lane & 7;
-    const int sidx = blockIdx.x % slices;
-    const int bh = blockIdx.x / slices;
-    const int h = bh % p.Hv, b = bh / p.Hv;
-    const int r0 = sidx * kFastRows;
-    const int i_row = r0 + warp * 4 + (lane >> 3);
-    const bool active = i_row < p.dv;
-
-    const int row = state_row(p, b, h == 0 && sidx == 0 && threadIdx.x == 0);
-    if (row < 0) return;
-    int t0, t1;
-    request_range(p, b, t0, t1);
-
-    const size_t soff = (((size_t)row * p.Hv + h) * p.dv + i_row) * DK + 4 * cg;
-    float4 S[NV];
+// Applies the staged tokens [0, nt) to one row slice held in registers.
+// Lane group cg (8 lanes per row) owns columns 32 j + 4 cg + [0, 4).
+template <int NV>
+__device__ __forceinline__ void apply_tokens(const Problem &p, const Stage &s, float4 (&S)[NV], int nt,
+                                             int tb, int h, int i_row, int cg, bool active) {
+    const bool perkey = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
+    const bool retrieval = rule_has_retrieval(p.rule);
+    const float *kap = p.rule == kGdn2 ? s.x : s.k;
+    const int dk = s.dkp;
+    for (int tt = 0; tt < nt; ++tt) {
+        const float *kk = s.k + tt * dk + 4 * cg;
+        const float *qq = s.q + tt * dk + 4 * cg;
+        const float *xx = kap + tt * dk + 4 * cg;
+        if (perkey) {
+            const float *aa = s.a + tt * dk + 4 * cg;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) S[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active && p.init) {
+            for (int j = 0; j < NV; ++j) {
+                const float4 a4 = ld_f4(aa + 32 * j);
+                S[j].x *= a4.x, S[j].y *= a4.y, S[j].z *= a4.z, S[j].w *= a4.w;
+            }
+        }
+        // independent partial sums (one per float4 lane component) keep the
+        // FMA chains short
+        float4 uu = make_float4(0.f, 0.f, 0.f, 0.f), ww = uu;
 #pragma unroll
-        for (int j = 0; j < NV; ++j) S[j] = __ldcs(reinterpret_cast<const float4 *>(p.init + soff + 32 * j));
+        for (int j = 0; j < NV; ++j) {
+            const float4 x4 = ld_f4(xx + 32 * j), q4 = ld_f4(qq + 32 * j);
+            uu.x = fmaf(S[j].x, x4.x, uu.x), uu.y = fmaf(S[j].y, x4.y, uu.y);
+            uu.z = fmaf(S[j].z, x4.z, uu.z), uu.w = fmaf(S[j].w, x4.w, uu.w);
+            ww.x = fmaf(S[j].x, q4.x, ww.x), ww.y = fmaf(S[j].y, q4.y, ww.y);
+            ww.z = fmaf(S[j].z, q4.z, ww.z), ww.w = fmaf(S[j].w, q4.w, ww.w);
+        }
+        float u = (uu.x + uu.y) + (uu.z + uu.w), w = (ww.x + ww.y) + (ww.z + ww.w);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            u += __shfl_xor_sync(0xffffffffu, u, o);
+            w += __shfl_xor_sync(0xffffffffu, w, o);
+        }
+        const float alpha = perkey ? 1.f : s.alpha[tt];
+        const float vi = active ? s.v[tt * s.vrows + i_row] : 0.f;
+        const float d = retrieval ? s.beta[tt] * (vi - alpha * u) : vi;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const float4 k4 = ld_f4(kk + 32 * j);
+            S[j].x = fmaf(alpha, S[j].x, d * k4.x);
+            S[j].y = fmaf(alpha, S[j].y, d * k4.y);
+            S[j].z = fmaf(alpha, S[j].z, d * k4.z);
+            S[j].w = fmaf(alpha, S[j].w, d * k4.w);
+        }
+        if (cg == 0 && active)
+            st_out(p, ((size_t)(tb + tt) * p.Hv + h) * p.dv + i_row, p.scale * fmaf(alpha, w, d * s.kq[tt]));
     }
-    if (t1 == t0) {  // empty request: the incoming state goes through unchanged
-        if (active && p.fin != p.init) {
+}
+
+// ---------------------------------------------------------------------------
+// Fast path: persistent, warp-specialised (dk in {32, 64, 128, 256}).
+//
+// Work item = one (request, value head) pair, processed as ceil(dv/32) row
+// slices of the state.  Three roles share each CTA:
+//  * warp 8, the state producer: one lane streams every slice (32 contiguous
+//    rows, 32*dk*4 bytes) into a kStages-deep shared-memory ring with bulk
+//    async copies (TMA), completing `full[s]`;
+//  * warp 9, the token stager: for the NEXT pair it reads the request range
+//    and slot, pulls the raw key/query/value rows in with cp.async, then
+//    writes the staged fp32 tokens (L2-normalised k and q, q.k, alpha, beta,
+//    per-key alpha, GDN-2 kappa) into one of two staging buffers
+//    (`tok_full[b]`);
+//  * warps 0-7, the consumers: per slice they wait on `full[s]`, copy the
+//    slice into registers, release the slot (`empty[s]`), apply the staged
+//    tokens and store the new state straight from registers; after the last
+//    slice of a pair they release the staging buffer (`tok_empty[b]`).
+// Requests longer than kTB tokens are staged by the consumers themselves,
+// kTB tokens at a time.  Every wait is bounded; one that runs out ORs
+// GDN_DEVERR_TIMEOUT into the error word and the CTA returns.
+// ---------------------------------------------------------------------------
+struct PipeLayout {
+    int dvp;          // staged value rows (dv)
+    int stage_floats; // floats per staging buffer
+    int raw_bytes;    // cp.async landing area of the stager
+    int ring_bytes;
+    int total_bytes;
+    bool has_a, has_x;
+};
+
+__host__ __device__ inline PipeLayout pipe_layout(const Problem &p) {
+    PipeLayout L;
+    L.has_a = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
+    L.has_x = p.rule == kGdn2;
+    L.dvp = (p.dv + 3) & ~3;
+    L.stage_floats = kTB * p.dk * (2 + (L.has_a ? 1 : 0) + (L.has_x ? 1 : 0)) + kTB * L.dvp + 3 * kTB + 4;
+    const int es = p.act_f16 ? 2 : 4;
+    const int des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    L.raw_bytes = kTB * (2 * p.dk * es + p.dv * es + (L.has_a ? p.dk * des : 0) + (L.has_x ? p.dk * bes : 0));
+    L.raw_bytes = (L.raw_bytes + 15) & ~15;
+    L.ring_bytes = kStages * kFastRows * p.dk * 4;
+    L.total_bytes = L.ring_bytes + 2 * L.stage_floats * 4 + L.raw_bytes + (2 * kStages + 4) * 8;
+    return L;
+}
+
+__device__ __forceinline__ Stage carve_pipe(float *base, const Problem &p, const PipeLayout &L) {
+    Stage s;
+    s.dkp = p.dk;
+    s.vrows = L.dvp;
+    s.k = base;
+    s.q = s.k + kTB * p.dk;
+    float *nx = s.q + kTB * p.dk;
+    s.a = L.has_a ? nx : nullptr;
+    nx += L.has_a ? kTB * p.dk : 0;
+    s.x = L.has_x ? nx : nullptr;
+    nx += L.has_x ? kTB * p.dk : 0;
+    s.v = nx;
+    nx += kTB * L.dvp;
+    s.alpha = nx;
+    s.beta = nx + kTB;
+    s.kq = nx + 2 * kTB;
+    return s;
+}
+
+__device__ __forceinline__ float ld_raw(const unsigned char *base, int idx, int f16) {
+    return f16 ? __half2float(reinterpret_cast<const __half *>(base)[idx]) : reinterpret_cast<const float *>(base)[idx];
+}
+
+// The stager warp's work for one pair with 0 < L <= kTB tokens starting at t0.
+template <int DK>
+__device__ void stage_pair_async(const Problem &p, const Stage &st, const PipeLayout &Ly, unsigned char *raw,
+                                 int h, int qh, int t0, int L, int lane) {
+    constexpr int EPL = DK / 32;
+    const int es = p.act_f16 ? 2 : 4;
+    const int des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    const bool has_decay = rule_has_decay(p.rule);
+    const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
+    const bool sig = (p.flags & kBetaSigmoid) != 0;
+    unsigned char *rk = raw;
+    unsigned char *rq = rk + kTB * DK * es;
+    unsigned char *rv = rq + kTB * DK * es;
+    unsigned char *ra = rv + kTB * p.dv * es;
+    unsigned char *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
+    const int kch = DK * es / 16, vch = p.dv * es / 16;
+    for (int idx = lane; idx < L * kch; idx += 32) {
+        const int tt = idx / kch, c = idx % kch;
+        const size_t off = (((size_t)(t0 + tt) * p.Hq + qh) * DK) * es + 16 * c;
+        ptx::cp_async16(rk + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.k) + off, 16);
+        ptx::cp_async16(rq + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.q) + off, 16);
+    }
+    for (int idx = lane; idx < L * vch; idx += 32) {
+        const int tt = idx / vch, c = idx % vch;
+        const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * p.dv) * es + 16 * c;
+        ptx::cp_async16(rv + tt * p.dv * es + 16 * c, static_cast<const unsigned char *>(p.v) + off, 16);
+    }
+    if (Ly.has_a) {
+        const int ach = DK * des / 16;
+        for (int idx = lane; idx < L * ach; idx += 32) {
+            const int tt = idx / ach, c = idx % ach;
+            const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * DK) * des + 16 * c;
+            ptx::cp_async16(ra + tt * DK * des + 16 * c, static_cast<const unsigned char *>(p.decay) + off, 16);
+        }
+    }
+    if (Ly.has_x) {
+        const int xch = DK * bes / 16;
+        for (int idx = lane; idx < L * xch; idx += 32) {
+            const int tt = idx / xch, c = idx % xch;
+            const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * DK) * bes + 16 * c;
+            ptx::cp_async16(rx + tt * DK * bes + 16 * c, static_cast<const unsigned char *>(p.beta) + off, 16);
+        }
+    }
+    // per-token scalars, one lane per token, in flight together with the copies
+    float g_l = 0.f, b_l = 1.f;
+    if (lane < L) {
+        const size_t th = (size_t)(t0 + lane) * p.Hv + h;
+        if (has_decay && !Ly.has_a) g_l = ld_any(p.decay, th, p.decay_f16);
+        if (beta_scalar) b_l = ld_any(p.beta, th, p.beta_f16);
+    }
+    ptx::cp_async_wait_all();
+    __syncwarp();
+    for (int tt = 0; tt < L; ++tt) {
+        float kv[EPL], qv[EPL];
+        float ssk = 0.f, ssq = 0.f;
 #pragma unroll
-            for (int j = 0; j < NV; ++j) __stcs(reinterpret_cast<float4 *>(p.fin + soff + 32 * j), S[j]);
+        for (int i = 0; i < EPL; ++i) {
+            const int c = lane + 32 * i;
+            kv[i] = ld_raw(rk, tt * DK + c, p.act_f16);
+            qv[i] = ld_raw(rq, tt * DK + c, p.act_f16);
+            ssk += kv[i] * kv[i];
+            ssq += qv[i] * qv[i];
+        }
+        const float ik = (p.flags & kL2k) ? rsqrtf(warp_sum(ssk) + 1e-12f) : 1.f;
+        const float iq = (p.flags & kL2q) ? rsqrtf(warp_sum(ssq) + 1e-12f) : 1.f;
+        float kq = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            kv[i] *= ik;
+            qv[i] *= iq;
+            kq += kv[i] * qv[i];
+        }
+        kq = warp_sum(kq);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int c = lane + 32 * i;
+            st.k[tt * DK + c] = kv[i];
+            st.q[tt * DK + c] = qv[i];
+            if (Ly.has_a) {
+                float g = ld_raw(ra, tt * DK + c, p.decay_f16);
+                if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[(size_t)h * DK + c]);
+                st.a[tt * DK + c] = expf(g);
+            }
+            if (Ly.has_x) {
+                float bb = ld_raw(rx, tt * DK + c, p.beta_f16);
+                if (sig) bb = sigmoid_f(bb);
+                st.x[tt * DK + c] = bb * kv[i];
+            }
+        }
+        if (lane == 0) st.kq[tt] = kq;
+    }
+    for (int idx = lane; idx < L * p.dv; idx += 32) {
+        const int tt = idx / p.dv, i = idx % p.dv;
+        st.v[tt * st.vrows + i] = ld_raw(rv, tt * p.dv + i, p.act_f16);
+    }
+    if (lane < L) {
+        float alpha = 1.f;
+        if (has_decay && !Ly.has_a) {
+            if (p.raw_gate) g_l = p.gate_scale[h] * softplus_f(g_l + p.gate_bias[h]);
+            alpha = expf(g_l);
+        }
+        st.alpha[lane] = alpha;
+        st.beta[lane] = beta_scalar ? (sig ? sigmoid_f(b_l) : b_l) : 1.f;
+    }
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Problem p, int slices, int pairs) {
+    constexpr int NV = DK / 32;  // float4s per lane per row
+    constexpr int kSlice = kFastRows * DK;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const PipeLayout Ly = pipe_layout(p);
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    float *stage_base = reinterpret_cast<float *>(smem_raw + Ly.ring_bytes);
+    unsigned char *raw = smem_raw + Ly.ring_bytes + 2 * Ly.stage_floats * 4;
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw + Ly.raw_bytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *tok_full = empty + kStages;
+    uint64_t *tok_empty = tok_full + 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kCW = kThreads / 32;  // consumer warps
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], kCW);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&tok_full[s], 1);
+            ptx::mbar_init(&tok_empty[s], kCW);
+        }
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kCW) {  // ---- state producer
+        if (lane == 0) {
+            int j = 0;
+            for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x) {
+                const int b = pair / p.Hv, h = pair % p.Hv;
+                const int row = p.slots ? p.slots[b] : b;
+                const bool valid = row >= 0 && row < p.rows && p.init != nullptr;
+                for (int sl = 0; sl < slices; ++sl, ++j) {
+                    const int s = j % kStages;
+                    if (!ptx::mbar_wait(&empty[s], ((j / kStages) & 1) ^ 1)) {
+                        if (p.err) atomicOr(p.err, 2);
+                        return;
+                    }
+                    const int r0 = sl * kFastRows;
+                    const int nrows = min(kFastRows, p.dv - r0);
+                    if (valid) {
+                        const uint32_t bytes = (uint32_t)nrows * DK * 4u;
+                        ptx::mbar_arrive_expect_tx(&full[s], bytes);
+                        ptx::bulk_g2s(ring + s * kSlice, p.init + (((size_t)row * p.Hv + h) * p.dv + r0) * DK,
+                                      bytes, &full[s]);
+                    } else {
+                        ptx::mbar_arrive(&full[s]);
+                    }
+                }
+            }
+        }
+        return;
+    }
+    if (warp == kCW + 1) {  // ---- token stager
+        int k = 0;
+        for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x, ++k) {
+            const int buf = k & 1;
+            if (!ptx::mbar_wait(&tok_empty[buf], ((k >> 1) & 1) ^ 1)) {
+                if (p.err && lane == 0) atomicOr(p.err, 2);
+                return;
+            }
+            const Stage st = carve_pipe(stage_base + buf * Ly.stage_floats, p, Ly);
+            int *hdr = reinterpret_cast<int *>(st.kq + kTB);
+            const int b = pair / p.Hv, h = pair % p.Hv;
+            const int row = state_row(p, b, h == 0 && lane == 0);
+            int t0, t1;
+            request_range(p, b, t0, t1);
+            const int L = t1 - t0;
+            if (row >= 0 && L > 0 && L <= kTB)
+                stage_pair_async<DK>(p, st, Ly, raw, h, (int)((long long)h * p.Hq / p.Hv), t0, L, lane);
+            if (lane == 0) {
+                hdr[0] = row;
+                hdr[1] = t0;
+                hdr[2] = t1;
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&tok_full[buf]);
         }
         return;
     }
 
-    const Stage s = carve(smem, DK, kFastRows);
-    const int qh = (int)((long long)h * p.Hq / p.Hv);
-    const bool perkey = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
-    const bool retrieval = rule_has_retrieval(p.rule);
-    const float *kap = p.rule == kGdn2 ? s.x : s.k;
-    const int rloc = i_row - r0;
-
-    for (int tb = t0; tb < t1; tb += kTB) {
-        const int nt = min(kTB, t1 - tb);
-        if (tb != t0) __syncthreads();
-        stage_tokens(p, s, h, qh, tb, nt, r0, kFastRows);
-        __syncthreads();
-        for (int tt = 0; tt < nt; ++tt) {
-            const float *kk = s.k + tt * DK + 4 * cg;
-            const float *qq = s.q + tt * DK + 4 * cg;
-            const float *xx = kap + tt * DK + 4 * cg;
-            if (perkey) {
-                const float *aa = s.a + tt * DK + 4 * cg;
-#pragma unroll
-                for (int j = 0; j < NV; ++j) {
-                    const float4 a4 = ld_f4(aa + 32 * j);
-                    S[j].x *= a4.x, S[j].y *= a4.y, S[j].z *= a4.z, S[j].w *= a4.w;
-                }
-            }
-            float u = 0.f, w = 0.f;
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                u += dot4(S[j], ld_f4(xx + 32 * j));
-                w += dot4(S[j], ld_f4(qq + 32 * j));
-            }
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                u += __shfl_xor_sync(0xffffffffu, u, o);
-                w += __shfl_xor_sync(0xffffffffu, w, o);
-            }
-            const float alpha = perkey ? 1.f : s.alpha[tt];
-            const float vi = s.v[tt * kFastRows + rloc];
-            const float d = retrieval ? s.beta[tt] * (vi - alpha * u) : vi;
-#pragma unroll
-            for (int j = 0; j < NV; ++j) {
-                const float4 k4 = ld_f4(kk + 32 * j);
-                S[j].x = fmaf(alpha, S[j].x, d * k4.x);
-                S[j].y = fmaf(alpha, S[j].y, d * k4.y);
-                S[j].z = fmaf(alpha, S[j].z, d * k4.z);
-                S[j].w = fmaf(alpha, S[j].w, d * k4.w);
-            }
-            if (cg == 0 && active)
-                st_out(p, ((size_t)(tb + tt) * p.Hv + h) * p.dv + i_row,
-                       p.scale * fmaf(alpha, w, d * s.kq[tt]));
+    // ---- consumer warps
+    const int cg = lane & 7;
+    const int rloc = warp * 4 + (lane >> 3);
+    int j = 0, k = 0;
+    for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x, ++k) {
+        const int buf = k & 1;
+        if (!ptx::mbar_wait(&tok_full[buf], (k >> 1) & 1)) {
+            if (p.err && tid == 0) atomicOr(p.err, 2);
+            return;
         }
-    }
-    if (active) {
+        const Stage st = carve_pipe(stage_base + buf * Ly.stage_floats, p, Ly);
+        const int *hdr = reinterpret_cast<const int *>(st.kq + kTB);
+        const int row = hdr[0], t0 = hdr[1], t1 = hdr[2];
+        const int h = pair % p.Hv;
+        const int L = t1 - t0;
+        const int qh = (int)((long long)h * p.Hq / p.Hv);
+        const bool one_block = L <= kTB;
+        for (int sl = 0; sl < slices; ++sl, ++j) {
+            const int s = j % kStages;
+            if (!ptx::mbar_wait(&full[s], (j / kStages) & 1)) {
+                if (p.err && tid == 0) atomicOr(p.err, 2);
+                return;
+            }
+            const int i_row = sl * kFastRows + rloc;
+            const bool active = i_row < p.dv;
+            float4 S[NV];
+            const bool have = active && row >= 0 && p.init != nullptr;
+            const float *src = ring + s * kSlice + rloc * DK + 4 * cg;
 #pragma unroll
-        for (int j = 0; j < NV; ++j) __stcs(reinterpret_cast<float4 *>(p.fin + soff + 32 * j), S[j]);
+            for (int jj = 0; jj < NV; ++jj) S[jj] = have ? ld_f4(src + 32 * jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty[s]);
+            if (row < 0) continue;
+            float *dst = p.fin + (((size_t)row * p.Hv + h) * p.dv + i_row) * DK + 4 * cg;
+            if (L == 0) {  // empty request: the incoming state goes through unchanged
+                if (active && p.fin != p.init) {
+#pragma unroll
+                    for (int jj = 0; jj < NV; ++jj) __stcs(reinterpret_cast<float4 *>(dst + 32 * jj), S[jj]);
+                }
+                continue;
+            }
+            for (int tb = t0; tb < t1; tb += kTB) {
+                const int nt = min(kTB, t1 - tb);
+                if (!one_block) {  // long request: stage kTB tokens at a time ourselves
+                    ptx::named_bar_sync(1, kThreads);
+                    stage_tokens(p, st, h, qh, tb, nt, 0, tid, kThreads);
+                    ptx::named_bar_sync(1, kThreads);
+                }
+                apply_tokens<NV>(p, st, S, nt, tb, h, i_row, cg, active);
+            }
+            if (active) {
+#pragma unroll
+                for (int jj = 0; jj < NV; ++jj) __stcs(reinterpret_cast<float4 *>(dst + 32 * jj), S[jj]);
+            }
+        }
+        if (!one_block) ptx::named_bar_sync(1, kThreads);  // every consumer is done with the buffer
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&tok_empty[buf]);
     }
 }
 
@@ -273,7 +559,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_generic_kernel(Problem p, 
     for (int tb = t0; tb < t1; tb += kTB) {
         const int nt = min(kTB, t1 - tb);
         if (tb != t0) __syncthreads();
-        stage_tokens(p, s, h, qh, tb, nt, r0, kGenericRows);
+        stage_tokens(p, s, h, qh, tb, nt, r0, threadIdx.x, blockDim.x);
         __syncthreads();
         for (int tt = 0; tt < nt; ++tt) {
             float u = 0.f, w = 0.f;
@@ -312,26 +598,56 @@ __global__ void __launch_bounds__(kThreads) recurrent_generic_kernel(Problem p, 
 
 static bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+template <int DK>
+static cudaError_t launch_pipe(const Problem &p, cudaStream_t stream) {
+    const int slices = (p.dv + kFastRows - 1) / kFastRows;
+    const int pairs = p.B * p.Hv;
+    const size_t smem = (size_t)pipe_layout(p).total_bytes;
+    // Dynamic shared memory above 48 KB must be enabled per device; the
+    // occupancy depends on the size, so both are redone when it changes.
+    static int cached_smem[64] = {0}, cached_per_sm[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    if (dev < 64 && cached_smem[dev] == (int)smem) {
+        per_sm = cached_per_sm[dev];
+    } else {
+        e = cudaFuncSetAttribute(recurrent_pipe_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, recurrent_pipe_kernel<DK>, kThreads + 64, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) per_sm = 1;
+        if (dev < 64) cached_smem[dev] = (int)smem, cached_per_sm[dev] = per_sm;
+    }
+    long long grid = (long long)sm_count() * per_sm;
+    if (grid > pairs) grid = pairs;
+    recurrent_pipe_kernel<DK><<<(unsigned)grid, kThreads + 64, smem, stream>>>(p, slices, pairs);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream) {
     const bool fast_dk = p.dk == 32 || p.dk == 64 || p.dk == 128 || p.dk == 256;
-    const bool fast = fast_dk && aligned16(p.fin) && (p.init == nullptr || aligned16(p.init));
-    const long long pairs = (long long)p.B * p.Hv;
+    const int es = p.act_f16 ? 2 : 4;
+    const bool per_key = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
+    // the stager's cp.async copies need 16-byte aligned rows
+    const bool rows16 = aligned16(p.q) && aligned16(p.k) && aligned16(p.v) && (p.dv * es) % 16 == 0 &&
+                        (!per_key || aligned16(p.decay)) && (p.rule != kGdn2 || aligned16(p.beta));
+    const bool fast = fast_dk && rows16 && aligned16(p.fin) && (p.init == nullptr || aligned16(p.init)) &&
+                      pipe_layout(p).total_bytes <= 200 * 1024;
     if (fast) {
-        const int slices = (p.dv + kFastRows - 1) / kFastRows;
-        const long long grid = pairs * slices;
-        const size_t smem = stage_bytes(p.dk, kFastRows);
         switch (p.dk) {
-            case 32: recurrent_fast_kernel<32><<<(unsigned)grid, kThreads, smem, stream>>>(p, slices); break;
-            case 64: recurrent_fast_kernel<64><<<(unsigned)grid, kThreads, smem, stream>>>(p, slices); break;
-            case 128: recurrent_fast_kernel<128><<<(unsigned)grid, kThreads, smem, stream>>>(p, slices); break;
-            default: recurrent_fast_kernel<256><<<(unsigned)grid, kThreads, smem, stream>>>(p, slices); break;
+            case 32: return launch_pipe<32>(p, stream);
+            case 64: return launch_pipe<64>(p, stream);
+            case 128: return launch_pipe<128>(p, stream);
+            default: return launch_pipe<256>(p, stream);
         }
-    } else {
-        const int slices = (p.dv + kGenericRows - 1) / kGenericRows;
-        const long long grid = pairs * slices;
-        const size_t smem = stage_bytes((p.dk + 3) & ~3, kGenericRows);
-        recurrent_generic_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p, slices);
     }
+    const long long pairs = (long long)p.B * p.Hv;
+    const int slices = (p.dv + kGenericRows - 1) / kGenericRows;
+    const long long grid = pairs * slices;
+    const size_t smem = stage_bytes((p.dk + 3) & ~3, kGenericRows);
+    recurrent_generic_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p, slices);
     return cudaGetLastError();
 }
 

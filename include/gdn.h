@@ -80,6 +80,7 @@ typedef enum gdn_rule {
 
 /* Bits OR-ed into *error_word by the device (never reset by the library). */
 #define GDN_DEVERR_BAD_SLOT 0x1 /* a slot id outside [0, num_state_rows): request skipped */
+#define GDN_DEVERR_TIMEOUT 0x2  /* a bounded wait on an asynchronous copy ran out: the CTA gave up */
 
 /*
  * One call of the recurrence over a batch of requests.

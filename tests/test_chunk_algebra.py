@@ -1,0 +1,79 @@
+"""Checks, in float64 on the CPU, the chunk-parallel reformulation that the
+CUDA chunked-prefill kernel implements, against the token-serial oracle.
+
+The pages say only that a chunk-parallel prefill exists, that its per-chunk
+system needs unit keys, and that the chunk size never changes the result
+("com.microsoft.GatedDeltaNet": key input, chunk_size attribute).  The
+per-chunk algebra used by the kernel is derived from the recurrence itself:
+for a chunk with incoming state M0 and in-chunk log-decay cumulants G,
+
+    A_rj = beta_r exp(G_r - G_j) (kappa_r . k_j)         (j < r)
+    T    = (I + A)^-1                                   (unit lower triangular)
+    U'   = T diag(beta) V,   W = T diag(beta e^G) Kappa
+    Delta = U' - W M0^T
+    O    = scale (diag(e^G) Q M0^T + P Delta),  P_rj = exp(G_r - G_j) (q_r . k_j), j <= r
+    M_C  = e^{G_C} M0 + Delta^T diag(e^{G_C - G}) K
+
+(kappa = k for the v1 rules, b .* k with beta = 1 for GDN-2; rules without
+retrieval use Delta = V).  This test is the derivation's check: it is not
+the oracle and the oracle does not use it.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+
+def _chunked(q, k, v, g, beta, kappa, M0, scale, C, retrieval):
+    T, dk = k.shape
+    M = M0.copy()
+    out = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, C):
+        sl = slice(c0, min(T, c0 + C))
+        Q, K, V, X = q[sl], k[sl], v[sl], kappa[sl]
+        G = np.cumsum(g[sl])
+        bt = beta[sl]
+        n = len(G)
+        D = np.exp(G[:, None] - G[None, :])
+        if retrieval:
+            A = np.tril(bt[:, None] * D * (X @ K.T), -1)
+            Tm = np.linalg.inv(np.eye(n) + A)
+            U = Tm @ (bt[:, None] * V)
+            W = Tm @ ((bt * np.exp(G))[:, None] * X)
+            Delta = U - W @ M.T
+        else:
+            Delta = V
+        P = np.tril(D * (Q @ K.T))
+        out[sl] = scale * (np.exp(G)[:, None] * (Q @ M.T) + P @ Delta)
+        M = np.exp(G[-1]) * M + Delta.T @ (np.exp(G[-1] - G)[:, None] * K)
+    return out, M
+
+
+@pytest.mark.parametrize("rule", ["linear", "gated", "delta", "gated_delta", "gdn2"])
+@pytest.mark.parametrize("C", [1, 4, 16, 64])
+def test_chunk_form_equals_token_loop(rule, C):
+    T, dk, dv = 50, 8, 6
+    p = workloads.make(seed=61, B=1, cu_seqlens=[0, T], hq=1, hv=1, dk=dk, dv=dv, act="f32",
+                       rule=rule, gate="log", logdecay_range=(-3.0, 0.0), beta_mode="direct",
+                       state="random", state_std=0.3, l2norm_k=False)
+    k = p["k"].double().numpy()[:, 0]
+    k = k / np.linalg.norm(k, axis=1, keepdims=True)
+    p["k"] = p["k"].double().new_tensor(k[:, None, :]).float()
+    k = p["k"].double().numpy()[:, 0]
+    q = p["q"].double().numpy()[:, 0]
+    v = p["v"].double().numpy()[:, 0]
+    g = p["decay"].double().numpy()[:, 0] if p["decay"] is not None else np.zeros(T)
+    if rule == "gdn2":
+        b = p["beta"].double().numpy()[:, 0]
+        kappa, beta = b * k, np.ones(T)
+    elif p["beta"] is not None:
+        kappa, beta = k, p["beta"].double().numpy()[:, 0]
+    else:
+        kappa, beta = k, np.ones(T)
+    M0 = p["initial_state"].double().numpy()[0, 0]
+    ref_o, ref_f, _ = oracle.run_problem(p)
+    o, M = _chunked(q, k, v, g, beta, kappa, M0, 1 / np.sqrt(dk), C,
+                    rule in ("delta", "gated_delta", "gdn2"))
+    np.testing.assert_allclose(o, ref_o[:, 0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(M, ref_f[0, 0], rtol=1e-10, atol=1e-12)

@@ -1,0 +1,189 @@
+"""GPU parity of gdn_chunked_prefill against the CPU oracle, through the C ABI.
+
+The chunked path multiplies fp16 operands on the tensor cores with fp32
+accumulation and keeps the state in fp32, so outputs and final states are
+held to 5e-3 of their max-norm (relative: max |x - ref| / max |ref|).
+"""
+import os
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from gpu_helpers import DEV, o_flat, rel_err, run, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+def _check(p, o, fin, ref_o, ref_fin, rows=None):
+    og = o_flat(o, p)
+    covered = ~np.isnan(ref_o)
+    assert np.isnan(og[~covered]).all()
+    e_o = rel_err(og[covered], ref_o[covered])
+    fg = fin.double().cpu().numpy()
+    if rows is not None:
+        fg = fg[rows]
+    e_s = rel_err(fg, ref_fin)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+    return e_o, e_s
+
+
+CASES = []
+for rule in ["linear", "gated", "delta", "gated_delta", "gdn2"]:
+    for act in ["f16", "f32"]:
+        CASES.append(dict(rule=rule, act=act, dk=128, dv=128, hq=1, hv=2))
+for dk, dv in [(16, 16), (32, 48), (64, 64), (64, 128), (128, 64), (128, 80)]:
+    CASES.append(dict(rule="gated_delta", act="f16", dk=dk, dv=dv, hq=2, hv=4))
+CASES += [
+    dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=2, hv=2, gate="log",
+         logdecay_range=(-4.0, 0.0)),
+    dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=1, beta_mode="direct",
+         l2norm_q=True),
+    dict(rule="gated_delta", act="f16", dk=64, dv=64, hq=1, hv=2, decay_per_key=True),
+    dict(rule="gdn2", act="f16", dk=64, dv=64, hq=1, hv=1, decay_per_key=True, write_gate=True),
+]
+
+
+def _cid(c):
+    return "-".join("%s=%s" % (k, v) for k, v in sorted(c.items()))
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_cid(c) for c in CASES])
+def test_chunked_parity_sweep(case):
+    kw = dict(seed=zlib.crc32(_cid(case).encode()) % 1000, B=5, lengths=[70, 0, 130, 1, 64],
+              state="random", state_std=0.3)
+    kw.update(case)
+    p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
+
+
+@pytest.mark.parametrize("chunk", [0, 16, 32, 64, 100, 1024])
+def test_chunk_size_hint_never_changes_result(chunk):
+    p = workloads.make(seed=71, B=2, lengths=[150, 77], hq=1, hv=2, dk=128, dv=128, act="f16",
+                       state="random")
+    o_ref, f_ref, d = run(p, path="chunked", chunk=64)
+    o, f, _ = run(p, path="chunked", chunk=chunk, d=d)
+    assert torch.equal(o.nan_to_num(7.0), o_ref.nan_to_num(7.0)) and torch.equal(f, f_ref)
+
+
+@pytest.mark.parametrize("rule", ["linear", "gated", "delta", "gated_delta"])
+def test_chunked_matches_recurrent(rule):
+    p = workloads.make(seed=72, B=3, lengths=[200, 65, 9], hq=2, hv=4, dk=128, dv=128, act="f16",
+                       rule=rule, state="random")
+    o1, f1, d = run(p, path="chunked")
+    o2, f2, _ = run(p, path="recurrent", d=d)
+    assert rel_err(o_flat(o1, p), o_flat(o2, p)) <= TOL
+    assert rel_err(f1.double().cpu().numpy(), f2.double().cpu().numpy()) <= TOL
+
+
+def test_split_resume_through_state():
+    p = workloads.make(seed=73, B=1, lengths=[300], hq=1, hv=2, dk=128, dv=128, act="f16",
+                       state="random")
+    o_all, f_all, d = run(p, path="chunked")
+    a = dict(p, total_tokens=130, cu_seqlens=torch.tensor([0, 130], dtype=torch.int32))
+    for key in ("q", "k", "v", "decay", "beta"):
+        a[key] = p[key][:130]
+    oa, fa, _ = run(a, path="chunked")
+    bpart = dict(p, total_tokens=170, cu_seqlens=torch.tensor([0, 170], dtype=torch.int32),
+                 initial_state=fa.cpu())
+    for key in ("q", "k", "v", "decay", "beta"):
+        bpart[key] = p[key][130:]
+    ob, fb, _ = run(bpart, path="chunked")
+    cat = torch.cat([oa, ob], 0)
+    assert rel_err(cat.double().cpu().numpy(), o_all.double().cpu().numpy()) <= TOL
+    assert rel_err(fb.double().cpu().numpy(), f_all.double().cpu().numpy()) <= TOL
+
+
+def test_chunked_slots_and_empty_requests():
+    p = workloads.make(seed=74, B=4, lengths=[90, 0, 40, 3], hq=2, hv=4, dk=128, dv=128, act="f16",
+                       state="random", num_slots=9, slot_mode="perm")
+    ref_o, ref_fin, _ = oracle.run_problem(p)
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
+    s1 = int(p["slot_ids"][1])
+    assert torch.equal(fin[s1].cpu(), p["initial_state"][s1])
+    touched = set(int(s) for s in p["slot_ids"])
+    for r in range(9):
+        if r not in touched:
+            assert torch.equal(fin[r].cpu(), p["initial_state"][r])
+
+
+def test_chunked_uncovered_tokens_and_clamping():
+    # -4 clamps to 0, 300 to 200; the decreasing pair (300, 20) gives an empty
+    # request.  (Decreasing entries that make clamped requests overlap are
+    # left out: the pages do not say which request's output wins.)
+    p = workloads.make(seed=75, B=4, T=200, cu_seqlens=[-4, 70, 70, 300, 20], hq=1, hv=2, dk=64,
+                       dv=64, act="f16", state="random")
+    ref_o, ref_fin, _ = oracle.run_problem(p)
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
+    assert torch.equal(fin[1].cpu(), p["initial_state"][1])
+    assert torch.equal(fin[3].cpu(), p["initial_state"][3])
+
+
+def test_chunked_bad_slot_sets_error_word():
+    p = workloads.make(seed=76, B=2, lengths=[10, 10], hq=1, hv=2, dk=128, dv=128, act="f16",
+                       state="random", num_slots=3)
+    p["slot_ids"] = torch.tensor([2, 3], dtype=torch.int32)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, fin, _ = run(p, path="chunked", error_word=err)
+    assert int(err.item()) & 1
+    assert np.isnan(o_flat(o, p)[10:]).all()
+
+
+def test_chunked_tiny_fp32_workload():
+    p = workloads.tiny_gated_delta()
+    ref_o, ref_fin, _ = oracle.run_problem(p)
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
+
+
+def test_chunked_deterministic():
+    p = workloads.make(seed=77, B=2, lengths=[100, 50], hq=1, hv=2, dk=128, dv=128, act="f16",
+                       state="random")
+    o1, f1, d = run(p, path="chunked")
+    o2, f2, _ = run(p, path="chunked", d=d)
+    assert torch.equal(o1.nan_to_num(3.0), o2.nan_to_num(3.0)) and torch.equal(f1, f2)
+
+
+# ---------------------------------------------------------------- full sizes
+def _full(p, sample):
+    o, fin, d = run(p, path="chunked")
+    torch.cuda.synchronize()
+    ref_o, ref_fin, _ = oracle.run_problem(p, requests=sample, threads=THREADS)
+    og = o_flat(o, p)
+    idx = ~np.isnan(ref_o[:, 0, 0])
+    e_o = rel_err(og[idx], ref_o[idx])
+    fg = fin.double().cpu().numpy()[sample]
+    e_s = rel_err(fg, ref_fin)
+    assert e_o <= TOL and e_s <= TOL, (e_o, e_s)
+    assert not np.isnan(og).any()
+
+
+def test_ragged_prefill_full_size_sampled():
+    """8 ragged requests, 16384 tokens, Hv = 32: the oracle checks the shortest
+    and the longest request (all heads)."""
+    p = workloads.ragged_prefill()
+    lens = [t1 - t0 for t0, t1 in workloads.token_ranges(p)]
+    sample = sorted({int(np.argmin(lens)), int(np.argmax(lens))})
+    _full(p, sample)
+
+
+@pytest.mark.parametrize("rule", ["linear", "gated", "delta", "gated_delta"])
+def test_long_prefill_full_size_sampled(rule):
+    """B = 4, S = 8192, H = 16, rank-4: the oracle checks sequence 3."""
+    _full(workloads.long_prefill(rule), [3])
+
+
+def test_gdn2_full_size_sampled():
+    """GDN-2 extension, B = 2, S = 4096, H = 16, per-key decay and erase gate."""
+    _full(workloads.gdn2(), [1])
