@@ -44,16 +44,20 @@ CHUNK = 64
 
 
 # ------------------------------------------------------------------ workloads
-def make_workload(name, seed_offset=0):
+def make_workload(name, seed_offset=0, shrink=1):
+    """The named workload; ``shrink`` > 1 divides its request count or
+    sequence length (a smaller case of the same kernel, for profiling)."""
     if name.startswith("decode-L"):
         L = int(name[len("decode-L"):])
-        return workloads.decode(L, seed=2 + seed_offset), "recurrent"
+        return workloads.decode(L, seed=2 + seed_offset, B=256 // shrink), "recurrent"
     if name == "ragged-prefill":
-        return workloads.ragged_prefill(seed=3 + seed_offset), "chunked"
+        return workloads.ragged_prefill(seed=3 + seed_offset, total=16384 // shrink,
+                                        max_len=4096 // shrink), "chunked"
     if name.startswith("long-prefill-"):
-        return workloads.long_prefill(name[len("long-prefill-"):], seed=4 + seed_offset), "chunked"
+        return workloads.long_prefill(name[len("long-prefill-"):], seed=4 + seed_offset,
+                                      S=8192 // shrink), "chunked"
     if name == "gdn2":
-        return workloads.gdn2(seed=5 + seed_offset), "chunked"
+        return workloads.gdn2(seed=5 + seed_offset, S=4096 // shrink), "chunked"
     raise SystemExit("unknown workload " + name)
 
 
@@ -96,6 +100,7 @@ class ClockSampler:
     def __init__(self, device_index=0):
         self.proc = None
         self.lines = []
+        self.skip = 0
         sel = []
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -103,7 +108,7 @@ class ClockSampler:
         except Exception:
             sel = []
         self.cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                    "-lms", "100"] + sel
+                    "-lms", "20"] + sel
 
     def start(self):
         try:
@@ -114,6 +119,12 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        # nvidia-smi takes a moment to start: wait for its first sample so that
+        # the samples taken afterwards fall inside the timed region
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.skip = len(self.lines)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -130,7 +141,8 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines[self.skip:] or self.lines[-1:]
+        for ln in lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -399,7 +411,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--workload", default="decode-L1")
-    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing")
+    ap.add_argument("--shrink", type=int, default=1,
+                    help="divide the workload's requests or length (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -426,7 +442,7 @@ def main():
         if dist:
             dist.barrier()
 
-    p, path = make_workload(args.workload, seed_offset=100 * rank)
+    p, path = make_workload(args.workload, seed_offset=100 * rank, shrink=args.shrink)
     d, o, fin, prob = prepare(api, p, path, dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -443,9 +459,13 @@ def main():
     ms = total_ms / args.steps
     value = toks * world / (ms * 1e-3)
 
-    e2e_ms, h2d, d2h = time_e2e(api, p, d, prob, path, max(1, min(args.steps, 50)), 3, stream, dev)
-    e2e_steps = max(1, min(args.steps, 50))
-    e2e_val = toks * world / (e2e_ms / e2e_steps * 1e-3)
+    if args.no_e2e:
+        e2e = None
+    else:
+        e2e_steps = max(1, min(args.steps, 50))
+        e2e_ms, h2d, d2h = time_e2e(api, p, d, prob, path, e2e_steps, 3, stream, dev)
+        e2e = {"value": toks * world / (e2e_ms / e2e_steps * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     hbm, tc, tc_s, src = peaks()
     kern_ms = statistics.fmean(per_launch)
@@ -466,16 +486,19 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 (fp16 activations)",
         "data": "synthetic (seeded, workloads.py)", "config": workload_config(p, args),
         "roofline": roof, "clocks": clk,
-        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": args.steps,
     }
     if rank == 0:
+        if args.shrink > 1:
+            line["config"]["shrink"] = args.shrink
+    if rank == 0 and not args.no_cpu:
         cores = cpu_cores()
         rate, sample, stoks, sdt = oracle_rate(p, 3.0, cores)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": "%d of %d requests, all %d value heads (%d tokens, %.1f s)"
                                           % (len(sample), p["batch"], p["hv"], stoks, sdt)}
+    if rank == 0:
         if not args.no_extra and world == 1:
             names = [n for n in ("decode-L1", "decode-L4", "ragged-prefill", "long-prefill-linear",
                                  "long-prefill-gated", "long-prefill-delta",
