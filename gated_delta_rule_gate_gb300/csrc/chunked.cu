@@ -613,6 +613,7 @@ cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_byte
         // build runs it through the token-serial kernel (same result).
         return launch_recurrent(p, stream);
     }
+    if (chunked_tc_eligible(p)) return launch_chunked_tc(p, stream);
     const bool g2 = p.rule == kGdn2;
     switch (p.dk) {
         case 16: return g2 ? launch_mma<16, true>(p, stream) : launch_mma<16, false>(p, stream);

@@ -34,4 +34,8 @@ size_t chunked_workspace_bytes(const Problem &p, int chunk);
 bool chunked_supported(const Problem &p, int chunk, const char **why);
 cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+// tcgen05 chunked kernel (dk = dv = 128, fp16, scalar decay, v1 rules).
+bool chunked_tc_eligible(const Problem &p);
+cudaError_t launch_chunked_tc(const Problem &p, cudaStream_t stream);
+
 }  // namespace gdn
