@@ -15,7 +15,7 @@
 //   S   <- e^{G_C} S + X                               (fp32, in registers)
 //
 // Operands are fp16 tiles in shared memory with the 128-byte swizzle.  The
-// key/query chunk lands (cp.async) as a 128-row K-major tile [K; Q]; its key
+// key/query chunk lands (tiled TMA) as a 128-row K-major tile [K; Q]; its key
 // rows double as the MN-major K^T operand of I2 and C4, and the value chunk
 // lands as the MN-major V^T operand, so nothing is transposed by hand.  The
 // fp32 state lives in registers of the 8 warps (row i, 64 columns each) and
@@ -24,6 +24,8 @@
 // chunk's loads are in flight while the current chunk computes.  One CTA of
 // 256 threads per (request, value head); one thread issues every MMA and
 // tracks completion through an mbarrier (bounded waits).
+#include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
+
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -46,14 +48,17 @@ constexpr int oR = 155648;        // 48 KB region: solve scratch, then W | DT | 
 constexpr int oW = oR;            // 16 KB: [64 r][128 c], K-major
 constexpr int oDT = oR + 16384;   // 16 KB: [128 i][64 j]
 constexpr int oDTs = oR + 32768;  // 16 KB
-constexpr int oAf = oR;           // fp32 [64][65]
-constexpr int oTf = oR + 16640;   // fp32 [64][65]
-constexpr int oX16 = oR + 33280;  // fp32 [4][16][17]
+constexpr int oO = oDT;           // 16 KB: output staging [64 r][128 i] (after the last MMAs)
+constexpr int oAf = oR;           // fp32 [64][68] the system matrix, transposed: At[j][r] = A[r][j]
+constexpr int oTf = oR + 17408;   // fp32 [64][68] its inverse
+constexpr int oY = oR + 34816;    // fp32 [32][36] product scratch of the solve
 constexpr int oScal = oR + 49152; // fp32 G, beta, e^G, e^{G_C - G}: 4 x 64
-constexpr int oBar = oScal + 1024;
-constexpr int TC_SMEM = oBar + 16 + 1024;  // + alignment slack
+constexpr int oBar = oScal + 1024;  // MMA barrier, two landing barriers, TMEM address
+constexpr int TC_SMEM = oBar + 32 + 1024;  // + alignment slack
 
-constexpr int FS = 65;
+constexpr int FA = 68;  // fp32 row stride of At (16-byte rows; lanes = consecutive r, conflict-free)
+constexpr int FT = 68;  // fp32 row stride of T (16-byte rows for vector reads)
+constexpr uint32_t kLandBytes = 3 * 16384;  // K, Q and V boxes of one chunk
 
 // byte offset of element (row, k) in a K-major 128B-swizzled tile with `rows`
 // rows per 64-column block
@@ -78,35 +83,32 @@ __device__ __forceinline__ void sync_tc() {
 }
 
 __device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, int32_t *err) {
-    const bool ok = ptx::mbar_wait(bar, phase);
+    const bool ok = ptx::mbar_wait_spin(bar, phase);
     phase ^= 1u;
     if (!ok && err && threadIdx.x == 0) atomicOr(err, 2);
     tc::fence_after();
     return ok;
 }
 
-__device__ __forceinline__ void issue_loads(const Problem &p, unsigned char *kq, unsigned char *vt, int c0, int n,
-                                            int h, int qh) {
-    const __half *kg = static_cast<const __half *>(p.k);
-    const __half *qg = static_cast<const __half *>(p.q);
-    const __half *vg = static_cast<const __half *>(p.v);
-    for (int idx = threadIdx.x; idx < 128 * 16; idx += TC_THREADS) {
-        const int row = idx >> 4, ch = idx & 15, rr = row & 63;
-        const bool ok = rr < n;
-        const __half *src = ok ? (row < 64 ? kg : qg) + (((size_t)(c0 + rr) * p.Hq + qh) * 128 + ch * 8) : kg;
-        ptx::cp_async16(kq + (ch >> 3) * 16384 + row * 128 + (((ch & 7) ^ (row & 7)) << 4), src, ok ? 16 : 0);
+// One chunk of keys, queries and values: six 64 x 64 fp16 boxes by TMA.  The
+// 128-byte swizzle of the tensor maps lays them out exactly as the K-major
+// [K; Q] operand and the MN-major V^T operand expect.
+__device__ __forceinline__ void issue_chunk(const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV,
+                                            unsigned char *kq, unsigned char *vt, uint64_t *bar, int c0, int h,
+                                            int qh) {
+    ptx::mbar_arrive_expect_tx(bar, kLandBytes);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+        ptx::tma_load_3d(kq + kb * 16384, tmK, 64 * kb, qh, c0, bar);
+        ptx::tma_load_3d(kq + kb * 16384 + 8192, tmQ, 64 * kb, qh, c0, bar);
+        ptx::tma_load_3d(vt + kb * 8192, tmV, 64 * kb, h, c0, bar);
     }
-    for (int idx = threadIdx.x; idx < 64 * 16; idx += TC_THREADS) {
-        const int j = idx >> 4, ch = idx & 15;
-        const bool ok = j < n;
-        const __half *src = ok ? vg + (((size_t)(c0 + j) * p.Hv + h) * 128 + ch * 8) : vg;
-        ptx::cp_async16(vt + (ch >> 3) * 8192 + j * 128 + (((ch & 7) ^ (j & 7)) << 4), src, ok ? 16 : 0);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 template <bool RETR>
-__global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    chunked_tc_kernel(Problem p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
     unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
@@ -114,11 +116,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
     unsigned char *sW = sm + oW, *sDT = sm + oDT, *sDTs = sm + oDTs;
     float *sAf = reinterpret_cast<float *>(sm + oAf);
     float *sTf = reinterpret_cast<float *>(sm + oTf);
-    float *sX16 = reinterpret_cast<float *>(sm + oX16);
+    float *sY = reinterpret_cast<float *>(sm + oY);
     float *sG = reinterpret_cast<float *>(sm + oScal);
     float *sB = sG + 64, *sEG = sG + 128, *sEGC = sG + 192;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + oBar);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + oBar + 8);
+    uint64_t *ldbar = bar + 1;  // [2], one per landing buffer
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + oBar + 24);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hc = warp >> 2;
@@ -152,13 +155,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
 
     if (tid == 0) {
         ptx::mbar_init(bar, 1);
+        ptx::mbar_init(&ldbar[0], 1);
+        ptx::mbar_init(&ldbar[1], 1);
         ptx::fence_mbar_init();
+        issue_chunk(&tmK, &tmQ, &tmV, sm + oKQ, sm + oV, &ldbar[0], t0, h, qh);
     }
     if (warp == 0) tc::tmem_alloc(tslot, TC_TMEM_COLS);
     // the fp16 mirror of the state
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) st_chunk(sS + hc * 16384, ell, ch, Sr + 8 * ch);
-    issue_loads(p, sm + oKQ, sm + oV, t0, min(TC_C, t1 - t0), h, qh);
     float graw = 0.f, braw = 0.f;
     if (tid < TC_C && tid < t1 - t0) {
         const size_t th = (size_t)(t0 + tid) * p.Hv + h;
@@ -169,27 +174,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
     sync_tc();
     const uint32_t tmem = *tslot;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    const uint32_t tI1 = tmem, tWT = tmem + 64, tD = tmem + 128, tO = tmem + 192, tX = tmem + 256;
+    const uint32_t tI1 = tmem, tD = tmem + 64, tO = tmem + 128, tX = tmem + 192, tW = tmem + 320;
+    unsigned char *sO = sm + oO;
     uint32_t phase = 0;
     bool ok = true;
     const uint32_t IDN64 = tc::idesc_f16(128, 64);
     const uint32_t IDN64_AMN = tc::idesc_f16(128, 64, true, false);
     const uint32_t IDN64_NEGB = tc::idesc_f16(128, 64, false, false, true);
     const uint32_t IDN128_BMN = tc::idesc_f16(128, 128, false, true);
+    const uint32_t IDM64N128_BMN = tc::idesc_f16(64, 128, false, true);
     const uint32_t aS = ptx::smem_u32(sS), aTa = ptx::smem_u32(sTa), aTb = ptx::smem_u32(sTb);
     const uint32_t aP = ptx::smem_u32(sP), aW = ptx::smem_u32(sW), aDT = ptx::smem_u32(sDT);
     const uint32_t aDTs = ptx::smem_u32(sDTs);
 
-    int buf = 0;
-    for (int c0 = t0; c0 < t1 && ok; c0 += TC_C, buf ^= 1) {
+    int buf = 0, ci = 0;
+    for (int c0 = t0; c0 < t1 && ok; c0 += TC_C, buf ^= 1, ++ci) {
         const int n = min(TC_C, t1 - c0);
         unsigned char *sKQ = sm + oKQ + buf * 32768;
         unsigned char *sV = sm + oV + buf * 16384;
         const uint32_t aKQ = ptx::smem_u32(sKQ), aV = ptx::smem_u32(sV);
-        ptx::cp_async_wait_all();
-        __syncthreads();  // this chunk's tiles have landed; the other buffer is free
-        if (c0 + TC_C < t1) issue_loads(p, sm + oKQ + (buf ^ 1) * 32768, sm + oV + (buf ^ 1) * 16384, c0 + TC_C,
-                                        min(TC_C, t1 - c0 - TC_C), h, qh);
+        if (!ptx::mbar_wait(&ldbar[buf], (ci >> 1) & 1)) {
+            if (p.err && tid == 0) atomicOr(p.err, 2);
+            ok = false;
+            break;
+        }
+        // the other buffer was released by the previous chunk: prefetch the next one
+        if (tid == 0 && c0 + TC_C < t1)
+            issue_chunk(&tmK, &tmQ, &tmV, sm + oKQ + (buf ^ 1) * 32768, sm + oV + (buf ^ 1) * 16384,
+                        &ldbar[buf ^ 1], c0 + TC_C, h, qh);
+        if (n < TC_C) {
+            // the boxes run past this request: clear the rows beyond it
+            const int nz = (TC_C - n) * 16;
+            for (int idx = tid; idx < 3 * nz; idx += TC_THREADS) {
+                const int which = idx / nz, rem = idx % nz, r = n + (rem >> 4), ch = rem & 15;
+                unsigned char *base = which == 2 ? sV + (ch >> 3) * 8192
+                                                 : sKQ + (ch >> 3) * 16384 + (which == 1 ? 8192 : 0);
+                *reinterpret_cast<uint4 *>(base + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            }
+        }
         if (tid < TC_C) {
             float g = 0.f, bt = 0.f;
             if (tid < n) {
@@ -217,24 +239,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
             }
             const float G1 = s, G0 = s - g1, GC = __shfl_sync(0xffffffffu, s, 31);
             sG[2 * lane] = G0, sG[2 * lane + 1] = G1;
-            sEG[2 * lane] = expf(G0), sEG[2 * lane + 1] = expf(G1);
-            sEGC[2 * lane] = expf(GC - G0), sEGC[2 * lane + 1] = expf(GC - G1);
+            sEG[2 * lane] = __expf(G0), sEG[2 * lane + 1] = __expf(G1);
+            sEGC[2 * lane] = __expf(GC - G0), sEGC[2 * lane + 1] = __expf(GC - G1);
         }
         {
+            // L2 norms: thread pair (2 r, 2 r + 1) owns row r, one 64-column block each
             const bool nk = (p.flags & kL2k) != 0, nq = (p.flags & kL2q) != 0;
-            if (nk || nq) {
-                const int kb = lane >> 4, c = (4 * lane) & 63;
-                for (int rr = warp; rr < 128; rr += 8) {
-                    if ((rr < 64 && !nk) || (rr >= 64 && !nq)) continue;
-                    uint2 *ptr = reinterpret_cast<uint2 *>(sKQ + kb * 16384 + rr * 128 +
-                                                           ((((c >> 3)) ^ (rr & 7)) << 4) + (c & 7) * 2);
-                    uint2 u = *ptr;
-                    float2 a = __half22float2(*reinterpret_cast<__half2 *>(&u.x));
-                    float2 d = __half22float2(*reinterpret_cast<__half2 *>(&u.y));
-                    const float inv = rsqrtf(warp_sum(a.x * a.x + a.y * a.y + d.x * d.x + d.y * d.y) + 1e-12f);
-                    u.x = ptx::pack_h2(a.x * inv, a.y * inv);
-                    u.y = ptx::pack_h2(d.x * inv, d.y * inv);
-                    *ptr = u;
+            const int rr = tid >> 1, kb = tid & 1;
+            if ((rr < 64 && nk) || (rr >= 64 && nq)) {
+                uint4 u[8];
+                float ss = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    u[c] = *reinterpret_cast<const uint4 *>(sKQ + kb * 16384 + rr * 128 + ((c ^ (rr & 7)) << 4));
+                    const __half2 *hp = reinterpret_cast<const __half2 *>(&u[c]);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float2 f = __half22float2(hp[w]);
+                        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                    }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                const float inv = rsqrtf(ss + 1e-12f);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    __half2 *hp = reinterpret_cast<__half2 *>(&u[c]);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float2 f = __half22float2(hp[w]);
+                        hp[w] = __floats2half2_rn(f.x * inv, f.y * inv);
+                    }
+                    *reinterpret_cast<uint4 *>(sKQ + kb * 16384 + rr * 128 + ((c ^ (rr & 7)) << 4)) = u[c];
                 }
             }
         }
@@ -260,7 +295,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         const int j = 32 * hc + jj;
-                        sAf[r * FS + j] = j < r ? sB[r] * expf(sG[r] - sG[j]) * v[jj] : 0.f;
+                        sAf[j * FA + r] = j < r ? sB[r] * __expf(sG[r] - sG[j]) * v[jj] : 0.f;
                     }
                 }
             } else {
@@ -268,7 +303,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = 32 * hc + jj;
-                    v[jj] = j <= r ? expf(sG[r] - sG[j]) * v[jj] : 0.f;
+                    v[jj] = j <= r ? __expf(sG[r] - sG[j]) * v[jj] : 0.f;
                 }
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) st_chunk(sP, r, 4 * hc + cc, v + 8 * cc);
@@ -292,64 +327,104 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
         sync_tc();
 
         if (RETR) {
-            // ---- T = (I + A)^-1 in fp32: 16x16 diagonal blocks, then blocked updates
+            // ---- T = (I + A)^-1 in fp32 by recursive doubling: invert the four
+            // 16x16 diagonal blocks, merge them into two 32x32 inverses, then one
+            // 64x64:  [[T0, 0], [L, T1]]^-1 block with L = -T1 A10 T0.
             if (warp < 4 && lane < 16) {
+                // column `lane` of the inverse of diagonal block `warp`, right-looking:
+                // once x[j] is final it updates every later row at once
                 float x[16];
-                const float *Ab = sAf + (16 * warp) * FS + 16 * warp;
+                const float *At = sAf + (16 * warp) * FA + 16 * warp;  // At[j][i] = A[i][j]
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float s = (i == lane) ? 1.f : 0.f;
+                for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
 #pragma unroll
-                    for (int j = 0; j < i; ++j) s -= Ab[i * FS + j] * x[j];
-                    x[i] = s;
+                for (int j = 0; j < 15; ++j) {
+                    float a[16];
+#pragma unroll
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        const float4 t = *reinterpret_cast<const float4 *>(At + j * FA + 4 * w4);
+                        a[4 * w4] = t.x, a[4 * w4 + 1] = t.y, a[4 * w4 + 2] = t.z, a[4 * w4 + 3] = t.w;
+                    }
+#pragma unroll
+                    for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-a[i], x[j], x[i]);
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) sTf[(16 * warp + i) * FS + 16 * warp + lane] = x[i];
+                for (int i = 0; i < 16; ++i) sTf[(16 * warp + i) * FT + 16 * warp + lane] = x[i];
+            } else if (warp >= 4) {
+                // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
+                const int u = tid - 128;  // 0..127, 4 entries each
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = 4 * u + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+                    sTf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
+                }
             }
             __syncthreads();
-            for (int d = 1; d < 4; ++d) {
-                const int jb = warp, ib = warp + d;
-                if (warp < 4 && ib < 4) {
-                    const int rr = lane >> 1, cc0 = (lane & 1) * 8;
-                    float xs[8];
+            {
+                // level 1: blocks (1,0) and (3,2); 128 threads per block, 2 outputs each
+                const int blk = tid >> 7, u = tid & 127;
+                const int r = u >> 3, c = 2 * (u & 7);  // row 0..15, columns c, c+1
+                const int o0 = 32 * blk;                // T_{b-1,b-1} at (o0, o0), A_{b,b-1} at (o0+16, o0)
+                float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) xs[e] = 0.f;
-                    for (int m = jb; m < ib; ++m) {
-#pragma unroll 4
-                        for (int qq = 0; qq < 16; ++qq) {
-                            const float a = sAf[(16 * ib + rr) * FS + 16 * m + qq];
-                            const float *tr = sTf + (16 * m + qq) * FS + 16 * jb + cc0;
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) xs[e] += a * tr[e];
-                        }
-                    }
-                    float *X = sX16 + warp * 16 * 17;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) X[rr * 17 + cc0 + e] = xs[e];
-                    __syncwarp();
-                    float ts[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ts[e] = 0.f;
-                    for (int qq = 0; qq <= rr; ++qq) {
-                        const float t = sTf[(16 * ib + rr) * FS + 16 * ib + qq];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) ts[e] += t * X[qq * 17 + cc0 + e];
-                    }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) sTf[(16 * ib + rr) * FS + 16 * jb + cc0 + e] = -ts[e];
-                    __syncwarp();
+                for (int k = 0; k < 16; ++k) {
+                    const float a = sAf[(o0 + k) * FA + o0 + 16 + r];
+                    y0 += a * sTf[(o0 + k) * FT + o0 + c];
+                    y1 += a * sTf[(o0 + k) * FT + o0 + c + 1];
                 }
+                sY[blk * 16 * 36 + r * 36 + c] = y0;
+                sY[blk * 16 * 36 + r * 36 + c + 1] = y1;
                 __syncthreads();
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float t = sTf[(o0 + 16 + r) * FT + o0 + 16 + k];
+                    l0 += t * sY[blk * 16 * 36 + k * 36 + c];
+                    l1 += t * sY[blk * 16 * 36 + k * 36 + c + 1];
+                }
+                sTf[(o0 + 16 + r) * FT + o0 + c] = -l0;
+                sTf[(o0 + 16 + r) * FT + o0 + c + 1] = -l1;
             }
+            __syncthreads();
+            {
+                // level 2: L = -T1 (A10 T0), 32x32 blocks; thread = (row, 4 columns)
+                const int r = tid >> 3, c = 4 * (tid & 7);
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    const float a = sAf[k * FA + 32 + r];
+                    const float4 t = *reinterpret_cast<const float4 *>(sTf + k * FT + c);
+                    y.x += a * t.x, y.y += a * t.y, y.z += a * t.z, y.w += a * t.w;
+                }
+                *reinterpret_cast<float4 *>(sY + r * 36 + c) = y;
+                __syncthreads();
+                float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) {
+                    const float t = sTf[(32 + r) * FT + 32 + k];
+                    const float4 yy = *reinterpret_cast<const float4 *>(sY + k * 36 + c);
+                    l.x += t * yy.x, l.y += t * yy.y, l.z += t * yy.z, l.w += t * yy.w;
+                }
+                *reinterpret_cast<float4 *>(sTf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
+            }
+            __syncthreads();
             {
                 const int r = tid >> 2, qq = tid & 3;
                 float ta[16], tb[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = 16 * qq + e;
-                    const float t = j <= r ? sTf[r * FS + j] : 0.f;
-                    tb[e] = t * sB[j];
-                    ta[e] = tb[e] * sEG[j];
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int j0 = 16 * qq + 4 * e4;
+                    const float4 t = *reinterpret_cast<const float4 *>(sTf + r * FT + j0);
+                    const float4 bb = *reinterpret_cast<const float4 *>(sB + j0);
+                    const float4 eg = *reinterpret_cast<const float4 *>(sEG + j0);
+                    const float tv[4] = {t.x, t.y, t.z, t.w}, bv[4] = {bb.x, bb.y, bb.z, bb.w};
+                    const float ev[4] = {eg.x, eg.y, eg.z, eg.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float tt = (j0 + e) <= r ? tv[e] : 0.f;
+                        tb[4 * e4 + e] = tt * bv[e];
+                        ta[4 * e4 + e] = tb[4 * e4 + e] * ev[e];
+                    }
                 }
                 st_chunk(sTa, r, 2 * qq, ta);
                 st_chunk(sTa, r, 2 * qq + 1, ta + 8);
@@ -361,10 +436,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
 
             // ---- I2 (W^T = K^T Ta^T), C1a (V^T Tb^T), C2 (S Qh^T)
             if (tid == 0) {
+                // W = Ta K: M = 64 tokens, N = 128 key channels (K as MN-major B)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tWT, tc::desc_sw128(aKQ + s * 2048, 16384), tc::desc_sw128(aTa + s * 32), IDN64_AMN,
-                                s > 0);
+                    tc::mma_f16(tW, tc::desc_sw128(aTa + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
+                                IDM64N128_BMN, s > 0);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     tc::mma_f16(tD, tc::desc_sw128(aV + s * 2048, 8192), tc::desc_sw128(aTb + s * 32), IDN64_AMN,
@@ -377,14 +453,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
             }
             ok = wait_mma(bar, phase, p.err) && ok;
             {
-                // W^T[c][r] (lane = key channel c) -> W tile [r][c]
+                // M = 64 result: token row r sits on lane 32 (r / 16) + r % 16
                 float v[32];
-                tc::ld32(tWT + lane_off + 32 * hc, v);
-                const int c = ell;
+                const int r = 16 * q4 + lane;
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int r = 32 * hc + jj;
-                    *reinterpret_cast<__half *>(sW + swz(r, c, 64)) = __float2half_rn(v[jj]);
+                for (int hh = 0; hh < 2; ++hh) {
+                    tc::ld32(tW + lane_off + 64 * hc + 32 * hh, v);
+                    if (lane < 16) {
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) st_chunk(sW + hc * 8192, r, 4 * hh + cc, v + 8 * cc);
+                    }
                 }
             }
             tc::fence_async_smem();
@@ -469,12 +547,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
             }
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) st_chunk(sS + hc * 16384, ell, ch, Sr + 8 * ch);
+            // O^T[i][r] -> staging tile O[r][i], then 16-byte row stores
             tc::ld32(tO + lane_off + 32 * hc, v);
-            __half *og = static_cast<__half *>(p.o);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int r = 32 * hc + jj;
-                if (r < n) og[((size_t)(c0 + r) * p.Hv + h) * 128 + ell] = __float2half_rn(p.scale * v[jj]);
+            for (int jj = 0; jj < 32; ++jj)
+                reinterpret_cast<__half *>(sO)[(32 * hc + jj) * 128 + ell] = __float2half_rn(p.scale * v[jj]);
+        }
+        tc::fence_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        {
+            const int r = tid >> 2, seg = tid & 3;
+            if (r < n) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(sO + r * 256 + seg * 64);
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.o) + ((size_t)(c0 + r) * p.Hv + h) * 128 +
+                                                       seg * 32);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) dst[w] = src[w];
             }
         }
         tc::fence_async_smem();
@@ -485,7 +574,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunked_tc_kernel(Problem p) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
         *reinterpret_cast<float4 *>(p.fin + srow + 4 * j) = make_float4(Sr[4 * j], Sr[4 * j + 1], Sr[4 * j + 2], Sr[4 * j + 3]);
-    ptx::cp_async_wait_all();
     sync_tc();
     if (warp == 0) tc::tmem_dealloc(*tslot, TC_TMEM_COLS);
 }
@@ -500,6 +588,36 @@ bool chunked_tc_eligible(const Problem &p) {
            al16(p.q) && al16(p.k) && al16(p.v) && al16(p.fin) && (p.init == nullptr || al16(p.init));
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [T, H, 128] fp16 rows -> boxes of 64 channels x 1 head x 64 tokens, 128-byte swizzle.
+static bool make_map(CUtensorMap *m, const void *base, int heads, int tokens) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)heads * 128 * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_chunked_tc(const Problem &p, cudaStream_t stream) {
     static int attr_done[64] = {0};
     int dev = 0;
@@ -512,11 +630,14 @@ cudaError_t launch_chunked_tc(const Problem &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_done[dev] = 1;
     }
+    CUtensorMap tk, tq, tv;
+    if (!make_map(&tk, p.k, p.Hq, p.T) || !make_map(&tq, p.q, p.Hq, p.T) || !make_map(&tv, p.v, p.Hv, p.T))
+        return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)((long long)p.B * p.Hv);
     if (rule_has_retrieval(p.rule))
-        chunked_tc_kernel<true><<<grid, TC_THREADS, TC_SMEM, stream>>>(p);
+        chunked_tc_kernel<true><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv);
     else
-        chunked_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM, stream>>>(p);
+        chunked_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv);
     return cudaGetLastError();
 }
 

@@ -170,3 +170,32 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
 
 }  // namespace tc
 }  // namespace gdn
+
+namespace gdn {
+namespace ptx {
+// Non-suspending bounded poll of an mbarrier phase (for short waits on the
+// tensor cores, where waking from a suspended try_wait costs more than the wait).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, uint32_t limit = (1u << 28)) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+// Tiled tensor load (TMA) of a 3-D box; completes its bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+        "[%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+}  // namespace ptx
+}  // namespace gdn

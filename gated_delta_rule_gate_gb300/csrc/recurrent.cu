@@ -150,7 +150,7 @@ __device__ __forceinline__ float4 ld_f4(const float *p) { return *reinterpret_ca
 // Lane group cg (8 lanes per row) owns columns 32 j + 4 cg + [0, 4).
 template <int NV>
 __device__ __forceinline__ void apply_tokens(const Problem &p, const Stage &s, float4 (&S)[NV], int nt,
-                                             int tb, int h, int i_row, int cg, bool active) {
+                                             int tb, int h, int i_row, int vcol, int cg, bool active) {
     const bool perkey = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
     const bool retrieval = rule_has_retrieval(p.rule);
     const float *kap = p.rule == kGdn2 ? s.x : s.k;
@@ -185,7 +185,7 @@ __device__ __forceinline__ void apply_tokens(const Problem &p, const Stage &s, f
             w += __shfl_xor_sync(0xffffffffu, w, o);
         }
         const float alpha = perkey ? 1.f : s.alpha[tt];
-        const float vi = active ? s.v[tt * s.vrows + i_row] : 0.f;
+        const float vi = active ? s.v[tt * s.vrows + vcol] : 0.f;
         const float d = retrieval ? s.beta[tt] * (vi - alpha * u) : vi;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
                     stage_tokens(p, st, h, qh, tb, nt, 0, tid, kThreads);
                     ptx::named_bar_sync(1, kThreads);
                 }
-                apply_tokens<NV>(p, st, S, nt, tb, h, i_row, cg, active);
+                apply_tokens<NV>(p, st, S, nt, tb, h, i_row, i_row, cg, active);
             }
             if (active) {
 #pragma unroll
@@ -516,6 +516,211 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
         if (!one_block) ptx::named_bar_sync(1, kThreads);  // every consumer is done with the buffer
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&tok_empty[buf]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Long requests (prefill through the token-serial form): one CTA per
+// (request, value head, 32-row slice), so a few long sequences still spread
+// over many SMs.  The state slice stays in registers for the whole request;
+// tokens go through in blocks of kTB: while block b is applied, the raw
+// key/query/value (and per-key decay / erase gate) rows of block b+1 are
+// already in flight with cp.async, and its scalar gates in registers.
+// ---------------------------------------------------------------------------
+struct LongLayout {
+    int stage_floats, raw_bytes, total_bytes;
+    bool has_a, has_x;
+};
+
+__host__ __device__ inline LongLayout long_layout(const Problem &p) {
+    LongLayout L;
+    L.has_a = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
+    L.has_x = p.rule == kGdn2;
+    L.stage_floats = kTB * p.dk * (2 + (L.has_a ? 1 : 0) + (L.has_x ? 1 : 0)) + kTB * kFastRows + 3 * kTB + 4;
+    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    L.raw_bytes = kTB * (2 * p.dk * es + kFastRows * es + (L.has_a ? p.dk * des : 0) + (L.has_x ? p.dk * bes : 0));
+    L.raw_bytes = (L.raw_bytes + 15) & ~15;
+    L.total_bytes = L.stage_floats * 4 + 2 * L.raw_bytes;
+    return L;
+}
+
+template <int DK>
+__device__ void issue_block_raw(const Problem &p, const LongLayout &Ly, unsigned char *raw, int h, int qh, int r0,
+                                int tb, int nt) {
+    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    unsigned char *rk = raw, *rq = rk + kTB * DK * es, *rv = rq + kTB * DK * es;
+    unsigned char *ra = rv + kTB * kFastRows * es, *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
+    const int kch = DK * es / 16;
+    const int vrows = min(kFastRows, p.dv - r0), vch = vrows * es / 16;
+    for (int idx = threadIdx.x; idx < nt * kch; idx += blockDim.x) {
+        const int tt = idx / kch, c = idx % kch;
+        const size_t off = (((size_t)(tb + tt) * p.Hq + qh) * DK) * es + 16 * c;
+        ptx::cp_async16(rk + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.k) + off, 16);
+        ptx::cp_async16(rq + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.q) + off, 16);
+    }
+    for (int idx = threadIdx.x; idx < nt * vch; idx += blockDim.x) {
+        const int tt = idx / vch, c = idx % vch;
+        const size_t off = (((size_t)(tb + tt) * p.Hv + h) * p.dv + r0) * es + 16 * c;
+        ptx::cp_async16(rv + tt * kFastRows * es + 16 * c, static_cast<const unsigned char *>(p.v) + off, 16);
+    }
+    if (Ly.has_a) {
+        const int ach = DK * des / 16;
+        for (int idx = threadIdx.x; idx < nt * ach; idx += blockDim.x) {
+            const int tt = idx / ach, c = idx % ach;
+            const size_t off = (((size_t)(tb + tt) * p.Hv + h) * DK) * des + 16 * c;
+            ptx::cp_async16(ra + tt * DK * des + 16 * c, static_cast<const unsigned char *>(p.decay) + off, 16);
+        }
+    }
+    if (Ly.has_x) {
+        const int xch = DK * bes / 16;
+        for (int idx = threadIdx.x; idx < nt * xch; idx += blockDim.x) {
+            const int tt = idx / xch, c = idx % xch;
+            const size_t off = (((size_t)(tb + tt) * p.Hv + h) * DK) * bes + 16 * c;
+            ptx::cp_async16(rx + tt * DK * bes + 16 * c, static_cast<const unsigned char *>(p.beta) + off, 16);
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, int slices) {
+    constexpr int NV = DK / 32;
+    constexpr int EPL = DK / 32;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const LongLayout Ly = long_layout(p);
+    float *stage_mem = reinterpret_cast<float *>(smem_raw);
+    unsigned char *raw0 = smem_raw + Ly.stage_floats * 4;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = lane & 7;
+    const int sidx = blockIdx.x % slices, bh = blockIdx.x / slices;
+    const int h = bh % p.Hv, b = bh / p.Hv;
+    const int r0 = sidx * kFastRows;
+    const int rloc = warp * 4 + (lane >> 3), i_row = r0 + rloc;
+    const bool active = i_row < p.dv;
+    const int row = state_row(p, b, h == 0 && sidx == 0 && tid == 0);
+    if (row < 0) return;
+    int t0, t1;
+    request_range(p, b, t0, t1);
+    const size_t soff = (((size_t)row * p.Hv + h) * p.dv + i_row) * DK + 4 * cg;
+    float4 S[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+        S[j] = (active && p.init) ? *reinterpret_cast<const float4 *>(p.init + soff + 32 * j) : make_float4(0, 0, 0, 0);
+    if (t1 == t0) {
+        if (active && p.fin != p.init) {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) *reinterpret_cast<float4 *>(p.fin + soff + 32 * j) = S[j];
+        }
+        return;
+    }
+    Stage st;
+    st.dkp = DK;
+    st.vrows = kFastRows;
+    st.k = stage_mem;
+    st.q = st.k + kTB * DK;
+    float *nx = st.q + kTB * DK;
+    st.a = Ly.has_a ? nx : nullptr;
+    nx += Ly.has_a ? kTB * DK : 0;
+    st.x = Ly.has_x ? nx : nullptr;
+    nx += Ly.has_x ? kTB * DK : 0;
+    st.v = nx;
+    nx += kTB * kFastRows;
+    st.alpha = nx;
+    st.beta = nx + kTB;
+    st.kq = nx + 2 * kTB;
+
+    const int qh = (int)((long long)h * p.Hq / p.Hv);
+    const bool has_decay = rule_has_decay(p.rule);
+    const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
+    const bool sig = (p.flags & kBetaSigmoid) != 0;
+    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    auto prefetch_scalars = [&](int tb, int nt, float &g, float &bb) {
+        g = 0.f, bb = 1.f;
+        if (tid < nt) {
+            const size_t th = (size_t)(tb + tid) * p.Hv + h;
+            if (has_decay && !Ly.has_a) g = ld_any(p.decay, th, p.decay_f16);
+            if (beta_scalar) bb = ld_any(p.beta, th, p.beta_f16);
+        }
+    };
+    float sg, sb;
+    issue_block_raw<DK>(p, Ly, raw0, h, qh, r0, t0, min(kTB, t1 - t0));
+    prefetch_scalars(t0, min(kTB, t1 - t0), sg, sb);
+    int blk = 0;
+    for (int tb = t0; tb < t1; tb += kTB, ++blk) {
+        const int nt = min(kTB, t1 - tb);
+        unsigned char *raw = raw0 + (blk & 1) * Ly.raw_bytes;
+        ptx::cp_async_wait_all();
+        __syncthreads();  // this block's rows landed; the previous block is fully applied
+        const float my_g = sg, my_b = sb;
+        if (tb + kTB < t1) {
+            const int nn = min(kTB, t1 - tb - kTB);
+            issue_block_raw<DK>(p, Ly, raw0 + ((blk + 1) & 1) * Ly.raw_bytes, h, qh, r0, tb + kTB, nn);
+            prefetch_scalars(tb + kTB, nn, sg, sb);
+        }
+        // stage: warp w takes token w
+        if (warp < nt) {
+            const int tt = warp;
+            const unsigned char *rk = raw, *rq = rk + kTB * DK * es, *rv = rq + kTB * DK * es;
+            const unsigned char *ra = rv + kTB * kFastRows * es, *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
+            (void)rv;
+            float kv[EPL], qv[EPL];
+            float ssk = 0.f, ssq = 0.f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int c = lane + 32 * i;
+                kv[i] = ld_raw(rk, tt * DK + c, p.act_f16);
+                qv[i] = ld_raw(rq, tt * DK + c, p.act_f16);
+                ssk += kv[i] * kv[i];
+                ssq += qv[i] * qv[i];
+            }
+            const float ik = (p.flags & kL2k) ? rsqrtf(warp_sum(ssk) + 1e-12f) : 1.f;
+            const float iq = (p.flags & kL2q) ? rsqrtf(warp_sum(ssq) + 1e-12f) : 1.f;
+            float kq = 0.f;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                kv[i] *= ik;
+                qv[i] *= iq;
+                kq += kv[i] * qv[i];
+            }
+            kq = warp_sum(kq);
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                const int c = lane + 32 * i;
+                st.k[tt * DK + c] = kv[i];
+                st.q[tt * DK + c] = qv[i];
+                if (Ly.has_a) {
+                    float g = ld_raw(ra, tt * DK + c, p.decay_f16);
+                    if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[(size_t)h * DK + c]);
+                    st.a[tt * DK + c] = expf(g);
+                }
+                if (Ly.has_x) {
+                    float bb = ld_raw(rx, tt * DK + c, p.beta_f16);
+                    if (sig) bb = sigmoid_f(bb);
+                    st.x[tt * DK + c] = bb * kv[i];
+                }
+            }
+            if (lane == 0) st.kq[tt] = kq;
+        }
+        {
+            const unsigned char *rv = raw + 2 * kTB * DK * es;
+            const int vrows = min(kFastRows, p.dv - r0);
+            for (int idx = tid; idx < nt * kFastRows; idx += kThreads) {
+                const int tt = idx / kFastRows, r = idx % kFastRows;
+                st.v[tt * kFastRows + r] = r < vrows ? ld_raw(rv, tt * kFastRows + r, p.act_f16) : 0.f;
+            }
+        }
+        if (tid < nt) {
+            float alpha = 1.f;
+            if (has_decay && !Ly.has_a) alpha = expf(p.raw_gate ? p.gate_scale[h] * softplus_f(my_g + p.gate_bias[h]) : my_g);
+            st.alpha[tid] = alpha;
+            st.beta[tid] = beta_scalar ? (sig ? sigmoid_f(my_b) : my_b) : 1.f;
+        }
+        __syncthreads();
+        apply_tokens<NV>(p, st, S, nt, tb, h, i_row, rloc, cg, active);
+    }
+    if (active) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) *reinterpret_cast<float4 *>(p.fin + soff + 32 * j) = S[j];
     }
 }
 
@@ -626,6 +831,24 @@ static cudaError_t launch_pipe(const Problem &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int DK>
+static cudaError_t launch_long(const Problem &p, cudaStream_t stream) {
+    const int slices = (p.dv + kFastRows - 1) / kFastRows;
+    const long long grid = (long long)p.B * p.Hv * slices;
+    const size_t smem = (size_t)long_layout(p).total_bytes;
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(recurrent_long_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, 120 * 1024);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_done[dev] = 1;
+    }
+    recurrent_long_kernel<DK><<<(unsigned)grid, kThreads, smem, stream>>>(p, slices);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream) {
     const bool fast_dk = p.dk == 32 || p.dk == 64 || p.dk == 128 || p.dk == 256;
     const int es = p.act_f16 ? 2 : 4;
@@ -635,6 +858,19 @@ cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream) {
                         (!per_key || aligned16(p.decay)) && (p.rule != kGdn2 || aligned16(p.beta));
     const bool fast = fast_dk && rows16 && aligned16(p.fin) && (p.init == nullptr || aligned16(p.init)) &&
                       pipe_layout(p).total_bytes <= 200 * 1024;
+    // Requests longer than a few token blocks on average: spread the slices of
+    // each (request, head) over their own CTAs instead of one persistent CTA.
+    const long long avg_len = p.seq_len ? p.seq_len : (p.B ? (long long)p.T / p.B : 0);
+    const bool long_rows = (p.dv * es) % 16 == 0 && aligned16(p.q) && aligned16(p.k) && aligned16(p.v) &&
+                           (!per_key || aligned16(p.decay)) && (p.rule != kGdn2 || aligned16(p.beta));
+    if (fast_dk && long_rows && avg_len > 4 * kTB && aligned16(p.fin) && (p.init == nullptr || aligned16(p.init))) {
+        switch (p.dk) {
+            case 32: return launch_long<32>(p, stream);
+            case 64: return launch_long<64>(p, stream);
+            case 128: return launch_long<128>(p, stream);
+            default: return launch_long<256>(p, stream);
+        }
+    }
     if (fast) {
         switch (p.dk) {
             case 32: return launch_pipe<32>(p, stream);

@@ -213,3 +213,29 @@ def test_decode_full_size_sampled(L):
     ui = torch.tensor(untouched)
     assert torch.equal(fin[ui.to(DEV)].cpu(), p["initial_state"][ui])
     assert not np.isnan(og).any()
+
+
+LONG_CASES = []
+for rule in ["linear", "gated", "delta", "gated_delta", "gdn2"]:
+    LONG_CASES.append(dict(rule=rule, act="f16", dk=128, dv=128, hq=1, hv=2))
+LONG_CASES += [
+    dict(rule="gated_delta", act="f32", dk=64, dv=64, hq=2, hv=4),
+    dict(rule="gated_delta", act="f16", dk=128, dv=96, hq=1, hv=2, decay_per_key=True),
+    dict(rule="gdn2", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True, write_gate=True,
+         gate_dtype="f32"),
+    dict(rule="gdn2", act="f32", dk=32, dv=32, hq=1, hv=2, decay_per_key=True),
+]
+
+
+@pytest.mark.parametrize("case", LONG_CASES, ids=[_case_id(c) for c in LONG_CASES])
+def test_recurrent_long_requests(case):
+    """Requests averaging more than 32 tokens take the one-CTA-per-slice
+    schedule with prefetched token blocks."""
+    kw = dict(seed=zlib.crc32(_case_id(case).encode()) % 1000, B=3, lengths=[150, 0, 67],
+              state="random", state_std=0.5, num_slots=5, slot_mode="perm")
+    kw.update(case)
+    p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p)
+    _check(p, o, fin, ref_o, ref_fin)
