@@ -200,6 +200,134 @@ __device__ __forceinline__ void apply_tokens(const Problem &p, const Stage &s, f
     }
 }
 
+// Applies the staged tokens [0, nt) to R row slices at once (R = 1 or 2): the
+// staged key/query loads are shared by the R rows and their reduction chains
+// interleave.  A scalar decay is kept as a lazy factor, S = c * S~, so each
+// token updates the state with one FMA per element:
+//   u = c' (S~ . kappa),  d = beta (v - u),  o = scale (c' (S~ . q) + d (k . q)),
+//   S~ += (d / c') k,  c' = c alpha
+// (renormalised into S~ when c' < 1e-20, and folded back before returning).
+template <int NV, int R>
+__device__ __forceinline__ void apply_tokens_multi(const Problem &p, const Stage &s, float4 (&S)[R][NV], int nt,
+                                                   int tb, int h, const int (&i_row)[R], const int (&vcol)[R],
+                                                   int cg, const bool (&active)[R]) {
+    const bool perkey = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
+    const bool retrieval = rule_has_retrieval(p.rule);
+    const float *kap = p.rule == kGdn2 ? s.x : s.k;
+    const int dk = s.dkp;
+    float c = 1.f;
+    const size_t ostride = (size_t)p.Hv * p.dv;
+    unsigned char *obase = static_cast<unsigned char *>(p.o) +
+                           ((size_t)tb * p.Hv + h) * p.dv * (p.act_f16 ? 2 : 4);
+    for (int tt = 0; tt < nt; ++tt) {
+        const float *kk = s.k + tt * dk + 4 * cg;
+        const float *qq = s.q + tt * dk + 4 * cg;
+        const float *xx = kap + tt * dk + 4 * cg;
+        if (perkey) {
+            const float *aa = s.a + tt * dk + 4 * cg;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                const float4 a4 = ld_f4(aa + 32 * j);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    S[r][j].x *= a4.x, S[r][j].y *= a4.y, S[r][j].z *= a4.z, S[r][j].w *= a4.w;
+            }
+        }
+        // packed fp32x2 FMAs (two lanes of a float4 per instruction)
+        float2 ua[R], ub[R], wa[R], wb[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) ua[r] = ub[r] = wa[r] = wb[r] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const float4 x4 = ld_f4(xx + 32 * j), q4 = ld_f4(qq + 32 * j);
+            const float2 xlo = make_float2(x4.x, x4.y), xhi = make_float2(x4.z, x4.w);
+            const float2 qlo = make_float2(q4.x, q4.y), qhi = make_float2(q4.z, q4.w);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float2 slo = make_float2(S[r][j].x, S[r][j].y), shi = make_float2(S[r][j].z, S[r][j].w);
+                ua[r] = __ffma2_rn(slo, xlo, ua[r]);
+                ub[r] = __ffma2_rn(shi, xhi, ub[r]);
+                wa[r] = __ffma2_rn(slo, qlo, wa[r]);
+                wb[r] = __ffma2_rn(shi, qhi, wb[r]);
+            }
+        }
+        // Butterfly over the 8 lanes of a row group: each exchange halves the set
+        // of partial sums a lane carries (4 shuffles for R = 2 instead of 12),
+        // leaving u (cg 0-1), w (cg 2-3) of row 0 and u (cg 4-5), w (cg 6-7)
+        // of row 1 (R = 2), or u (cg 0-3), w (cg 4-7) (R = 1); u is then
+        // broadcast to the whole group and the lane holding w writes o.
+        float val;
+        if (R == 2) {
+            const float u0 = (ua[0].x + ua[0].y) + (ub[0].x + ub[0].y), w0 = (wa[0].x + wa[0].y) + (wb[0].x + wb[0].y);
+            const float u1 = (ua[R - 1].x + ua[R - 1].y) + (ub[R - 1].x + ub[R - 1].y);
+            const float w1 = (wa[R - 1].x + wa[R - 1].y) + (wb[R - 1].x + wb[R - 1].y);
+            const bool hi = (cg & 4) != 0;
+            const float ra = __shfl_xor_sync(0xffffffffu, hi ? u0 : u1, 4);
+            const float rb = __shfl_xor_sync(0xffffffffu, hi ? w0 : w1, 4);
+            const float ka = (hi ? u1 : u0) + ra, kb = (hi ? w1 : w0) + rb;
+            const bool b1 = (cg & 2) != 0;
+            val = (b1 ? kb : ka) + __shfl_xor_sync(0xffffffffu, b1 ? ka : kb, 2);
+        } else {
+            const float u0 = (ua[0].x + ua[0].y) + (ub[0].x + ub[0].y), w0 = (wa[0].x + wa[0].y) + (wb[0].x + wb[0].y);
+            const bool hi = (cg & 4) != 0;
+            val = (hi ? w0 : u0) + __shfl_xor_sync(0xffffffffu, hi ? u0 : w0, 4);
+            val += __shfl_xor_sync(0xffffffffu, val, 2);
+        }
+        val += __shfl_xor_sync(0xffffffffu, val, 1);
+        const int gbase = (threadIdx.x & 31) & ~7;
+        float u[R];
+        u[0] = __shfl_sync(0xffffffffu, val, gbase);
+        if (R == 2) u[R - 1] = __shfl_sync(0xffffffffu, val, gbase + 4);
+        float cn = c * s.alpha[tt];  // alpha is 1 without scalar decay
+        const float bt = s.beta[tt], kq = s.kq[tt];
+        float d[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float vi = active[r] ? s.v[tt * s.vrows + vcol[r]] : 0.f;
+            d[r] = retrieval ? bt * (vi - cn * u[r]) : vi;
+            // the lane that holds this row's w writes its output
+            const int wl = R == 2 ? (r == 0 ? 2 : 6) : 4;
+            if (cg == wl && active[r]) {
+                const float ov = p.scale * fmaf(cn, val, d[r] * kq);
+                if (p.act_f16)
+                    reinterpret_cast<__half *>(obase)[(size_t)tt * ostride + i_row[r]] = __float2half_rn(ov);
+                else
+                    reinterpret_cast<float *>(obase)[(size_t)tt * ostride + i_row[r]] = ov;
+            }
+        }
+        if (cn < 1e-20f) {  // fold the factor in before it underflows (uniform across the CTA)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int j = 0; j < NV; ++j) S[r][j].x *= cn, S[r][j].y *= cn, S[r][j].z *= cn, S[r][j].w *= cn;
+            cn = 1.f;
+        }
+        const float rc = __frcp_rn(cn);
+        float e[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) e[r] = d[r] * rc;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const float4 k4 = ld_f4(kk + 32 * j);
+            const float2 klo = make_float2(k4.x, k4.y), khi = make_float2(k4.z, k4.w);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float2 ee = make_float2(e[r], e[r]);
+                const float2 lo = __ffma2_rn(ee, klo, make_float2(S[r][j].x, S[r][j].y));
+                const float2 hi = __ffma2_rn(ee, khi, make_float2(S[r][j].z, S[r][j].w));
+                S[r][j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+        c = cn;
+    }
+    if (c != 1.f) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int j = 0; j < NV; ++j) S[r][j].x *= c, S[r][j].y *= c, S[r][j].z *= c, S[r][j].w *= c;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Fast path: persistent, warp-specialised (dk in {32, 64, 128, 256}).
 //
@@ -374,6 +502,63 @@ __device__ void stage_pair_async(const Problem &p, const Stage &st, const PipeLa
     }
 }
 
+// The consumer side of one (request, head) pair: waits for each state slice in
+// the ring, applies the staged tokens R slices at a time and stores the result.
+// `j` counts ring uses across the CTA's pairs; it is set to -1 if a wait runs out.
+template <int DK, int R>
+__device__ __forceinline__ void consume_slices(const Problem &p, const Stage &st, const float *ring, uint64_t *full,
+                                               uint64_t *empty, int &j, int slices, int row, int h, int qh, int t0,
+                                               int t1, int tid, int lane, int cg, int rloc) {
+    constexpr int NV = DK / 32;
+    constexpr int kSlice = kFastRows * DK;
+    const int L = t1 - t0;
+    const bool one_block = L <= kTB;
+    for (int sl = 0; sl < slices; sl += R) {
+        float4 S[R][NV];
+        int i_row[R];
+        bool active[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int s = j % kStages;
+            if (!ptx::mbar_wait(&full[s], (j / kStages) & 1)) {
+                if (p.err && tid == 0) atomicOr(p.err, 2);
+                j = -1;
+                return;
+            }
+            ++j;
+            i_row[r] = (sl + r) * kFastRows + rloc;
+            active[r] = i_row[r] < p.dv;
+            const bool have = active[r] && row >= 0 && p.init != nullptr;
+            const float *src = ring + s * kSlice + rloc * DK + 4 * cg;
+#pragma unroll
+            for (int jj = 0; jj < NV; ++jj) S[r][jj] = have ? ld_f4(src + 32 * jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty[s]);
+        }
+        if (row < 0) continue;
+        if (L > 0) {
+            for (int tb = t0; tb < t1; tb += kTB) {
+                const int nt = min(kTB, t1 - tb);
+                if (!one_block) {  // long request: stage kTB tokens at a time ourselves
+                    ptx::named_bar_sync(1, kThreads);
+                    stage_tokens(p, st, h, qh, tb, nt, 0, tid, kThreads);
+                    ptx::named_bar_sync(1, kThreads);
+                }
+                apply_tokens_multi<NV, R>(p, st, S, nt, tb, h, i_row, i_row, cg, active);
+            }
+        } else if (p.fin == p.init) {
+            continue;  // empty request, in place: nothing changes
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (active[r]) {
+                float *dst = p.fin + (((size_t)row * p.Hv + h) * p.dv + i_row[r]) * DK + 4 * cg;
+#pragma unroll
+                for (int jj = 0; jj < NV; ++jj) __stcs(reinterpret_cast<float4 *>(dst + 32 * jj), S[r][jj]);
+            }
+    }
+}
+
 template <int DK>
 __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Problem p, int slices, int pairs) {
     constexpr int NV = DK / 32;  // float4s per lane per row
@@ -431,19 +616,26 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
         return;
     }
     if (warp == kCW + 1) {  // ---- token stager
+        // request range and slot of the next pair are read one pair ahead
+        auto header = [&](int pair, int &row, int &t0, int &t1) {
+            const int b = pair / p.Hv, h = pair % p.Hv;
+            row = state_row(p, b, h == 0 && lane == 0);
+            request_range(p, b, t0, t1);
+        };
+        int nrow = -1, nt0 = 0, nt1 = 0;
+        if (blockIdx.x < pairs) header(blockIdx.x, nrow, nt0, nt1);
         int k = 0;
         for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x, ++k) {
             const int buf = k & 1;
+            const int row = nrow, t0 = nt0, t1 = nt1;
+            if (pair + (int)gridDim.x < pairs) header(pair + gridDim.x, nrow, nt0, nt1);
             if (!ptx::mbar_wait(&tok_empty[buf], ((k >> 1) & 1) ^ 1)) {
                 if (p.err && lane == 0) atomicOr(p.err, 2);
                 return;
             }
             const Stage st = carve_pipe(stage_base + buf * Ly.stage_floats, p, Ly);
             int *hdr = reinterpret_cast<int *>(st.kq + kTB);
-            const int b = pair / p.Hv, h = pair % p.Hv;
-            const int row = state_row(p, b, h == 0 && lane == 0);
-            int t0, t1;
-            request_range(p, b, t0, t1);
+            const int h = pair % p.Hv;
             const int L = t1 - t0;
             if (row >= 0 && L > 0 && L <= kTB)
                 stage_pair_async<DK>(p, st, Ly, raw, h, (int)((long long)h * p.Hq / p.Hv), t0, L, lane);
@@ -475,44 +667,13 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
         const int L = t1 - t0;
         const int qh = (int)((long long)h * p.Hq / p.Hv);
         const bool one_block = L <= kTB;
-        for (int sl = 0; sl < slices; ++sl, ++j) {
-            const int s = j % kStages;
-            if (!ptx::mbar_wait(&full[s], (j / kStages) & 1)) {
-                if (p.err && tid == 0) atomicOr(p.err, 2);
-                return;
-            }
-            const int i_row = sl * kFastRows + rloc;
-            const bool active = i_row < p.dv;
-            float4 S[NV];
-            const bool have = active && row >= 0 && p.init != nullptr;
-            const float *src = ring + s * kSlice + rloc * DK + 4 * cg;
-#pragma unroll
-            for (int jj = 0; jj < NV; ++jj) S[jj] = have ? ld_f4(src + 32 * jj) : make_float4(0.f, 0.f, 0.f, 0.f);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&empty[s]);
-            if (row < 0) continue;
-            float *dst = p.fin + (((size_t)row * p.Hv + h) * p.dv + i_row) * DK + 4 * cg;
-            if (L == 0) {  // empty request: the incoming state goes through unchanged
-                if (active && p.fin != p.init) {
-#pragma unroll
-                    for (int jj = 0; jj < NV; ++jj) __stcs(reinterpret_cast<float4 *>(dst + 32 * jj), S[jj]);
-                }
-                continue;
-            }
-            for (int tb = t0; tb < t1; tb += kTB) {
-                const int nt = min(kTB, t1 - tb);
-                if (!one_block) {  // long request: stage kTB tokens at a time ourselves
-                    ptx::named_bar_sync(1, kThreads);
-                    stage_tokens(p, st, h, qh, tb, nt, 0, tid, kThreads);
-                    ptx::named_bar_sync(1, kThreads);
-                }
-                apply_tokens<NV>(p, st, S, nt, tb, h, i_row, i_row, cg, active);
-            }
-            if (active) {
-#pragma unroll
-                for (int jj = 0; jj < NV; ++jj) __stcs(reinterpret_cast<float4 *>(dst + 32 * jj), S[jj]);
-            }
-        }
+        // R state slices per pass (2 when the slice count is even): the staged
+        // key/query loads are shared and the rows' reduction chains interleave
+        if ((slices & 1) == 0)
+            consume_slices<DK, 2>(p, st, ring, full, empty, j, slices, row, h, qh, t0, t1, tid, lane, cg, rloc);
+        else
+            consume_slices<DK, 1>(p, st, ring, full, empty, j, slices, row, h, qh, t0, t1, tid, lane, cg, rloc);
+        if (j < 0) return;  // a wait ran out
         if (!one_block) ptx::named_bar_sync(1, kThreads);  // every consumer is done with the buffer
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&tok_empty[buf]);
