@@ -49,7 +49,7 @@ def make_workload(name, seed_offset=0, shrink=1):
     sequence length (a smaller case of the same kernel, for profiling)."""
     if name.startswith("decode-L"):
         L = int(name[len("decode-L"):])
-        return workloads.decode(L, seed=2 + seed_offset, B=256 // shrink), "recurrent"
+        return workloads.decode(L, seed=2 + seed_offset, B=256 // shrink, num_slots=1024 // shrink), "recurrent"
     if name == "ragged-prefill":
         return workloads.ragged_prefill(seed=3 + seed_offset, total=16384 // shrink,
                                         max_len=4096 // shrink), "chunked"
@@ -264,14 +264,29 @@ def time_e2e(api, p, d, prob, path, steps, warmup, stream, dev):
     return t0.elapsed_time(t1), h2d, d2h
 
 
-def kernel_source_digest(path):
-    f = os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc",
-                     "recurrent.cu" if path == "recurrent" else "chunked.cu")
+def kernel_name(p, path):
+    """The kernel the library dispatches for this workload (mirrors the host
+    dispatch in the CUDA sources)."""
+    if path == "recurrent":
+        L = p.get("seq_len") or p["total_tokens"] // max(p["batch"], 1)
+        return ("recurrent_long_kernel<%d>" if L > 32 else "recurrent_pipe_kernel<%d>") % p["dk"]
+    per_key = p.get("decay_per_key") and p["rule"] in ("gated", "gated_delta", "gdn2")
+    if per_key:
+        return "recurrent_long_kernel<%d>" % p["dk"]
+    if p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16" and p["rule"] != "gdn2":
+        return "chunked_tc_kernel<%s>" % ("true" if p["rule"] in ("delta", "gated_delta") else "false")
+    return "chunked_mma_kernel<%d,%s>" % (p["dk"], "true" if p["rule"] == "gdn2" else "false")
+
+
+def kernel_source_digest(path, kernel=""):
+    name = "recurrent.cu" if kernel.startswith("recurrent") else (
+        "chunked_tc.cu" if kernel.startswith("chunked_tc") else "chunked.cu")
+    f = os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc", name)
     with open(f, "rb") as fh:
         return hashlib.sha256(fh.read()).hexdigest()[:16]
 
 
-def ncu_traffic(workload, path):
+def ncu_traffic(workload, path, kernel=""):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source; None otherwise."""
     f = os.path.join(PROFILES, "traffic.json")
@@ -281,7 +296,7 @@ def ncu_traffic(workload, path):
     except (OSError, ValueError):
         return None
     ent = data.get(workload)
-    if not ent or ent.get("source_sha256_16") != kernel_source_digest(path):
+    if not ent or ent.get("source_sha256_16") != kernel_source_digest(path, kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -326,7 +341,7 @@ def cpu_cores():
 def run_reference(args, rank):
     if rank != 0:
         return
-    p, path = make_workload(args.workload)
+    p, path = make_workload(args.workload, shrink=args.shrink)
     cores = cpu_cores()
     import oracle
     ranges = workloads.token_ranges(p)
@@ -472,8 +487,8 @@ def main():
     ab = algorithmic_bytes(p)
     achieved = ab / (kern_ms * 1e-3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": ncu_traffic(args.workload, path),
-            "kernel": "recurrent_fast_kernel<128>" if path == "recurrent" else "chunked_prefill_kernel",
+            "frac": achieved / hbm, "traffic": ncu_traffic(args.workload, path, kernel_name(p, path)),
+            "kernel": kernel_name(p, path),
             "algorithmic_bytes_per_launch": ab, "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)"}
     if path == "chunked":
         af = algorithmic_flops(p)
@@ -483,7 +498,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (fp16 activations)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, workloads.py)", "config": workload_config(p, args),
         "roofline": roof, "clocks": clk,
         "e2e": e2e,
