@@ -36,6 +36,7 @@ constexpr int kStages = 4;       // state slices in flight per CTA, fast path
 
 struct Stage {
     float *k, *q, *a, *x, *v, *alpha, *beta, *kq;
+    int *hdr;  // pipe kernel: row, t0, t1 of the staged pair
     int dkp, vrows;
 };
 
@@ -51,6 +52,7 @@ __device__ __forceinline__ Stage carve(float *smem, int dkp, int vrows) {
     s.alpha = s.v + kTB * vrows;
     s.beta = s.alpha + kTB;
     s.kq = s.beta + kTB;
+    s.hdr = nullptr;
     return s;
 }
 
@@ -389,6 +391,7 @@ __device__ __forceinline__ Stage carve_pipe(float *base, const Problem &p, const
     s.alpha = nx;
     s.beta = nx + kTB;
     s.kq = nx + 2 * kTB;
+    s.hdr = reinterpret_cast<int *>(s.kq + kTB);
     return s;
 }
 
@@ -396,16 +399,30 @@ __device__ __forceinline__ float ld_raw(const unsigned char *base, int idx, int 
     return f16 ? __half2float(reinterpret_cast<const __half *>(base)[idx]) : reinterpret_cast<const float *>(base)[idx];
 }
 
-// The stager warp's work for one pair with 0 < L <= kTB tokens starting at t0.
+// Per-lane scalars the stager loads together with its copies: lane tt < L
+// holds token tt's decay input and beta as loaded (fp16 in the low half, or
+// fp32 bits; converted after the copies have landed, so the loads overlap
+// them); gs, gb are the head's gate scale and bias.
+struct TokScalars {
+    uint32_t g, b;
+    float gs, gb;
+};
+
+__device__ __forceinline__ uint32_t ld_bits(const void *p, size_t i, int f16) {
+    return f16 ? (uint32_t) reinterpret_cast<const unsigned short *>(p)[i] : reinterpret_cast<const uint32_t *>(p)[i];
+}
+__device__ __forceinline__ float bits_to_f(uint32_t x, int f16) {
+    return f16 ? __half2float(__ushort_as_half((unsigned short)x)) : __uint_as_float(x);
+}
+
+// The stager's copies for one pair with 0 < L <= kTB tokens starting at t0:
+// raw key/query/value rows (and per-key decay, erase gate) land in `raw` by
+// cp.async; the per-token scalars come back in `ts`.
 template <int DK>
-__device__ void stage_pair_async(const Problem &p, const Stage &st, const PipeLayout &Ly, unsigned char *raw,
-                                 int h, int qh, int t0, int L, int lane) {
-    constexpr int EPL = DK / 32;
+__device__ __forceinline__ void issue_pair(const Problem &p, const PipeLayout &Ly, unsigned char *raw, int h, int qh,
+                                           int t0, int L, int lane, TokScalars &ts) {
     const int es = p.act_f16 ? 2 : 4;
     const int des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
-    const bool has_decay = rule_has_decay(p.rule);
-    const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
-    const bool sig = (p.flags & kBetaSigmoid) != 0;
     unsigned char *rk = raw;
     unsigned char *rq = rk + kTB * DK * es;
     unsigned char *rv = rq + kTB * DK * es;
@@ -439,41 +456,67 @@ __device__ void stage_pair_async(const Problem &p, const Stage &st, const PipeLa
             ptx::cp_async16(rx + tt * DK * bes + 16 * c, static_cast<const unsigned char *>(p.beta) + off, 16);
         }
     }
-    // per-token scalars, one lane per token, in flight together with the copies
-    float g_l = 0.f, b_l = 1.f;
+    ts.g = ts.b = 0u;
+    ts.gs = ts.gb = 0.f;
     if (lane < L) {
         const size_t th = (size_t)(t0 + lane) * p.Hv + h;
-        if (has_decay && !Ly.has_a) g_l = ld_any(p.decay, th, p.decay_f16);
-        if (beta_scalar) b_l = ld_any(p.beta, th, p.beta_f16);
+        if (rule_has_decay(p.rule) && !Ly.has_a) {
+            ts.g = ld_bits(p.decay, th, p.decay_f16);
+            if (p.raw_gate) {
+                ts.gs = p.gate_scale[h];
+                ts.gb = p.gate_bias[h];
+            }
+        }
+        if (p.rule == kDelta || p.rule == kGatedDelta) ts.b = ld_bits(p.beta, th, p.beta_f16);
     }
-    ptx::cp_async_wait_all();
-    __syncwarp();
-    for (int tt = 0; tt < L; ++tt) {
-        float kv[EPL], qv[EPL];
-        float ssk = 0.f, ssq = 0.f;
+}
+
+// L2 normalisation and k . q of staged tokens g0 .. g0 + TG - 1 (those below
+// L), written as the fp32 rows the consumers read.  The TG tokens' warp
+// reductions are interleaved.
+template <int DK, int TG>
+__device__ __forceinline__ void stage_token_group(const Problem &p, const Stage &st, const PipeLayout &Ly,
+                                                  const unsigned char *rk, const unsigned char *rq,
+                                                  const unsigned char *ra, const unsigned char *rx, int h, int g0,
+                                                  int L, int lane) {
+    constexpr int EPL = DK / 32;
+    const bool sig = (p.flags & kBetaSigmoid) != 0;
+    float ssk[TG], ssq[TG], kq[TG];
+#pragma unroll
+    for (int u = 0; u < TG; ++u) {
+        const int tt = g0 + u;
+        ssk[u] = ssq[u] = kq[u] = 0.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int c = lane + 32 * i;
-            kv[i] = ld_raw(rk, tt * DK + c, p.act_f16);
-            qv[i] = ld_raw(rq, tt * DK + c, p.act_f16);
-            ssk += kv[i] * kv[i];
-            ssq += qv[i] * qv[i];
+            const float kx = tt < L ? ld_raw(rk, tt * DK + c, p.act_f16) : 0.f;
+            const float qx = tt < L ? ld_raw(rq, tt * DK + c, p.act_f16) : 0.f;
+            ssk[u] = fmaf(kx, kx, ssk[u]);
+            ssq[u] = fmaf(qx, qx, ssq[u]);
+            kq[u] = fmaf(kx, qx, kq[u]);
         }
-        const float ik = (p.flags & kL2k) ? rsqrtf(warp_sum(ssk) + 1e-12f) : 1.f;
-        const float iq = (p.flags & kL2q) ? rsqrtf(warp_sum(ssq) + 1e-12f) : 1.f;
-        float kq = 0.f;
+    }
+    const bool l2k = (p.flags & kL2k) != 0, l2q = (p.flags & kL2q) != 0;
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            kv[i] *= ik;
-            qv[i] *= iq;
-            kq += kv[i] * qv[i];
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int u = 0; u < TG; ++u) {
+            if (l2k) ssk[u] += __shfl_xor_sync(0xffffffffu, ssk[u], off);
+            if (l2q) ssq[u] += __shfl_xor_sync(0xffffffffu, ssq[u], off);
+            kq[u] += __shfl_xor_sync(0xffffffffu, kq[u], off);
         }
-        kq = warp_sum(kq);
+#pragma unroll
+    for (int u = 0; u < TG; ++u) {
+        const int tt = g0 + u;
+        if (tt >= L) break;
+        const float ik = l2k ? rsqrtf(ssk[u] + 1e-12f) : 1.f;
+        const float iq = l2q ? rsqrtf(ssq[u] + 1e-12f) : 1.f;
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
             const int c = lane + 32 * i;
-            st.k[tt * DK + c] = kv[i];
-            st.q[tt * DK + c] = qv[i];
+            const float kn = ld_raw(rk, tt * DK + c, p.act_f16) * ik;
+            st.k[tt * DK + c] = kn;
+            st.q[tt * DK + c] = ld_raw(rq, tt * DK + c, p.act_f16) * iq;
             if (Ly.has_a) {
                 float g = ld_raw(ra, tt * DK + c, p.decay_f16);
                 if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[(size_t)h * DK + c]);
@@ -482,23 +525,62 @@ __device__ void stage_pair_async(const Problem &p, const Stage &st, const PipeLa
             if (Ly.has_x) {
                 float bb = ld_raw(rx, tt * DK + c, p.beta_f16);
                 if (sig) bb = sigmoid_f(bb);
-                st.x[tt * DK + c] = bb * kv[i];
+                st.x[tt * DK + c] = bb * kn;
             }
         }
-        if (lane == 0) st.kq[tt] = kq;
+        if (lane == 0) st.kq[tt] = kq[u] * ik * iq;
     }
-    for (int idx = lane; idx < L * p.dv; idx += 32) {
-        const int tt = idx / p.dv, i = idx % p.dv;
-        st.v[tt * st.vrows + i] = ld_raw(rv, tt * p.dv + i, p.act_f16);
+}
+
+// The stager's processing of one pair once its copies have landed: L2
+// normalisation, k . q, the decay and beta scalars, and the staged fp32
+// token rows the consumers read.
+template <int DK>
+__device__ void finish_pair(const Problem &p, const Stage &st, const PipeLayout &Ly, const unsigned char *raw, int h,
+                            int L, int lane, const TokScalars &ts) {
+    const int es = p.act_f16 ? 2 : 4;
+    const int des = p.decay_f16 ? 2 : 4;
+    const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
+    const bool sig = (p.flags & kBetaSigmoid) != 0;
+    const unsigned char *rk = raw;
+    const unsigned char *rq = rk + kTB * DK * es;
+    const unsigned char *rv = rq + kTB * DK * es;
+    const unsigned char *ra = rv + kTB * p.dv * es;
+    const unsigned char *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
+    int g0 = 0;
+    for (; g0 + 4 <= L; g0 += 4) stage_token_group<DK, 4>(p, st, Ly, rk, rq, ra, rx, h, g0, L, lane);
+    if (L - g0 == 1)
+        stage_token_group<DK, 1>(p, st, Ly, rk, rq, ra, rx, h, g0, L, lane);
+    else if (L - g0 == 2)
+        stage_token_group<DK, 2>(p, st, Ly, rk, rq, ra, rx, h, g0, L, lane);
+    else if (L - g0 == 3)
+        stage_token_group<DK, 4>(p, st, Ly, rk, rq, ra, rx, h, g0, L, lane);
+    // value rows: 16-byte chunks (dv * element size is a multiple of 16)
+    const int vch = p.dv * es / 16;
+    for (int idx = lane; idx < L * vch; idx += 32) {
+        const int tt = idx / vch, c = idx % vch;
+        const uint4 w = *reinterpret_cast<const uint4 *>(rv + tt * p.dv * es + 16 * c);
+        float *dst = st.v + tt * st.vrows;
+        if (p.act_f16) {
+            const __half2 *hp = reinterpret_cast<const __half2 *>(&w);
+            const float2 f0 = __half22float2(hp[0]), f1 = __half22float2(hp[1]);
+            const float2 f2 = __half22float2(hp[2]), f3 = __half22float2(hp[3]);
+            *reinterpret_cast<float4 *>(dst + 8 * c) = make_float4(f0.x, f0.y, f1.x, f1.y);
+            *reinterpret_cast<float4 *>(dst + 8 * c + 4) = make_float4(f2.x, f2.y, f3.x, f3.y);
+        } else {
+            *reinterpret_cast<uint4 *>(dst + 4 * c) = w;
+        }
     }
     if (lane < L) {
         float alpha = 1.f;
-        if (has_decay && !Ly.has_a) {
-            if (p.raw_gate) g_l = p.gate_scale[h] * softplus_f(g_l + p.gate_bias[h]);
-            alpha = expf(g_l);
+        if (rule_has_decay(p.rule) && !Ly.has_a) {
+            const float graw = bits_to_f(ts.g, p.decay_f16);
+            const float g = p.raw_gate ? ts.gs * softplus_f(graw + ts.gb) : graw;
+            alpha = expf(g);
         }
+        const float b0 = bits_to_f(ts.b, p.beta_f16);
         st.alpha[lane] = alpha;
-        st.beta[lane] = beta_scalar ? (sig ? sigmoid_f(b_l) : b_l) : 1.f;
+        st.beta[lane] = beta_scalar ? (sig ? sigmoid_f(b0) : b0) : 1.f;
     }
 }
 
@@ -634,15 +716,19 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
                 return;
             }
             const Stage st = carve_pipe(stage_base + buf * Ly.stage_floats, p, Ly);
-            int *hdr = reinterpret_cast<int *>(st.kq + kTB);
             const int h = pair % p.Hv;
             const int L = t1 - t0;
-            if (row >= 0 && L > 0 && L <= kTB)
-                stage_pair_async<DK>(p, st, Ly, raw, h, (int)((long long)h * p.Hq / p.Hv), t0, L, lane);
+            if (row >= 0 && L > 0 && L <= kTB) {
+                TokScalars ts;
+                issue_pair<DK>(p, Ly, raw, h, (int)((long long)h * p.Hq / p.Hv), t0, L, lane, ts);
+                ptx::cp_async_wait_all();
+                __syncwarp();
+                finish_pair<DK>(p, st, Ly, raw, h, L, lane, ts);
+            }
             if (lane == 0) {
-                hdr[0] = row;
-                hdr[1] = t0;
-                hdr[2] = t1;
+                st.hdr[0] = row;
+                st.hdr[1] = t0;
+                st.hdr[2] = t1;
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&tok_full[buf]);
@@ -661,7 +747,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
             return;
         }
         const Stage st = carve_pipe(stage_base + buf * Ly.stage_floats, p, Ly);
-        const int *hdr = reinterpret_cast<const int *>(st.kq + kTB);
+        const int *hdr = st.hdr;
         const int row = hdr[0], t0 = hdr[1], t1 = hdr[2];
         const int h = pair % p.Hv;
         const int L = t1 - t0;
@@ -789,6 +875,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, 
     st.alpha = nx;
     st.beta = nx + kTB;
     st.kq = nx + 2 * kTB;
+    st.hdr = nullptr;
 
     const int qh = (int)((long long)h * p.Hq / p.Hv);
     const bool has_decay = rule_has_decay(p.rule);

@@ -94,6 +94,32 @@ def test_recurrent_parity_sweep(case):
     _check(p, o, fin, ref_o, ref_fin)
 
 
+SMALL_BLOCK = []
+for rule in ["linear", "gated", "delta", "gated_delta", "gdn2"]:
+    for dk, dv in [(128, 128), (64, 40), (32, 64)]:
+        SMALL_BLOCK.append(dict(rule=rule, dk=dk, dv=dv))
+
+
+@pytest.mark.parametrize("case", SMALL_BLOCK, ids=[_case_id(c) for c in SMALL_BLOCK])
+def test_decode_blocks_of_one_to_four_tokens(case):
+    """Requests of 1..4 tokens through the decode schedule, every rule: each
+    (request, head) pair is staged as one token block, its norms reduced
+    together.  dv = 40 leaves inactive rows inside a slice pair; the slab is
+    updated in place through permuted slots."""
+    kw = dict(seed=zlib.crc32(_case_id(case).encode()) % 1000, B=7, lengths=[1, 2, 3, 4, 0, 4, 2],
+              hq=1, hv=2, act="f16", state="random", state_std=0.5, num_slots=9, slot_mode="perm")
+    kw.update(case)
+    p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p, in_place=True)
+    og = o_flat(o, p)
+    assert rel_err(og, ref_o) <= TOL_O["f16"]
+    slots = [int(s) for s in p["slot_ids"]]
+    fg = fin[torch.tensor(slots, device=DEV)].double().cpu().numpy()
+    assert rel_err(fg, ref_fin[slots]) <= TOL_STATE
+
+
 @pytest.mark.parametrize("in_place", [False, True])
 def test_slots_routing_and_untouched_rows(in_place):
     p = workloads.make(seed=51, B=5, lengths=[2, 1, 0, 4, 3], hq=4, hv=8, dk=128, dv=128,
