@@ -586,7 +586,9 @@ bool al16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 
 
 }  // namespace
 
-size_t chunked_workspace_bytes(const Problem &, int) { return 0; }
+size_t chunked_workspace_bytes(const Problem &p, int) {
+    return chunked_tc_eligible(p) ? chunked_tc_workspace_bytes(p) : 0;
+}
 
 bool chunked_supported(const Problem &p, int, const char **why) {
     if (!(p.dk == 16 || p.dk == 32 || p.dk == 64 || p.dk == 128)) {
@@ -606,14 +608,12 @@ bool chunked_supported(const Problem &p, int, const char **why) {
 
 cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_bytes, cudaStream_t stream) {
     (void)chunk;
-    (void)ws;
-    (void)ws_bytes;
     if ((p.flags & kPerKey) && rule_has_decay(p.rule)) {
         // Per-key decay does not factor through the key contraction; this
         // build runs it through the token-serial kernel (same result).
         return launch_recurrent(p, stream);
     }
-    if (chunked_tc_eligible(p)) return launch_chunked_tc(p, stream);
+    if (chunked_tc_eligible(p)) return launch_chunked_tc(p, ws, ws_bytes, stream);
     const bool g2 = p.rule == kGdn2;
     switch (p.dk) {
         case 16: return g2 ? launch_mma<16, true>(p, stream) : launch_mma<16, false>(p, stream);

@@ -3,28 +3,39 @@
 // activations, scalar decay, rules linear / gated / delta / gated_delta.
 //
 // Same per-chunk algebra as chunked.cu (derived from the token recurrence;
-// see the comment there), written "transposed" so that the M = 128 side of
-// every tensor-core product is the value axis of the V-major state: lane i
-// of tensor memory is value row i.  For one chunk of C = 64 tokens:
+// see the comment there).  For one chunk of C = 64 tokens, with
+// A = strict-lower(diag(beta) e^{G_r - G_j} K K^T), T = (I + A)^-1,
+// Ta = T diag(beta e^G), Tb = T diag(beta):
 //
-//   I1:  [K; Q] K^T      -> rows 0..63: K K^T (the system), rows 64..127: Q K^T
-//   I2:  W^T  = K^T Ta^T       Ta = T diag(beta e^G),  T = (I + A)^-1
-//   C1:  D^T  = V^T Tb^T - S W^T   Tb = T diag(beta)   (D = the token corrections)
-//   C2:  O^T  = S Qh^T + D^T P^T   Qh = diag(e^G) Q,  P = decayed causal Q K^T
+//   I1:  [K; Q] K^T      -> rows 64..127: Q K^T (P = its decayed causal part)
+//   I2:  W^T  = K^T Ta^T
+//   C1:  D^T  = V^T Tb^T - S W^T                       (D = the token corrections)
+//   C2:  O^T  = S Qh^T + D^T P^T   Qh = diag(e^G) Q
 //   C4:  X    = (D^T diag(e^{G_C - G})) K
 //   S   <- e^{G_C} S + X                               (fp32, in registers)
 //
-// Operands are fp16 tiles in shared memory with the 128-byte swizzle.  The
-// key/query chunk lands (tiled TMA) as a 128-row K-major tile [K; Q]; its key
-// rows double as the MN-major K^T operand of I2 and C4, and the value chunk
-// lands as the MN-major V^T operand, so nothing is transposed by hand.  The
-// fp32 state lives in registers of the 8 warps (row i, 64 columns each) and
-// is mirrored each chunk into an fp16 K-major tile, the A operand of C1/C2.
-// The unit-lower-triangular solve runs in fp32 on the CUDA cores.  The next
-// chunk's loads are in flight while the current chunk computes.  One CTA of
-// 256 threads per (request, value head); one thread issues every MMA and
-// tracks completion through an mbarrier (bounded waits).
+// Two kernels run the delta rules.  The key-side system does not depend on
+// the state, so chunk_solve_kernel builds A with one tensor-core product and
+// solves it in fp32 for every (chunk, head) at once, all chunks in parallel,
+// and writes Tb (fp16) to the workspace.  chunked_tc_kernel then walks each
+// (request, value head) chunk by chunk; it loads Tb by TMA together with the
+// chunk's keys, queries and values and forms Ta = Tb diag(e^G) itself.  The
+// rules without retrieval (D = V) need no solve.
+//
+// chunked_tc_kernel is written "transposed" so that the M = 128 side of every
+// tensor-core product is the value axis of the V-major state: lane i of
+// tensor memory is value row i.  Operands are fp16 tiles in shared memory
+// with the 128-byte swizzle.  The key/query chunk lands (tiled TMA) as a
+// 128-row K-major tile [K; Q]; its key rows double as the MN-major K^T
+// operand of I2 and C4, and the value chunk lands as the MN-major V^T
+// operand, so nothing is transposed by hand.  The fp32 state lives in
+// registers of the 8 warps (row i, 64 columns each) and is mirrored each
+// chunk into an fp16 K-major tile, the A operand of C1/C2.  The next chunk's
+// loads are in flight while the current chunk computes.  One CTA of 256
+// threads per (request, value head); one thread issues every MMA and tracks
+// completion through an mbarrier (bounded waits).
 #include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -33,38 +44,41 @@
 namespace gdn {
 namespace {
 
-constexpr int TC_C = 64;        // tokens per chunk
+constexpr int TC_C = 64;         // tokens per chunk
 constexpr int TC_THREADS = 256;  // 8 warps
 constexpr int TC_TMEM_COLS = 512;
+constexpr int kTbBytes = TC_C * TC_C * 2;  // one fp16 Tb tile
 
-// shared memory layout (bytes from a 1024-aligned base)
+// shared memory layout of chunked_tc_kernel (bytes from a 1024-aligned base)
 constexpr int oKQ = 0;            // 2 x 32 KB: [K; Q] landing tiles, 128 rows x 128 dk, K-major
 constexpr int oV = 65536;         // 2 x 16 KB: V landing tiles, MN-major (rows = tokens)
 constexpr int oS = 98304;         // 32 KB: fp16 state, 128 rows x 128 dk, K-major
 constexpr int oTa = 131072;       // 8 KB: [64 r][64 j]
-constexpr int oTb = 139264;       // 8 KB
-constexpr int oP = 147456;        // 8 KB
-constexpr int oR = 155648;        // 48 KB region: solve scratch, then W | DT | DTs
+constexpr int oTb = 139264;       // 2 x 8 KB: Tb landing tiles [64 r][64 j]
+constexpr int oP = 155648;        // 8 KB
+constexpr int oR = 163840;        // 48 KB: W | DT | DTs
 constexpr int oW = oR;            // 16 KB: [64 r][128 c], K-major
 constexpr int oDT = oR + 16384;   // 16 KB: [128 i][64 j]
 constexpr int oDTs = oR + 32768;  // 16 KB
 constexpr int oO = oDT;           // 16 KB: output staging [64 r][128 i] (after the last MMAs)
-constexpr int oAf = oR;           // fp32 [64][68] the system matrix, transposed: At[j][r] = A[r][j]
-constexpr int oTf = oR + 17408;   // fp32 [64][68] its inverse
-constexpr int oY = oR + 34816;    // fp32 [32][36] product scratch of the solve
 constexpr int oScal = oR + 49152; // fp32 G, beta, e^G, e^{G_C - G}: 4 x 64
 constexpr int oBar = oScal + 1024;  // MMA barrier, two landing barriers, TMEM address
 constexpr int TC_SMEM = oBar + 32 + 1024;  // + alignment slack
 
-constexpr int FA = 68;  // fp32 row stride of At (16-byte rows; lanes = consecutive r, conflict-free)
-constexpr int FT = 68;  // fp32 row stride of T (16-byte rows for vector reads)
 constexpr uint32_t kLandBytes = 3 * 16384;  // K, Q and V boxes of one chunk
 
-// byte offset of element (row, k) in a K-major 128B-swizzled tile with `rows`
-// rows per 64-column block
-__device__ __forceinline__ int swz(int row, int k, int rows) {
-    return (k >> 6) * rows * 128 + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) + (k & 7) * 2;
-}
+// shared memory layout of chunk_solve_kernel
+constexpr int SV_THREADS = 128;
+constexpr int FA = 68;  // fp32 row stride of At (16-byte rows; lanes = consecutive r, conflict-free)
+constexpr int FT = 68;  // fp32 row stride of T (16-byte rows for vector reads)
+constexpr int sK = 0;                      // 16 KB: K, 2 blocks of [64 tokens][64 dk], K-major
+constexpr int sAt = 16384;                 // fp32 [64][FA], At[j][r] = A[r][j]
+constexpr int sTf = sAt + 64 * FA * 4;     // fp32 [64][FT], T
+constexpr int sY = sTf + 64 * FT * 4;      // fp32 [32][36] product scratch
+constexpr int sSc = sY + 32 * 36 * 4;      // fp32 G, beta, 1/|k|: 3 x 64
+constexpr int sBar = sSc + 3 * 64 * 4;     // landing barrier, MMA barrier, TMEM address
+constexpr int SV_SMEM = sBar + 32 + 1024;  // + alignment slack
+
 // writes 8 consecutive fp16 values (one 16-byte chunk) of row `row`, chunk
 // `ch` (0..7) of a 64-column block
 __device__ __forceinline__ void st_chunk(unsigned char *tile, int row, int ch, const float *x) {
@@ -90,33 +104,348 @@ __device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, int32_t
     return ok;
 }
 
-// One chunk of keys, queries and values: six 64 x 64 fp16 boxes by TMA.  The
-// 128-byte swizzle of the tensor maps lays them out exactly as the K-major
-// [K; Q] operand and the MN-major V^T operand expect.
+// number of chunks of request b
+__device__ __forceinline__ int request_chunks(const Problem &p, int b) {
+    int t0, t1;
+    request_range(p, b, t0, t1);
+    return (t1 - t0 + TC_C - 1) / TC_C;
+}
+
+// ---------------------------------------------------------------------------
+// Workspace slots: chunk j of request b has slot offs[b] + j, offs being the
+// exclusive prefix sum of the requests' chunk counts (offs[B] = the total).
+// One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *offs) {
+    __shared__ int wsum[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (p.B + 1023) / 1024;
+    const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
+    int s = 0;
+    for (int b = b0; b < b1; ++b) s += request_chunks(p, b);
+    // exclusive block scan of s
+    int x = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    int base = x - s + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        offs[b] = base;
+        base += request_chunks(p, b);
+    }
+    if (tid == 1023) offs[p.B] = wsum[31];
+}
+
+// ---------------------------------------------------------------------------
+// Tb = (I + A)^-1 diag(beta) of one (chunk, value head).  Grid (slots, Hv),
+// 128 threads.  A = strict-lower(diag(beta) e^{G_r - G_j} Kn Kn^T), Kn the
+// key rows after the optional L2 norm, from one M = 64 tensor-core product of
+// the raw fp16 keys (the norms are applied to the fp32 result).  The solve
+// is fp32 recursive doubling: the four 16 x 16 diagonal blocks by
+// substitution, then [[T0, 0], [L, T1]] with L = -T1 A10 T0 twice.  Padding
+// tokens of a short last chunk get beta = 0 and zero keys, so their rows and
+// columns of Tb are zero.
+__global__ void __launch_bounds__(SV_THREADS) chunk_solve_kernel(Problem p, const __grid_constant__ CUtensorMap tmK,
+                                                                 const int *offs, __half *tb, int cap) {
+    extern __shared__ unsigned char smraw[];
+    const uint32_t sb0 = ptx::smem_u32(smraw);
+    unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
+    const int slot = blockIdx.x, h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (slot >= cap || slot >= offs[p.B]) return;
+    // the request owning this slot: the last b with offs[b] <= slot
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offs[mid] <= slot)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int b = lo;
+    int t0, t1;
+    request_range(p, b, t0, t1);
+    const int c0 = t0 + TC_C * (slot - offs[b]);
+    const int n = min(TC_C, t1 - c0);
+    if (n <= 0) return;
+    const int qh = (int)((long long)h * p.Hq / p.Hv);
+
+    unsigned char *sKt = sm + sK;
+    float *At = reinterpret_cast<float *>(sm + sAt);
+    float *Tf = reinterpret_cast<float *>(sm + sTf);
+    float *Y = reinterpret_cast<float *>(sm + sY);
+    float *sG = reinterpret_cast<float *>(sm + sSc);
+    float *sB = sG + 64, *sInv = sG + 128;
+    uint64_t *ldbar = reinterpret_cast<uint64_t *>(sm + sBar);
+    uint64_t *mbar = ldbar + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + sBar + 16);
+
+    if (tid == 0) {
+        ptx::mbar_init(ldbar, 1);
+        ptx::mbar_init(mbar, 1);
+        ptx::fence_mbar_init();
+        ptx::mbar_arrive_expect_tx(ldbar, 16384);
+        ptx::tma_load_3d(sKt, &tmK, 0, qh, c0, ldbar);
+        ptx::tma_load_3d(sKt + 8192, &tmK, 64, qh, c0, ldbar);
+    }
+    if (warp == 0) tc::tmem_alloc(tslot, 64);
+    if (tid < TC_C) {
+        float g = 0.f, bt = 0.f;
+        if (tid < n) {
+            const size_t th = (size_t)(c0 + tid) * p.Hv + h;
+            if (rule_has_decay(p.rule)) {
+                g = ld_any(p.decay, th, p.decay_f16);
+                if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[h]);
+            }
+            bt = ld_any(p.beta, th, p.beta_f16);
+            if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
+        }
+        sG[tid] = g;
+        sB[tid] = bt;
+    }
+    __syncthreads();
+    if (warp == 0) {  // G = inclusive cumulative sum of the log decays
+        const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
+        float s = g0 + g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        sG[2 * lane] = s - g1;
+        sG[2 * lane + 1] = s;
+    }
+    // every thread waits; the barrier makes the outcome uniform across the CTA
+    bool ok = __syncthreads_and(ptx::mbar_wait(ldbar, 0)) != 0;
+    if (!ok && p.err && tid == 0) atomicOr(p.err, 2);
+    if (ok) {
+        if (n < TC_C) {  // the boxes run past this request: clear the rows beyond it
+            for (int idx = tid; idx < (TC_C - n) * 16; idx += SV_THREADS) {
+                const int r = n + (idx >> 4), ch = idx & 15;
+                *reinterpret_cast<uint4 *>(sKt + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(0, 0, 0, 0);
+            }
+        }
+        __syncthreads();
+        {  // 1 / |k_r|: thread pair (2r, 2r + 1), one 64-column block each
+            const int r = tid >> 1, kb = tid & 1;
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(sKt + kb * 8192 + r * 128 + ((c ^ (r & 7)) << 4));
+                const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float2 f = __half22float2(hp[w]);
+                    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (kb == 0) sInv[r] = (p.flags & kL2k) ? rsqrtf(ss + 1e-12f) : 1.f;
+        }
+    }
+    tc::fence_async_smem();
+    sync_tc();
+    const uint32_t tmem = *tslot;
+    if (ok && tid == 0) {
+        // K K^T: M = 64 tokens, N = 64 tokens, K = 128 channels
+        const uint32_t aK = ptx::smem_u32(sKt);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint64_t d = tc::desc_sw128(aK + (s >> 2) * 8192 + (s & 3) * 32);
+            tc::mma_f16(tmem, d, d, tc::idesc_f16(64, 64), s > 0);
+        }
+        tc::commit(mbar);
+    }
+    if (ok) {
+        uint32_t phase = 0;
+        ok = wait_mma(mbar, phase, p.err);
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (ok) {
+        // row r = 16 warp + lane sits on tensor-memory lane 32 warp + lane (M = 64)
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        const int r = 16 * warp + lane;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float v[32];
+            tc::ld32(tmem + lane_off + 32 * hh, v);
+            if (lane < 16) {
+                const float br = sB[r] * sInv[r], Gr = sG[r];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * hh + jj;
+                    At[j * FA + r] = j < r ? br * __expf(Gr - sG[j]) * sInv[j] * v[jj] : 0.f;
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (ok) {
+        if (lane < 16) {
+            // column `lane` of the inverse of diagonal block `warp`, right-looking:
+            // once x[j] is final it updates every later row at once
+            float x[16];
+            const float *Ab = At + (16 * warp) * FA + 16 * warp;  // Ab[j][i] = A[i][j]
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < 15; ++j) {
+                float a[16];
+#pragma unroll
+                for (int w4 = 0; w4 < 4; ++w4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(Ab + j * FA + 4 * w4);
+                    a[4 * w4] = t.x, a[4 * w4 + 1] = t.y, a[4 * w4 + 2] = t.z, a[4 * w4 + 3] = t.w;
+                }
+#pragma unroll
+                for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-a[i], x[j], x[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tf[(16 * warp + i) * FT + 16 * warp + lane] = x[i];
+        }
+        // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = 4 * tid + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+            Tf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        // level 1: blocks (1,0) and (3,2): Y = A_{b,b-1} T_{b-1}, then L = -T_b Y
+        const int r = tid >> 3, c = 2 * (tid & 7);  // row 0..15, columns c, c+1
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            const int o0 = 32 * blk;
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float a = At[(o0 + k) * FA + o0 + 16 + r];
+                y0 = fmaf(a, Tf[(o0 + k) * FT + o0 + c], y0);
+                y1 = fmaf(a, Tf[(o0 + k) * FT + o0 + c + 1], y1);
+            }
+            Y[blk * 16 * 36 + r * 36 + c] = y0;
+            Y[blk * 16 * 36 + r * 36 + c + 1] = y1;
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        const int r = tid >> 3, c = 2 * (tid & 7);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+            const int o0 = 32 * blk;
+            float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float t = Tf[(o0 + 16 + r) * FT + o0 + 16 + k];
+                l0 = fmaf(t, Y[blk * 16 * 36 + k * 36 + c], l0);
+                l1 = fmaf(t, Y[blk * 16 * 36 + k * 36 + c + 1], l1);
+            }
+            Tf[(o0 + 16 + r) * FT + o0 + c] = -l0;
+            Tf[(o0 + 16 + r) * FT + o0 + c + 1] = -l1;
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        // level 2: Y = A_10 T_0 (32 x 32), thread = (row, 2 x 4 columns)
+        const int r = tid >> 2;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int c = 4 * (tid & 3) + 16 * half;
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float a = At[k * FA + 32 + r];
+                const float4 t = *reinterpret_cast<const float4 *>(Tf + k * FT + c);
+                y.x = fmaf(a, t.x, y.x), y.y = fmaf(a, t.y, y.y), y.z = fmaf(a, t.z, y.z), y.w = fmaf(a, t.w, y.w);
+            }
+            *reinterpret_cast<float4 *>(Y + r * 36 + c) = y;
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        // L = -T_1 Y
+        const int r = tid >> 2;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int c = 4 * (tid & 3) + 16 * half;
+            float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+                const float t = Tf[(32 + r) * FT + 32 + k];
+                const float4 yy = *reinterpret_cast<const float4 *>(Y + k * 36 + c);
+                l.x = fmaf(t, yy.x, l.x), l.y = fmaf(t, yy.y, l.y), l.z = fmaf(t, yy.z, l.z), l.w = fmaf(t, yy.w, l.w);
+            }
+            *reinterpret_cast<float4 *>(Tf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        // Tb[r][j] = T[r][j] beta_j (j <= r), fp16 rows of 128 bytes
+        const int r = tid >> 1, j0 = 32 * (tid & 1);
+        __half *dst = tb + (((size_t)slot * p.Hv + h) * TC_C + r) * TC_C + j0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = j0 + 8 * w + e;
+                x[e] = j <= r ? Tf[r * FT + j] * sB[j] : 0.f;
+            }
+            uint4 u;
+            u.x = ptx::pack_h2(x[0], x[1]);
+            u.y = ptx::pack_h2(x[2], x[3]);
+            u.z = ptx::pack_h2(x[4], x[5]);
+            u.w = ptx::pack_h2(x[6], x[7]);
+            *reinterpret_cast<uint4 *>(dst + 8 * w) = u;
+        }
+    }
+    sync_tc();
+    if (warp == 0) tc::tmem_dealloc(tmem, 64);
+}
+
+// ---------------------------------------------------------------------------
+// One chunk of keys, queries and values (six 64 x 64 fp16 boxes) and, for the
+// delta rules, its Tb tile, by TMA.  The 128-byte swizzle of the tensor maps
+// lays them out exactly as the K-major [K; Q] operand, the MN-major V^T
+// operand and the K-major Tb^T operand expect.
 __device__ __forceinline__ void issue_chunk(const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV,
-                                            unsigned char *kq, unsigned char *vt, uint64_t *bar, int c0, int h,
-                                            int qh) {
-    ptx::mbar_arrive_expect_tx(bar, kLandBytes);
+                                            const CUtensorMap *tmT, unsigned char *kq, unsigned char *vt,
+                                            unsigned char *tbt, uint64_t *bar, int c0, int h, int qh, int trow) {
+    ptx::mbar_arrive_expect_tx(bar, kLandBytes + (tbt ? (uint32_t)kTbBytes : 0u));
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
         ptx::tma_load_3d(kq + kb * 16384, tmK, 64 * kb, qh, c0, bar);
         ptx::tma_load_3d(kq + kb * 16384 + 8192, tmQ, 64 * kb, qh, c0, bar);
         ptx::tma_load_3d(vt + kb * 8192, tmV, 64 * kb, h, c0, bar);
     }
+    if (tbt) ptx::tma_load_2d(tbt, tmT, 0, trow, bar);
 }
 
 template <bool RETR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     chunked_tc_kernel(Problem p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmV) {
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmT,
+                      const int *offs, int cap) {
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
     unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
-    unsigned char *sS = sm + oS, *sTa = sm + oTa, *sTb = sm + oTb, *sP = sm + oP;
+    unsigned char *sS = sm + oS, *sTa = sm + oTa, *sP = sm + oP;
     unsigned char *sW = sm + oW, *sDT = sm + oDT, *sDTs = sm + oDTs;
-    float *sAf = reinterpret_cast<float *>(sm + oAf);
-    float *sTf = reinterpret_cast<float *>(sm + oTf);
-    float *sY = reinterpret_cast<float *>(sm + oY);
     float *sG = reinterpret_cast<float *>(sm + oScal);
     float *sB = sG + 64, *sEG = sG + 128, *sEGC = sG + 192;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + oBar);
@@ -134,6 +463,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int qh = (int)((long long)h * p.Hq / p.Hv);
     const bool has_decay = rule_has_decay(p.rule);
     const bool sig = (p.flags & kBetaSigmoid) != 0;
+    int slot0 = 0;
+    if (RETR && t1 > t0) {
+        slot0 = offs[b];
+        if (slot0 + (t1 - t0 + TC_C - 1) / TC_C > cap) {
+            // only overlapping requests can outgrow the workspace: skip this one
+            if (p.err && tid == 0) atomicOr(p.err, 4);
+            return;
+        }
+    }
+    // the head's gate parameters
+    const float gsc = (has_decay && p.raw_gate) ? p.gate_scale[h] : 0.f;
+    const float gbi = (has_decay && p.raw_gate) ? p.gate_bias[h] : 0.f;
 
     // ---- the fp32 state: row ell, columns [64 hc, 64 hc + 64)
     float Sr[64];
@@ -158,7 +499,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         ptx::mbar_init(&ldbar[0], 1);
         ptx::mbar_init(&ldbar[1], 1);
         ptx::fence_mbar_init();
-        issue_chunk(&tmK, &tmQ, &tmV, sm + oKQ, sm + oV, &ldbar[0], t0, h, qh);
+        issue_chunk(&tmK, &tmQ, &tmV, &tmT, sm + oKQ, sm + oV, RETR ? sm + oTb : nullptr, &ldbar[0], t0, h, qh,
+                    (slot0 * p.Hv + h) * TC_C);
     }
     if (warp == 0) tc::tmem_alloc(tslot, TC_TMEM_COLS);
     // the fp16 mirror of the state
@@ -183,7 +525,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t IDN64_NEGB = tc::idesc_f16(128, 64, false, false, true);
     const uint32_t IDN128_BMN = tc::idesc_f16(128, 128, false, true);
     const uint32_t IDM64N128_BMN = tc::idesc_f16(64, 128, false, true);
-    const uint32_t aS = ptx::smem_u32(sS), aTa = ptx::smem_u32(sTa), aTb = ptx::smem_u32(sTb);
+    const uint32_t aS = ptx::smem_u32(sS), aTa = ptx::smem_u32(sTa);
     const uint32_t aP = ptx::smem_u32(sP), aW = ptx::smem_u32(sW), aDT = ptx::smem_u32(sDT);
     const uint32_t aDTs = ptx::smem_u32(sDTs);
 
@@ -192,16 +534,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int n = min(TC_C, t1 - c0);
         unsigned char *sKQ = sm + oKQ + buf * 32768;
         unsigned char *sV = sm + oV + buf * 16384;
-        const uint32_t aKQ = ptx::smem_u32(sKQ), aV = ptx::smem_u32(sV);
-        if (!ptx::mbar_wait(&ldbar[buf], (ci >> 1) & 1)) {
+        unsigned char *sTb = sm + oTb + buf * kTbBytes;
+        const uint32_t aKQ = ptx::smem_u32(sKQ), aV = ptx::smem_u32(sV), aTb = ptx::smem_u32(sTb);
+        // the barrier makes every exit from this loop uniform across the CTA
+        if (!__syncthreads_and(ptx::mbar_wait(&ldbar[buf], (ci >> 1) & 1))) {
             if (p.err && tid == 0) atomicOr(p.err, 2);
             ok = false;
             break;
         }
         // the other buffer was released by the previous chunk: prefetch the next one
         if (tid == 0 && c0 + TC_C < t1)
-            issue_chunk(&tmK, &tmQ, &tmV, sm + oKQ + (buf ^ 1) * 32768, sm + oV + (buf ^ 1) * 16384,
-                        &ldbar[buf ^ 1], c0 + TC_C, h, qh);
+            issue_chunk(&tmK, &tmQ, &tmV, &tmT, sm + oKQ + (buf ^ 1) * 32768, sm + oV + (buf ^ 1) * 16384,
+                        RETR ? sm + oTb + (buf ^ 1) * kTbBytes : nullptr, &ldbar[buf ^ 1], c0 + TC_C, h, qh,
+                        ((slot0 + ci + 1) * p.Hv + h) * TC_C);
         if (n < TC_C) {
             // the boxes run past this request: clear the rows beyond it
             const int nz = (TC_C - n) * 16;
@@ -215,7 +560,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (tid < TC_C) {
             float g = 0.f, bt = 0.f;
             if (tid < n) {
-                if (has_decay) g = p.raw_gate ? p.gate_scale[h] * softplus_f(graw + p.gate_bias[h]) : graw;
+                if (has_decay) g = p.raw_gate ? gsc * softplus_f(graw + gbi) : graw;
                 bt = RETR ? (sig ? sigmoid_f(braw) : braw) : 1.f;
             }
             sG[tid] = g;
@@ -276,7 +621,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc::fence_async_smem();
         sync_tc();
 
-        // ---- I1: [K; Q] K^T
+        // ---- I1: [K; Q] K^T (only the Q K^T half is read)
         if (tid == 0) {
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -285,29 +630,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc::commit(bar);
         }
+        if (RETR) {
+            // Ta = Tb diag(e^G) while I1 runs, 16 entries (two 16-byte chunks) per thread
+            const int r = tid >> 2, c2 = 2 * (tid & 3);
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int ch = c2 + w;
+                const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+                uint4 u = *reinterpret_cast<const uint4 *>(sTb + off);
+                __half2 *hp = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(hp[e]);
+                    hp[e] = __floats2half2_rn(f.x * sEG[8 * ch + 2 * e], f.y * sEG[8 * ch + 2 * e + 1]);
+                }
+                *reinterpret_cast<uint4 *>(sTa + off) = u;
+            }
+        }
         ok = wait_mma(bar, phase, p.err);
-        {
+        if (ell >= 64) {
+            // P[r][j] = e^{G_r - G_j} q_r . k_j (j <= r)
             float v[32];
             tc::ld32(tI1 + lane_off + 32 * hc, v);
-            if (ell < 64) {
-                if (RETR) {
-                    const int r = ell;
+            const int r = ell - 64;
+            const float Gr = sG[r];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = 32 * hc + jj;
-                        sAf[j * FA + r] = j < r ? sB[r] * __expf(sG[r] - sG[j]) * v[jj] : 0.f;
-                    }
-                }
-            } else {
-                const int r = ell - 64;
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * hc + jj;
-                    v[jj] = j <= r ? __expf(sG[r] - sG[j]) * v[jj] : 0.f;
-                }
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) st_chunk(sP, r, 4 * hc + cc, v + 8 * cc);
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = 32 * hc + jj;
+                v[jj] = j <= r ? __expf(Gr - sG[j]) * v[jj] : 0.f;
             }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) st_chunk(sP, r, 4 * hc + cc, v + 8 * cc);
         }
         // query rows -> e^{G_r} q_r in place (I1 has consumed the raw rows)
         for (int idx = tid; idx < 64 * 16; idx += TC_THREADS) {
@@ -327,113 +680,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         sync_tc();
 
         if (RETR) {
-            // ---- T = (I + A)^-1 in fp32 by recursive doubling: invert the four
-            // 16x16 diagonal blocks, merge them into two 32x32 inverses, then one
-            // 64x64:  [[T0, 0], [L, T1]]^-1 block with L = -T1 A10 T0.
-            if (warp < 4 && lane < 16) {
-                // column `lane` of the inverse of diagonal block `warp`, right-looking:
-                // once x[j] is final it updates every later row at once
-                float x[16];
-                const float *At = sAf + (16 * warp) * FA + 16 * warp;  // At[j][i] = A[i][j]
-#pragma unroll
-                for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-                for (int j = 0; j < 15; ++j) {
-                    float a[16];
-#pragma unroll
-                    for (int w4 = 0; w4 < 4; ++w4) {
-                        const float4 t = *reinterpret_cast<const float4 *>(At + j * FA + 4 * w4);
-                        a[4 * w4] = t.x, a[4 * w4 + 1] = t.y, a[4 * w4 + 2] = t.z, a[4 * w4 + 3] = t.w;
-                    }
-#pragma unroll
-                    for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-a[i], x[j], x[i]);
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sTf[(16 * warp + i) * FT + 16 * warp + lane] = x[i];
-            } else if (warp >= 4) {
-                // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
-                const int u = tid - 128;  // 0..127, 4 entries each
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int idx = 4 * u + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
-                    sTf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
-                }
-            }
-            __syncthreads();
-            {
-                // level 1: blocks (1,0) and (3,2); 128 threads per block, 2 outputs each
-                const int blk = tid >> 7, u = tid & 127;
-                const int r = u >> 3, c = 2 * (u & 7);  // row 0..15, columns c, c+1
-                const int o0 = 32 * blk;                // T_{b-1,b-1} at (o0, o0), A_{b,b-1} at (o0+16, o0)
-                float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float a = sAf[(o0 + k) * FA + o0 + 16 + r];
-                    y0 += a * sTf[(o0 + k) * FT + o0 + c];
-                    y1 += a * sTf[(o0 + k) * FT + o0 + c + 1];
-                }
-                sY[blk * 16 * 36 + r * 36 + c] = y0;
-                sY[blk * 16 * 36 + r * 36 + c + 1] = y1;
-                __syncthreads();
-                float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float t = sTf[(o0 + 16 + r) * FT + o0 + 16 + k];
-                    l0 += t * sY[blk * 16 * 36 + k * 36 + c];
-                    l1 += t * sY[blk * 16 * 36 + k * 36 + c + 1];
-                }
-                sTf[(o0 + 16 + r) * FT + o0 + c] = -l0;
-                sTf[(o0 + 16 + r) * FT + o0 + c + 1] = -l1;
-            }
-            __syncthreads();
-            {
-                // level 2: L = -T1 (A10 T0), 32x32 blocks; thread = (row, 4 columns)
-                const int r = tid >> 3, c = 4 * (tid & 7);
-                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int k = 0; k < 32; ++k) {
-                    const float a = sAf[k * FA + 32 + r];
-                    const float4 t = *reinterpret_cast<const float4 *>(sTf + k * FT + c);
-                    y.x += a * t.x, y.y += a * t.y, y.z += a * t.z, y.w += a * t.w;
-                }
-                *reinterpret_cast<float4 *>(sY + r * 36 + c) = y;
-                __syncthreads();
-                float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int k = 0; k < 32; ++k) {
-                    const float t = sTf[(32 + r) * FT + 32 + k];
-                    const float4 yy = *reinterpret_cast<const float4 *>(sY + k * 36 + c);
-                    l.x += t * yy.x, l.y += t * yy.y, l.z += t * yy.z, l.w += t * yy.w;
-                }
-                *reinterpret_cast<float4 *>(sTf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
-            }
-            __syncthreads();
-            {
-                const int r = tid >> 2, qq = tid & 3;
-                float ta[16], tb[16];
-#pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                    const int j0 = 16 * qq + 4 * e4;
-                    const float4 t = *reinterpret_cast<const float4 *>(sTf + r * FT + j0);
-                    const float4 bb = *reinterpret_cast<const float4 *>(sB + j0);
-                    const float4 eg = *reinterpret_cast<const float4 *>(sEG + j0);
-                    const float tv[4] = {t.x, t.y, t.z, t.w}, bv[4] = {bb.x, bb.y, bb.z, bb.w};
-                    const float ev[4] = {eg.x, eg.y, eg.z, eg.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float tt = (j0 + e) <= r ? tv[e] : 0.f;
-                        tb[4 * e4 + e] = tt * bv[e];
-                        ta[4 * e4 + e] = tb[4 * e4 + e] * ev[e];
-                    }
-                }
-                st_chunk(sTa, r, 2 * qq, ta);
-                st_chunk(sTa, r, 2 * qq + 1, ta + 8);
-                st_chunk(sTb, r, 2 * qq, tb);
-                st_chunk(sTb, r, 2 * qq + 1, tb + 8);
-            }
-            tc::fence_async_smem();
-            sync_tc();
-
             // ---- I2 (W^T = K^T Ta^T), C1a (V^T Tb^T), C2 (S Qh^T)
             if (tid == 0) {
                 // W = Ta K: M = 64 tokens, N = 128 key channels (K as MN-major B)
@@ -555,7 +801,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         tc::fence_async_smem();
         tc::fence_before();
-        __syncthreads();
+        ok = __syncthreads_and(ok) != 0;
         {
             const int r = tid >> 2, seg = tid & 3;
             if (r < n) {
@@ -580,12 +826,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 bool al16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// workspace: chunk offsets (B + 1 ints, rounded up to 1 KB), then the Tb tiles
+size_t offs_bytes(const Problem &p) { return (((size_t)p.B + 1) * sizeof(int) + 1023) & ~(size_t)1023; }
+// slots for every chunk of pairwise disjoint requests: sum ceil(len / C) <= T / C + B
+int slot_capacity(const Problem &p) { return (int)((long long)p.T / TC_C + p.B + 1); }
+
 }  // namespace
 
 bool chunked_tc_eligible(const Problem &p) {
     const bool rule_ok = p.rule == kLinear || p.rule == kGated || p.rule == kDelta || p.rule == kGatedDelta;
     return rule_ok && p.dk == 128 && p.dv == 128 && p.act_f16 && !((p.flags & kPerKey) && rule_has_decay(p.rule)) &&
            al16(p.q) && al16(p.k) && al16(p.v) && al16(p.fin) && (p.init == nullptr || al16(p.init));
+}
+
+size_t chunked_tc_workspace_bytes(const Problem &p) {
+    if (!rule_has_retrieval(p.rule) || p.B == 0) return 0;
+    return offs_bytes(p) + (size_t)slot_capacity(p) * p.Hv * kTbBytes;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -618,7 +874,20 @@ static bool make_map(CUtensorMap *m, const void *base, int heads, int tokens) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_chunked_tc(const Problem &p, cudaStream_t stream) {
+// Tb tiles: rows of 64 fp16, one 64 x 64 box per (slot, head), 128-byte swizzle.
+static bool make_map_tb(CUtensorMap *m, const void *base, long long rows) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {64 * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream) {
     static int attr_done[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -628,16 +897,32 @@ cudaError_t launch_chunked_tc(const Problem &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunked_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SV_SMEM);
+        if (e != cudaSuccess) return e;
         if (dev < 64) attr_done[dev] = 1;
     }
-    CUtensorMap tk, tq, tv;
+    CUtensorMap tk, tq, tv, tt;
     if (!make_map(&tk, p.k, p.Hq, p.T) || !make_map(&tq, p.q, p.Hq, p.T) || !make_map(&tv, p.v, p.Hv, p.T))
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)((long long)p.B * p.Hv);
-    if (rule_has_retrieval(p.rule))
-        chunked_tc_kernel<true><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv);
-    else
-        chunked_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv);
+    if (grid == 0) return cudaSuccess;
+    if (!rule_has_retrieval(p.rule)) {
+        tt = tk;  // unused without retrieval
+        chunked_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv, tt, nullptr, 0);
+        return cudaGetLastError();
+    }
+    if (ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
+    int *offs = static_cast<int *>(ws);
+    __half *tb = reinterpret_cast<__half *>(static_cast<unsigned char *>(ws) + offs_bytes(p));
+    const int cap = slot_capacity(p);
+    if (!make_map_tb(&tt, tb, (long long)cap * p.Hv * TC_C)) return cudaErrorInvalidValue;
+    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(p, offs);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    chunk_solve_kernel<<<dim3((unsigned)cap, (unsigned)p.Hv), SV_THREADS, SV_SMEM, stream>>>(p, tk, offs, tb, cap);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    chunked_tc_kernel<true><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv, tt, offs, cap);
     return cudaGetLastError();
 }
 

@@ -34,8 +34,11 @@ size_t chunked_workspace_bytes(const Problem &p, int chunk);
 bool chunked_supported(const Problem &p, int chunk, const char **why);
 cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_bytes, cudaStream_t stream);
 
-// tcgen05 chunked kernel (dk = dv = 128, fp16, scalar decay, v1 rules).
+// tcgen05 chunked kernels (dk = dv = 128, fp16, scalar decay, v1 rules).  The
+// delta rules take a workspace of chunked_tc_workspace_bytes() for the
+// per-chunk triangular solves.
 bool chunked_tc_eligible(const Problem &p);
-cudaError_t launch_chunked_tc(const Problem &p, cudaStream_t stream);
+size_t chunked_tc_workspace_bytes(const Problem &p);
+cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace gdn

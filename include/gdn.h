@@ -81,6 +81,8 @@ typedef enum gdn_rule {
 /* Bits OR-ed into *error_word by the device (never reset by the library). */
 #define GDN_DEVERR_BAD_SLOT 0x1 /* a slot id outside [0, num_state_rows): request skipped */
 #define GDN_DEVERR_TIMEOUT 0x2  /* a bounded wait on an asynchronous copy ran out: the CTA gave up */
+#define GDN_DEVERR_OVERLAP 0x4  /* chunked prefill: the requests' chunks outgrew the workspace, which only
+                                   requests sharing tokens can do; the requests past it were skipped */
 
 /*
  * One call of the recurrence over a batch of requests.

@@ -110,6 +110,39 @@ def test_chunked_rejects_unsupported_head_sizes():
     assert N.load().gdn_chunked_prefill_workspace_size(ctypes.byref(p), 64) == ctypes.c_size_t(-1).value
 
 
+def test_chunked_workspace_size():
+    """The tensor-core path of the delta rules asks for a workspace: chunk
+    offsets (B + 1 ints, rounded up to 1 KiB) and one 64 x 64 fp16 tile per
+    (chunk slot, value head), with T / 64 + B + 1 slots.  The rules without
+    retrieval and the other shapes need none."""
+    lib = N.load()
+    size = lambda p: lib.gdn_chunked_prefill_workspace_size(ctypes.byref(p), 64)
+    B, T, hv = 4, 4 * 8192, 16
+    p = _problem(batch=B, total_tokens=T, num_heads_q=16, num_heads_v=hv, head_dim_k=128,
+                 head_dim_v=128)
+    assert size(p) == 1024 + (T // 64 + B + 1) * hv * 64 * 64 * 2
+    p.rule, p.decay = N.RULES["delta"], None
+    assert size(p) == 1024 + (T // 64 + B + 1) * hv * 64 * 64 * 2
+    p.rule, p.beta = N.RULES["linear"], None
+    assert size(p) == 0
+    p.rule, p.decay = N.RULES["gated"], FAKE
+    assert size(p) == 0
+    assert size(_problem()) == 0  # dk = dv = 16 runs without a workspace
+
+
+def test_chunked_rejects_a_small_workspace():
+    p = _problem(batch=1, total_tokens=64, num_heads_q=1, num_heads_v=1, head_dim_k=128,
+                 head_dim_v=128)
+    need = N.load().gdn_chunked_prefill_workspace_size(ctypes.byref(p), 64)
+    assert need > 0
+    st = N.load().gdn_chunked_prefill(ctypes.byref(p), 64, ctypes.c_void_p(FAKE), need - 1, None)
+    assert st == N.GDN_ERR_WORKSPACE
+    st = N.load().gdn_chunked_prefill(ctypes.byref(p), 64, None, need, None)
+    assert st == N.GDN_ERR_WORKSPACE
+    st = N.load().gdn_chunked_prefill(ctypes.byref(p), 64, ctypes.c_void_p(FAKE + 16), need, None)
+    assert st == N.GDN_ERR_WORKSPACE  # not 256-byte aligned
+
+
 def test_gate_rejects():
     lib = N.load()
     a = N.GdnGateArgs()

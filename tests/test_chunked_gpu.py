@@ -140,6 +140,25 @@ def test_chunked_bad_slot_sets_error_word():
     assert np.isnan(o_flat(o, p)[10:]).all()
 
 
+def test_chunked_overlapping_requests_outgrow_the_workspace():
+    """cu_seqlens [0, 640, 0, 640, 0, 640]: requests 0, 2 and 4 each cover all
+    640 tokens (10 chunks), more than the T / 64 + B + 1 = 16 workspace slots
+    that disjoint requests can need.  Request 0 runs; 2 and 4 are skipped
+    with GDN_DEVERR_OVERLAP (0x4), their state rows left unwritten."""
+    p = workloads.make(seed=78, B=5, T=640, cu_seqlens=[0, 640, 0, 640, 0, 640], hq=1, hv=1,
+                       dk=128, dv=128, act="f16", state="random")
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, fin, _ = run(p, path="chunked", error_word=err)
+    assert int(err.item()) & 4
+    ref_o, ref_fin, _ = oracle.run_problem(p, requests=[0])
+    assert rel_err(o_flat(o, p), ref_o) <= TOL
+    fg = fin.double().cpu().numpy()
+    assert rel_err(fg[[0]], ref_fin) <= TOL
+    assert np.isnan(fg[2]).all() and np.isnan(fg[4]).all()
+    for b in (1, 3):  # empty requests pass their state through
+        assert torch.equal(fin[b].cpu(), p["initial_state"][b])
+
+
 def test_chunked_tiny_fp32_workload():
     p = workloads.tiny_gated_delta()
     ref_o, ref_fin, _ = oracle.run_problem(p)
