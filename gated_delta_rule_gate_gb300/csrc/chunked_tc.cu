@@ -824,6 +824,494 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) tc::tmem_dealloc(*tslot, TC_TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined chain kernel: the same per-chunk algebra with the state-free work
+// of chunk c + 1 overlapped with the state chain of chunk c, and the chain
+// reduced to two tensor-core rounds per chunk:
+//
+//   C12: [D^T | O^T]  = S [-W; Qh]^T                  (N = 128, K-major B)
+//   C34: [O^T | S  ] += D^T [P^T | Kt]                 (N = 192, MN-major B)
+//
+// where D^T starts from U^T = V^T Tb^T (computed ahead into its own tensor
+// memory, added in the epilogue), Kt = diag(e^{G_C - G}) K, P^T comes from
+// the product K Q^T, and the fp32 state S lives in tensor memory: the
+// epilogue of C12 scales it by e^{G_C} in place and C34 accumulates
+// X = D^T Kt into it.  The rules without retrieval use Tb = I and W = 0
+// (D = V).
+//
+// Roles (16 warps): warps 0..7 run the state chain (thread = value row
+// 32 (warp % 4) + lane, column half warp / 4); their thread 0 issues the
+// loads and the products C12 / C34 as soon as its role has made them ready.
+// Warps 8..15 prepare the next chunk (gates and their cumulants, L2 norms,
+// Ta = Tb diag(e^G), Kt, then P^T, -W and Qh once the K Q^T / W products are
+// done); their thread 0 issues those products and U.  Each issuing thread
+// commits only its own products.  Roles hand over through mbarriers (bounded
+// waits); each role makes a failed wait uniform before leaving.
+constexpr int PQ_THREADS = 512;
+constexpr int kPrep = 256;    // preparation threads
+constexpr int qKQ = 0;        // 2 x 32 KB: [K; Q] landing tiles (K rows become -W, Q rows Qh)
+constexpr int qV = 65536;     // 2 x 16 KB: V landing tiles (MN-major V^T operand)
+constexpr int qTb = 98304;    // 2 x 8 KB: Tb tiles
+constexpr int qPK = 114688;   // 2 x 24 KB: MN-major blocks [64 j][64]: P^T, Kt (d < 64), Kt (d >= 64)
+constexpr int qTa = 163840;   // 8 KB
+constexpr int qDT = 172032;   // 16 KB: D^T [128 i][64 j]; output staging after C34
+constexpr int qS = 188416;    // 32 KB: fp16 mirror of the state
+constexpr int qSc = 221184;   // 3 x 1 KB: G, e^G, e^{G_C - G} (64 each) per chunk, chunk % 3
+constexpr int qBar = 224256;  // mbarriers, TMEM address
+constexpr int PQ_SMEM = qBar + 256 + 1024;
+// tensor memory columns
+constexpr uint32_t pU = 0, pD = 64, pO = 128, pS = 192, pI1 = 320, pW = 384;
+
+// byte offset of 16-byte chunk `ch` of row `r` in a 128-byte-swizzled block
+__device__ __forceinline__ int sw(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
+
+// scales the eight fp16 values of one 16-byte chunk by f
+__device__ __forceinline__ uint4 scale_chunk(uint4 u, float f) {
+    __half2 *hp = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float2 x = __half22float2(hp[w]);
+        hp[w] = __floats2half2_rn(x.x * f, x.y * f);
+    }
+    return u;
+}
+
+template <bool RETR>
+__global__ void __launch_bounds__(PQ_THREADS, 1)
+    chunked_pipe_kernel(Problem p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmT,
+                        const int *offs, int cap) {
+    extern __shared__ unsigned char smraw[];
+    const uint32_t sb0 = ptx::smem_u32(smraw);
+    unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + qBar);
+    uint64_t *land = bars + 0;    // [2] TMA landed
+    uint64_t *barU = bars + 2;    // U^T = V^T Tb^T done
+    uint64_t *prepB = bars + 4;   // [2] -W, Qh, P^T, Kt ready
+    uint64_t *barPM = bars + 6;   // [2] K Q^T and W done
+    uint64_t *barD = bars + 8;    // C12 done
+    uint64_t *barX = bars + 9;    // [2] C34 done
+    uint64_t *dready = bars + 11; // D^T written (U^T read), S scaled
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + qBar + 128);
+    unsigned char *sS = sm + qS, *sTa = sm + qTa, *sDT = sm + qDT;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x % p.Hv, b = blockIdx.x / p.Hv;
+    const int row = state_row(p, b, h == 0 && tid == 0);
+    if (row < 0) return;
+    int t0, t1;
+    request_range(p, b, t0, t1);
+    const int qh = (int)((long long)h * p.Hq / p.Hv);
+    const int nch = (t1 - t0 + TC_C - 1) / TC_C;
+    int slot0 = 0;
+    if (RETR && nch > 0) {
+        slot0 = offs[b];
+        if (slot0 + nch > cap) {
+            // only overlapping requests can outgrow the workspace: skip this one
+            if (p.err && tid == 0) atomicOr(p.err, 4);
+            return;
+        }
+    }
+    const size_t sbase = ((size_t)row * p.Hv + h) * 128 * 128;
+    if (nch == 0) {  // empty request: copy the incoming state through
+        if (p.fin != p.init) {
+            for (int idx = tid; idx < 128 * 32; idx += PQ_THREADS)
+                reinterpret_cast<float4 *>(p.fin + sbase)[idx] =
+                    p.init ? reinterpret_cast<const float4 *>(p.init + sbase)[idx] : make_float4(0, 0, 0, 0);
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        for (int i = 0; i < 12; ++i) ptx::mbar_init(&bars[i], 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) tc::tmem_alloc(tslot, TC_TMEM_COLS);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tslot;
+// ---- loads and products (each issued by one thread of the role that needs it)
+    const uint32_t aS = ptx::smem_u32(sS), aTa = ptx::smem_u32(sTa), aDT = ptx::smem_u32(sDT);
+    auto tma = [&](int c) {
+        const int bf = c & 1;
+        ptx::mbar_arrive_expect_tx(&land[bf], kLandBytes + (RETR ? (uint32_t)kTbBytes : 0u));
+        unsigned char *kq = sm + qKQ + bf * 32768, *vt = sm + qV + bf * 16384;
+        const int c0 = t0 + TC_C * c;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            ptx::tma_load_3d(kq + kb * 16384, &tmK, 64 * kb, qh, c0, &land[bf]);
+            ptx::tma_load_3d(kq + kb * 16384 + 8192, &tmQ, 64 * kb, qh, c0, &land[bf]);
+            ptx::tma_load_3d(vt + kb * 8192, &tmV, 64 * kb, h, c0, &land[bf]);
+        }
+        if (RETR) ptx::tma_load_2d(sm + qTb + bf * kTbBytes, &tmT, 0, ((slot0 + c) * p.Hv + h) * TC_C, &land[bf]);
+    };
+    // K Q^T (M = 64) and W = Ta K (M = 64, N = 128)
+    auto prep_mma = [&](int c) {
+        const int bf = c & 1;
+        const uint32_t aKQ = ptx::smem_u32(sm + qKQ + bf * 32768);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            tc::mma_f16(tmem + pI1, tc::desc_sw128(aKQ + (s >> 2) * 16384 + (s & 3) * 32),
+                        tc::desc_sw128(aKQ + 8192 + (s >> 2) * 16384 + (s & 3) * 32), tc::idesc_f16(64, 64),
+                        s > 0);
+        if (RETR) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                tc::mma_f16(tmem + pW, tc::desc_sw128(aTa + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
+                            tc::idesc_f16(64, 128, false, true), s > 0);
+        }
+        tc::commit(&barPM[bf]);
+    };
+    // U^T = V^T Tb^T (M = 128, N = 64)
+    auto u_mma = [&](int c) {
+        const int bf = c & 1;
+        const uint32_t aV = ptx::smem_u32(sm + qV + bf * 16384), aTb = ptx::smem_u32(sm + qTb + bf * kTbBytes);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            tc::mma_f16(tmem + pU, tc::desc_sw128(aV + s * 2048, 8192), tc::desc_sw128(aTb + s * 32),
+                        tc::idesc_f16(128, 64, true, false), s > 0);
+        tc::commit(barU);
+    };
+    // C12: [D^T | O^T] = S [-W; Qh]^T once the preparation of chunk c is done
+    auto c12 = [&](int c) -> bool {
+        const int bf = c & 1;
+        if (!ptx::mbar_wait(&prepB[bf], (c >> 1) & 1)) return false;
+        tc::fence_after();
+        const uint32_t aKQ = ptx::smem_u32(sm + qKQ + bf * 32768);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            tc::mma_f16(tmem + pD, tc::desc_sw128(aS + (s >> 2) * 16384 + (s & 3) * 32),
+                        tc::desc_sw128(aKQ + (s >> 2) * 16384 + (s & 3) * 32), tc::idesc_f16(128, 128), s > 0);
+        tc::commit(barD);
+        return true;
+    };
+    // C34: [O^T | S] += D^T [P^T | Kt]   (B MN-major: three 64-wide blocks)
+    auto c34 = [&](int c) {
+        const int bf = c & 1;
+        const uint32_t aPK = ptx::smem_u32(sm + qPK + bf * 24576);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            tc::mma_f16(tmem + pO, tc::desc_sw128(aDT + s * 32), tc::desc_sw128(aPK + s * 2048, 8192),
+                        tc::idesc_f16(128, 192, false, true), true);
+        tc::commit(&barX[bf]);
+    };
+
+    if (warp < 8) {
+        // ===================== state chain (256 threads)
+        const int q4 = warp & 3, hc = warp >> 2, i = 32 * q4 + lane, ct = tid;
+        const uint32_t lo = tmem + ((uint32_t)(32 * q4) << 16);
+        const size_t srow = sbase + (size_t)i * 128 + 64 * hc;
+        {
+            float v[32];
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 f = p.init ? *reinterpret_cast<const float4 *>(p.init + srow + 32 * pc + 4 * j)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[4 * j] = f.x, v[4 * j + 1] = f.y, v[4 * j + 2] = f.z, v[4 * j + 3] = f.w;
+                }
+                tc::st32(lo + pS + 64 * hc + 32 * pc, v);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * 16384, i, 4 * pc + cc, v + 8 * cc);
+            }
+            tc::wait_st();
+        }
+        tc::fence_async_smem();
+        tc::fence_before();
+        ptx::named_bar_sync(1, 256);
+        bool ok = true;
+        if (ct == 0) {
+            tc::fence_after();
+            tma(0);
+            if (nch > 1) tma(1);
+            ok = c12(0);
+        }
+        for (int c = 0; c < nch; ++c) {
+            const int bf = c & 1;
+            const float *scal = reinterpret_cast<const float *>(sm + qSc + (c % 3) * 1024);
+            const int n = min(TC_C, t1 - (t0 + TC_C * c));
+            // ---- C12 and U done: D^T = U^T + (-S W^T) -> fp16 operand; S *= e^{G_C}
+            ok = ptx::named_bar_and(1, 256, ok && ptx::mbar_wait(barD, c & 1) && ptx::mbar_wait(barU, c & 1));
+            if (!ok) break;
+            tc::fence_after();
+            {
+                float u[32], d[32];
+                tc::ld32(lo + pU + 32 * hc, u);
+                tc::ld32(lo + pD + 32 * hc, d);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) u[jj] += d[jj];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) st_chunk(sDT, i, 4 * hc + cc, u + 8 * cc);
+                const float eC = scal[64 + TC_C - 1];
+#pragma unroll
+                for (int pc = 0; pc < 2; ++pc) {
+                    tc::ld32(lo + pS + 64 * hc + 32 * pc, d);
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) d[jj] *= eC;
+                    tc::st32(lo + pS + 64 * hc + 32 * pc, d);
+                }
+                tc::wait_st();
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(1, 256);
+            if (ct == 0) {
+                ptx::mbar_arrive(dready);
+                tc::fence_after();
+                c34(c);
+                // chunk c's landing buffer is free: C12, U and the preparation have run
+                if (c + 2 < nch) tma(c + 2);
+            }
+            // ---- C34 done: mirror the state, read O^T, start C12 of the next chunk
+            ok = ptx::named_bar_and(1, 256, ptx::mbar_wait(&barX[bf], (c >> 1) & 1));
+            if (!ok) break;
+            tc::fence_after();
+            float o[32];
+            {
+                float v[32];
+#pragma unroll
+                for (int pc = 0; pc < 2; ++pc) {
+                    tc::ld32(lo + pS + 64 * hc + 32 * pc, v);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * 16384, i, 4 * pc + cc, v + 8 * cc);
+                }
+                tc::ld32(lo + pO + 32 * hc, o);
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(1, 256);
+            if (ct == 0 && c + 1 < nch) ok = c12(c + 1);
+            // ---- outputs of chunk c: O^T[i][r] -> staging O[r][i] -> 16-byte row stores
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+                reinterpret_cast<__half *>(sDT)[(32 * hc + jj) * 128 + i] = __float2half_rn(p.scale * o[jj]);
+            ptx::named_bar_sync(1, 256);
+            {
+                const int r = ct >> 2, seg = ct & 3;
+                if (r < n) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(sDT + r * 256 + seg * 64);
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.o) +
+                                                           ((size_t)(t0 + TC_C * c + r) * p.Hv + h) * 128 + seg * 32);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) dst[w] = src[w];
+                }
+            }
+        }
+        if (!ok && p.err && ct == 0) atomicOr(p.err, 2);
+        if (ok) {
+            float v[32];
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+                tc::ld32(lo + pS + 64 * hc + 32 * pc, v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4 *>(p.fin + srow + 32 * pc + 4 * j) =
+                        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+        }
+    } else if (warp < 16) {
+        // ===================== next-chunk preparation (256 threads)
+        const int pt = tid - 256, pw = warp - 8, pq = pw & 3, ph = pw >> 2;
+        const uint32_t lo = tmem + ((uint32_t)(32 * pq) << 16);
+        const bool has_decay = rule_has_decay(p.rule);
+        const float gsc = (has_decay && p.raw_gate) ? p.gate_scale[h] : 0.f;
+        const float gbi = (has_decay && p.raw_gate) ? p.gate_bias[h] : 0.f;
+        float graw = 0.f;
+        if (has_decay && pt < TC_C && pt < t1 - t0) graw = ld_any(p.decay, (size_t)(t0 + pt) * p.Hv + h, p.decay_f16);
+        bool ok = true;
+        for (int c = 0; c < nch; ++c) {
+            const int bf = c & 1;
+            const int c0 = t0 + TC_C * c, n = min(TC_C, t1 - c0);
+            unsigned char *sKQ = sm + qKQ + bf * 32768, *sV = sm + qV + bf * 16384;
+            unsigned char *sTb = sm + qTb + bf * kTbBytes, *sPK = sm + qPK + bf * 24576;
+            float *sG = reinterpret_cast<float *>(sm + qSc + (c % 3) * 1024);
+            float *sEG = sG + 64, *sEGC = sG + 128;
+            // gates of chunk c (raw values were loaded one chunk ahead)
+            if (pt < TC_C) {
+                float g = 0.f;
+                if (has_decay && pt < n) g = p.raw_gate ? gsc * softplus_f(graw + gbi) : graw;
+                sG[pt] = g;
+                graw = 0.f;
+                if (has_decay && c0 + TC_C + pt < t1)
+                    graw = ld_any(p.decay, (size_t)(c0 + TC_C + pt) * p.Hv + h, p.decay_f16);
+            }
+            ptx::named_bar_sync(2, kPrep);
+            if (pw == 0) {
+                const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
+                float s = g0 + g1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, s, o);
+                    if (lane >= o) s += y;
+                }
+                const float G1 = s, G0 = s - g1, GC = __shfl_sync(0xffffffffu, s, 31);
+                sG[2 * lane] = G0, sG[2 * lane + 1] = G1;
+                sEG[2 * lane] = __expf(G0), sEG[2 * lane + 1] = __expf(G1);
+                sEGC[2 * lane] = __expf(GC - G0), sEGC[2 * lane + 1] = __expf(GC - G1);
+            }
+            ok = ptx::named_bar_and(2, kPrep, ptx::mbar_wait(&land[bf], (c >> 1) & 1));
+            if (!ok) break;
+            if (n < TC_C) {  // the boxes run past this request: clear the rows beyond it
+                const int nz = (TC_C - n) * 16;
+                for (int idx = pt; idx < 3 * nz; idx += kPrep) {
+                    const int which = idx / nz, rem = idx % nz, r = n + (rem >> 4), ch = rem & 15;
+                    unsigned char *base = which == 2 ? sV + (ch >> 3) * 8192
+                                                     : sKQ + (ch >> 3) * 16384 + (which == 1 ? 8192 : 0);
+                    *reinterpret_cast<uint4 *>(base + sw(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            if (!RETR) {
+                // Tb = I: U^T = V^T
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int idx = 2 * pt + w, r = idx >> 3, ch = idx & 7;
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = (8 * ch + e == r) ? 1.f : 0.f;
+                    st_chunk(sTb, r, ch, x);
+                }
+            }
+            ptx::named_bar_sync(2, kPrep);
+            {
+                // L2 norms: four threads per row, four chunks each (key rows, then query rows)
+                const int r = pt >> 2, part = pt & 3;
+#pragma unroll
+                for (int qk = 0; qk < 2; ++qk) {
+                    if (qk == 0 ? (p.flags & kL2k) == 0 : (p.flags & kL2q) == 0) continue;
+                    const int rr = r + 64 * qk;
+                    uint4 u[4];
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int ch = 4 * part + w;
+                        u[w] = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(rr, ch & 7));
+                        const __half2 *hp = reinterpret_cast<const __half2 *>(&u[w]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(hp[e]);
+                            s0 = fmaf(f.x, f.x, s0);
+                            s1 = fmaf(f.y, f.y, s1);
+                        }
+                    }
+                    float ss = s0 + s1;
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                    const float inv = rsqrtf(ss + 1e-12f);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const int ch = 4 * part + w;
+                        *reinterpret_cast<uint4 *>(sKQ + (ch >> 3) * 16384 + sw(rr, ch & 7)) = scale_chunk(u[w], inv);
+                    }
+                }
+                if (RETR) {
+                    // Ta = Tb diag(e^G)
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int idx = 2 * pt + w, tr = idx >> 3, ch = idx & 7;
+                        uint4 u = *reinterpret_cast<const uint4 *>(sTb + sw(tr, ch));
+                        __half2 *hp = reinterpret_cast<__half2 *>(&u);
+                        const float4 e0 = *reinterpret_cast<const float4 *>(sEG + 8 * ch);
+                        const float4 e1 = *reinterpret_cast<const float4 *>(sEG + 8 * ch + 4);
+                        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __half22float2(hp[e]);
+                            hp[e] = __floats2half2_rn(f.x * ev[2 * e], f.y * ev[2 * e + 1]);
+                        }
+                        *reinterpret_cast<uint4 *>(sTa + sw(tr, ch)) = u;
+                    }
+                }
+            }
+            // PK[bf] was last read by C34 of chunk c - 2
+            bool okx = true;
+            if (c >= 2) okx = ptx::mbar_wait(&barX[bf], ((c - 2) >> 1) & 1);
+            ok = ptx::named_bar_and(2, kPrep, okx);  // also: the norms are done
+            if (!ok) break;
+            // Kt[j][d] = e^{G_C - G_j} k_j[d]: PK blocks 1 and 2, same rows as the key tile
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int idx = pt + kPrep * w, j = idx >> 4, ch = idx & 15;
+                const uint4 u = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(j, ch & 7));
+                *reinterpret_cast<uint4 *>(sPK + 8192 + (ch >> 3) * 8192 + sw(j, ch & 7)) = scale_chunk(u, sEGC[j]);
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(2, kPrep);
+            bool oki = true;
+            if (pt == 0) {
+                tc::fence_after();
+                prep_mma(c);
+                // U of the previous chunk has been read once its D^T epilogue is done
+                if (c > 0) oki = ptx::mbar_wait(dready, (c - 1) & 1);
+                if (oki) {
+                    tc::fence_after();
+                    u_mma(c);
+                }
+            }
+            // ---- K Q^T and W = Ta K done
+            ok = ptx::named_bar_and(2, kPrep, oki && ptx::mbar_wait(&barPM[bf], (c >> 1) & 1));
+            if (!ok) break;
+            tc::fence_after();
+            {
+                // M = 64 results: row 16 pq + lane (lane < 16) sits on lane 32 pq + lane
+                const int rj = 16 * pq + lane;
+                float v[32];
+                // P^T[j][r] = e^{G_r - G_j} k_j . q_r for r >= j; columns [32 ph, 32 ph + 32)
+                tc::ld32(lo + pI1 + 32 * ph, v);
+                if (lane < 16) {
+                    const float Gj = sG[rj];
+                    float gr[32];
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(sG + 32 * ph + 4 * e4);
+                        gr[4 * e4] = g4.x, gr[4 * e4 + 1] = g4.y, gr[4 * e4 + 2] = g4.z, gr[4 * e4 + 3] = g4.w;
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int r = 32 * ph + jj;
+                        v[jj] = r >= rj ? __expf(gr[jj] - Gj) * v[jj] : 0.f;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(sPK, rj, 4 * ph + cc, v + 8 * cc);
+                }
+                if (RETR) {
+                    // -W rows over the key rows: columns [64 ph, 64 ph + 64)
+#pragma unroll
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        tc::ld32(lo + pW + 64 * ph + 32 * k2, v);
+                        if (lane < 16) {
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) v[jj] = -v[jj];
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc) st_chunk(sKQ + ph * 16384, rj, 4 * k2 + cc, v + 8 * cc);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int idx = pt + kPrep * w, r = idx >> 4, ch = idx & 15;
+                if (!RETR)  // W = 0: clear the key rows
+                    *reinterpret_cast<uint4 *>(sKQ + (ch >> 3) * 16384 + sw(r, ch & 7)) = make_uint4(0, 0, 0, 0);
+                // query rows -> e^{G_r} q_r in place (K Q^T has read the raw rows)
+                uint4 *ptr = reinterpret_cast<uint4 *>(sKQ + (ch >> 3) * 16384 + sw(64 + r, ch & 7));
+                *ptr = scale_chunk(*ptr, sEG[r]);
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(2, kPrep);
+            if (pt == 0) ptx::mbar_arrive(&prepB[bf]);
+        }
+        if (!ok && p.err && pt == 0) atomicOr(p.err, 2);
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 0) tc::tmem_dealloc(tmem, TC_TMEM_COLS);
+}
+
 bool al16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 // workspace: chunk offsets (B + 1 ints, rounded up to 1 KB), then the Tb tiles
@@ -899,6 +1387,10 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SV_SMEM);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunked_pipe_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PQ_SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunked_pipe_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PQ_SMEM);
+        if (e != cudaSuccess) return e;
         if (dev < 64) attr_done[dev] = 1;
     }
     CUtensorMap tk, tq, tv, tt;
@@ -908,7 +1400,7 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     if (grid == 0) return cudaSuccess;
     if (!rule_has_retrieval(p.rule)) {
         tt = tk;  // unused without retrieval
-        chunked_tc_kernel<false><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv, tt, nullptr, 0);
+        chunked_pipe_kernel<false><<<grid, PQ_THREADS, PQ_SMEM, stream>>>(p, tk, tq, tv, tt, nullptr, 0);
         return cudaGetLastError();
     }
     if (ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
@@ -922,7 +1414,7 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     chunk_solve_kernel<<<dim3((unsigned)cap, (unsigned)p.Hv), SV_THREADS, SV_SMEM, stream>>>(p, tk, offs, tb, cap);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunked_tc_kernel<true><<<grid, TC_THREADS, TC_SMEM, stream>>>(p, tk, tq, tv, tt, offs, cap);
+    chunked_pipe_kernel<true><<<grid, PQ_THREADS, PQ_SMEM, stream>>>(p, tk, tq, tv, tt, offs, cap);
     return cudaGetLastError();
 }
 
