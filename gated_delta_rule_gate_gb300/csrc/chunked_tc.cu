@@ -841,12 +841,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 //
 // Roles (16 warps): warps 0..7 run the state chain (thread = value row
 // 32 (warp % 4) + lane, column half warp / 4); their thread 0 issues the
-// loads and the products C12 / C34 as soon as its role has made them ready.
-// Warps 8..15 prepare the next chunk (gates and their cumulants, L2 norms,
-// Ta = Tb diag(e^G), Kt, then P^T, -W and Qh once the K Q^T / W products are
-// done); their thread 0 issues those products and U.  Each issuing thread
-// commits only its own products.  Roles hand over through mbarriers (bounded
-// waits); each role makes a failed wait uniform before leaving.
+// loads, U, C12 and C34.  Warps 8..15 prepare the next chunk: gates and their
+// cumulants, L2 norms with the decay-scaled copy Kt, Ta = Tb diag(e^G); their
+// thread 0 then issues K Q^T and W (and signals that U's operands are ready),
+// and P^T, -W and Qh follow once those products are done ("chunk ready").
+// Each issuing thread commits only its own products.  Roles hand over through
+// mbarriers (bounded waits); each role makes a failed wait uniform before
+// leaving.
 constexpr int PQ_THREADS = 512;
 constexpr int kPrep = 256;    // preparation threads
 constexpr int qKQ = 0;        // 2 x 32 KB: [K; Q] landing tiles (K rows become -W, Q rows Qh)
@@ -856,22 +857,55 @@ constexpr int qPK = 114688;   // 2 x 24 KB: MN-major blocks [64 j][64]: P^T, Kt 
 constexpr int qTa = 163840;   // 8 KB
 constexpr int qDT = 172032;   // 16 KB: D^T [128 i][64 j]; output staging after C34
 constexpr int qS = 188416;    // 32 KB: fp16 mirror of the state
-constexpr int qSc = 221184;   // 3 x 1 KB: G, e^G, e^{G_C - G} (64 each) per chunk, chunk % 3
-constexpr int qBar = 224256;  // mbarriers, TMEM address
+constexpr int qSc = 221184;   // 3 slots (chunk % 3) of per-token factors, 7 x 64 fp32 each
+constexpr int kScal = 7 * 64 * 4;
+constexpr int qBar = qSc + 3 * kScal;  // mbarriers, TMEM address
 constexpr int PQ_SMEM = qBar + 256 + 1024;
 // tensor memory columns
 constexpr uint32_t pU = 0, pD = 64, pO = 128, pS = 192, pI1 = 320, pW = 384;
+// per-token factors of one chunk (offsets in floats): G (cumulative log decay), e^G,
+// KF = e^{G_C - G} / |k| (rows of Kt), TF = -e^G / |k| (columns of Ta), QF = scale e^G / |q|
+// (rows of Qh), QS = scale / |q| (columns of P^T), IK = 1 / |k| (rows of P^T)
+constexpr int fG = 0, fEG = 64, fKF = 128, fTF = 192, fQF = 256, fQS = 320, fIK = 384;
 
 // byte offset of 16-byte chunk `ch` of row `r` in a 128-byte-swizzled block
 __device__ __forceinline__ int sw(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
 
-// scales the eight fp16 values of one 16-byte chunk by f
+// Scales the eight fp16 values of one 16-byte chunk by f: fp16 products while
+// the factor is well inside the fp16 range, fp32 products beyond it (the
+// factor 1 / |x| of an all-zero padding row is 1e6: 0 x 1e6 must stay 0).
+constexpr float kHalfSafe = 8192.f;
 __device__ __forceinline__ uint4 scale_chunk(uint4 u, float f) {
+    __half2 *hp = reinterpret_cast<__half2 *>(&u);
+    if (fabsf(f) <= kHalfSafe) {
+        const __half2 f2 = __float2half2_rn(f);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) hp[w] = __hmul2(hp[w], f2);
+    } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float2 x = __half22float2(hp[w]);
+            hp[w] = __floats2half2_rn(x.x * f, x.y * f);
+        }
+    }
+    return u;
+}
+// scales the eight fp16 values of one chunk by eight factors (same rule)
+__device__ __forceinline__ uint4 scale_chunk8(uint4 u, const float *f) {
+    const float4 a = *reinterpret_cast<const float4 *>(f), b = *reinterpret_cast<const float4 *>(f + 4);
+    const float fv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(fv[e]));
     __half2 *hp = reinterpret_cast<__half2 *>(&u);
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        const float2 x = __half22float2(hp[w]);
-        hp[w] = __floats2half2_rn(x.x * f, x.y * f);
+        if (m <= kHalfSafe) {
+            hp[w] = __hmul2(hp[w], __floats2half2_rn(fv[2 * w], fv[2 * w + 1]));
+        } else {
+            const float2 x = __half22float2(hp[w]);
+            hp[w] = __floats2half2_rn(x.x * fv[2 * w], x.y * fv[2 * w + 1]);
+        }
     }
     return u;
 }
@@ -887,11 +921,11 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + qBar);
     uint64_t *land = bars + 0;    // [2] TMA landed
     uint64_t *barU = bars + 2;    // U^T = V^T Tb^T done
+    uint64_t *prepA = bars + 3;   // operands of K Q^T, W and U ready (one phase per chunk)
     uint64_t *prepB = bars + 4;   // [2] -W, Qh, P^T, Kt ready
     uint64_t *barPM = bars + 6;   // [2] K Q^T and W done
     uint64_t *barD = bars + 8;    // C12 done
     uint64_t *barX = bars + 9;    // [2] C34 done
-    uint64_t *dready = bars + 11; // D^T written (U^T read), S scaled
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + qBar + 128);
     unsigned char *sS = sm + qS, *sTa = sm + qTa, *sDT = sm + qDT;
 
@@ -923,7 +957,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     }
 
     if (tid == 0) {
-        for (int i = 0; i < 12; ++i) ptx::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 11; ++i) ptx::mbar_init(&bars[i], 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(tslot, TC_TMEM_COLS);
@@ -973,10 +1007,18 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                         tc::idesc_f16(128, 64, true, false), s > 0);
         tc::commit(barU);
     };
+    // U of chunk c once its V and Tb tiles are ready (U's tensor memory was read by
+    // the D^T epilogue of chunk c - 1 before this is called)
+    auto u_product = [&](int c) -> bool {
+        if (!ptx::mbar_wait_sleep(prepA, c & 1)) return false;
+        tc::fence_after();
+        u_mma(c);
+        return true;
+    };
     // C12: [D^T | O^T] = S [-W; Qh]^T once the preparation of chunk c is done
     auto c12 = [&](int c) -> bool {
         const int bf = c & 1;
-        if (!ptx::mbar_wait(&prepB[bf], (c >> 1) & 1)) return false;
+        if (!ptx::mbar_wait_sleep(&prepB[bf], (c >> 1) & 1)) return false;
         tc::fence_after();
         const uint32_t aKQ = ptx::smem_u32(sm + qKQ + bf * 32768);
 #pragma unroll
@@ -1026,14 +1068,14 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
             tc::fence_after();
             tma(0);
             if (nch > 1) tma(1);
-            ok = c12(0);
+            ok = u_product(0) && c12(0);
         }
         for (int c = 0; c < nch; ++c) {
             const int bf = c & 1;
-            const float *scal = reinterpret_cast<const float *>(sm + qSc + (c % 3) * 1024);
+            const float *scal = reinterpret_cast<const float *>(sm + qSc + (c % 3) * kScal);
             const int n = min(TC_C, t1 - (t0 + TC_C * c));
             // ---- C12 and U done: D^T = U^T + (-S W^T) -> fp16 operand; S *= e^{G_C}
-            ok = ptx::named_bar_and(1, 256, ok && ptx::mbar_wait(barD, c & 1) && ptx::mbar_wait(barU, c & 1));
+            ok = ptx::named_bar_and(1, 256, ok && ptx::mbar_wait_sleep(barD, c & 1) && ptx::mbar_wait_sleep(barU, c & 1));
             if (!ok) break;
             tc::fence_after();
             {
@@ -1044,7 +1086,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                 for (int jj = 0; jj < 32; ++jj) u[jj] += d[jj];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) st_chunk(sDT, i, 4 * hc + cc, u + 8 * cc);
-                const float eC = scal[64 + TC_C - 1];
+                const float eC = scal[fEG + TC_C - 1];
 #pragma unroll
                 for (int pc = 0; pc < 2; ++pc) {
                     tc::ld32(lo + pS + 64 * hc + 32 * pc, d);
@@ -1058,14 +1100,14 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
             tc::fence_before();
             ptx::named_bar_sync(1, 256);
             if (ct == 0) {
-                ptx::mbar_arrive(dready);
                 tc::fence_after();
                 c34(c);
                 // chunk c's landing buffer is free: C12, U and the preparation have run
                 if (c + 2 < nch) tma(c + 2);
+                if (c + 1 < nch) ok = u_product(c + 1);
             }
             // ---- C34 done: mirror the state, read O^T, start C12 of the next chunk
-            ok = ptx::named_bar_and(1, 256, ptx::mbar_wait(&barX[bf], (c >> 1) & 1));
+            ok = ptx::named_bar_and(1, 256, ok && ptx::mbar_wait_sleep(&barX[bf], (c >> 1) & 1));
             if (!ok) break;
             tc::fence_after();
             float o[32];
@@ -1086,7 +1128,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
             // ---- outputs of chunk c: O^T[i][r] -> staging O[r][i] -> 16-byte row stores
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj)
-                reinterpret_cast<__half *>(sDT)[(32 * hc + jj) * 128 + i] = __float2half_rn(p.scale * o[jj]);
+                reinterpret_cast<__half *>(sDT)[(32 * hc + jj) * 128 + i] = __float2half_rn(o[jj]);
             ptx::named_bar_sync(1, 256);
             {
                 const int r = ct >> 2, seg = ct & 3;
@@ -1113,45 +1155,70 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
         }
     } else if (warp < 16) {
         // ===================== next-chunk preparation (256 threads)
+        // The key and query tiles stay as loaded; the L2 norms, decays and the output
+        // scale enter through per-token factors: Kt rows, Ta columns (which also carry
+        // the sign of -W), Qh rows and the rows / columns of P^T.
         const int pt = tid - 256, pw = warp - 8, pq = pw & 3, ph = pw >> 2;
         const uint32_t lo = tmem + ((uint32_t)(32 * pq) << 16);
         const bool has_decay = rule_has_decay(p.rule);
+        const bool nk = (p.flags & kL2k) != 0, nq = (p.flags & kL2q) != 0;
         const float gsc = (has_decay && p.raw_gate) ? p.gate_scale[h] : 0.f;
         const float gbi = (has_decay && p.raw_gate) ? p.gate_bias[h] : 0.f;
-        float graw = 0.f;
-        if (has_decay && pt < TC_C && pt < t1 - t0) graw = ld_any(p.decay, (size_t)(t0 + pt) * p.Hv + h, p.decay_f16);
+        if (!RETR) {
+            // Tb = I (U^T = V^T), in both buffers, once
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int idx = pt + kPrep * w, bf = idx >> 9, r = (idx >> 3) & 63, ch = idx & 7;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = (8 * ch + e == r) ? 1.f : 0.f;
+                st_chunk(sm + qTb + bf * kTbBytes, r, ch, x);
+            }
+        }
+        // raw gate bits of the next chunk, converted only when used (the load is not waited on early)
+        uint32_t graw = 0u;
+        auto gload = [&](int t) -> uint32_t {
+            const size_t th = (size_t)t * p.Hv + h;
+            return p.decay_f16 ? (uint32_t) reinterpret_cast<const unsigned short *>(p.decay)[th]
+                               : reinterpret_cast<const uint32_t *>(p.decay)[th];
+        };
+        if (has_decay && pt < TC_C && pt < t1 - t0) graw = gload(t0 + pt);
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
             const int bf = c & 1;
             const int c0 = t0 + TC_C * c, n = min(TC_C, t1 - c0);
             unsigned char *sKQ = sm + qKQ + bf * 32768, *sV = sm + qV + bf * 16384;
             unsigned char *sTb = sm + qTb + bf * kTbBytes, *sPK = sm + qPK + bf * 24576;
-            float *sG = reinterpret_cast<float *>(sm + qSc + (c % 3) * 1024);
-            float *sEG = sG + 64, *sEGC = sG + 128;
+            float *F = reinterpret_cast<float *>(sm + qSc + (c % 3) * kScal);
             // gates of chunk c (raw values were loaded one chunk ahead)
             if (pt < TC_C) {
                 float g = 0.f;
-                if (has_decay && pt < n) g = p.raw_gate ? gsc * softplus_f(graw + gbi) : graw;
-                sG[pt] = g;
-                graw = 0.f;
-                if (has_decay && c0 + TC_C + pt < t1)
-                    graw = ld_any(p.decay, (size_t)(c0 + TC_C + pt) * p.Hv + h, p.decay_f16);
+                if (has_decay && pt < n) {
+                    const float a = p.decay_f16 ? __half2float(__ushort_as_half((unsigned short)graw))
+                                                : __uint_as_float(graw);
+                    g = p.raw_gate ? gsc * softplus_f(a + gbi) : a;
+                }
+                F[fG + pt] = g;
+                graw = 0u;
+                if (has_decay && c0 + TC_C + pt < t1) graw = gload(c0 + TC_C + pt);
             }
             ptx::named_bar_sync(2, kPrep);
             if (pw == 0) {
-                const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
-                float s = g0 + g1;
+                const float g0 = F[fG + 2 * lane], g1 = F[fG + 2 * lane + 1];
+                float sacc = g0 + g1;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, s, o);
-                    if (lane >= o) s += y;
+                    const float y = __shfl_up_sync(0xffffffffu, sacc, o);
+                    if (lane >= o) sacc += y;
                 }
-                const float G1 = s, G0 = s - g1, GC = __shfl_sync(0xffffffffu, s, 31);
-                sG[2 * lane] = G0, sG[2 * lane + 1] = G1;
-                sEG[2 * lane] = __expf(G0), sEG[2 * lane + 1] = __expf(G1);
-                sEGC[2 * lane] = __expf(GC - G0), sEGC[2 * lane + 1] = __expf(GC - G1);
+                const float G1 = sacc, G0 = sacc - g1;
+                F[fG + 2 * lane] = G0, F[fG + 2 * lane + 1] = G1;
+                F[fEG + 2 * lane] = __expf(G0), F[fEG + 2 * lane + 1] = __expf(G1);
             }
-            ok = ptx::named_bar_and(2, kPrep, ptx::mbar_wait(&land[bf], (c >> 1) & 1));
+            // PK[bf] was last read by C34 of chunk c - 2
+            bool okw = ptx::mbar_wait_sleep(&land[bf], (c >> 1) & 1);
+            if (c >= 2) okw = okw && ptx::mbar_wait_sleep(&barX[bf], ((c - 2) >> 1) & 1);
+            ok = ptx::named_bar_and(2, kPrep, okw);
             if (!ok) break;
             if (n < TC_C) {  // the boxes run past this request: clear the rows beyond it
                 const int nz = (TC_C - n) * 16;
@@ -1161,33 +1228,50 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                                                      : sKQ + (ch >> 3) * 16384 + (which == 1 ? 8192 : 0);
                     *reinterpret_cast<uint4 *>(base + sw(r, ch & 7)) = make_uint4(0, 0, 0, 0);
                 }
+                ptx::named_bar_sync(2, kPrep);
             }
-            if (!RETR) {
-                // Tb = I: U^T = V^T
-#pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int idx = 2 * pt + w, r = idx >> 3, ch = idx & 7;
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = (8 * ch + e == r) ? 1.f : 0.f;
-                    st_chunk(sTb, r, ch, x);
-                }
-            }
-            ptx::named_bar_sync(2, kPrep);
             {
-                // L2 norms: four threads per row, four chunks each (key rows, then query rows)
+                // four threads per row, four chunks each
                 const int r = pt >> 2, part = pt & 3;
+                const float eGC = __expf(F[fG + TC_C - 1] - F[fG + r]);  // e^{G_C - G_r} (<= 1)
+                // key rows: 1 / |k_r|, and Kt = e^{G_C - G_r} k_r / |k_r| into PK blocks 1 and 2
+                uint4 u[4];
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int qk = 0; qk < 2; ++qk) {
-                    if (qk == 0 ? (p.flags & kL2k) == 0 : (p.flags & kL2q) == 0) continue;
-                    const int rr = r + 64 * qk;
-                    uint4 u[4];
-                    float s0 = 0.f, s1 = 0.f;
+                for (int w = 0; w < 4; ++w) {
+                    const int ch = 4 * part + w;
+                    u[w] = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(r, ch & 7));
+                    const __half2 *hp = reinterpret_cast<const __half2 *>(&u[w]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(hp[e]);
+                        s0 = fmaf(f.x, f.x, s0);
+                        s1 = fmaf(f.y, f.y, s1);
+                    }
+                }
+                float ss = s0 + s1;
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                const float ik = nk ? rsqrtf(ss + 1e-12f) : 1.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int ch = 4 * part + w;
+                    *reinterpret_cast<uint4 *>(sPK + 8192 + (ch >> 3) * 8192 + sw(r, ch & 7)) =
+                        scale_chunk(u[w], eGC * ik);
+                }
+                if (part == 0) {
+                    F[fIK + r] = ik;
+                    F[fTF + r] = -F[fEG + r] * ik;
+                }
+                // query rows: 1 / |q_r| (when asked for)
+                float iq = 1.f;
+                if (nq) {
+                    s0 = s1 = 0.f;
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         const int ch = 4 * part + w;
-                        u[w] = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(rr, ch & 7));
-                        const __half2 *hp = reinterpret_cast<const __half2 *>(&u[w]);
+                        const uint4 uq = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(64 + r, ch & 7));
+                        const __half2 *hp = reinterpret_cast<const __half2 *>(&uq);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = __half22float2(hp[e]);
@@ -1195,98 +1279,72 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                             s1 = fmaf(f.y, f.y, s1);
                         }
                     }
-                    float ss = s0 + s1;
+                    ss = s0 + s1;
                     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                    const float inv = rsqrtf(ss + 1e-12f);
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int ch = 4 * part + w;
-                        *reinterpret_cast<uint4 *>(sKQ + (ch >> 3) * 16384 + sw(rr, ch & 7)) = scale_chunk(u[w], inv);
-                    }
+                    iq = rsqrtf(ss + 1e-12f);
                 }
-                if (RETR) {
-                    // Ta = Tb diag(e^G)
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int idx = 2 * pt + w, tr = idx >> 3, ch = idx & 7;
-                        uint4 u = *reinterpret_cast<const uint4 *>(sTb + sw(tr, ch));
-                        __half2 *hp = reinterpret_cast<__half2 *>(&u);
-                        const float4 e0 = *reinterpret_cast<const float4 *>(sEG + 8 * ch);
-                        const float4 e1 = *reinterpret_cast<const float4 *>(sEG + 8 * ch + 4);
-                        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __half22float2(hp[e]);
-                            hp[e] = __floats2half2_rn(f.x * ev[2 * e], f.y * ev[2 * e + 1]);
-                        }
-                        *reinterpret_cast<uint4 *>(sTa + sw(tr, ch)) = u;
-                    }
+                if (part == 0) {
+                    F[fQF + r] = p.scale * F[fEG + r] * iq;
+                    F[fQS + r] = p.scale * iq;
                 }
             }
-            // PK[bf] was last read by C34 of chunk c - 2
-            bool okx = true;
-            if (c >= 2) okx = ptx::mbar_wait(&barX[bf], ((c - 2) >> 1) & 1);
-            ok = ptx::named_bar_and(2, kPrep, okx);  // also: the norms are done
-            if (!ok) break;
-            // Kt[j][d] = e^{G_C - G_j} k_j[d]: PK blocks 1 and 2, same rows as the key tile
+            ptx::named_bar_sync(2, kPrep);
+            if (RETR) {
+                // Ta = -Tb diag(e^G / |k|): W = Ta K comes out as -W (the K rows stay unnormalised)
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int idx = pt + kPrep * w, j = idx >> 4, ch = idx & 15;
-                const uint4 u = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(j, ch & 7));
-                *reinterpret_cast<uint4 *>(sPK + 8192 + (ch >> 3) * 8192 + sw(j, ch & 7)) = scale_chunk(u, sEGC[j]);
+                for (int w = 0; w < 2; ++w) {
+                    const int idx = 2 * pt + w, tr = idx >> 3, ch = idx & 7;
+                    const uint4 u = *reinterpret_cast<const uint4 *>(sTb + sw(tr, ch));
+                    *reinterpret_cast<uint4 *>(sTa + sw(tr, ch)) = scale_chunk8(u, F + fTF + 8 * ch);
+                }
             }
+            // the operands of K Q^T, W and U are ready: issue the first two, signal U
             tc::fence_async_smem();
             tc::fence_before();
             ptx::named_bar_sync(2, kPrep);
-            bool oki = true;
             if (pt == 0) {
                 tc::fence_after();
                 prep_mma(c);
-                // U of the previous chunk has been read once its D^T epilogue is done
-                if (c > 0) oki = ptx::mbar_wait(dready, (c - 1) & 1);
-                if (oki) {
-                    tc::fence_after();
-                    u_mma(c);
-                }
+                ptx::mbar_arrive(prepA);
             }
             // ---- K Q^T and W = Ta K done
-            ok = ptx::named_bar_and(2, kPrep, oki && ptx::mbar_wait(&barPM[bf], (c >> 1) & 1));
+            ok = ptx::named_bar_and(2, kPrep, ptx::mbar_wait_sleep(&barPM[bf], (c >> 1) & 1));
             if (!ok) break;
             tc::fence_after();
             {
-                // M = 64 results: row 16 pq + lane (lane < 16) sits on lane 32 pq + lane
-                const int rj = 16 * pq + lane;
-                float v[32];
-                // P^T[j][r] = e^{G_r - G_j} k_j . q_r for r >= j; columns [32 ph, 32 ph + 32)
-                tc::ld32(lo + pI1 + 32 * ph, v);
-                if (lane < 16) {
-                    const float Gj = sG[rj];
-                    float gr[32];
+                // M = 64 results: rows 16 pq .. 16 pq + 15 sit on lanes 32 pq .. 32 pq + 15; the
+                // 16x256b shape spreads them over the warp: rows ja, ja + 8, column pairs 2 (lane % 4)
+                const int ja = 16 * pq + (lane >> 2), jb = ja + 8, cp = 2 * (lane & 3);
+                // P^T[j][r] = scale e^{G_r - G_j} k_j . q_r / (|k_j| |q_r|) for r >= j
+                {
+                    float v[16];
+                    tc::ld16x256<4>(lo + pI1 + 32 * ph, v);
+                    const float Ga = F[fG + ja], Gb = F[fG + jb], ka = F[fIK + ja], kb = F[fIK + jb];
 #pragma unroll
-                    for (int e4 = 0; e4 < 8; ++e4) {
-                        const float4 g4 = *reinterpret_cast<const float4 *>(sG + 32 * ph + 4 * e4);
-                        gr[4 * e4] = g4.x, gr[4 * e4 + 1] = g4.y, gr[4 * e4 + 2] = g4.z, gr[4 * e4 + 3] = g4.w;
+                    for (int k = 0; k < 4; ++k) {
+                        const int r0 = 32 * ph + 8 * k + cp;
+                        const float2 g = *reinterpret_cast<const float2 *>(F + fG + r0);
+                        const float2 qs = *reinterpret_cast<const float2 *>(F + fQS + r0);
+                        const float a0 = r0 >= ja ? __expf(g.x - Ga) * ka * qs.x * v[4 * k] : 0.f;
+                        const float a1 = r0 + 1 >= ja ? __expf(g.y - Ga) * ka * qs.y * v[4 * k + 1] : 0.f;
+                        const float b0 = r0 >= jb ? __expf(g.x - Gb) * kb * qs.x * v[4 * k + 2] : 0.f;
+                        const float b1 = r0 + 1 >= jb ? __expf(g.y - Gb) * kb * qs.y * v[4 * k + 3] : 0.f;
+                        const int ch = 4 * ph + k;
+                        *reinterpret_cast<uint32_t *>(sPK + sw(ja, ch) + 2 * cp) = ptx::pack_h2(a0, a1);
+                        *reinterpret_cast<uint32_t *>(sPK + sw(jb, ch) + 2 * cp) = ptx::pack_h2(b0, b1);
                     }
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int r = 32 * ph + jj;
-                        v[jj] = r >= rj ? __expf(gr[jj] - Gj) * v[jj] : 0.f;
-                    }
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) st_chunk(sPK, rj, 4 * ph + cc, v + 8 * cc);
                 }
                 if (RETR) {
-                    // -W rows over the key rows: columns [64 ph, 64 ph + 64)
+                    // -W over the key rows: columns [64 ph, 64 ph + 64) = key block ph
+                    float v[32];
+                    tc::ld16x256<8>(lo + pW + 64 * ph, v);
 #pragma unroll
-                    for (int k2 = 0; k2 < 2; ++k2) {
-                        tc::ld32(lo + pW + 64 * ph + 32 * k2, v);
-                        if (lane < 16) {
-#pragma unroll
-                            for (int jj = 0; jj < 32; ++jj) v[jj] = -v[jj];
-#pragma unroll
-                            for (int cc = 0; cc < 4; ++cc) st_chunk(sKQ + ph * 16384, rj, 4 * k2 + cc, v + 8 * cc);
-                        }
+                    for (int k = 0; k < 8; ++k) {
+                        *reinterpret_cast<uint32_t *>(sKQ + ph * 16384 + sw(ja, k) + 2 * cp) =
+                            ptx::pack_h2(v[4 * k], v[4 * k + 1]);
+                        *reinterpret_cast<uint32_t *>(sKQ + ph * 16384 + sw(jb, k) + 2 * cp) =
+                            ptx::pack_h2(v[4 * k + 2], v[4 * k + 3]);
                     }
                 }
             }
@@ -1295,9 +1353,9 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                 const int idx = pt + kPrep * w, r = idx >> 4, ch = idx & 15;
                 if (!RETR)  // W = 0: clear the key rows
                     *reinterpret_cast<uint4 *>(sKQ + (ch >> 3) * 16384 + sw(r, ch & 7)) = make_uint4(0, 0, 0, 0);
-                // query rows -> e^{G_r} q_r in place (K Q^T has read the raw rows)
+                // query rows -> scale e^{G_r} q_r / |q_r| in place (K Q^T has read the raw rows)
                 uint4 *ptr = reinterpret_cast<uint4 *>(sKQ + (ch >> 3) * 16384 + sw(64 + r, ch & 7));
-                *ptr = scale_chunk(*ptr, sEG[r]);
+                *ptr = scale_chunk(*ptr, F[fQF + r]);
             }
             tc::fence_async_smem();
             tc::fence_before();
