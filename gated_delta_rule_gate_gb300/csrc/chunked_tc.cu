@@ -5,35 +5,21 @@
 // Same per-chunk algebra as chunked.cu (derived from the token recurrence;
 // see the comment there).  For one chunk of C = 64 tokens, with
 // A = strict-lower(diag(beta) e^{G_r - G_j} K K^T), T = (I + A)^-1,
-// Ta = T diag(beta e^G), Tb = T diag(beta):
+// Ta = T diag(beta e^G), Tb = T diag(beta), W = Ta K, U = Tb V:
 //
-//   I1:  [K; Q] K^T      -> rows 64..127: Q K^T (P = its decayed causal part)
-//   I2:  W^T  = K^T Ta^T
-//   C1:  D^T  = V^T Tb^T - S W^T                       (D = the token corrections)
-//   C2:  O^T  = S Qh^T + D^T P^T   Qh = diag(e^G) Q
-//   C4:  X    = (D^T diag(e^{G_C - G})) K
-//   S   <- e^{G_C} S + X                               (fp32, in registers)
+//   D = U - W S^T                 (the token corrections, D^T = U^T - S W^T)
+//   O = scale (diag(e^G) Q S^T + P D),   P = decayed causal Q K^T
+//   S <- e^{G_C} S + D^T diag(e^{G_C - G}) K
 //
 // Two kernels run the delta rules.  The key-side system does not depend on
 // the state, so chunk_solve_kernel builds A with one tensor-core product and
-// solves it in fp32 for every (chunk, head) at once, all chunks in parallel,
-// and writes Tb (fp16) to the workspace.  chunked_tc_kernel then walks each
-// (request, value head) chunk by chunk; it loads Tb by TMA together with the
-// chunk's keys, queries and values and forms Ta = Tb diag(e^G) itself.  The
-// rules without retrieval (D = V) need no solve.
-//
-// chunked_tc_kernel is written "transposed" so that the M = 128 side of every
-// tensor-core product is the value axis of the V-major state: lane i of
-// tensor memory is value row i.  Operands are fp16 tiles in shared memory
-// with the 128-byte swizzle.  The key/query chunk lands (tiled TMA) as a
-// 128-row K-major tile [K; Q]; its key rows double as the MN-major K^T
-// operand of I2 and C4, and the value chunk lands as the MN-major V^T
-// operand, so nothing is transposed by hand.  The fp32 state lives in
-// registers of the 8 warps (row i, 64 columns each) and is mirrored each
-// chunk into an fp16 K-major tile, the A operand of C1/C2.  The next chunk's
-// loads are in flight while the current chunk computes.  One CTA of 256
-// threads per (request, value head); one thread issues every MMA and tracks
-// completion through an mbarrier (bounded waits).
+// solves it in fp32 for every (chunk, head), all chunks in parallel, and
+// writes Tb (fp16) to the workspace.  chunked_pipe_kernel then walks each
+// (request, value head) chunk by chunk, with the state in tensor memory; it
+// loads Tb by TMA together with the chunk's keys, queries and values.  The
+// rules without retrieval (D = V) need no solve.  The layout of each kernel
+// is described above it.
+#include <algorithm>
 #include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
 #include <cuda_fp16.h>
 
@@ -44,40 +30,27 @@
 namespace gdn {
 namespace {
 
-constexpr int TC_C = 64;         // tokens per chunk
-constexpr int TC_THREADS = 256;  // 8 warps
+constexpr int TC_C = 64;  // tokens per chunk
 constexpr int TC_TMEM_COLS = 512;
 constexpr int kTbBytes = TC_C * TC_C * 2;  // one fp16 Tb tile
 
-// shared memory layout of chunked_tc_kernel (bytes from a 1024-aligned base)
-constexpr int oKQ = 0;            // 2 x 32 KB: [K; Q] landing tiles, 128 rows x 128 dk, K-major
-constexpr int oV = 65536;         // 2 x 16 KB: V landing tiles, MN-major (rows = tokens)
-constexpr int oS = 98304;         // 32 KB: fp16 state, 128 rows x 128 dk, K-major
-constexpr int oTa = 131072;       // 8 KB: [64 r][64 j]
-constexpr int oTb = 139264;       // 2 x 8 KB: Tb landing tiles [64 r][64 j]
-constexpr int oP = 155648;        // 8 KB
-constexpr int oR = 163840;        // 48 KB: W | DT | DTs
-constexpr int oW = oR;            // 16 KB: [64 r][128 c], K-major
-constexpr int oDT = oR + 16384;   // 16 KB: [128 i][64 j]
-constexpr int oDTs = oR + 32768;  // 16 KB
-constexpr int oO = oDT;           // 16 KB: output staging [64 r][128 i] (after the last MMAs)
-constexpr int oScal = oR + 49152; // fp32 G, beta, e^G, e^{G_C - G}: 4 x 64
-constexpr int oBar = oScal + 1024;  // MMA barrier, two landing barriers, TMEM address
-constexpr int TC_SMEM = oBar + 32 + 1024;  // + alignment slack
-
 constexpr uint32_t kLandBytes = 3 * 16384;  // K, Q and V boxes of one chunk
 
-// shared memory layout of chunk_solve_kernel
-constexpr int SV_THREADS = 128;
+// shared memory layout of chunk_solve_kernel (persistent: a producer warp and
+// four solver warps, two task buffers)
+constexpr int SV_SOLVERS = 128;
+constexpr int SV_THREADS = SV_SOLVERS + 32;
 constexpr int FA = 68;  // fp32 row stride of At (16-byte rows; lanes = consecutive r, conflict-free)
 constexpr int FT = 68;  // fp32 row stride of T (16-byte rows for vector reads)
-constexpr int sK = 0;                      // 16 KB: K, 2 blocks of [64 tokens][64 dk], K-major
-constexpr int sAt = 16384;                 // fp32 [64][FA], At[j][r] = A[r][j]
+constexpr int sK = 0;                      // 2 x 16 KB: K, 2 blocks of [64 tokens][64 dk], K-major
+constexpr int sAt = 32768;                 // fp32 [64][FA], At[j][r] = A[r][j]
 constexpr int sTf = sAt + 64 * FA * 4;     // fp32 [64][FT], T
 constexpr int sY = sTf + 64 * FT * 4;      // fp32 [32][36] product scratch
-constexpr int sSc = sY + 32 * 36 * 4;      // fp32 G, beta, 1/|k|: 3 x 64
-constexpr int sBar = sSc + 3 * 64 * 4;     // landing barrier, MMA barrier, TMEM address
-constexpr int SV_SMEM = sBar + 32 + 1024;  // + alignment slack
+constexpr int sGin = sY + 32 * 36 * 4;     // 2 x (log decay, beta) of 64 tokens, from the producer
+constexpr int sSc = sGin + 2 * 128 * 4;    // fp32 G, beta, 1/|k| of the current task: 3 x 64
+constexpr int sHdr = sSc + 3 * 64 * 4;     // 2 x {request, head, first token, tokens}
+constexpr int sBar = sHdr + 2 * 16;        // full[2], empty[2], MMA barrier, TMEM address
+constexpr int SV_SMEM = sBar + 64 + 1024;  // + alignment slack
 
 // writes 8 consecutive fp16 values (one 16-byte chunk) of row `row`, chunk
 // `ch` (0..7) of a 64-column block
@@ -90,20 +63,6 @@ __device__ __forceinline__ void st_chunk(unsigned char *tile, int row, int ch, c
     *reinterpret_cast<uint4 *>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) = u;
 }
 
-__device__ __forceinline__ void sync_tc() {
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-}
-
-__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, int32_t *err) {
-    const bool ok = ptx::mbar_wait_spin(bar, phase);
-    phase ^= 1u;
-    if (!ok && err && threadIdx.x == 0) atomicOr(err, 2);
-    tc::fence_after();
-    return ok;
-}
-
 // number of chunks of request b
 __device__ __forceinline__ int request_chunks(const Problem &p, int b) {
     int t0, t1;
@@ -113,9 +72,9 @@ __device__ __forceinline__ int request_chunks(const Problem &p, int b) {
 
 // ---------------------------------------------------------------------------
 // Workspace slots: chunk j of request b has slot offs[b] + j, offs being the
-// exclusive prefix sum of the requests' chunk counts (offs[B] = the total).
-// One CTA of 1024 threads.
-__global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *offs) {
+// exclusive prefix sum of the requests' chunk counts (offs[B] = the total);
+// slot_req[slot] is the request owning a slot.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *offs, int *slot_req, int cap) {
     __shared__ int wsum[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (p.B + 1023) / 1024;
@@ -144,684 +103,318 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *off
     int base = x - s + (warp > 0 ? wsum[warp - 1] : 0);
     for (int b = b0; b < b1; ++b) {
         offs[b] = base;
-        base += request_chunks(p, b);
+        const int nb = request_chunks(p, b);
+        for (int j = 0; j < nb && base + j < cap; ++j) slot_req[base + j] = b;
+        base += nb;
     }
     if (tid == 1023) offs[p.B] = wsum[31];
 }
 
 // ---------------------------------------------------------------------------
-// Tb = (I + A)^-1 diag(beta) of one (chunk, value head).  Grid (slots, Hv),
-// 128 threads.  A = strict-lower(diag(beta) e^{G_r - G_j} Kn Kn^T), Kn the
-// key rows after the optional L2 norm, from one M = 64 tensor-core product of
-// the raw fp16 keys (the norms are applied to the fp32 result).  The solve
-// is fp32 recursive doubling: the four 16 x 16 diagonal blocks by
-// substitution, then [[T0, 0], [L, T1]] with L = -T1 A10 T0 twice.  Padding
-// tokens of a short last chunk get beta = 0 and zero keys, so their rows and
-// columns of Tb are zero.
+// Tb = (I + A)^-1 diag(beta) for every (chunk slot, value head) task.
+// A = strict-lower(diag(beta) e^{G_r - G_j} Kn Kn^T), Kn the key rows after
+// the optional L2 norm, from one M = 64 tensor-core product of the raw fp16
+// keys (the norms are applied to the fp32 result).  The solve is fp32
+// recursive doubling: the four 16 x 16 diagonal blocks by substitution, then
+// [[T0, 0], [L, T1]] with L = -T1 A10 T0 twice.  Padding tokens of a short
+// last chunk get beta = 0 and zero keys, so their rows and columns of Tb are
+// zero.
+//
+// Persistent CTAs: a producer warp walks the CTA's tasks (slot, head) two
+// ahead of the solvers (request lookup, the gates in fp32, the key tile by
+// TMA) into two buffers; four solver warps run the product, the system and
+// its solve.  Waits are bounded.
 __global__ void __launch_bounds__(SV_THREADS) chunk_solve_kernel(Problem p, const __grid_constant__ CUtensorMap tmK,
-                                                                 const int *offs, __half *tb, int cap) {
+                                                                 const int *offs, const int *slot_req, __half *tb,
+                                                                 int cap) {
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
     unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
-    const int slot = blockIdx.x, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (slot >= cap || slot >= offs[p.B]) return;
-    // the request owning this slot: the last b with offs[b] <= slot
-    int lo = 0, hi = p.B - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (offs[mid] <= slot)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const int b = lo;
-    int t0, t1;
-    request_range(p, b, t0, t1);
-    const int c0 = t0 + TC_C * (slot - offs[b]);
-    const int n = min(TC_C, t1 - c0);
-    if (n <= 0) return;
-    const int qh = (int)((long long)h * p.Hq / p.Hv);
-
-    unsigned char *sKt = sm + sK;
+    const int total = min(offs[p.B], cap);
+    const long long ntasks = (long long)total * p.Hv;
     float *At = reinterpret_cast<float *>(sm + sAt);
     float *Tf = reinterpret_cast<float *>(sm + sTf);
     float *Y = reinterpret_cast<float *>(sm + sY);
+    float *gin = reinterpret_cast<float *>(sm + sGin);
     float *sG = reinterpret_cast<float *>(sm + sSc);
     float *sB = sG + 64, *sInv = sG + 128;
-    uint64_t *ldbar = reinterpret_cast<uint64_t *>(sm + sBar);
-    uint64_t *mbar = ldbar + 1;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + sBar + 16);
-
+    int *hdr = reinterpret_cast<int *>(sm + sHdr);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + sBar);
+    uint64_t *empty = full + 2;
+    uint64_t *mbar = full + 4;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + sBar + 40);
     if (tid == 0) {
-        ptx::mbar_init(ldbar, 1);
-        ptx::mbar_init(mbar, 1);
+        for (int i = 0; i < 5; ++i) ptx::mbar_init(&full[i], 1);
         ptx::fence_mbar_init();
-        ptx::mbar_arrive_expect_tx(ldbar, 16384);
-        ptx::tma_load_3d(sKt, &tmK, 0, qh, c0, ldbar);
-        ptx::tma_load_3d(sKt + 8192, &tmK, 64, qh, c0, ldbar);
     }
     if (warp == 0) tc::tmem_alloc(tslot, 64);
-    if (tid < TC_C) {
-        float g = 0.f, bt = 0.f;
-        if (tid < n) {
-            const size_t th = (size_t)(c0 + tid) * p.Hv + h;
-            if (rule_has_decay(p.rule)) {
-                g = ld_any(p.decay, th, p.decay_f16);
-                if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[h]);
-            }
-            bt = ld_any(p.beta, th, p.beta_f16);
-            if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
-        }
-        sG[tid] = g;
-        sB[tid] = bt;
-    }
+    tc::fence_before();
     __syncthreads();
-    if (warp == 0) {  // G = inclusive cumulative sum of the log decays
-        const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
-        float s = g0 + g1;
+    tc::fence_after();
+    const uint32_t tmem = *tslot;
+    const long long G = gridDim.x;
+
+    if (warp == 4) {
+        // ===================== producer
+        int i = 0;
+        for (long long t = blockIdx.x; t < ntasks; t += G, ++i) {
+            const int bf = i & 1;
+            if (!ptx::mbar_wait_sleep(&empty[bf], ((i >> 1) & 1) ^ 1)) {
+                if (p.err && lane == 0) atomicOr(p.err, 2);
+                break;
+            }
+            const int slot = (int)(t / p.Hv), h = (int)(t % p.Hv);
+            const int b = slot_req[slot];
+            int t0, t1;
+            request_range(p, b, t0, t1);
+            const int c0 = t0 + TC_C * (slot - offs[b]);
+            const int n = min(TC_C, t1 - c0);
+            float *g2 = gin + bf * 128;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
-        }
-        sG[2 * lane] = s - g1;
-        sG[2 * lane + 1] = s;
-    }
-    // every thread waits; the barrier makes the outcome uniform across the CTA
-    bool ok = __syncthreads_and(ptx::mbar_wait(ldbar, 0)) != 0;
-    if (!ok && p.err && tid == 0) atomicOr(p.err, 2);
-    if (ok) {
-        if (n < TC_C) {  // the boxes run past this request: clear the rows beyond it
-            for (int idx = tid; idx < (TC_C - n) * 16; idx += SV_THREADS) {
-                const int r = n + (idx >> 4), ch = idx & 15;
-                *reinterpret_cast<uint4 *>(sKt + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(0, 0, 0, 0);
+            for (int e = 0; e < 2; ++e) {
+                const int tt = lane + 32 * e;
+                float g = 0.f, bt = 0.f;
+                if (tt < n) {
+                    const size_t th = (size_t)(c0 + tt) * p.Hv + h;
+                    if (rule_has_decay(p.rule)) {
+                        g = ld_any(p.decay, th, p.decay_f16);
+                        if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[h]);
+                    }
+                    bt = ld_any(p.beta, th, p.beta_f16);
+                    if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
+                }
+                g2[tt] = g;
+                g2[64 + tt] = bt;
+            }
+            if (lane == 0) {
+                int *hd = hdr + 4 * bf;
+                hd[0] = b, hd[1] = h, hd[2] = c0, hd[3] = n;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                const int qh = (int)((long long)h * p.Hq / p.Hv);
+                unsigned char *kt = sm + sK + bf * 16384;
+                ptx::mbar_arrive_expect_tx(&full[bf], 16384);
+                ptx::tma_load_3d(kt, &tmK, 0, qh, c0, &full[bf]);
+                ptx::tma_load_3d(kt + 8192, &tmK, 64, qh, c0, &full[bf]);
             }
         }
-        __syncthreads();
-        {  // 1 / |k_r|: thread pair (2r, 2r + 1), one 64-column block each
-            const int r = tid >> 1, kb = tid & 1;
-            float ss = 0.f;
+    } else {
+        // ===================== solvers (128 threads)
+        bool ok = true;
+        uint32_t mphase = 0;
+        int i = 0;
+        for (long long t = blockIdx.x; t < ntasks; t += G, ++i) {
+            const int bf = i & 1;
+            ok = ptx::named_bar_and(1, SV_SOLVERS, ptx::mbar_wait_sleep(&full[bf], (i >> 1) & 1));
+            if (!ok) break;
+            const int *hd = hdr + 4 * bf;
+            const int slot = (int)(t / p.Hv), h = hd[1], n = hd[3];
+            unsigned char *sKt = sm + sK + bf * 16384;
+            const float *g2 = gin + bf * 128;
+            if (n < TC_C) {  // the boxes run past this request: clear the rows beyond it
+                for (int idx = tid; idx < (TC_C - n) * 16; idx += SV_SOLVERS) {
+                    const int r = n + (idx >> 4), ch = idx & 15;
+                    *reinterpret_cast<uint4 *>(sKt + (ch >> 3) * 8192 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            if (warp == 0) {  // G = inclusive cumulative sum of the log decays; beta
+                const float x0 = g2[2 * lane], x1 = g2[2 * lane + 1];
+                float sacc = x0 + x1;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(sKt + kb * 8192 + r * 128 + ((c ^ (r & 7)) << 4));
-                const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, sacc, o);
+                    if (lane >= o) sacc += y;
+                }
+                sG[2 * lane] = sacc - x1;
+                sG[2 * lane + 1] = sacc;
+                sB[2 * lane] = g2[64 + 2 * lane];
+                sB[2 * lane + 1] = g2[64 + 2 * lane + 1];
+            }
+            ptx::named_bar_sync(1, SV_SOLVERS);
+            {  // 1 / |k_r|: thread pair (2r, 2r + 1), one 64-column block each
+                const int r = tid >> 1, kb = tid & 1;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(sKt + kb * 8192 + r * 128 + ((c ^ (r & 7)) << 4));
+                    const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float2 f = __half22float2(hp[w]);
+                        s0 = fmaf(f.x, f.x, s0);
+                        s1 = fmaf(f.y, f.y, s1);
+                    }
+                }
+                float ss = s0 + s1;
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (kb == 0) sInv[r] = (p.flags & kL2k) ? rsqrtf(ss + 1e-12f) : 1.f;
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(1, SV_SOLVERS);
+            if (tid == 0) {
+                tc::fence_after();
+                // K K^T: M = 64 tokens, N = 64 tokens, K = 128 channels
+                const uint32_t aK = ptx::smem_u32(sKt);
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) {
+                    const uint64_t d = tc::desc_sw128(aK + (s2 >> 2) * 8192 + (s2 & 3) * 32);
+                    tc::mma_f16(tmem, d, d, tc::idesc_f16(64, 64), s2 > 0);
+                }
+                tc::commit(mbar);
+            }
+            ok = ptx::named_bar_and(1, SV_SOLVERS, ptx::mbar_wait_sleep(mbar, mphase));
+            mphase ^= 1u;
+            if (!ok) break;
+            tc::fence_after();
+            // the key tile and the gate buffer are free for the producer
+            if (tid == 0) ptx::mbar_arrive(&empty[bf]);
+            {
+                // rows 16 warp .. 16 warp + 15 sit on tensor-memory lanes 32 warp .. + 15 (M = 64);
+                // the 16x256b shape gives thread `lane` rows ra, ra + 8 and column pairs 2 (lane % 4)
+                const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+                const int ra = 16 * warp + (lane >> 2), rb = ra + 8, cp = 2 * (lane & 3);
+                const float fa = sB[ra] * sInv[ra], fb = sB[rb] * sInv[rb], Ga = sG[ra], Gb = sG[rb];
+                float v[32];
+                tc::ld16x256<8>(tmem + lane_off, v);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int j = 8 * k + cp;
+                    const float2 gj = *reinterpret_cast<const float2 *>(sG + j);
+                    const float2 ij = *reinterpret_cast<const float2 *>(sInv + j);
+                    At[j * FA + ra] = j < ra ? fa * __expf(Ga - gj.x) * ij.x * v[4 * k] : 0.f;
+                    At[(j + 1) * FA + ra] = j + 1 < ra ? fa * __expf(Ga - gj.y) * ij.y * v[4 * k + 1] : 0.f;
+                    At[j * FA + rb] = j < rb ? fb * __expf(Gb - gj.x) * ij.x * v[4 * k + 2] : 0.f;
+                    At[(j + 1) * FA + rb] = j + 1 < rb ? fb * __expf(Gb - gj.y) * ij.y * v[4 * k + 3] : 0.f;
+                }
+            }
+            tc::fence_before();
+            ptx::named_bar_sync(1, SV_SOLVERS);
+            if (lane < 16) {
+                // column `lane` of the inverse of diagonal block `warp`, right-looking:
+                // once x[j] is final it updates every later row at once
+                float x[16];
+                const float *Ab = At + (16 * warp) * FA + 16 * warp;  // Ab[j][i] = A[i][j]
+#pragma unroll
+                for (int q = 0; q < 16; ++q) x[q] = (q == lane) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < 15; ++j) {
+                    float a[16];
+#pragma unroll
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        const float4 tv = *reinterpret_cast<const float4 *>(Ab + j * FA + 4 * w4);
+                        a[4 * w4] = tv.x, a[4 * w4 + 1] = tv.y, a[4 * w4 + 2] = tv.z, a[4 * w4 + 3] = tv.w;
+                    }
+#pragma unroll
+                    for (int q = j + 1; q < 16; ++q) x[q] = fmaf(-a[q], x[j], x[q]);
+                }
+#pragma unroll
+                for (int q = 0; q < 16; ++q) Tf[(16 * warp + q) * FT + 16 * warp + lane] = x[q];
+            }
+            // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int idx = 4 * tid + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+                Tf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
+            }
+            ptx::named_bar_sync(1, SV_SOLVERS);
+            {
+                // level 1: blocks (1,0) and (3,2): Y = A_{b,b-1} T_{b-1}, then L = -T_b Y
+                const int r = tid >> 3, c = 2 * (tid & 7);  // row 0..15, columns c, c+1
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const int o0 = 32 * blk;
+                    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float a = At[(o0 + k) * FA + o0 + 16 + r];
+                        y0 = fmaf(a, Tf[(o0 + k) * FT + o0 + c], y0);
+                        y1 = fmaf(a, Tf[(o0 + k) * FT + o0 + c + 1], y1);
+                    }
+                    Y[blk * 16 * 36 + r * 36 + c] = y0;
+                    Y[blk * 16 * 36 + r * 36 + c + 1] = y1;
+                }
+                ptx::named_bar_sync(1, SV_SOLVERS);
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const int o0 = 32 * blk;
+                    float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float tv = Tf[(o0 + 16 + r) * FT + o0 + 16 + k];
+                        l0 = fmaf(tv, Y[blk * 16 * 36 + k * 36 + c], l0);
+                        l1 = fmaf(tv, Y[blk * 16 * 36 + k * 36 + c + 1], l1);
+                    }
+                    Tf[(o0 + 16 + r) * FT + o0 + c] = -l0;
+                    Tf[(o0 + 16 + r) * FT + o0 + c + 1] = -l1;
+                }
+            }
+            ptx::named_bar_sync(1, SV_SOLVERS);
+            {
+                // level 2: Y = A_10 T_0 (32 x 32), then L = -T_1 Y; thread = (row, 2 x 4 columns).
+                // T_0 and T_1 are lower triangular: Y[r][c] sums k >= c, L[r][c] sums k <= r.
+                const int r = tid >> 2;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c = 4 * (tid & 3) + 16 * half;
+                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (int k = c; k < 32; ++k) {
+                        const float a = At[k * FA + 32 + r];
+                        const float4 tv = *reinterpret_cast<const float4 *>(Tf + k * FT + c);
+                        y.x = fmaf(a, tv.x, y.x), y.y = fmaf(a, tv.y, y.y), y.z = fmaf(a, tv.z, y.z),
+                        y.w = fmaf(a, tv.w, y.w);
+                    }
+                    *reinterpret_cast<float4 *>(Y + r * 36 + c) = y;
+                }
+                ptx::named_bar_sync(1, SV_SOLVERS);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c = 4 * (tid & 3) + 16 * half;
+                    float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (int k = 0; k <= r; ++k) {
+                        const float tv = Tf[(32 + r) * FT + 32 + k];
+                        const float4 yy = *reinterpret_cast<const float4 *>(Y + k * 36 + c);
+                        l.x = fmaf(tv, yy.x, l.x), l.y = fmaf(tv, yy.y, l.y), l.z = fmaf(tv, yy.z, l.z),
+                        l.w = fmaf(tv, yy.w, l.w);
+                    }
+                    *reinterpret_cast<float4 *>(Tf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
+                }
+            }
+            ptx::named_bar_sync(1, SV_SOLVERS);
+            {
+                // Tb[r][j] = T[r][j] beta_j (j <= r), fp16 rows of 128 bytes
+                const int r = tid >> 1, j0 = 32 * (tid & 1);
+                __half *dst = tb + (((size_t)slot * p.Hv + h) * TC_C + r) * TC_C + j0;
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    const float2 f = __half22float2(hp[w]);
-                    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = j0 + 8 * w + e;
+                        x[e] = j <= r ? Tf[r * FT + j] * sB[j] : 0.f;
+                    }
+                    uint4 u;
+                    u.x = ptx::pack_h2(x[0], x[1]);
+                    u.y = ptx::pack_h2(x[2], x[3]);
+                    u.z = ptx::pack_h2(x[4], x[5]);
+                    u.w = ptx::pack_h2(x[6], x[7]);
+                    *reinterpret_cast<uint4 *>(dst + 8 * w) = u;
                 }
             }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            if (kb == 0) sInv[r] = (p.flags & kL2k) ? rsqrtf(ss + 1e-12f) : 1.f;
+            // At, Tf, Y and the task scalars are rewritten by the next task
+            ptx::named_bar_sync(1, SV_SOLVERS);
         }
-    }
-    tc::fence_async_smem();
-    sync_tc();
-    const uint32_t tmem = *tslot;
-    if (ok && tid == 0) {
-        // K K^T: M = 64 tokens, N = 64 tokens, K = 128 channels
-        const uint32_t aK = ptx::smem_u32(sKt);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint64_t d = tc::desc_sw128(aK + (s >> 2) * 8192 + (s & 3) * 32);
-            tc::mma_f16(tmem, d, d, tc::idesc_f16(64, 64), s > 0);
-        }
-        tc::commit(mbar);
-    }
-    if (ok) {
-        uint32_t phase = 0;
-        ok = wait_mma(mbar, phase, p.err);
-    }
-    ok = __syncthreads_and(ok) != 0;
-    if (ok) {
-        // row r = 16 warp + lane sits on tensor-memory lane 32 warp + lane (M = 64)
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        const int r = 16 * warp + lane;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float v[32];
-            tc::ld32(tmem + lane_off + 32 * hh, v);
-            if (lane < 16) {
-                const float br = sB[r] * sInv[r], Gr = sG[r];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * hh + jj;
-                    At[j * FA + r] = j < r ? br * __expf(Gr - sG[j]) * sInv[j] * v[jj] : 0.f;
-                }
-            }
-        }
+        if (!ok && p.err && tid == 0) atomicOr(p.err, 2);
     }
     tc::fence_before();
     __syncthreads();
-    if (ok) {
-        if (lane < 16) {
-            // column `lane` of the inverse of diagonal block `warp`, right-looking:
-            // once x[j] is final it updates every later row at once
-            float x[16];
-            const float *Ab = At + (16 * warp) * FA + 16 * warp;  // Ab[j][i] = A[i][j]
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-            for (int j = 0; j < 15; ++j) {
-                float a[16];
-#pragma unroll
-                for (int w4 = 0; w4 < 4; ++w4) {
-                    const float4 t = *reinterpret_cast<const float4 *>(Ab + j * FA + 4 * w4);
-                    a[4 * w4] = t.x, a[4 * w4 + 1] = t.y, a[4 * w4 + 2] = t.z, a[4 * w4 + 3] = t.w;
-                }
-#pragma unroll
-                for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-a[i], x[j], x[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tf[(16 * warp + i) * FT + 16 * warp + lane] = x[i];
-        }
-        // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int idx = 4 * tid + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
-            Tf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
-        }
-    }
-    __syncthreads();
-    if (ok) {
-        // level 1: blocks (1,0) and (3,2): Y = A_{b,b-1} T_{b-1}, then L = -T_b Y
-        const int r = tid >> 3, c = 2 * (tid & 7);  // row 0..15, columns c, c+1
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            const int o0 = 32 * blk;
-            float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float a = At[(o0 + k) * FA + o0 + 16 + r];
-                y0 = fmaf(a, Tf[(o0 + k) * FT + o0 + c], y0);
-                y1 = fmaf(a, Tf[(o0 + k) * FT + o0 + c + 1], y1);
-            }
-            Y[blk * 16 * 36 + r * 36 + c] = y0;
-            Y[blk * 16 * 36 + r * 36 + c + 1] = y1;
-        }
-    }
-    __syncthreads();
-    if (ok) {
-        const int r = tid >> 3, c = 2 * (tid & 7);
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-            const int o0 = 32 * blk;
-            float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float t = Tf[(o0 + 16 + r) * FT + o0 + 16 + k];
-                l0 = fmaf(t, Y[blk * 16 * 36 + k * 36 + c], l0);
-                l1 = fmaf(t, Y[blk * 16 * 36 + k * 36 + c + 1], l1);
-            }
-            Tf[(o0 + 16 + r) * FT + o0 + c] = -l0;
-            Tf[(o0 + 16 + r) * FT + o0 + c + 1] = -l1;
-        }
-    }
-    __syncthreads();
-    if (ok) {
-        // level 2: Y = A_10 T_0 (32 x 32), thread = (row, 2 x 4 columns)
-        const int r = tid >> 2;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int c = 4 * (tid & 3) + 16 * half;
-            float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const float a = At[k * FA + 32 + r];
-                const float4 t = *reinterpret_cast<const float4 *>(Tf + k * FT + c);
-                y.x = fmaf(a, t.x, y.x), y.y = fmaf(a, t.y, y.y), y.z = fmaf(a, t.z, y.z), y.w = fmaf(a, t.w, y.w);
-            }
-            *reinterpret_cast<float4 *>(Y + r * 36 + c) = y;
-        }
-    }
-    __syncthreads();
-    if (ok) {
-        // L = -T_1 Y
-        const int r = tid >> 2;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int c = 4 * (tid & 3) + 16 * half;
-            float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const float t = Tf[(32 + r) * FT + 32 + k];
-                const float4 yy = *reinterpret_cast<const float4 *>(Y + k * 36 + c);
-                l.x = fmaf(t, yy.x, l.x), l.y = fmaf(t, yy.y, l.y), l.z = fmaf(t, yy.z, l.z), l.w = fmaf(t, yy.w, l.w);
-            }
-            *reinterpret_cast<float4 *>(Tf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
-        }
-    }
-    __syncthreads();
-    if (ok) {
-        // Tb[r][j] = T[r][j] beta_j (j <= r), fp16 rows of 128 bytes
-        const int r = tid >> 1, j0 = 32 * (tid & 1);
-        __half *dst = tb + (((size_t)slot * p.Hv + h) * TC_C + r) * TC_C + j0;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = j0 + 8 * w + e;
-                x[e] = j <= r ? Tf[r * FT + j] * sB[j] : 0.f;
-            }
-            uint4 u;
-            u.x = ptx::pack_h2(x[0], x[1]);
-            u.y = ptx::pack_h2(x[2], x[3]);
-            u.z = ptx::pack_h2(x[4], x[5]);
-            u.w = ptx::pack_h2(x[6], x[7]);
-            *reinterpret_cast<uint4 *>(dst + 8 * w) = u;
-        }
-    }
-    sync_tc();
+    tc::fence_after();
     if (warp == 0) tc::tmem_dealloc(tmem, 64);
-}
-
-// ---------------------------------------------------------------------------
-// One chunk of keys, queries and values (six 64 x 64 fp16 boxes) and, for the
-// delta rules, its Tb tile, by TMA.  The 128-byte swizzle of the tensor maps
-// lays them out exactly as the K-major [K; Q] operand, the MN-major V^T
-// operand and the K-major Tb^T operand expect.
-__device__ __forceinline__ void issue_chunk(const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV,
-                                            const CUtensorMap *tmT, unsigned char *kq, unsigned char *vt,
-                                            unsigned char *tbt, uint64_t *bar, int c0, int h, int qh, int trow) {
-    ptx::mbar_arrive_expect_tx(bar, kLandBytes + (tbt ? (uint32_t)kTbBytes : 0u));
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-        ptx::tma_load_3d(kq + kb * 16384, tmK, 64 * kb, qh, c0, bar);
-        ptx::tma_load_3d(kq + kb * 16384 + 8192, tmQ, 64 * kb, qh, c0, bar);
-        ptx::tma_load_3d(vt + kb * 8192, tmV, 64 * kb, h, c0, bar);
-    }
-    if (tbt) ptx::tma_load_2d(tbt, tmT, 0, trow, bar);
-}
-
-template <bool RETR>
-__global__ void __launch_bounds__(TC_THREADS, 1)
-    chunked_tc_kernel(Problem p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmT,
-                      const int *offs, int cap) {
-    extern __shared__ unsigned char smraw[];
-    const uint32_t sb0 = ptx::smem_u32(smraw);
-    unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
-    unsigned char *sS = sm + oS, *sTa = sm + oTa, *sP = sm + oP;
-    unsigned char *sW = sm + oW, *sDT = sm + oDT, *sDTs = sm + oDTs;
-    float *sG = reinterpret_cast<float *>(sm + oScal);
-    float *sB = sG + 64, *sEG = sG + 128, *sEGC = sG + 192;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + oBar);
-    uint64_t *ldbar = bar + 1;  // [2], one per landing buffer
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + oBar + 24);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hc = warp >> 2;
-    const int ell = 32 * q4 + lane;  // tensor-memory lane = row served by this thread
-    const int h = blockIdx.x % p.Hv, b = blockIdx.x / p.Hv;
-    const int row = state_row(p, b, h == 0 && tid == 0);
-    if (row < 0) return;
-    int t0, t1;
-    request_range(p, b, t0, t1);
-    const int qh = (int)((long long)h * p.Hq / p.Hv);
-    const bool has_decay = rule_has_decay(p.rule);
-    const bool sig = (p.flags & kBetaSigmoid) != 0;
-    int slot0 = 0;
-    if (RETR && t1 > t0) {
-        slot0 = offs[b];
-        if (slot0 + (t1 - t0 + TC_C - 1) / TC_C > cap) {
-            // only overlapping requests can outgrow the workspace: skip this one
-            if (p.err && tid == 0) atomicOr(p.err, 4);
-            return;
-        }
-    }
-    // the head's gate parameters
-    const float gsc = (has_decay && p.raw_gate) ? p.gate_scale[h] : 0.f;
-    const float gbi = (has_decay && p.raw_gate) ? p.gate_bias[h] : 0.f;
-
-    // ---- the fp32 state: row ell, columns [64 hc, 64 hc + 64)
-    float Sr[64];
-    const size_t srow = (((size_t)row * p.Hv + h) * 128 + ell) * 128 + 64 * hc;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const float4 v = p.init ? *reinterpret_cast<const float4 *>(p.init + srow + 4 * j) : make_float4(0, 0, 0, 0);
-        Sr[4 * j] = v.x, Sr[4 * j + 1] = v.y, Sr[4 * j + 2] = v.z, Sr[4 * j + 3] = v.w;
-    }
-    if (t1 == t0) {  // empty request: copy the incoming state through
-        if (p.fin != p.init) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *reinterpret_cast<float4 *>(p.fin + srow + 4 * j) =
-                    make_float4(Sr[4 * j], Sr[4 * j + 1], Sr[4 * j + 2], Sr[4 * j + 3]);
-        }
-        return;
-    }
-
-    if (tid == 0) {
-        ptx::mbar_init(bar, 1);
-        ptx::mbar_init(&ldbar[0], 1);
-        ptx::mbar_init(&ldbar[1], 1);
-        ptx::fence_mbar_init();
-        issue_chunk(&tmK, &tmQ, &tmV, &tmT, sm + oKQ, sm + oV, RETR ? sm + oTb : nullptr, &ldbar[0], t0, h, qh,
-                    (slot0 * p.Hv + h) * TC_C);
-    }
-    if (warp == 0) tc::tmem_alloc(tslot, TC_TMEM_COLS);
-    // the fp16 mirror of the state
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) st_chunk(sS + hc * 16384, ell, ch, Sr + 8 * ch);
-    float graw = 0.f, braw = 0.f;
-    if (tid < TC_C && tid < t1 - t0) {
-        const size_t th = (size_t)(t0 + tid) * p.Hv + h;
-        if (has_decay) graw = ld_any(p.decay, th, p.decay_f16);
-        if (RETR) braw = ld_any(p.beta, th, p.beta_f16);
-    }
-    tc::fence_async_smem();
-    sync_tc();
-    const uint32_t tmem = *tslot;
-    const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    const uint32_t tI1 = tmem, tD = tmem + 64, tO = tmem + 128, tX = tmem + 192, tW = tmem + 320;
-    unsigned char *sO = sm + oO;
-    uint32_t phase = 0;
-    bool ok = true;
-    const uint32_t IDN64 = tc::idesc_f16(128, 64);
-    const uint32_t IDN64_AMN = tc::idesc_f16(128, 64, true, false);
-    const uint32_t IDN64_NEGB = tc::idesc_f16(128, 64, false, false, true);
-    const uint32_t IDN128_BMN = tc::idesc_f16(128, 128, false, true);
-    const uint32_t IDM64N128_BMN = tc::idesc_f16(64, 128, false, true);
-    const uint32_t aS = ptx::smem_u32(sS), aTa = ptx::smem_u32(sTa);
-    const uint32_t aP = ptx::smem_u32(sP), aW = ptx::smem_u32(sW), aDT = ptx::smem_u32(sDT);
-    const uint32_t aDTs = ptx::smem_u32(sDTs);
-
-    int buf = 0, ci = 0;
-    for (int c0 = t0; c0 < t1 && ok; c0 += TC_C, buf ^= 1, ++ci) {
-        const int n = min(TC_C, t1 - c0);
-        unsigned char *sKQ = sm + oKQ + buf * 32768;
-        unsigned char *sV = sm + oV + buf * 16384;
-        unsigned char *sTb = sm + oTb + buf * kTbBytes;
-        const uint32_t aKQ = ptx::smem_u32(sKQ), aV = ptx::smem_u32(sV), aTb = ptx::smem_u32(sTb);
-        // the barrier makes every exit from this loop uniform across the CTA
-        if (!__syncthreads_and(ptx::mbar_wait(&ldbar[buf], (ci >> 1) & 1))) {
-            if (p.err && tid == 0) atomicOr(p.err, 2);
-            ok = false;
-            break;
-        }
-        // the other buffer was released by the previous chunk: prefetch the next one
-        if (tid == 0 && c0 + TC_C < t1)
-            issue_chunk(&tmK, &tmQ, &tmV, &tmT, sm + oKQ + (buf ^ 1) * 32768, sm + oV + (buf ^ 1) * 16384,
-                        RETR ? sm + oTb + (buf ^ 1) * kTbBytes : nullptr, &ldbar[buf ^ 1], c0 + TC_C, h, qh,
-                        ((slot0 + ci + 1) * p.Hv + h) * TC_C);
-        if (n < TC_C) {
-            // the boxes run past this request: clear the rows beyond it
-            const int nz = (TC_C - n) * 16;
-            for (int idx = tid; idx < 3 * nz; idx += TC_THREADS) {
-                const int which = idx / nz, rem = idx % nz, r = n + (rem >> 4), ch = rem & 15;
-                unsigned char *base = which == 2 ? sV + (ch >> 3) * 8192
-                                                 : sKQ + (ch >> 3) * 16384 + (which == 1 ? 8192 : 0);
-                *reinterpret_cast<uint4 *>(base + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-            }
-        }
-        if (tid < TC_C) {
-            float g = 0.f, bt = 0.f;
-            if (tid < n) {
-                if (has_decay) g = p.raw_gate ? gsc * softplus_f(graw + gbi) : graw;
-                bt = RETR ? (sig ? sigmoid_f(braw) : braw) : 1.f;
-            }
-            sG[tid] = g;
-            sB[tid] = bt;
-            graw = braw = 0.f;
-            if (c0 + TC_C + tid < t1) {
-                const size_t th = (size_t)(c0 + TC_C + tid) * p.Hv + h;
-                if (has_decay) graw = ld_any(p.decay, th, p.decay_f16);
-                if (RETR) braw = ld_any(p.beta, th, p.beta_f16);
-            }
-        }
-        __syncthreads();
-        // ---- cumulants (warp 0) and the L2 norms of the key / query rows
-        if (warp == 0) {
-            const float g0 = sG[2 * lane], g1 = sG[2 * lane + 1];
-            float s = g0 + g1;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += y;
-            }
-            const float G1 = s, G0 = s - g1, GC = __shfl_sync(0xffffffffu, s, 31);
-            sG[2 * lane] = G0, sG[2 * lane + 1] = G1;
-            sEG[2 * lane] = __expf(G0), sEG[2 * lane + 1] = __expf(G1);
-            sEGC[2 * lane] = __expf(GC - G0), sEGC[2 * lane + 1] = __expf(GC - G1);
-        }
-        {
-            // L2 norms: thread pair (2 r, 2 r + 1) owns row r, one 64-column block each
-            const bool nk = (p.flags & kL2k) != 0, nq = (p.flags & kL2q) != 0;
-            const int rr = tid >> 1, kb = tid & 1;
-            if ((rr < 64 && nk) || (rr >= 64 && nq)) {
-                uint4 u[8];
-                float ss = 0.f;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    u[c] = *reinterpret_cast<const uint4 *>(sKQ + kb * 16384 + rr * 128 + ((c ^ (rr & 7)) << 4));
-                    const __half2 *hp = reinterpret_cast<const __half2 *>(&u[c]);
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const float2 f = __half22float2(hp[w]);
-                        ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-                    }
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                const float inv = rsqrtf(ss + 1e-12f);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    __half2 *hp = reinterpret_cast<__half2 *>(&u[c]);
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const float2 f = __half22float2(hp[w]);
-                        hp[w] = __floats2half2_rn(f.x * inv, f.y * inv);
-                    }
-                    *reinterpret_cast<uint4 *>(sKQ + kb * 16384 + rr * 128 + ((c ^ (rr & 7)) << 4)) = u[c];
-                }
-            }
-        }
-        tc::fence_async_smem();
-        sync_tc();
-
-        // ---- I1: [K; Q] K^T (only the Q K^T half is read)
-        if (tid == 0) {
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t d = tc::desc_sw128(aKQ + (s >> 2) * 16384 + (s & 3) * 32);
-                tc::mma_f16(tI1, d, d, IDN64, s > 0);
-            }
-            tc::commit(bar);
-        }
-        if (RETR) {
-            // Ta = Tb diag(e^G) while I1 runs, 16 entries (two 16-byte chunks) per thread
-            const int r = tid >> 2, c2 = 2 * (tid & 3);
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                const int ch = c2 + w;
-                const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-                uint4 u = *reinterpret_cast<const uint4 *>(sTb + off);
-                __half2 *hp = reinterpret_cast<__half2 *>(&u);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __half22float2(hp[e]);
-                    hp[e] = __floats2half2_rn(f.x * sEG[8 * ch + 2 * e], f.y * sEG[8 * ch + 2 * e + 1]);
-                }
-                *reinterpret_cast<uint4 *>(sTa + off) = u;
-            }
-        }
-        ok = wait_mma(bar, phase, p.err);
-        if (ell >= 64) {
-            // P[r][j] = e^{G_r - G_j} q_r . k_j (j <= r)
-            float v[32];
-            tc::ld32(tI1 + lane_off + 32 * hc, v);
-            const int r = ell - 64;
-            const float Gr = sG[r];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = 32 * hc + jj;
-                v[jj] = j <= r ? __expf(Gr - sG[j]) * v[jj] : 0.f;
-            }
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) st_chunk(sP, r, 4 * hc + cc, v + 8 * cc);
-        }
-        // query rows -> e^{G_r} q_r in place (I1 has consumed the raw rows)
-        for (int idx = tid; idx < 64 * 16; idx += TC_THREADS) {
-            const int r = idx >> 4, ch = idx & 15, rr = 64 + r;
-            uint4 *ptr = reinterpret_cast<uint4 *>(sKQ + (ch >> 3) * 16384 + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4));
-            uint4 u = *ptr;
-            const float e = sEG[r];
-            __half2 *hp = reinterpret_cast<__half2 *>(&u);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                float2 f = __half22float2(hp[w]);
-                hp[w] = __floats2half2_rn(f.x * e, f.y * e);
-            }
-            *ptr = u;
-        }
-        tc::fence_async_smem();
-        sync_tc();
-
-        if (RETR) {
-            // ---- I2 (W^T = K^T Ta^T), C1a (V^T Tb^T), C2 (S Qh^T)
-            if (tid == 0) {
-                // W = Ta K: M = 64 tokens, N = 128 key channels (K as MN-major B)
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tW, tc::desc_sw128(aTa + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
-                                IDM64N128_BMN, s > 0);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tD, tc::desc_sw128(aV + s * 2048, 8192), tc::desc_sw128(aTb + s * 32), IDN64_AMN,
-                                s > 0);
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    tc::mma_f16(tO, tc::desc_sw128(aS + (s >> 2) * 16384 + (s & 3) * 32),
-                                tc::desc_sw128(aKQ + 8192 + (s >> 2) * 16384 + (s & 3) * 32), IDN64, s > 0);
-                tc::commit(bar);
-            }
-            ok = wait_mma(bar, phase, p.err) && ok;
-            {
-                // M = 64 result: token row r sits on lane 32 (r / 16) + r % 16
-                float v[32];
-                const int r = 16 * q4 + lane;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    tc::ld32(tW + lane_off + 64 * hc + 32 * hh, v);
-                    if (lane < 16) {
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) st_chunk(sW + hc * 8192, r, 4 * hh + cc, v + 8 * cc);
-                    }
-                }
-            }
-            tc::fence_async_smem();
-            sync_tc();
-            // ---- C1b: D^T += S (-W)^T
-            if (tid == 0) {
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    tc::mma_f16(tD, tc::desc_sw128(aS + (s >> 2) * 16384 + (s & 3) * 32),
-                                tc::desc_sw128(aW + (s >> 2) * 8192 + (s & 3) * 32), IDN64_NEGB, true);
-                tc::commit(bar);
-            }
-            ok = wait_mma(bar, phase, p.err) && ok;
-            {
-                float v[32], vs[32];
-                tc::ld32(tD + lane_off + 32 * hc, v);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) vs[jj] = v[jj] * sEGC[32 * hc + jj];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    st_chunk(sDT, ell, 4 * hc + cc, v + 8 * cc);
-                    st_chunk(sDTs, ell, 4 * hc + cc, vs + 8 * cc);
-                }
-            }
-            tc::fence_async_smem();
-            sync_tc();
-            // ---- C3 (O^T += D^T P^T) and C4 (X = DTs K)
-            if (tid == 0) {
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tO, tc::desc_sw128(aDT + s * 32), tc::desc_sw128(aP + s * 32), IDN64, true);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tX, tc::desc_sw128(aDTs + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
-                                IDN128_BMN, s > 0);
-                tc::commit(bar);
-            }
-        } else {
-            // rules without retrieval: D = V.  DTs = V^T diag(e^{G_C - G}) by hand.
-            {
-                const int i = ell;
-                float vs[32];
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * hc + jj;
-                    const __half hv = *reinterpret_cast<const __half *>(
-                        sV + (i >> 6) * 8192 + j * 128 + (((((i & 63) >> 3)) ^ (j & 7)) << 4) + (i & 7) * 2);
-                    vs[jj] = __half2float(hv) * sEGC[j];
-                }
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) st_chunk(sDTs, i, 4 * hc + cc, vs + 8 * cc);
-            }
-            tc::fence_async_smem();
-            sync_tc();
-            if (tid == 0) {
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    tc::mma_f16(tO, tc::desc_sw128(aS + (s >> 2) * 16384 + (s & 3) * 32),
-                                tc::desc_sw128(aKQ + 8192 + (s >> 2) * 16384 + (s & 3) * 32), IDN64, s > 0);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tO, tc::desc_sw128(aV + s * 2048, 8192), tc::desc_sw128(aP + s * 32), IDN64_AMN,
-                                true);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tX, tc::desc_sw128(aDTs + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
-                                IDN128_BMN, s > 0);
-                tc::commit(bar);
-            }
-        }
-        ok = wait_mma(bar, phase, p.err) && ok;
-
-        // ---- S <- e^{G_C} S + X;  O stores
-        {
-            const float eC = sEG[TC_C - 1];
-            float v[32];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                tc::ld32(tX + lane_off + 64 * hc + 32 * hh, v);
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) Sr[32 * hh + jj] = fmaf(eC, Sr[32 * hh + jj], v[jj]);
-            }
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) st_chunk(sS + hc * 16384, ell, ch, Sr + 8 * ch);
-            // O^T[i][r] -> staging tile O[r][i], then 16-byte row stores
-            tc::ld32(tO + lane_off + 32 * hc, v);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                reinterpret_cast<__half *>(sO)[(32 * hc + jj) * 128 + ell] = __float2half_rn(p.scale * v[jj]);
-        }
-        tc::fence_async_smem();
-        tc::fence_before();
-        ok = __syncthreads_and(ok) != 0;
-        {
-            const int r = tid >> 2, seg = tid & 3;
-            if (r < n) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(sO + r * 256 + seg * 64);
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.o) + ((size_t)(c0 + r) * p.Hv + h) * 128 +
-                                                       seg * 32);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) dst[w] = src[w];
-            }
-        }
-        tc::fence_async_smem();
-        tc::fence_before();
-    }
-
-    // ---- final state, then release tensor memory
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-        *reinterpret_cast<float4 *>(p.fin + srow + 4 * j) = make_float4(Sr[4 * j], Sr[4 * j + 1], Sr[4 * j + 2], Sr[4 * j + 3]);
-    sync_tc();
-    if (warp == 0) tc::tmem_dealloc(*tslot, TC_TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -1086,15 +679,17 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                 for (int jj = 0; jj < 32; ++jj) u[jj] += d[jj];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) st_chunk(sDT, i, 4 * hc + cc, u + 8 * cc);
-                const float eC = scal[fEG + TC_C - 1];
+                if (rule_has_decay(p.rule)) {
+                    const float eC = scal[fEG + TC_C - 1];
 #pragma unroll
-                for (int pc = 0; pc < 2; ++pc) {
-                    tc::ld32(lo + pS + 64 * hc + 32 * pc, d);
+                    for (int pc = 0; pc < 2; ++pc) {
+                        tc::ld32(lo + pS + 64 * hc + 32 * pc, d);
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) d[jj] *= eC;
-                    tc::st32(lo + pS + 64 * hc + 32 * pc, d);
+                        for (int jj = 0; jj < 32; ++jj) d[jj] *= eC;
+                        tc::st32(lo + pS + 64 * hc + 32 * pc, d);
+                    }
+                    tc::wait_st();
                 }
-                tc::wait_st();
             }
             tc::fence_async_smem();
             tc::fence_before();
@@ -1372,10 +967,13 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
 
 bool al16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-// workspace: chunk offsets (B + 1 ints, rounded up to 1 KB), then the Tb tiles
-size_t offs_bytes(const Problem &p) { return (((size_t)p.B + 1) * sizeof(int) + 1023) & ~(size_t)1023; }
 // slots for every chunk of pairwise disjoint requests: sum ceil(len / C) <= T / C + B
 int slot_capacity(const Problem &p) { return (int)((long long)p.T / TC_C + p.B + 1); }
+// workspace: chunk offsets (B + 1 ints) and the slot -> request table (one int per
+// slot), rounded up to 1 KB, then the Tb tiles
+size_t offs_bytes(const Problem &p) {
+    return (((size_t)p.B + 1 + (size_t)slot_capacity(p)) * sizeof(int) + 1023) & ~(size_t)1023;
+}
 
 }  // namespace
 
@@ -1439,10 +1037,6 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(chunked_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunked_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-        if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SV_SMEM);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunked_pipe_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PQ_SMEM);
@@ -1466,10 +1060,14 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     __half *tb = reinterpret_cast<__half *>(static_cast<unsigned char *>(ws) + offs_bytes(p));
     const int cap = slot_capacity(p);
     if (!make_map_tb(&tt, tb, (long long)cap * p.Hv * TC_C)) return cudaErrorInvalidValue;
-    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(p, offs);
+    int *slot_req = offs + p.B + 1;
+    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(p, offs, slot_req, cap);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunk_solve_kernel<<<dim3((unsigned)cap, (unsigned)p.Hv), SV_THREADS, SV_SMEM, stream>>>(p, tk, offs, tb, cap);
+    // persistent solver CTAs: three per SM (shared memory), at most one per task
+    const long long tasks = (long long)cap * p.Hv;
+    const long long sgrid = std::min<long long>(tasks, 3LL * sm_count());
+    chunk_solve_kernel<<<(unsigned)sgrid, SV_THREADS, SV_SMEM, stream>>>(p, tk, offs, slot_req, tb, cap);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     chunked_pipe_kernel<true><<<grid, PQ_THREADS, PQ_SMEM, stream>>>(p, tk, tq, tv, tt, offs, cap);

@@ -112,17 +112,20 @@ def test_chunked_rejects_unsupported_head_sizes():
 
 def test_chunked_workspace_size():
     """The tensor-core path of the delta rules asks for a workspace: chunk
-    offsets (B + 1 ints, rounded up to 1 KiB) and one 64 x 64 fp16 tile per
-    (chunk slot, value head), with T / 64 + B + 1 slots.  The rules without
-    retrieval and the other shapes need none."""
+    offsets (B + 1 ints) and a slot -> request table (one int per slot),
+    rounded up to 1 KiB, then one 64 x 64 fp16 tile per (chunk slot, value
+    head), with T / 64 + B + 1 slots.  The rules without retrieval and the
+    other shapes need none."""
     lib = N.load()
     size = lambda p: lib.gdn_chunked_prefill_workspace_size(ctypes.byref(p), 64)
     B, T, hv = 4, 4 * 8192, 16
+    slots = T // 64 + B + 1
+    meta = -(-(B + 1 + slots) * 4 // 1024) * 1024
     p = _problem(batch=B, total_tokens=T, num_heads_q=16, num_heads_v=hv, head_dim_k=128,
                  head_dim_v=128)
-    assert size(p) == 1024 + (T // 64 + B + 1) * hv * 64 * 64 * 2
+    assert size(p) == meta + slots * hv * 64 * 64 * 2
     p.rule, p.decay = N.RULES["delta"], None
-    assert size(p) == 1024 + (T // 64 + B + 1) * hv * 64 * 64 * 2
+    assert size(p) == meta + slots * hv * 64 * 64 * 2
     p.rule, p.beta = N.RULES["linear"], None
     assert size(p) == 0
     p.rule, p.decay = N.RULES["gated"], FAKE
