@@ -274,13 +274,20 @@ def kernel_name(p, path):
     if per_key:
         return "recurrent_long_kernel<%d>" % p["dk"]
     if p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16" and p["rule"] != "gdn2":
-        return "chunked_tc_kernel<%s>" % ("true" if p["rule"] in ("delta", "gated_delta") else "false")
+        return "chunked_pipe_kernel<%s>" % ("true" if p["rule"] in ("delta", "gated_delta") else "false")
     return "chunked_mma_kernel<%d,%s>" % (p["dk"], "true" if p["rule"] == "gdn2" else "false")
+
+
+def launches_per_call(p, path):
+    """Kernels one library call launches: the delta rules' tensor-core prefill
+    runs the chunk-offset scan and the per-chunk solves before the chain."""
+    k = kernel_name(p, path)
+    return 3 if k == "chunked_pipe_kernel<true>" else 1
 
 
 def kernel_source_digest(path, kernel=""):
     name = "recurrent.cu" if kernel.startswith("recurrent") else (
-        "chunked_tc.cu" if kernel.startswith("chunked_tc") else "chunked.cu")
+        "chunked_tc.cu" if kernel.startswith(("chunked_pipe", "chunk_solve")) else "chunked.cu")
     f = os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc", name)
     with open(f, "rb") as fh:
         return hashlib.sha256(fh.read()).hexdigest()[:16]
@@ -502,7 +509,7 @@ def main():
         "data": "synthetic (seeded, workloads.py)", "config": workload_config(p, args),
         "roofline": roof, "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call(p, path),
     }
     if rank == 0:
         if args.shrink > 1:

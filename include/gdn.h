@@ -212,11 +212,21 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  * fp32 accumulation; the state itself stays fp32 across chunks.
  * ("com.microsoft.GatedDeltaNet", Attributes, chunk_size: any value is
  * accepted and none changes the result beyond rounding; <= 0 selects 64.)
- * Extra constraints (GDN_ERR_UNSUPPORTED otherwise): dk and dv multiples of
- * 16 with dk <= 256, dv <= 256.  fp32 activations are rounded to fp16 for the
- * products.  `workspace` must hold gdn_chunked_prefill_workspace_size() bytes
- * (NULL allowed when that is 0), 256-byte aligned; GDN_ERR_WORKSPACE
- * otherwise.
+ * Extra constraints (GDN_ERR_UNSUPPORTED otherwise): dk in {16, 32, 64, 128},
+ * dv a multiple of 16 (<= 256), q, k, v, o and the state 16-byte aligned.
+ * fp32 activations are rounded to fp16 for the products.  Per-key decay runs
+ * the token-serial form (same result).
+ *
+ * Workspace: owned by the caller, device memory of at least
+ * gdn_chunked_prefill_workspace_size() bytes, 256-byte aligned (NULL allowed
+ * when that is 0); GDN_ERR_WORKSPACE otherwise.  It is non-zero for the delta
+ * rules with dk = dv = 128 and fp16 activations: per-request chunk offsets and
+ * a chunk-slot -> request table, then one fp16 64 x 64 tile of the solved
+ * per-chunk system per (chunk slot, value head), for T / 64 + B + 1 slots.
+ * Its contents are scratch, rewritten by every call on the stream; two calls
+ * in flight at once need two workspaces.  Requests that share tokens can need
+ * more slots than that; the ones past the capacity are skipped and
+ * GDN_DEVERR_OVERLAP is set.
  */
 gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *workspace,
                                size_t workspace_bytes, gdn_stream stream);
