@@ -17,7 +17,8 @@ FLAG_L2NORM_Q, FLAG_L2NORM_K, FLAG_BETA_SIGMOID, FLAG_DECAY_PER_KEY = 0x1, 0x2, 
 DEVERR_BAD_SLOT = 0x1
 
 EXPORTS = ("gdn_gate", "gdn_recurrent_step", "gdn_chunked_prefill_workspace_size",
-           "gdn_chunked_prefill", "gdn_status_string", "gdn_last_error_message")
+           "gdn_chunked_prefill", "gdn_chunked_prefill_noalloc", "gdn_status_string",
+           "gdn_last_error_message")
 
 _vp = ctypes.c_void_p
 
@@ -86,6 +87,8 @@ def load():
         lib.gdn_chunked_prefill.argtypes = [ctypes.POINTER(GdnProblem), ctypes.c_int32, _vp,
                                             ctypes.c_size_t, _vp]
         lib.gdn_chunked_prefill.restype = ctypes.c_int
+        lib.gdn_chunked_prefill_noalloc.argtypes = [ctypes.POINTER(GdnProblem), ctypes.c_int32, _vp]
+        lib.gdn_chunked_prefill_noalloc.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_last_error_message.argtypes = []

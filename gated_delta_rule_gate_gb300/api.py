@@ -154,3 +154,14 @@ def gdn_chunked_prefill(problem=None, chunk_size=64, workspace=None, *, stream=N
                                     _stream(stream)))
     problem._ws = workspace
     return problem
+
+
+def gdn_chunked_prefill_noalloc(problem=None, chunk_size=64, *, stream=None, **kw):
+    """gdn_chunked_prefill with the library's static per-device scratch
+    instead of a workspace: no device memory is allocated around the call.
+    Calls on one device must not overlap (they share the scratch); the first
+    call on a device must not be inside a stream capture."""
+    if problem is None:
+        problem = make_problem(**kw)
+    N.check(N.load().gdn_chunked_prefill_noalloc(ctypes.byref(problem), int(chunk_size), _stream(stream)))
+    return problem

@@ -37,6 +37,30 @@ gdn_status ok() {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Library-owned scratch of gdn_chunked_prefill_noalloc: one per device, set
+// aside when the module loads, so that entry point allocates nothing.  Every
+// call on a device shares it (see the header).
+constexpr size_t kNoAllocBytes = (size_t)72 << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Its address on the current device, looked up once per device (the first
+// call must not be inside a stream capture).
+cudaError_t noalloc_scratch(void **ptr) {
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
+
 size_t dtype_size(int dt) { return dt == GDN_DTYPE_F16 || dt == GDN_DTYPE_BF16 ? 2 : 4; }
 
 gdn_status check_dtype(int dt, const char *what) {
@@ -246,6 +270,25 @@ gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *w
         return fail(GDN_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
     if (d.B == 0) return ok();
     return cuda_status(gdn::launch_chunked(d, chunk_size, ws, ws_bytes, (cudaStream_t)stream));
+}
+
+gdn_status gdn_chunked_prefill_noalloc(const gdn_problem *p, int32_t chunk_size, gdn_stream stream) {
+    gdn::Problem d;
+    gdn_status st = validate(p, &d);
+    if (st != GDN_OK) return st;
+    const char *why = nullptr;
+    if (!gdn::chunked_supported(d, chunk_size, &why)) return fail(GDN_ERR_UNSUPPORTED, "chunked prefill: %s", why);
+    const size_t need = gdn::chunked_workspace_bytes(d, chunk_size);
+    if (need > kNoAllocBytes)
+        return fail(GDN_ERR_WORKSPACE, "needs %zu bytes of scratch, the library's static scratch holds %zu", need,
+                    kNoAllocBytes);
+    if (d.B == 0) return ok();
+    void *ws = nullptr;
+    if (need > 0) {
+        const cudaError_t e = noalloc_scratch(&ws);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return cuda_status(gdn::launch_chunked(d, chunk_size, ws, need, (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -231,6 +231,26 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
 gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *workspace,
                                size_t workspace_bytes, gdn_stream stream);
 
+/*
+ * gdn_chunked_prefill_noalloc -- gdn_chunked_prefill with the library's own
+ * scratch instead of a caller workspace.  None of the reference pages has a
+ * counterpart of this entry point; it exists for callers that cannot allocate
+ * device memory around the call.
+ *
+ * The scratch is one static device array of 72 MiB per device (set aside
+ * when libgdn loads; this entry point allocates nothing).  Problems whose
+ * gdn_chunked_prefill_workspace_size() exceeds it are rejected on the host
+ * with GDN_ERR_WORKSPACE before anything is enqueued (the long and ragged
+ * prefill configurations, about 68-70 MB, fit).  Every call on a device
+ * shares the array: two calls in flight at the same time on that device
+ * (different streams, threads or processes sharing the context) race on it,
+ * so the caller serialises them.  The first call on each device looks the
+ * array's address up (cudaGetSymbolAddress) and sets kernel attributes: make
+ * it outside any stream capture; later calls can be captured in a CUDA graph.
+ * Same arguments, constraints, results and error bits as gdn_chunked_prefill.
+ */
+gdn_status gdn_chunked_prefill_noalloc(const gdn_problem *p, int32_t chunk_size, gdn_stream stream);
+
 /* Static description of a status code ("ok", "invalid argument", ...). */
 const char *gdn_status_string(gdn_status status);
 
