@@ -279,10 +279,11 @@ def kernel_name(p, path):
 
 
 def launches_per_call(p, path):
-    """Kernels one library call launches: the delta rules' tensor-core prefill
-    runs the chunk-offset scan and the per-chunk solves before the chain."""
+    """Kernels one library call launches: the tensor-core prefill runs the
+    chunk-offset scan and the per-chunk pass (solves for the delta rules,
+    per-token factors for all) before the chain."""
     k = kernel_name(p, path)
-    return 3 if k == "chunked_pipe_kernel<true>" else 1
+    return 3 if k.startswith("chunked_pipe_kernel") else 1
 
 
 def kernel_source_digest(path, kernel=""):

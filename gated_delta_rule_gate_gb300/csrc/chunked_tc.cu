@@ -33,6 +33,7 @@ namespace {
 constexpr int TC_C = 64;  // tokens per chunk
 constexpr int TC_TMEM_COLS = 512;
 constexpr int kTbBytes = TC_C * TC_C * 2;  // one fp16 Tb tile
+constexpr int kFacFloats = 2 * TC_C;       // per (chunk, head): G and 1 / |k| of the 64 tokens
 
 constexpr uint32_t kLandBytes = 3 * 16384;  // K, Q and V boxes of one chunk
 
@@ -124,9 +125,10 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *off
 // ahead of the solvers (request lookup, the gates in fp32, the key tile by
 // TMA) into two buffers; four solver warps run the product, the system and
 // its solve.  Waits are bounded.
+template <bool RETR>
 __global__ void __launch_bounds__(SV_THREADS) chunk_solve_kernel(Problem p, const __grid_constant__ CUtensorMap tmK,
                                                                  const int *offs, const int *slot_req, __half *tb,
-                                                                 int cap) {
+                                                                 float *fac, int cap) {
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
     unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
@@ -181,8 +183,10 @@ __global__ void __launch_bounds__(SV_THREADS) chunk_solve_kernel(Problem p, cons
                         g = ld_any(p.decay, th, p.decay_f16);
                         if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[h]);
                     }
-                    bt = ld_any(p.beta, th, p.beta_f16);
-                    if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
+                    if (RETR) {
+                        bt = ld_any(p.beta, th, p.beta_f16);
+                        if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
+                    }
                 }
                 g2[tt] = g;
                 g2[64 + tt] = bt;
@@ -255,6 +259,18 @@ __global__ void __launch_bounds__(SV_THREADS) chunk_solve_kernel(Problem p, cons
             tc::fence_async_smem();
             tc::fence_before();
             ptx::named_bar_sync(1, SV_SOLVERS);
+            {
+                // the chunk's per-token factors for the chain kernel: G (cumulative log
+                // decay) and 1 / |k|
+                float *fd = fac + ((size_t)slot * p.Hv + h) * kFacFloats;
+                fd[tid] = tid < 64 ? sG[tid] : sInv[tid - 64];
+            }
+            if (!RETR) {
+                // no system to solve: the key tile and gate buffer are free again
+                ptx::named_bar_sync(1, SV_SOLVERS);
+                if (tid == 0) ptx::mbar_arrive(&empty[bf]);
+                continue;
+            }
             if (tid == 0) {
                 tc::fence_after();
                 // K K^T: M = 64 tokens, N = 64 tokens, K = 128 channels
@@ -448,7 +464,7 @@ constexpr int qV = 65536;     // 2 x 16 KB: V landing tiles (MN-major V^T operan
 constexpr int qTb = 98304;    // 2 x 8 KB: Tb tiles
 constexpr int qPK = 114688;   // 2 x 24 KB: MN-major blocks [64 j][64]: P^T, Kt (d < 64), Kt (d >= 64)
 constexpr int qTa = 163840;   // 8 KB
-constexpr int qDT = 172032;   // 16 KB: D^T [128 i][64 j]; output staging after C34
+constexpr int qDT = 172032;   // 16 KB: D^T [128 i][64 j]
 constexpr int qS = 188416;    // 32 KB: fp16 mirror of the state
 constexpr int qSc = 221184;   // 3 slots (chunk % 3) of per-token factors, 7 x 64 fp32 each
 constexpr int kScal = 7 * 64 * 4;
@@ -456,10 +472,11 @@ constexpr int qBar = qSc + 3 * kScal;  // mbarriers, TMEM address
 constexpr int PQ_SMEM = qBar + 256 + 1024;
 // tensor memory columns
 constexpr uint32_t pU = 0, pD = 64, pO = 128, pS = 192, pI1 = 320, pW = 384;
-// per-token factors of one chunk (offsets in floats): G (cumulative log decay), e^G,
-// KF = e^{G_C - G} / |k| (rows of Kt), TF = -e^G / |k| (columns of Ta), QF = scale e^G / |q|
-// (rows of Qh), QS = scale / |q| (columns of P^T), IK = 1 / |k| (rows of P^T)
-constexpr int fG = 0, fEG = 64, fKF = 128, fTF = 192, fQF = 256, fQS = 320, fIK = 384;
+// per-token factors of one chunk (offsets in floats): G (cumulative log decay) and IK = 1 / |k|
+// as the solve kernel wrote them (one bulk copy), then e^G, KF = e^{G_C - G} / |k| (rows of Kt),
+// TF = -e^G / |k| (columns of Ta), QF = scale e^G / |q| (rows of Qh), QS = scale / |q|
+// (columns of P^T)
+constexpr int fG = 0, fIK = 64, fEG = 128, fKF = 192, fTF = 256, fQF = 320, fQS = 384;
 
 // byte offset of 16-byte chunk `ch` of row `r` in a 128-byte-swizzled block
 __device__ __forceinline__ int sw(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
@@ -507,7 +524,7 @@ template <bool RETR>
 __global__ void __launch_bounds__(PQ_THREADS, 1)
     chunked_pipe_kernel(Problem p, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmT,
-                        const int *offs, int cap) {
+                        const int *offs, const float *fac, int cap) {
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
     unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
@@ -515,7 +532,8 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     uint64_t *land = bars + 0;    // [2] TMA landed
     uint64_t *barU = bars + 2;    // U^T = V^T Tb^T done
     uint64_t *prepA = bars + 3;   // operands of K Q^T, W and U ready (one phase per chunk)
-    uint64_t *prepB = bars + 4;   // [2] -W, Qh, P^T, Kt ready
+    uint64_t *prepB = bars + 4;   // [2] -W and Qh ready (C12's operands)
+    uint64_t *prepC = bars + 11;  // [2] P^T and Kt ready (C34's operands)
     uint64_t *barPM = bars + 6;   // [2] K Q^T and W done
     uint64_t *barD = bars + 8;    // C12 done
     uint64_t *barX = bars + 9;    // [2] C34 done
@@ -531,7 +549,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     const int qh = (int)((long long)h * p.Hq / p.Hv);
     const int nch = (t1 - t0 + TC_C - 1) / TC_C;
     int slot0 = 0;
-    if (RETR && nch > 0) {
+    if (nch > 0) {
         slot0 = offs[b];
         if (slot0 + nch > cap) {
             // only overlapping requests can outgrow the workspace: skip this one
@@ -550,7 +568,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     }
 
     if (tid == 0) {
-        for (int i = 0; i < 11; ++i) ptx::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 13; ++i) ptx::mbar_init(&bars[i], 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(tslot, TC_TMEM_COLS);
@@ -562,7 +580,10 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
     const uint32_t aS = ptx::smem_u32(sS), aTa = ptx::smem_u32(sTa), aDT = ptx::smem_u32(sDT);
     auto tma = [&](int c) {
         const int bf = c & 1;
-        ptx::mbar_arrive_expect_tx(&land[bf], kLandBytes + (RETR ? (uint32_t)kTbBytes : 0u));
+        ptx::mbar_arrive_expect_tx(&land[bf], kLandBytes + kFacFloats * 4 + (RETR ? (uint32_t)kTbBytes : 0u));
+        // the chunk's G and 1 / |k| into the factor slot of chunk c
+        ptx::bulk_g2s(sm + qSc + (c % 3) * kScal, fac + ((size_t)(slot0 + c) * p.Hv + h) * kFacFloats,
+                      kFacFloats * 4, &land[bf]);
         unsigned char *kq = sm + qKQ + bf * 32768, *vt = sm + qV + bf * 16384;
         const int c0 = t0 + TC_C * c;
 #pragma unroll
@@ -622,14 +643,17 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
         return true;
     };
     // C34: [O^T | S] += D^T [P^T | Kt]   (B MN-major: three 64-wide blocks)
-    auto c34 = [&](int c) {
+    auto c34 = [&](int c) -> bool {
         const int bf = c & 1;
+        if (!ptx::mbar_wait_sleep(&prepC[bf], (c >> 1) & 1)) return false;
+        tc::fence_after();
         const uint32_t aPK = ptx::smem_u32(sm + qPK + bf * 24576);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
             tc::mma_f16(tmem + pO, tc::desc_sw128(aDT + s * 32), tc::desc_sw128(aPK + s * 2048, 8192),
                         tc::idesc_f16(128, 192, false, true), true);
         tc::commit(&barX[bf]);
+        return true;
     };
 
     if (warp < 8) {
@@ -696,10 +720,10 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
             ptx::named_bar_sync(1, 256);
             if (ct == 0) {
                 tc::fence_after();
-                c34(c);
+                ok = c34(c);
                 // chunk c's landing buffer is free: C12, U and the preparation have run
                 if (c + 2 < nch) tma(c + 2);
-                if (c + 1 < nch) ok = u_product(c + 1);
+                if (c + 1 < nch) ok = ok && u_product(c + 1);
             }
             // ---- C34 done: mirror the state, read O^T, start C12 of the next chunk
             ok = ptx::named_bar_and(1, 256, ok && ptx::mbar_wait_sleep(&barX[bf], (c >> 1) & 1));
@@ -720,20 +744,14 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
             tc::fence_before();
             ptx::named_bar_sync(1, 256);
             if (ct == 0 && c + 1 < nch) ok = c12(c + 1);
-            // ---- outputs of chunk c: O^T[i][r] -> staging O[r][i] -> 16-byte row stores
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                reinterpret_cast<__half *>(sDT)[(32 * hc + jj) * 128 + i] = __float2half_rn(o[jj]);
-            ptx::named_bar_sync(1, 256);
+            // ---- outputs of chunk c: O^T[i][r] straight to O[r][i] (a warp writes 64 contiguous
+            // bytes of each token row)
             {
-                const int r = ct >> 2, seg = ct & 3;
-                if (r < n) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(sDT + r * 256 + seg * 64);
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(p.o) +
-                                                           ((size_t)(t0 + TC_C * c + r) * p.Hv + h) * 128 + seg * 32);
+                __half *orow = static_cast<__half *>(p.o) + ((size_t)(t0 + TC_C * c + 32 * hc) * p.Hv + h) * 128 + i;
+                const size_t rstride = (size_t)p.Hv * 128;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) dst[w] = src[w];
-                }
+                for (int jj = 0; jj < 32; ++jj)
+                    if (32 * hc + jj < n) orow[jj * rstride] = __float2half_rn(o[jj]);
             }
         }
         if (!ok && p.err && ct == 0) atomicOr(p.err, 2);
@@ -750,15 +768,14 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
         }
     } else if (warp < 16) {
         // ===================== next-chunk preparation (256 threads)
-        // The key and query tiles stay as loaded; the L2 norms, decays and the output
-        // scale enter through per-token factors: Kt rows, Ta columns (which also carry
-        // the sign of -W), Qh rows and the rows / columns of P^T.
+        // The key and query tiles stay as loaded.  The decays, the L2 norms and the
+        // output scale enter through per-token factors (the solve kernel supplies G and
+        // 1 / |k|): Kt rows, Ta columns (which also carry the sign of -W), Qh rows and
+        // the rows / columns of P^T.  Two signals per chunk: C12's operands (-W, Qh),
+        // then C34's (P^T; Kt is written earlier).
         const int pt = tid - 256, pw = warp - 8, pq = pw & 3, ph = pw >> 2;
         const uint32_t lo = tmem + ((uint32_t)(32 * pq) << 16);
-        const bool has_decay = rule_has_decay(p.rule);
-        const bool nk = (p.flags & kL2k) != 0, nq = (p.flags & kL2q) != 0;
-        const float gsc = (has_decay && p.raw_gate) ? p.gate_scale[h] : 0.f;
-        const float gbi = (has_decay && p.raw_gate) ? p.gate_bias[h] : 0.f;
+        const bool nq = (p.flags & kL2q) != 0;
         if (!RETR) {
             // Tb = I (U^T = V^T), in both buffers, once
 #pragma unroll
@@ -770,14 +787,6 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                 st_chunk(sm + qTb + bf * kTbBytes, r, ch, x);
             }
         }
-        // raw gate bits of the next chunk, converted only when used (the load is not waited on early)
-        uint32_t graw = 0u;
-        auto gload = [&](int t) -> uint32_t {
-            const size_t th = (size_t)t * p.Hv + h;
-            return p.decay_f16 ? (uint32_t) reinterpret_cast<const unsigned short *>(p.decay)[th]
-                               : reinterpret_cast<const uint32_t *>(p.decay)[th];
-        };
-        if (has_decay && pt < TC_C && pt < t1 - t0) graw = gload(t0 + pt);
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
             const int bf = c & 1;
@@ -785,32 +794,7 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
             unsigned char *sKQ = sm + qKQ + bf * 32768, *sV = sm + qV + bf * 16384;
             unsigned char *sTb = sm + qTb + bf * kTbBytes, *sPK = sm + qPK + bf * 24576;
             float *F = reinterpret_cast<float *>(sm + qSc + (c % 3) * kScal);
-            // gates of chunk c (raw values were loaded one chunk ahead)
-            if (pt < TC_C) {
-                float g = 0.f;
-                if (has_decay && pt < n) {
-                    const float a = p.decay_f16 ? __half2float(__ushort_as_half((unsigned short)graw))
-                                                : __uint_as_float(graw);
-                    g = p.raw_gate ? gsc * softplus_f(a + gbi) : a;
-                }
-                F[fG + pt] = g;
-                graw = 0u;
-                if (has_decay && c0 + TC_C + pt < t1) graw = gload(c0 + TC_C + pt);
-            }
-            ptx::named_bar_sync(2, kPrep);
-            if (pw == 0) {
-                const float g0 = F[fG + 2 * lane], g1 = F[fG + 2 * lane + 1];
-                float sacc = g0 + g1;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, sacc, o);
-                    if (lane >= o) sacc += y;
-                }
-                const float G1 = sacc, G0 = sacc - g1;
-                F[fG + 2 * lane] = G0, F[fG + 2 * lane + 1] = G1;
-                F[fEG + 2 * lane] = __expf(G0), F[fEG + 2 * lane + 1] = __expf(G1);
-            }
-            // PK[bf] was last read by C34 of chunk c - 2
+            // landed (tiles and factors); PK[bf] was last read by C34 of chunk c - 2
             bool okw = ptx::mbar_wait_sleep(&land[bf], (c >> 1) & 1);
             if (c >= 2) okw = okw && ptx::mbar_wait_sleep(&barX[bf], ((c - 2) >> 1) & 1);
             ok = ptx::named_bar_and(2, kPrep, okw);
@@ -823,20 +807,17 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                                                      : sKQ + (ch >> 3) * 16384 + (which == 1 ? 8192 : 0);
                     *reinterpret_cast<uint4 *>(base + sw(r, ch & 7)) = make_uint4(0, 0, 0, 0);
                 }
-                ptx::named_bar_sync(2, kPrep);
             }
-            {
-                // four threads per row, four chunks each
+            if (nq) {
+                // 1 / |q_r|, four threads per query row (kept in QS until the factors below)
+                ptx::named_bar_sync(2, kPrep);
                 const int r = pt >> 2, part = pt & 3;
-                const float eGC = __expf(F[fG + TC_C - 1] - F[fG + r]);  // e^{G_C - G_r} (<= 1)
-                // key rows: 1 / |k_r|, and Kt = e^{G_C - G_r} k_r / |k_r| into PK blocks 1 and 2
-                uint4 u[4];
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
                     const int ch = 4 * part + w;
-                    u[w] = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(r, ch & 7));
-                    const __half2 *hp = reinterpret_cast<const __half2 *>(&u[w]);
+                    const uint4 uq = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(64 + r, ch & 7));
+                    const __half2 *hp = reinterpret_cast<const __half2 *>(&uq);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 f = __half22float2(hp[e]);
@@ -847,42 +828,17 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                 float ss = s0 + s1;
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                 ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                const float ik = nk ? rsqrtf(ss + 1e-12f) : 1.f;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int ch = 4 * part + w;
-                    *reinterpret_cast<uint4 *>(sPK + 8192 + (ch >> 3) * 8192 + sw(r, ch & 7)) =
-                        scale_chunk(u[w], eGC * ik);
-                }
-                if (part == 0) {
-                    F[fIK + r] = ik;
-                    F[fTF + r] = -F[fEG + r] * ik;
-                }
-                // query rows: 1 / |q_r| (when asked for)
-                float iq = 1.f;
-                if (nq) {
-                    s0 = s1 = 0.f;
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const int ch = 4 * part + w;
-                        const uint4 uq = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(64 + r, ch & 7));
-                        const __half2 *hp = reinterpret_cast<const __half2 *>(&uq);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __half22float2(hp[e]);
-                            s0 = fmaf(f.x, f.x, s0);
-                            s1 = fmaf(f.y, f.y, s1);
-                        }
-                    }
-                    ss = s0 + s1;
-                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                    iq = rsqrtf(ss + 1e-12f);
-                }
-                if (part == 0) {
-                    F[fQF + r] = p.scale * F[fEG + r] * iq;
-                    F[fQS + r] = p.scale * iq;
-                }
+                if (part == 0) F[fQS + r] = rsqrtf(ss + 1e-12f);
+                ptx::named_bar_sync(2, kPrep);
+            }
+            if (pt < TC_C) {
+                const float G = F[fG + pt], ik = F[fIK + pt], eg = __expf(G);
+                const float iq = nq ? F[fQS + pt] : 1.f;
+                F[fEG + pt] = eg;
+                F[fKF + pt] = __expf(F[fG + TC_C - 1] - G) * ik;  // e^{G_C - G} <= 1
+                F[fTF + pt] = -eg * ik;
+                F[fQF + pt] = p.scale * eg * iq;
+                F[fQS + pt] = p.scale * iq;
             }
             ptx::named_bar_sync(2, kPrep);
             if (RETR) {
@@ -903,44 +859,32 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
                 prep_mma(c);
                 ptx::mbar_arrive(prepA);
             }
-            // ---- K Q^T and W = Ta K done
+            // Kt[j][d] = e^{G_C - G_j} k_j[d] / |k_j| into PK blocks 1 and 2, while those run
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int idx = pt + kPrep * w, j = idx >> 4, ch = idx & 15;
+                const uint4 u = *reinterpret_cast<const uint4 *>(sKQ + (ch >> 3) * 16384 + sw(j, ch & 7));
+                *reinterpret_cast<uint4 *>(sPK + 8192 + (ch >> 3) * 8192 + sw(j, ch & 7)) = scale_chunk(u, F[fKF + j]);
+            }
+            // ---- K Q^T and W = Ta K done (and every thread is past its Kt rows)
             ok = ptx::named_bar_and(2, kPrep, ptx::mbar_wait_sleep(&barPM[bf], (c >> 1) & 1));
             if (!ok) break;
             tc::fence_after();
-            {
-                // M = 64 results: rows 16 pq .. 16 pq + 15 sit on lanes 32 pq .. 32 pq + 15; the
-                // 16x256b shape spreads them over the warp: rows ja, ja + 8, column pairs 2 (lane % 4)
-                const int ja = 16 * pq + (lane >> 2), jb = ja + 8, cp = 2 * (lane & 3);
-                // P^T[j][r] = scale e^{G_r - G_j} k_j . q_r / (|k_j| |q_r|) for r >= j
-                {
-                    float v[16];
-                    tc::ld16x256<4>(lo + pI1 + 32 * ph, v);
-                    const float Ga = F[fG + ja], Gb = F[fG + jb], ka = F[fIK + ja], kb = F[fIK + jb];
+            // M = 64 results: rows 16 pq .. 16 pq + 15 sit on lanes 32 pq .. 32 pq + 15; the
+            // 16x256b shape spreads them over the warp: rows ja, ja + 8, column pairs 2 (lane % 4)
+            const int ja = 16 * pq + (lane >> 2), jb = ja + 8, cp = 2 * (lane & 3);
+            float vp[16];
+            tc::ld16x256<4>(lo + pI1 + 32 * ph, vp);
+            if (RETR) {
+                // -W over the key rows: columns [64 ph, 64 ph + 64) = key block ph
+                float v[32];
+                tc::ld16x256<8>(lo + pW + 64 * ph, v);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int r0 = 32 * ph + 8 * k + cp;
-                        const float2 g = *reinterpret_cast<const float2 *>(F + fG + r0);
-                        const float2 qs = *reinterpret_cast<const float2 *>(F + fQS + r0);
-                        const float a0 = r0 >= ja ? __expf(g.x - Ga) * ka * qs.x * v[4 * k] : 0.f;
-                        const float a1 = r0 + 1 >= ja ? __expf(g.y - Ga) * ka * qs.y * v[4 * k + 1] : 0.f;
-                        const float b0 = r0 >= jb ? __expf(g.x - Gb) * kb * qs.x * v[4 * k + 2] : 0.f;
-                        const float b1 = r0 + 1 >= jb ? __expf(g.y - Gb) * kb * qs.y * v[4 * k + 3] : 0.f;
-                        const int ch = 4 * ph + k;
-                        *reinterpret_cast<uint32_t *>(sPK + sw(ja, ch) + 2 * cp) = ptx::pack_h2(a0, a1);
-                        *reinterpret_cast<uint32_t *>(sPK + sw(jb, ch) + 2 * cp) = ptx::pack_h2(b0, b1);
-                    }
-                }
-                if (RETR) {
-                    // -W over the key rows: columns [64 ph, 64 ph + 64) = key block ph
-                    float v[32];
-                    tc::ld16x256<8>(lo + pW + 64 * ph, v);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        *reinterpret_cast<uint32_t *>(sKQ + ph * 16384 + sw(ja, k) + 2 * cp) =
-                            ptx::pack_h2(v[4 * k], v[4 * k + 1]);
-                        *reinterpret_cast<uint32_t *>(sKQ + ph * 16384 + sw(jb, k) + 2 * cp) =
-                            ptx::pack_h2(v[4 * k + 2], v[4 * k + 3]);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    *reinterpret_cast<uint32_t *>(sKQ + ph * 16384 + sw(ja, k) + 2 * cp) =
+                        ptx::pack_h2(v[4 * k], v[4 * k + 1]);
+                    *reinterpret_cast<uint32_t *>(sKQ + ph * 16384 + sw(jb, k) + 2 * cp) =
+                        ptx::pack_h2(v[4 * k + 2], v[4 * k + 3]);
                 }
             }
 #pragma unroll
@@ -956,6 +900,27 @@ __global__ void __launch_bounds__(PQ_THREADS, 1)
             tc::fence_before();
             ptx::named_bar_sync(2, kPrep);
             if (pt == 0) ptx::mbar_arrive(&prepB[bf]);
+            {
+                // P^T[j][r] = scale e^{G_r - G_j} k_j . q_r / (|k_j| |q_r|) for r >= j
+                const float Ga = F[fG + ja], Gb = F[fG + jb], ka = F[fIK + ja], kb = F[fIK + jb];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r0 = 32 * ph + 8 * k + cp;
+                    const float2 g = *reinterpret_cast<const float2 *>(F + fG + r0);
+                    const float2 qs = *reinterpret_cast<const float2 *>(F + fQS + r0);
+                    const float a0 = r0 >= ja ? __expf(g.x - Ga) * ka * qs.x * vp[4 * k] : 0.f;
+                    const float a1 = r0 + 1 >= ja ? __expf(g.y - Ga) * ka * qs.y * vp[4 * k + 1] : 0.f;
+                    const float b0 = r0 >= jb ? __expf(g.x - Gb) * kb * qs.x * vp[4 * k + 2] : 0.f;
+                    const float b1 = r0 + 1 >= jb ? __expf(g.y - Gb) * kb * qs.y * vp[4 * k + 3] : 0.f;
+                    const int ch = 4 * ph + k;
+                    *reinterpret_cast<uint32_t *>(sPK + sw(ja, ch) + 2 * cp) = ptx::pack_h2(a0, a1);
+                    *reinterpret_cast<uint32_t *>(sPK + sw(jb, ch) + 2 * cp) = ptx::pack_h2(b0, b1);
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(2, kPrep);
+            if (pt == 0) ptx::mbar_arrive(&prepC[bf]);
         }
         if (!ok && p.err && pt == 0) atomicOr(p.err, 2);
     }
@@ -983,9 +948,13 @@ bool chunked_tc_eligible(const Problem &p) {
            al16(p.q) && al16(p.k) && al16(p.v) && al16(p.fin) && (p.init == nullptr || al16(p.init));
 }
 
+// workspace: [offsets | slot table] [Tb tiles (delta rules)] [per-chunk factors]
+size_t tb_bytes(const Problem &p) {
+    return rule_has_retrieval(p.rule) ? (size_t)slot_capacity(p) * p.Hv * kTbBytes : 0;
+}
 size_t chunked_tc_workspace_bytes(const Problem &p) {
-    if (!rule_has_retrieval(p.rule) || p.B == 0) return 0;
-    return offs_bytes(p) + (size_t)slot_capacity(p) * p.Hv * kTbBytes;
+    if (p.B == 0) return 0;
+    return offs_bytes(p) + tb_bytes(p) + (size_t)slot_capacity(p) * p.Hv * kFacFloats * 4;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1037,7 +1006,9 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(chunk_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SV_SMEM);
+        e = cudaFuncSetAttribute(chunk_solve_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SV_SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunk_solve_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SV_SMEM);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunked_pipe_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PQ_SMEM);
         if (e != cudaSuccess) return e;
@@ -1050,27 +1021,36 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)((long long)p.B * p.Hv);
     if (grid == 0) return cudaSuccess;
-    if (!rule_has_retrieval(p.rule)) {
-        tt = tk;  // unused without retrieval
-        chunked_pipe_kernel<false><<<grid, PQ_THREADS, PQ_SMEM, stream>>>(p, tk, tq, tv, tt, nullptr, 0);
-        return cudaGetLastError();
-    }
     if (ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
+    const bool retr = rule_has_retrieval(p.rule);
     int *offs = static_cast<int *>(ws);
-    __half *tb = reinterpret_cast<__half *>(static_cast<unsigned char *>(ws) + offs_bytes(p));
-    const int cap = slot_capacity(p);
-    if (!make_map_tb(&tt, tb, (long long)cap * p.Hv * TC_C)) return cudaErrorInvalidValue;
     int *slot_req = offs + p.B + 1;
+    unsigned char *wsb = static_cast<unsigned char *>(ws);
+    __half *tb = reinterpret_cast<__half *>(wsb + offs_bytes(p));
+    float *fac = reinterpret_cast<float *>(wsb + offs_bytes(p) + tb_bytes(p));
+    const int cap = slot_capacity(p);
+    if (retr) {
+        if (!make_map_tb(&tt, tb, (long long)cap * p.Hv * TC_C)) return cudaErrorInvalidValue;
+    } else {
+        tt = tk;  // unused without retrieval
+    }
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(p, offs, slot_req, cap);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // persistent solver CTAs: three per SM (shared memory), at most one per task
     const long long tasks = (long long)cap * p.Hv;
     const long long sgrid = std::min<long long>(tasks, 3LL * sm_count());
-    chunk_solve_kernel<<<(unsigned)sgrid, SV_THREADS, SV_SMEM, stream>>>(p, tk, offs, slot_req, tb, cap);
+    if (retr)
+        chunk_solve_kernel<true><<<(unsigned)sgrid, SV_THREADS, SV_SMEM, stream>>>(p, tk, offs, slot_req, tb, fac, cap);
+    else
+        chunk_solve_kernel<false><<<(unsigned)sgrid, SV_THREADS, SV_SMEM, stream>>>(p, tk, offs, slot_req, tb, fac,
+                                                                                   cap);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunked_pipe_kernel<true><<<grid, PQ_THREADS, PQ_SMEM, stream>>>(p, tk, tq, tv, tt, offs, cap);
+    if (retr)
+        chunked_pipe_kernel<true><<<grid, PQ_THREADS, PQ_SMEM, stream>>>(p, tk, tq, tv, tt, offs, fac, cap);
+    else
+        chunked_pipe_kernel<false><<<grid, PQ_THREADS, PQ_SMEM, stream>>>(p, tk, tq, tv, tt, offs, fac, cap);
     return cudaGetLastError();
 }
 
