@@ -274,21 +274,21 @@ def kernel_name(p, path):
     if per_key:
         return "recurrent_long_kernel<%d>" % p["dk"]
     if p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16" and p["rule"] != "gdn2":
-        return "chunked_pipe_kernel<%s>" % ("true" if p["rule"] in ("delta", "gated_delta") else "false")
+        return "chunk_chain_kernel<%s>" % ("false" if p["rule"] == "linear" else "true")
     return "chunked_mma_kernel<%d,%s>" % (p["dk"], "true" if p["rule"] == "gdn2" else "false")
 
 
 def launches_per_call(p, path):
     """Kernels one library call launches: the tensor-core prefill runs the
-    chunk-offset scan and the per-chunk pass (solves for the delta rules,
-    per-token factors for all) before the chain."""
+    chunk-offset scan and the per-chunk operand pass (with the triangular
+    solves for the delta rules) before the chain."""
     k = kernel_name(p, path)
-    return 3 if k.startswith("chunked_pipe_kernel") else 1
+    return 3 if k.startswith("chunk_chain_kernel") else 1
 
 
 def kernel_source_digest(path, kernel=""):
     name = "recurrent.cu" if kernel.startswith("recurrent") else (
-        "chunked_tc.cu" if kernel.startswith(("chunked_pipe", "chunk_solve")) else "chunked.cu")
+        "chunked_tc.cu" if kernel.startswith(("chunk_chain", "chunk_prepare")) else "chunked.cu")
     f = os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc", name)
     with open(f, "rb") as fh:
         return hashlib.sha256(fh.read()).hexdigest()[:16]

@@ -40,7 +40,7 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Library-owned scratch of gdn_chunked_prefill_noalloc: one per device, set
 // aside when the module loads, so that entry point allocates nothing.  Every
 // call on a device shares it (see the header).
-constexpr size_t kNoAllocBytes = (size_t)72 << 20;
+constexpr size_t kNoAllocBytes = (size_t)768 << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 // Its address on the current device, looked up once per device (the first

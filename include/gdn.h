@@ -219,10 +219,12 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  *
  * Workspace: owned by the caller, device memory of at least
  * gdn_chunked_prefill_workspace_size() bytes, 256-byte aligned (NULL allowed
- * when that is 0); GDN_ERR_WORKSPACE otherwise.  It is non-zero for the delta
- * rules with dk = dv = 128 and fp16 activations: per-request chunk offsets and
- * a chunk-slot -> request table, then one fp16 64 x 64 tile of the solved
- * per-chunk system per (chunk slot, value head), for T / 64 + B + 1 slots.
+ * when that is 0); GDN_ERR_WORKSPACE otherwise.  It is non-zero for every rule
+ * with dk = dv = 128, fp16 activations and no per-key decay (the tensor-core
+ * path), and 0 otherwise.  Layout, for T / 64 + B + 1 chunk slots:
+ * per-request chunk offsets, a chunk-slot -> request table and the requests
+ * ordered by length (rounded up to 1 KB); then one 88 KB image per (chunk
+ * slot, value head) of the chunk's state-independent operands (fp16).
  * Its contents are scratch, rewritten by every call on the stream; two calls
  * in flight at once need two workspaces.  Requests that share tokens can need
  * more slots than that; the ones past the capacity are skipped and
@@ -237,11 +239,11 @@ gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *w
  * counterpart of this entry point; it exists for callers that cannot allocate
  * device memory around the call.
  *
- * The scratch is one static device array of 72 MiB per device (set aside
+ * The scratch is one static device array of 768 MiB per device (set aside
  * when libgdn loads; this entry point allocates nothing).  Problems whose
  * gdn_chunked_prefill_workspace_size() exceeds it are rejected on the host
  * with GDN_ERR_WORKSPACE before anything is enqueued (the long and ragged
- * prefill configurations, about 68-70 MB, fit).  Every call on a device
+ * prefill configurations, about 745-765 MB, fit).  Every call on a device
  * shares the array: two calls in flight at the same time on that device
  * (different streams, threads or processes sharing the context) race on it,
  * so the caller serialises them.  The first call on each device looks the

@@ -112,26 +112,25 @@ def test_chunked_rejects_unsupported_head_sizes():
 
 def test_chunked_workspace_size():
     """The tensor-core path (dk = dv = 128, fp16) asks for a workspace: chunk
-    offsets (B + 1 ints) and a slot -> request table (one int per slot),
-    rounded up to 1 KiB; for the delta rules one 64 x 64 fp16 tile per (chunk
-    slot, value head); then 128 fp32 per-token factors per (chunk slot, value
-    head); with T / 64 + B + 1 slots.  The other shapes need none."""
+    offsets (B + 1 ints), a slot -> request table (one int per slot) and the
+    request order (B ints), rounded up to 1 KiB; then one 88 KiB operand image
+    per (chunk slot, value head), with T / 64 + B + 1 slots, for every rule.
+    The other shapes need none."""
     lib = N.load()
     size = lambda p: lib.gdn_chunked_prefill_workspace_size(ctypes.byref(p), 64)
     B, T, hv = 4, 4 * 8192, 16
     slots = T // 64 + B + 1
-    meta = -(-(B + 1 + slots) * 4 // 1024) * 1024
-    factors = slots * hv * 128 * 4
-    tb = slots * hv * 64 * 64 * 2
+    head = -(-(2 * B + 1 + slots) * 4 // 1024) * 1024
+    images = slots * hv * 88 * 1024
     p = _problem(batch=B, total_tokens=T, num_heads_q=16, num_heads_v=hv, head_dim_k=128,
                  head_dim_v=128)
-    assert size(p) == meta + tb + factors
+    assert size(p) == head + images
     p.rule, p.decay = N.RULES["delta"], None
-    assert size(p) == meta + tb + factors
+    assert size(p) == head + images
     p.rule, p.beta = N.RULES["linear"], None
-    assert size(p) == meta + factors
+    assert size(p) == head + images
     p.rule, p.decay = N.RULES["gated"], FAKE
-    assert size(p) == meta + factors
+    assert size(p) == head + images
     assert size(_problem()) == 0  # dk = dv = 16 runs without a workspace
 
 

@@ -13,7 +13,7 @@ from gated_delta_rule_gate_gb300 import _native as N
 from gated_delta_rule_gate_gb300 import api
 
 FAKE = 0x100000  # 256-byte aligned, never dereferenced by the host
-SCRATCH = 72 << 20
+SCRATCH = 768 << 20
 
 
 def _problem(**over):
@@ -36,7 +36,7 @@ def test_exported_and_declared():
 
 
 def test_oversize_rejected_on_the_host():
-    """A problem whose workspace exceeds the 72 MiB scratch is refused before
+    """A problem whose workspace exceeds the 768 MiB scratch is refused before
     anything is enqueued (no GPU needed)."""
     lib = N.load()
     p = _problem(batch=4, total_tokens=4 * 32768, num_heads_q=32, num_heads_v=32)
@@ -80,7 +80,7 @@ def test_same_result_as_the_workspace_entry_point(rule):
 @pytest.mark.gpu
 def test_full_size_ragged_prefill_fits_the_scratch():
     """The ragged prefill configuration (16384 tokens, Hv = 32) needs about
-    70 MB of workspace: it runs on the static scratch."""
+    765 MB of workspace: it runs on the static scratch."""
     import workloads
     from gpu_helpers import run
     p = workloads.ragged_prefill()
