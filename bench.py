@@ -274,7 +274,7 @@ def kernel_name(p, path):
     if per_key:
         return "recurrent_long_kernel<%d>" % p["dk"]
     if p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16" and p["rule"] != "gdn2":
-        return "chunk_chain_kernel<%s>" % ("false" if p["rule"] == "linear" else "true")
+        return "chunk_chain_kernel<%d>" % {"linear": 0, "gated": 1}.get(p["rule"], 2)
     return "chunked_mma_kernel<%d,%s>" % (p["dk"], "true" if p["rule"] == "gdn2" else "false")
 
 

@@ -157,37 +157,38 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *off
 // ---------------------------------------------------------------------------
 // chunk_prepare_kernel: the operand image of every (chunk slot, value head).
 //
-// Per task, in order (M = 64 products put row m on tensor-memory lane
-// 32 (m / 16) + m % 16; the 16x256b load gives thread t of a warp rows
-// t / 4 and t / 4 + 8 and the column pairs 2 (t % 4) of every 8):
+// Per task, in order (an M = 64 product puts row m on tensor-memory lane
+// 32 (m / 16) + m % 16, where the 16x256b load gives thread t of a warp rows
+// t / 4 and t / 4 + 8 and the column pairs 2 (t % 4) of every 8; an M = 128
+// product puts row m on lane m):
 //   1. gates, G = cumulative log decay, beta, 1 / |k|, 1 / |q|; per-token
 //      factors; the key rows scaled into Kt (to the image);
-//   2. products K K^T (delta rules) and Q K^T;
-//   3. warps 0-3: A from K K^T and the fp32 solve T = (I + A)^-1 (16 x 16
-//      diagonal blocks by substitution, then two recursive-doubling merges
-//      [[T0, 0], [L, T1]], L = -T1 A10 T0), written as fp16 Tb = T diag(beta)
-//      and Ta' = -T diag(beta e^G / |k|);  warps 4-7: P from Q K^T (to the
-//      image), the query rows scaled in place into Qh;
-//   4. products U = Tb V and Wn = Ta' K (= -W);
-//   5. warps 0-3: U to the image; warps 4-7: Wn into the freed key tile;
-//   6. products Wn^T Kt and P Wn;
-//   7. warps 0-3: E = Wn^T Kt + (e^{G_C} - 1) I to the image; warps 4-7:
-//      Q' = Qh + P Wn to the image.
-// The rules without retrieval stop after step 3's P, with U = V, Q' = Qh and
-// E = (e^{G_C} - 1) I (gated only).  Padding tokens of a short last chunk get
+//   2. one product [K; Q] K^T (M = 128: the key rows of the delta rules' system
+//      and the query rows of P);
+//   3. warps on lanes 0-63: A from K K^T;  warps on lanes 64-127: P from Q K^T
+//      (to the image);
+//   4. all eight warps: the fp32 solve T = (I + A)^-1 (16 x 16 diagonal blocks
+//      by substitution, four threads per column, then two recursive-doubling
+//      merges [[T0, 0], [L, T1]], L = -T1 A10 T0), written as fp16
+//      Tb = T diag(beta) and Ta' = -T diag(beta e^G / |k|);
+//   5. products U = Tb V and Wn = Ta' K (= -W);
+//   6. U to the image, Wn over the key rows;
+//   7. products Wn^T Kt and P Wn;
+//   8. Q' = Qh + P Wn and E = Wn^T Kt + (e^{G_C} - 1) I to the image.
+// The rules without retrieval stop after step 3, with U = V and Q' = Qh; for
+// the gated rule the image's E area holds only e^{G_C}.  Padding tokens of a short last chunk get
 // zero keys, queries, values, log decay and beta, so every operand row or
 // column that belongs to them is zero.
 //
-// Persistent CTAs, two per SM: a producer warp (task lookup, the gates in
-// fp32, the key / query / value tiles by TMA) and eight worker warps.  Waits
-// are bounded.
+// Persistent CTAs, two per SM: a producer warp (task lookup and gates in fp32
+// one task ahead, the key / query / value tiles by TMA as soon as the
+// previous task releases them) and eight worker warps.  Waits are bounded.
 constexpr int PR_WORK = 256;
 constexpr int PR_THREADS = PR_WORK + 32;
 constexpr int FA = 68;  // fp32 row stride of At (16-byte rows; lanes = consecutive r, conflict-free)
 constexpr int FT = 68;  // fp32 row stride of T (16-byte rows for vector reads)
-constexpr int rK = 0;                    // 16 KB: K tile, 2 blocks [64 t][64 d]; later Wn [64 t][128 i]
-constexpr int rQ = 16384;                // 16 KB: Q tile; later Qh, then Q'
-constexpr int rV = 32768;                // 16 KB: V tile; later U
+constexpr int rKQ = 0;                   // 32 KB: 2 blocks (64 channels each) of [64 key rows; 64 query rows]
+constexpr int rV = 32768;                // 16 KB: V tile, 2 blocks [64 t][64 v]; later U
 constexpr int rAt = 49152;               // fp32 [64][FA], At[j][r] = A[r][j]; later Tb, Ta'; later E
 constexpr int rTf = rAt + 64 * FA * 4;   // fp32 [64][FT], T (its unused upper-right block holds Y)
 constexpr int rTb = rAt, rTa = rAt + 8192;
@@ -204,6 +205,10 @@ static_assert(rKt % 1024 == 0 && rP % 1024 == 0, "prepare layout: swizzled tiles
 static_assert(2 * (PR_SMEM + 1024) <= 228 * 1024, "prepare: two CTAs per SM");
 // per-token factor arrays (offsets in floats from rSc)
 constexpr int fG = 0, fB = 64, fIK = 128, fIQ = 192, fKF = 256, fTF = 320, fQF = 384, fQS = 448;
+// shared-memory offset of 16-byte chunk `ch` (0..15) of key row r / query row r / value row r
+__device__ __forceinline__ int kq_off(int r, int ch, bool query) {
+    return (ch >> 3) * 16384 + (query ? 8192 : 0) + sw(r, ch & 7);
+}
 
 template <bool RETR>
 __global__ void __launch_bounds__(PR_THREADS, 2)
@@ -250,8 +255,8 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             request_range(p, b, t0, t1);
             x.c0 = t0 + TC_C * (x.slot - offs[b]);
             x.n = min(TC_C, t1 - x.c0);
-            const float gs = (rule_has_decay(p.rule) && p.raw_gate) ? p.gate_scale[x.h] : 0.f;
-            const float gb = (rule_has_decay(p.rule) && p.raw_gate) ? p.gate_bias[x.h] : 0.f;
+            const bool raw = rule_has_decay(p.rule) && p.raw_gate;
+            const float gs = raw ? p.gate_scale[x.h] : 0.f, gb = raw ? p.gate_bias[x.h] : 0.f;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int tt = lane + 32 * e;
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                if (p.raw_gate && rule_has_decay(p.rule) && lane + 32 * e < x.n) x.g[e] = gs * softplus_f(x.g[e] + gb);
+                if (raw && lane + 32 * e < x.n) x.g[e] = gs * softplus_f(x.g[e] + gb);
                 if (RETR && (p.flags & kBetaSigmoid) && lane + 32 * e < x.n) x.bt[e] = sigmoid_f(x.bt[e]);
             }
             return x;
@@ -288,8 +293,8 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 ptx::mbar_arrive_expect_tx(land, 3 * 16384);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
-                    ptx::tma_load_3d(sm + rK + kb * 8192, &tmK, 64 * kb, qh, nx.c0, land);
-                    ptx::tma_load_3d(sm + rQ + kb * 8192, &tmQ, 64 * kb, qh, nx.c0, land);
+                    ptx::tma_load_3d(sm + rKQ + kb * 16384, &tmK, 64 * kb, qh, nx.c0, land);
+                    ptx::tma_load_3d(sm + rKQ + kb * 16384 + 8192, &tmQ, 64 * kb, qh, nx.c0, land);
                     ptx::tma_load_3d(sm + rV + kb * 8192, &tmV, 64 * kb, nx.h, nx.c0, land);
                 }
             }
@@ -299,10 +304,11 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
         // ===================== workers (256 threads)
         const bool nq = (p.flags & kL2q) != 0;
         const bool decay = rule_has_decay(p.rule);
-        const int q = warp & 3;  // tensor-memory lane quarter of this warp
+        const int q = warp & 3;    // tensor-memory lane quarter of this warp
+        const int hh = warp >> 2;  // column half of this warp in the epilogues
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         const int ra = 16 * q + (lane >> 2), rb = ra + 8, cp = 2 * (lane & 3);
-        const uint32_t aK = ptx::smem_u32(sm + rK), aQ = ptx::smem_u32(sm + rQ), aV = ptx::smem_u32(sm + rV);
+        const uint32_t aKQ = ptx::smem_u32(sm + rKQ), aV = ptx::smem_u32(sm + rV);
         const uint32_t aKt = ptx::smem_u32(sm + rKt), aP = ptx::smem_u32(sm + rP);
         const uint32_t aTb = ptx::smem_u32(sm + rTb), aTa = ptx::smem_u32(sm + rTa);
         bool ok = true;
@@ -319,8 +325,8 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 const int nz = (TC_C - n) * 16;
                 for (int idx = tid; idx < 3 * nz; idx += PR_WORK) {
                     const int which = idx / nz, rem = idx % nz, r = n + (rem >> 4), ch = rem & 15;
-                    *reinterpret_cast<uint4 *>(sm + which * 16384 + (ch >> 3) * 8192 + sw(r, ch & 7)) =
-                        make_uint4(0, 0, 0, 0);
+                    const int off = which == 2 ? rV + (ch >> 3) * 8192 + sw(r, ch & 7) : kq_off(r, ch, which == 1);
+                    *reinterpret_cast<uint4 *>(sm + off) = make_uint4(0, 0, 0, 0);
                 }
                 ptx::named_bar_sync(3, PR_WORK);
             }
@@ -337,27 +343,36 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 F[fB + 2 * lane] = gin[64 + 2 * lane];
                 F[fB + 2 * lane + 1] = gin[64 + 2 * lane + 1];
             }
-            {  // 1 / |k_r| (threads 0..127) and 1 / |q_r| (128..255): two threads per row
-                const int which = tid >> 7, r = (tid >> 1) & 63, part = tid & 1;
-                const bool want = which == 0 ? (p.flags & kL2k) != 0 : nq;
-                float ss = 0.f;
-                if (want) {
-                    float s0 = 0.f, s1 = 0.f;
+            // the previous task's image copies have read their staging areas
+            if (tid == 0) ptx::bulk_wait_read();
+            tc::fence_async_smem();
+            tc::fence_before();
+            ptx::named_bar_sync(3, PR_WORK);
+            if (tid == 0) {
+                tc::fence_after();
+                // [K; Q] [K; Q]^T -> columns [0, 128): M = N = 128, K = 128.  Columns [0, 64) hold
+                // K K^T over Q K^T; the diagonal holds the squared norms of the key and query rows.
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(sm + which * 16384 + part * 8192 + sw(r, w));
-                        const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __half22float2(hp[e]);
-                            s0 = fmaf(f.x, f.x, s0);
-                            s1 = fmaf(f.y, f.y, s1);
-                        }
-                    }
-                    ss = s0 + s1;
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t o = (s >> 2) * 16384 + (s & 3) * 32;
+                    tc::mma_f16(tmem, tc::desc_sw128(aKQ + o), tc::desc_sw128(aKQ + o), tc::idesc_f16(128, 128), s > 0);
                 }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                if (part == 0) F[(which == 0 ? fIK : fIQ) + r] = want ? rsqrtf(ss + 1e-12f) : 1.f;
+                tc::commit(bar1);
+            }
+            ok = ptx::named_bar_and(3, PR_WORK, ptx::mbar_wait_sleep(bar1, ph));
+            if (!ok) break;
+            tc::fence_after();
+            if (warp < 4) {
+                // 1 / |k_r| and 1 / |q_r| from the diagonal: row m = 32 q + lane sits on lane m
+                float v[32];
+                tc::ld32(tmem + lane_off + 32 * q, v);
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (e == lane) d = v[e];
+                const int m = 32 * q + lane;
+                if (m < TC_C) F[fIK + m] = (p.flags & kL2k) ? rsqrtf(d + 1e-12f) : 1.f;
+                else F[fIQ + m - TC_C] = nq ? rsqrtf(d + 1e-12f) : 1.f;
             }
             ptx::named_bar_sync(3, PR_WORK);
             if (tid < TC_C) {
@@ -367,226 +382,173 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 F[fQF + tid] = p.scale * eg * iq;
                 F[fQS + tid] = p.scale * iq;
             }
+            ptx::named_bar_sync(3, PR_WORK);
+            // Kt rows = e^{G_C - G_t} k_t / |k_t| into their tile (image layout; the operand of E);
+            // without retrieval also U = V and Q' = Qh straight to the image
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int idx = tid + PR_WORK * w, tr = idx >> 4, ch = idx & 15;
+                const int io = (ch >> 3) * 8192 + sw(tr, ch & 7);  // image (and Kt / V tile) offset
+                *reinterpret_cast<uint4 *>(sm + rKt + io) =
+                    scale_chunk(*reinterpret_cast<const uint4 *>(sm + kq_off(tr, ch, false)), F[fKF + tr]);
+                if (!RETR) {
+                    *reinterpret_cast<uint4 *>(dst + IM_U + io) = *reinterpret_cast<const uint4 *>(sm + rV + io);
+                    *reinterpret_cast<uint4 *>(dst + IM_Q + io) =
+                        scale_chunk(*reinterpret_cast<const uint4 *>(sm + kq_off(tr, ch, true)), F[fQF + tr]);
+                }
+            }
+            tc::fence_async_smem();
+            if (!RETR) {
+                // the gated rule's chain scales the state by e^{G_C} itself: only that goes to the image
+                if (decay && tid == 0) *reinterpret_cast<float *>(dst + IM_E) = __expf(F[fG + TC_C - 1]);
+                ptx::named_bar_sync(3, PR_WORK);
+                if (tid == 0) {
+                    ptx::bulk_s2g(dst + IM_KT, sm + rKt, 16384);
+                    ptx::bulk_commit();
+                    // without retrieval nothing reads the key, query and value tiles any more
+                    ptx::mbar_arrive(tfree);
+                }
+            }
+            {
+                // thread = row 32 (q % 2) + lane of K K^T (q < 2) or of Q K^T (q >= 2), columns
+                // [32 hh, 32 hh + 32)
+                const int r = 32 * (q & 1) + lane, j0 = 32 * hh;
+                float v[32];
+                tc::ld32(tmem + lane_off + j0, v);
+                const float Gr = F[fG + r];
+                // the factors e^{G_r - G_j} / |k_j| of this thread's 32 columns
+                float w[32];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(F + fG + j0 + 4 * m);
+                    const float4 i4 = *reinterpret_cast<const float4 *>(F + fIK + j0 + 4 * m);
+                    w[4 * m] = __expf(Gr - g4.x) * i4.x;
+                    w[4 * m + 1] = __expf(Gr - g4.y) * i4.y;
+                    w[4 * m + 2] = __expf(Gr - g4.z) * i4.z;
+                    w[4 * m + 3] = __expf(Gr - g4.w) * i4.w;
+                }
+                if (q >= 2) {
+                    // P[r][t] = scale e^{G_r - G_t} q_r . k_t / (|q_r| |k_t|) for t <= r
+                    const float qr = F[fQS + r];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = j0 + e <= r ? qr * w[e] * v[e] : 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(sm + rP, r, 4 * hh + cc, v + 8 * cc);
+                } else if (RETR) {
+                    // A[r][j] = beta_r e^{G_r - G_j} k_r . k_j / (|k_r| |k_j|), j < r, stored transposed
+                    const float fr = F[fB + r] * F[fIK + r];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) At[(j0 + e) * FA + r] = j0 + e < r ? fr * w[e] * v[e] : 0.f;
+                }
+            }
             tc::fence_async_smem();
             tc::fence_before();
             ptx::named_bar_sync(3, PR_WORK);
             if (tid == 0) {
-                tc::fence_after();
-                // K K^T -> columns [0, 64) and Q K^T -> [64, 128): M = 64, N = 64, K = 128
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t o = (s >> 2) * 8192 + (s & 3) * 32;
-                    if (RETR) tc::mma_f16(tmem, tc::desc_sw128(aK + o), tc::desc_sw128(aK + o), tc::idesc_f16(64, 64), s > 0);
-                    tc::mma_f16(tmem + 64, tc::desc_sw128(aQ + o), tc::desc_sw128(aK + o), tc::idesc_f16(64, 64), s > 0);
-                }
-                tc::commit(bar1);
-            }
-            // Kt rows = e^{G_C - G_t} k_t / |k_t| (shared memory for E, and the image); without
-            // retrieval also U = V and Q' = Qh straight to the image
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int idx = tid + PR_WORK * w, tr = idx >> 4, ch = idx & 15;
-                const int off = (ch >> 3) * 8192 + sw(tr, ch & 7);
-                const uint4 u = scale_chunk(*reinterpret_cast<const uint4 *>(sm + rK + off), F[fKF + tr]);
-                if (RETR) *reinterpret_cast<uint4 *>(sm + rKt + off) = u;
-                *reinterpret_cast<uint4 *>(dst + IM_KT + off) = u;
-                if (!RETR) {
-                    *reinterpret_cast<uint4 *>(dst + IM_U + off) = *reinterpret_cast<const uint4 *>(sm + rV + off);
-                    *reinterpret_cast<uint4 *>(dst + IM_Q + off) =
-                        scale_chunk(*reinterpret_cast<const uint4 *>(sm + rQ + off), F[fQF + tr]);
-                }
-            }
-            if (!RETR && decay) {
-                // E = (e^{G_C} - 1) I
-                const float gm1 = expm1f(F[fG + TC_C - 1]);
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const int idx = tid + PR_WORK * w, jb = idx >> 10, ii = (idx >> 3) & 127, c = idx & 7;
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = (64 * jb + 8 * c + e == ii) ? gm1 : 0.f;
-                    uint4 u;
-                    u.x = ptx::pack_h2(x[0], x[1]);
-                    u.y = ptx::pack_h2(x[2], x[3]);
-                    u.z = ptx::pack_h2(x[4], x[5]);
-                    u.w = ptx::pack_h2(x[6], x[7]);
-                    *reinterpret_cast<uint4 *>(dst + IM_E + jb * 16384 + sw(ii, c)) = u;
-                }
-            }
-            // ---- K K^T and Q K^T done
-            ok = ptx::named_bar_and(3, PR_WORK, ptx::mbar_wait_sleep(bar1, ph));
-            if (!ok) break;
-            tc::fence_after();
-            // without retrieval nothing reads the key, query and value tiles any more
-            if (!RETR && tid == 0) ptx::mbar_arrive(tfree);
-            if (warp >= 4) {
-                // P[r][t] = scale e^{G_r - G_t} q_r . k_t / (|q_r| |k_t|) for t <= r
-                const int gt = tid - 128;
-                float v[32];
-                tc::ld16x256<8>(tmem + lane_off + 64, v);
-                const float Ga = F[fG + ra], Gb = F[fG + rb], qa = F[fQS + ra], qb = F[fQS + rb];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int j = 8 * k + cp;
-                    const float2 gj = *reinterpret_cast<const float2 *>(F + fG + j);
-                    const float2 ij = *reinterpret_cast<const float2 *>(F + fIK + j);
-                    const float a0 = j <= ra ? qa * __expf(Ga - gj.x) * ij.x * v[4 * k] : 0.f;
-                    const float a1 = j + 1 <= ra ? qa * __expf(Ga - gj.y) * ij.y * v[4 * k + 1] : 0.f;
-                    const float b0 = j <= rb ? qb * __expf(Gb - gj.x) * ij.x * v[4 * k + 2] : 0.f;
-                    const float b1 = j + 1 <= rb ? qb * __expf(Gb - gj.y) * ij.y * v[4 * k + 3] : 0.f;
-                    *reinterpret_cast<uint32_t *>(sm + rP + sw(ra, k) + 2 * cp) = ptx::pack_h2(a0, a1);
-                    *reinterpret_cast<uint32_t *>(sm + rP + sw(rb, k) + 2 * cp) = ptx::pack_h2(b0, b1);
-                }
-                ptx::named_bar_sync(2, 128);
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int idx = gt + 128 * w;
-                    *reinterpret_cast<uint4 *>(dst + IM_P + 16 * idx) = *reinterpret_cast<const uint4 *>(sm + rP + 16 * idx);
-                }
-                if (RETR) {
-                    // query rows -> Qh = scale e^{G_r} q_r / |q_r| in place (Q K^T has read them)
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        const int idx = gt + 128 * w, r = idx >> 4, ch = idx & 15;
-                        uint4 *ptr = reinterpret_cast<uint4 *>(sm + rQ + (ch >> 3) * 8192 + sw(r, ch & 7));
-                        *ptr = scale_chunk(*ptr, F[fQF + r]);
-                    }
-                }
-            } else if (RETR) {
-                // A[r][j] = beta_r e^{G_r - G_j} k_r . k_j / (|k_r| |k_j|), j < r, stored transposed
-                {
-                    const float fa = F[fB + ra] * F[fIK + ra], fb = F[fB + rb] * F[fIK + rb];
-                    const float Ga = F[fG + ra], Gb = F[fG + rb];
-                    float v[32];
-                    tc::ld16x256<8>(tmem + lane_off, v);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int j = 8 * k + cp;
-                        const float2 gj = *reinterpret_cast<const float2 *>(F + fG + j);
-                        const float2 ij = *reinterpret_cast<const float2 *>(F + fIK + j);
-                        At[j * FA + ra] = j < ra ? fa * __expf(Ga - gj.x) * ij.x * v[4 * k] : 0.f;
-                        At[(j + 1) * FA + ra] = j + 1 < ra ? fa * __expf(Ga - gj.y) * ij.y * v[4 * k + 1] : 0.f;
-                        At[j * FA + rb] = j < rb ? fb * __expf(Gb - gj.x) * ij.x * v[4 * k + 2] : 0.f;
-                        At[(j + 1) * FA + rb] = j + 1 < rb ? fb * __expf(Gb - gj.y) * ij.y * v[4 * k + 3] : 0.f;
-                    }
-                }
-                ptx::named_bar_sync(1, 128);
-                if (lane < 16) {
-                    // column `lane` of the inverse of diagonal block `warp`, right-looking:
-                    // once x[j] is final it updates every later row at once
-                    float x[16];
-                    const float *Ab = At + (16 * warp) * FA + 16 * warp;  // Ab[j][i] = A[i][j]
-#pragma unroll
-                    for (int qq = 0; qq < 16; ++qq) x[qq] = (qq == lane) ? 1.f : 0.f;
-#pragma unroll
-                    for (int j = 0; j < 15; ++j) {
-                        float a[16];
-#pragma unroll
-                        for (int w4 = 0; w4 < 4; ++w4) {
-                            const float4 tv = *reinterpret_cast<const float4 *>(Ab + j * FA + 4 * w4);
-                            a[4 * w4] = tv.x, a[4 * w4 + 1] = tv.y, a[4 * w4 + 2] = tv.z, a[4 * w4 + 3] = tv.w;
-                        }
-#pragma unroll
-                        for (int qq = j + 1; qq < 16; ++qq) x[qq] = fmaf(-a[qq], x[j], x[qq]);
-                    }
-#pragma unroll
-                    for (int qq = 0; qq < 16; ++qq) Tf[(16 * warp + qq) * FT + 16 * warp + lane] = x[qq];
-                }
-                // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int idx = 4 * tid + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
-                    Tf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
-                }
-                ptx::named_bar_sync(1, 128);
-                {
-                    // level 1: blocks (1,0) and (3,2): Y = A_{b,b-1} T_{b-1}, then L = -T_b Y
-                    const int r = tid >> 3, c = 2 * (tid & 7);  // row 0..15, columns c, c+1
-#pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const int o0 = 32 * blk;
-                        float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float a = At[(o0 + k) * FA + o0 + 16 + r];
-                            y0 = fmaf(a, Tf[(o0 + k) * FT + o0 + c], y0);
-                            y1 = fmaf(a, Tf[(o0 + k) * FT + o0 + c + 1], y1);
-                        }
-                        Y[(16 * blk + r) * FT + c] = y0;
-                        Y[(16 * blk + r) * FT + c + 1] = y1;
-                    }
-                    ptx::named_bar_sync(1, 128);
-#pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const int o0 = 32 * blk;
-                        float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const float tv = Tf[(o0 + 16 + r) * FT + o0 + 16 + k];
-                            l0 = fmaf(tv, Y[(16 * blk + k) * FT + c], l0);
-                            l1 = fmaf(tv, Y[(16 * blk + k) * FT + c + 1], l1);
-                        }
-                        Tf[(o0 + 16 + r) * FT + o0 + c] = -l0;
-                        Tf[(o0 + 16 + r) * FT + o0 + c + 1] = -l1;
-                    }
-                }
-                ptx::named_bar_sync(1, 128);
-                {
-                    // level 2: Y = A_10 T_0 (32 x 32), then L = -T_1 Y; thread = (row, 2 x 4 columns).
-                    // T_0 and T_1 are lower triangular: Y[r][c] sums k >= c, L[r][c] sums k <= r.
-                    const int r = tid >> 2;
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int c = 4 * (tid & 3) + 16 * half;
-                        float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                        for (int k = c; k < 32; ++k) {
-                            const float a = At[k * FA + 32 + r];
-                            const float4 tv = *reinterpret_cast<const float4 *>(Tf + k * FT + c);
-                            y.x = fmaf(a, tv.x, y.x), y.y = fmaf(a, tv.y, y.y), y.z = fmaf(a, tv.z, y.z),
-                            y.w = fmaf(a, tv.w, y.w);
-                        }
-                        *reinterpret_cast<float4 *>(Y + r * FT + c) = y;
-                    }
-                    ptx::named_bar_sync(1, 128);
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int c = 4 * (tid & 3) + 16 * half;
-                        float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                        for (int k = 0; k <= r; ++k) {
-                            const float tv = Tf[(32 + r) * FT + 32 + k];
-                            const float4 yy = *reinterpret_cast<const float4 *>(Y + k * FT + c);
-                            l.x = fmaf(tv, yy.x, l.x), l.y = fmaf(tv, yy.y, l.y), l.z = fmaf(tv, yy.z, l.z),
-                            l.w = fmaf(tv, yy.w, l.w);
-                        }
-                        *reinterpret_cast<float4 *>(Tf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
-                    }
-                }
-                ptx::named_bar_sync(1, 128);
-                {
-                    // Tb[r][j] = T[r][j] beta_j and Ta'[r][j] = -T[r][j] beta_j e^{G_j} / |k_j| (j <= r),
-                    // fp16, K-major (the At rows are no longer read)
-                    const int r = tid >> 1, j0 = 32 * (tid & 1);
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        float x[8], y[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = j0 + 8 * w + e;
-                            x[e] = j <= r ? Tf[r * FT + j] * F[fB + j] : 0.f;
-                            y[e] = x[e] * F[fTF + j];
-                        }
-                        st_chunk(sm + rTb, r, (j0 >> 3) + w, x);
-                        st_chunk(sm + rTa, r, (j0 >> 3) + w, y);
-                    }
-                }
+                ptx::bulk_s2g(dst + IM_P, sm + rP, 8192);
+                if (RETR) ptx::bulk_s2g(dst + IM_KT, sm + rKt, 16384);
+                ptx::bulk_commit();
             }
             if (!RETR) {
-                // every operand is in the image
-                tc::fence_before();
                 ph ^= 1u;
                 continue;
+            }
+            {
+                // diagonal blocks: column c of the inverse of block b, rows 4 s .. 4 s + 3 of it,
+                // right-looking (once x[j] is final it updates every later row at once)
+                const int b = tid >> 6, c = (tid >> 2) & 15, s4 = 4 * (tid & 3);
+                float x[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[e] = (s4 + e == c) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < 15; ++j) {
+                    const float xj = __shfl_sync(0xffffffffu, x[j & 3], (lane & ~3) | (j >> 2));
+                    const float4 a = *reinterpret_cast<const float4 *>(At + (16 * b + j) * FA + 16 * b + s4);
+                    x[0] = s4 > j ? fmaf(-a.x, xj, x[0]) : x[0];
+                    x[1] = s4 + 1 > j ? fmaf(-a.y, xj, x[1]) : x[1];
+                    x[2] = s4 + 2 > j ? fmaf(-a.z, xj, x[2]) : x[2];
+                    x[3] = s4 + 3 > j ? fmaf(-a.w, xj, x[3]) : x[3];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Tf[(16 * b + s4 + e) * FT + 16 * b + c] = x[e];
+                // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int idx = 2 * tid + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
+                    Tf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
+                }
+            }
+            ptx::named_bar_sync(3, PR_WORK);
+            {
+                // level 1: blocks (1,0) and (3,2): Y = A_{b,b-1} T_{b-1}, then L = -T_b Y
+                const int blk = tid >> 7, r = (tid >> 3) & 15, c = 2 * (tid & 7), o0 = 32 * blk;
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float a = At[(o0 + k) * FA + o0 + 16 + r];
+                    const float2 tv = *reinterpret_cast<const float2 *>(Tf + (o0 + k) * FT + o0 + c);
+                    y0 = fmaf(a, tv.x, y0);
+                    y1 = fmaf(a, tv.y, y1);
+                }
+                *reinterpret_cast<float2 *>(Y + (16 * blk + r) * FT + c) = make_float2(y0, y1);
+                ptx::named_bar_sync(3, PR_WORK);
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float tv = Tf[(o0 + 16 + r) * FT + o0 + 16 + k];
+                    const float2 yy = *reinterpret_cast<const float2 *>(Y + (16 * blk + k) * FT + c);
+                    l0 = fmaf(tv, yy.x, l0);
+                    l1 = fmaf(tv, yy.y, l1);
+                }
+                *reinterpret_cast<float2 *>(Tf + (o0 + 16 + r) * FT + o0 + c) = make_float2(-l0, -l1);
+            }
+            ptx::named_bar_sync(3, PR_WORK);
+            {
+                // level 2: Y = A_10 T_0 (32 x 32), then L = -T_1 Y; thread = (row, 4 columns).
+                // T_0 and T_1 are lower triangular: Y[r][c] sums k >= c, L[r][c] sums k <= r.
+                const int r = tid >> 3, c = 4 * (tid & 7);
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                for (int k = c; k < 32; ++k) {
+                    const float a = At[k * FA + 32 + r];
+                    const float4 tv = *reinterpret_cast<const float4 *>(Tf + k * FT + c);
+                    y.x = fmaf(a, tv.x, y.x), y.y = fmaf(a, tv.y, y.y), y.z = fmaf(a, tv.z, y.z), y.w = fmaf(a, tv.w, y.w);
+                }
+                *reinterpret_cast<float4 *>(Y + r * FT + c) = y;
+                ptx::named_bar_sync(3, PR_WORK);
+                float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                for (int k = 0; k <= r; ++k) {
+                    const float tv = Tf[(32 + r) * FT + 32 + k];
+                    const float4 yy = *reinterpret_cast<const float4 *>(Y + k * FT + c);
+                    l.x = fmaf(tv, yy.x, l.x), l.y = fmaf(tv, yy.y, l.y), l.z = fmaf(tv, yy.z, l.z), l.w = fmaf(tv, yy.w, l.w);
+                }
+                *reinterpret_cast<float4 *>(Tf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
+            }
+            ptx::named_bar_sync(3, PR_WORK);
+            {
+                // Tb[r][j] = T[r][j] beta_j and Ta'[r][j] = -T[r][j] beta_j e^{G_j} / |k_j| (j <= r),
+                // fp16, K-major (the At rows are no longer read); thread = (row, 16 columns)
+                const int r = tid & 63, j0 = 16 * (tid >> 6);
+                float x[16], y[16];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float4 tv = *reinterpret_cast<const float4 *>(Tf + r * FT + j0 + 4 * m);
+                    const float4 bv = *reinterpret_cast<const float4 *>(F + fB + j0 + 4 * m);
+                    const float4 fv = *reinterpret_cast<const float4 *>(F + fTF + j0 + 4 * m);
+                    const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
+                    const float f4[4] = {fv.x, fv.y, fv.z, fv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        x[4 * m + e] = j0 + 4 * m + e <= r ? t4[e] * b4[e] : 0.f;
+                        y[4 * m + e] = x[4 * m + e] * f4[e];
+                    }
+                }
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    st_chunk(sm + rTb, r, (j0 >> 3) + cc, x + 8 * cc);
+                    st_chunk(sm + rTa, r, (j0 >> 3) + cc, y + 8 * cc);
+                }
             }
             tc::fence_async_smem();
             tc::fence_before();
@@ -598,7 +560,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 for (int s = 0; s < 4; ++s) {
                     tc::mma_f16(tmem, tc::desc_sw128(aTb + s * 32), tc::desc_sw128(aV + s * 2048, 8192),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
-                    tc::mma_f16(tmem + 128, tc::desc_sw128(aTa + s * 32), tc::desc_sw128(aK + s * 2048, 8192),
+                    tc::mma_f16(tmem + 128, tc::desc_sw128(aTa + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
                 }
                 tc::commit(bar2);
@@ -608,16 +570,17 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             tc::fence_after();
             {
                 // warps 0-3: U rows into the freed value tile (image layout); warps 4-7: Wn rows
-                // into the freed key tile (the operand of Wn^T Kt and P Wn)
-                const uint32_t col = warp < 4 ? 0u : 128u;
-                unsigned char *tile = sm + (warp < 4 ? rV : rK);
+                // over the key rows (the operand of Wn^T Kt and P Wn)
+                const uint32_t col = hh == 0 ? 0u : 128u;
+                unsigned char *tile = sm + (hh == 0 ? rV : rKQ);
+                const int bstride = hh == 0 ? 8192 : 16384;
                 float v[64];
                 tc::ld16x256x16(tmem + lane_off + col, v);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    *reinterpret_cast<uint32_t *>(tile + (k >> 3) * 8192 + sw(ra, k & 7) + 2 * cp) =
+                    *reinterpret_cast<uint32_t *>(tile + (k >> 3) * bstride + sw(ra, k & 7) + 2 * cp) =
                         ptx::pack_h2(v[4 * k], v[4 * k + 1]);
-                    *reinterpret_cast<uint32_t *>(tile + (k >> 3) * 8192 + sw(rb, k & 7) + 2 * cp) =
+                    *reinterpret_cast<uint32_t *>(tile + (k >> 3) * bstride + sw(rb, k & 7) + 2 * cp) =
                         ptx::pack_h2(v[4 * k + 2], v[4 * k + 3]);
                 }
             }
@@ -625,76 +588,82 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             tc::fence_before();
             ptx::named_bar_sync(3, PR_WORK);
             if (tid == 0) {
+                // U to the image (while the last two products run)
+                ptx::bulk_s2g(dst + IM_U, sm + rV, 16384);
+                ptx::bulk_commit();
                 tc::fence_after();
                 // Wn^T Kt -> [0, 128): M = 128 (i), N = 128 (j), K = 64 (t), both operands M/N-major
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem, tc::desc_sw128(aK + s * 2048, 8192), tc::desc_sw128(aKt + s * 2048, 8192),
+                    tc::mma_f16(tmem, tc::desc_sw128(aKQ + s * 2048, 16384), tc::desc_sw128(aKt + s * 2048, 8192),
                                 tc::idesc_f16(128, 128, true, true), s > 0);
                 // P Wn -> [128, 256): M = 64 (r), N = 128 (i), K = 64 (t)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem + 128, tc::desc_sw128(aP + s * 32), tc::desc_sw128(aK + s * 2048, 8192),
+                    tc::mma_f16(tmem + 128, tc::desc_sw128(aP + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
                 tc::commit(bar3);
-            }
-            if (warp < 4) {
-                // U to the image (while the last two products run)
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const int idx = tid + 128 * w;
-                    *reinterpret_cast<uint4 *>(dst + IM_U + 16 * idx) = *reinterpret_cast<const uint4 *>(sm + rV + 16 * idx);
-                }
             }
             ok = ptx::named_bar_and(3, PR_WORK, ptx::mbar_wait_sleep(bar3, ph));
             if (!ok) break;
             tc::fence_after();
-            const int hh = warp >> 2;  // column half of this warp
             {
-                // Q' = Qh + P Wn, in place in the query tile (columns [64 hh, 64 hh + 64) of i)
+                // Q' = scale e^{G_r} q_r / |q_r| + (P Wn)_r, in place over the query rows
+                // (columns [64 hh, 64 hh + 64) of i)
+                const float fa = F[fQF + ra], fb = F[fQF + rb];
                 float v[32];
                 tc::ld16x256<8>(tmem + lane_off + 128 + 64 * hh, v);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    __half2 *pa = reinterpret_cast<__half2 *>(sm + rQ + hh * 8192 + sw(ra, k) + 2 * cp);
-                    __half2 *pb = reinterpret_cast<__half2 *>(sm + rQ + hh * 8192 + sw(rb, k) + 2 * cp);
+                    __half2 *pa = reinterpret_cast<__half2 *>(sm + rKQ + hh * 16384 + 8192 + sw(ra, k) + 2 * cp);
+                    __half2 *pb = reinterpret_cast<__half2 *>(sm + rKQ + hh * 16384 + 8192 + sw(rb, k) + 2 * cp);
                     const float2 xa = __half22float2(*pa), xb = __half22float2(*pb);
-                    *pa = __floats2half2_rn(xa.x + v[4 * k], xa.y + v[4 * k + 1]);
-                    *pb = __floats2half2_rn(xb.x + v[4 * k + 2], xb.y + v[4 * k + 3]);
+                    *pa = __floats2half2_rn(fmaf(fa, xa.x, v[4 * k]), fmaf(fa, xa.y, v[4 * k + 1]));
+                    *pb = __floats2half2_rn(fmaf(fb, xb.x, v[4 * k + 2]), fmaf(fb, xb.y, v[4 * k + 3]));
                 }
             }
-            ptx::named_bar_sync(3, PR_WORK);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int idx = tid + PR_WORK * w;
-                *reinterpret_cast<uint4 *>(dst + IM_Q + 16 * idx) = *reinterpret_cast<const uint4 *>(sm + rQ + 16 * idx);
-            }
-            // the key, query and value tiles are free for the producer's next loads
             tc::fence_async_smem();
             ptx::named_bar_sync(3, PR_WORK);
-            if (tid == 0) ptx::mbar_arrive(tfree);
+            if (tid == 0) {
+                ptx::bulk_s2g(dst + IM_Q, sm + rKQ + 8192, 8192);
+                ptx::bulk_s2g(dst + IM_Q + 8192, sm + rKQ + 16384 + 8192, 8192);
+                ptx::bulk_commit();
+                // the key, query and value tiles are free for the producer's next loads once
+                // the copies have read them
+                ptx::bulk_wait_read();
+                ptx::mbar_arrive(tfree);
+            }
             {
                 // E = Wn^T Kt + (e^{G_C} - 1) I: row i = 32 q + lane, columns [64 hh, 64 hh + 64),
                 // staged in the At region
                 const int ii = 32 * q + lane;
-                const float gm1 = decay ? expm1f(F[fG + TC_C - 1]) : 0.f;
                 float v[64];
                 tc::ld64(tmem + lane_off + 64 * hh, v);
+                if (decay && hh == (q >> 1)) {  // this warp's rows meet the diagonal at column ii
+                    const float gm1 = expm1f(F[fG + TC_C - 1]);
+                    if (q & 1) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e)
-                    if (64 * hh + e == ii) v[e] += gm1;
+                        for (int e = 0; e < 32; ++e)
+                            if (e == lane) v[32 + e] += gm1;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e == lane) v[e] += gm1;
+                    }
+                }
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) st_chunk(sm + rAt + hh * 16384, ii, cc, v + 8 * cc);
             }
+            tc::fence_async_smem();
             tc::fence_before();
             ptx::named_bar_sync(3, PR_WORK);
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const int idx = tid + PR_WORK * w;
-                *reinterpret_cast<uint4 *>(dst + IM_E + 16 * idx) = *reinterpret_cast<const uint4 *>(sm + rAt + 16 * idx);
+            if (tid == 0) {
+                ptx::bulk_s2g(dst + IM_E, sm + rAt, 32768);
+                ptx::bulk_commit();
             }
             ph ^= 1u;
         }
+        if (tid == 0) ptx::bulk_wait();  // every image copy has landed before the CTA leaves
         if (!ok && p.err && tid == 0) atomicOr(p.err, 2);
     }
     tc::fence_before();
@@ -712,14 +681,18 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
 //   UK:  S   += U^T Kt    (state-independent; issued once S_c has been read)
 //   UP:  O^T  = U^T P^T   (state-independent; into one of two O buffers)
 //   SQ:  O^T += Sh Q'^T   (once Sh = S_c is in shared memory)
-//   SE:  S   += Sh E      (the only product on the chain; none for `linear`)
-// Roles (14 warps): warps 0-7 read S after each chunk (thread = value row
+//   SE:  S   += Sh E      (the only product on the chain; delta rules only)
+// The gated rule has E = (e^{G_C} - 1) I: instead of a product, the state
+// warps scale S by e^{G_C} in tensor memory when they read it (the prepare
+// kernel leaves e^{G_C} at the start of the image's E area).  Roles
+// (14 warps): warps 0-7 read S after each chunk (thread = value row
 // 32 (warp % 4) + lane, column half warp / 4), write Sh and, after the last
 // chunk, the final state; warps 8-11 read O^T and store the outputs; warp 12
-// loads the images; warp 13 issues the products.  SQ is issued before SE, so
-// the completion of SE also frees Sh for the next chunk.  Hand-overs are
-// mbarriers with bounded, sleeping waits; each role makes a failed wait
-// uniform before leaving.
+// loads the images; warp 13 issues the products, SQ before SE, so that the
+// completion of a chunk's last product also frees Sh.  With 64 chains on 64
+// SMs the chain streams about 60 GB/s of images per SM: the loads, not the
+// tensor cores, set its pace.  Hand-overs are mbarriers with bounded,
+// sleeping waits; each role makes a failed wait uniform before leaving.
 constexpr int CH_THREADS = 448;
 constexpr int cImg = 0;                       // 2 x IM_BYTES
 constexpr int cS = 2 * IM_BYTES;              // 32 KB: Sh, 2 blocks [128 v][64 i]
@@ -727,8 +700,10 @@ constexpr int cBar = cS + 32768;              // 11 mbarriers, TMEM address
 constexpr int CH_SMEM = cBar + 128 + 1024;
 static_assert(cS % 1024 == 0, "chain layout");
 constexpr uint32_t tS = 0, tO = 128;          // tensor-memory columns: S, two O^T buffers
+// what the state step of a rule needs beyond U^T Kt
+enum : int { kStepPlain = 0, kStepDecay = 1, kStepE = 2 };
 
-template <bool HAS_E>
+template <int STEP>
 __global__ void __launch_bounds__(CH_THREADS, 1)
     chunk_chain_kernel(Problem p, const int *offs, const int *order, const unsigned char *img, int cap) {
     extern __shared__ unsigned char smraw[];
@@ -786,7 +761,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         const int q4 = warp & 3, hc = warp >> 2, i = 32 * q4 + lane;
         const uint32_t lo = tmem + ((uint32_t)(32 * q4) << 16) + tS + 64 * hc;
         const size_t srow = sbase + (size_t)i * 128 + 64 * hc;
+        // e^{G_C} of chunk c, as the prepare kernel left it in the chunk's image
+        auto gamma = [&](int c) {
+            return *reinterpret_cast<const float *>(img + ((size_t)(slot0 + c) * p.Hv + h) * IM_BYTES + IM_E);
+        };
         {
+            const float g0 = STEP == kStepDecay ? gamma(0) : 1.f;
             float v[32];
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc) {
@@ -796,9 +776,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                     v[4 * j] = f.x, v[4 * j + 1] = f.y, v[4 * j + 2] = f.z, v[4 * j + 3] = f.w;
                 }
-                tc::st32(lo + 32 * pc, v);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * 16384, i, 4 * pc + cc, v + 8 * cc);
+                if (STEP == kStepDecay) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= g0;
+                }
+                tc::st32(lo + 32 * pc, v);
             }
             tc::wait_st();
         }
@@ -811,12 +795,24 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         }
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
+            const float gn = (STEP == kStepDecay && c + 1 < nch) ? gamma(c + 1) : 1.f;
             ok = ptx::named_bar_and(1, 256, ptx::mbar_wait_sleep(barS, c & 1));
             if (!ok) break;
             tc::fence_after();
             float v0[32], v1[32];
             tc::ld32(lo, v0);
             tc::ld32(lo + 32, v1);
+            if (STEP == kStepDecay && c + 1 < nch) {
+                // S <- e^{G_C} S of the next chunk before its U^T Kt lands
+                float w[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = v0[j] * gn;
+                tc::st32(lo, w);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = v1[j] * gn;
+                tc::st32(lo + 32, w);
+                tc::wait_st();
+            }
             tc::fence_before();
             ptx::named_bar_sync(1, 256);
             if (tid == 0) ptx::mbar_arrive(rsread);
@@ -869,7 +865,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     } else if (warp == 12) {
         // ===================== image loads, two buffers
         if (lane == 0) {
-            const uint32_t skip = HAS_E ? 0u : (uint32_t)IM_Q;  // `linear` has no E
+            const uint32_t skip = STEP == kStepE ? 0u : (uint32_t)IM_Q;  // only the delta rules load E
             for (int c = 0; c < nch; ++c) {
                 const int bf = c & 1;
                 if (c >= 2 && !ptx::mbar_wait_sleep(&freeb[bf], ((c - 2) >> 1) & 1)) {
@@ -879,7 +875,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 const unsigned char *src = img + ((size_t)(slot0 + c) * p.Hv + h) * IM_BYTES;
                 unsigned char *dstb = sm + cImg + bf * IM_BYTES;
                 ptx::mbar_arrive_expect_tx(&land[bf], IM_BYTES - skip);
-                if (HAS_E) ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);  // E and Q'
+                if (STEP == kStepE) ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);  // E and Q'
                 else ptx::bulk_g2s(dstb + IM_Q, src + IM_Q, IM_U - IM_Q, &land[bf]);
                 ptx::bulk_g2s(dstb + IM_U, src + IM_U, IM_BYTES - IM_U, &land[bf]);  // U, P, Kt
             }
@@ -900,6 +896,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 for (int s = 0; s < 4; ++s)
                     tc::mma_f16(tmem + tS, tc::desc_sw128(base + IM_U + s * 2048, 8192),
                                 tc::desc_sw128(base + IM_KT + s * 2048, 8192), tc::idesc_f16(128, 128, true, true), true);
+
                 if (c >= 2) {
                     ok = ptx::mbar_wait_sleep(&ofree[bf], ((c - 2) >> 1) & 1);
                     if (!ok) break;
@@ -920,7 +917,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                                 tc::desc_sw128(base + IM_Q + (s >> 2) * 8192 + (s & 3) * 32), tc::idesc_f16(128, 64),
                                 true);
                 tc::commit(&barO[bf]);
-                if (HAS_E) {
+                if (STEP == kStepE) {
                     // SE: S += Sh E (N = 128 j, K = 128 i; B N-major)
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
@@ -928,6 +925,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                                     tc::desc_sw128(base + IM_E + s * 2048, 16384), tc::idesc_f16(128, 128, false, true),
                                     true);
                 }
+                // every product of chunk c is done: S_{c+1} is complete and Sh is free
                 tc::commit(barS);
                 tc::commit(&freeb[bf]);
             }
@@ -1004,9 +1002,11 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_prepare_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
+        e = cudaFuncSetAttribute(chunk_chain_kernel<kStepPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
+        e = cudaFuncSetAttribute(chunk_chain_kernel<kStepDecay>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(chunk_chain_kernel<kStepE>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_done[dev] = 1;
     }
@@ -1037,9 +1037,11 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.rule == kLinear)
-        chunk_chain_kernel<false><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+        chunk_chain_kernel<kStepPlain><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+    else if (p.rule == kGated)
+        chunk_chain_kernel<kStepDecay><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
     else
-        chunk_chain_kernel<true><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+        chunk_chain_kernel<kStepE><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
     return cudaGetLastError();
 }
 
