@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *off
 //   5. products U = Tb V and Wn = Ta' K (= -W);
 //   6. U to the image, Wn over the key rows;
 //   7. products Wn^T Kt and P Wn;
-//   8. Q' = Qh + P Wn and E = Wn^T Kt + (e^{G_C} - 1) I to the image.
+//   8. Q' = Qh + P Wn (staged over Kt) and E = Wn^T Kt + (e^{G_C} - 1) I to the image.
 // The rules without retrieval stop after step 3, with U = V and Q' = Qh; for
 // the gated rule the image's E area holds only e^{G_C}.  Padding tokens of a short last chunk get
 // zero keys, queries, values, log decay and beta, so every operand row or
@@ -298,7 +298,18 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                     ptx::tma_load_3d(sm + rV + kb * 8192, &tmV, 64 * kb, nx.h, nx.c0, land);
                 }
             }
-            if (t + G < ntasks) nx = fetch(t + G);
+            if (t + G < ntasks) {
+                nx = fetch(t + G);
+                if (lane == 0) {  // its tiles into L2 while this task runs
+                    const int qh = (int)((long long)nx.h * p.Hq / p.Hv);
+#pragma unroll
+                    for (int kb = 0; kb < 2; ++kb) {
+                        ptx::prefetch_tile_3d(&tmK, 64 * kb, qh, nx.c0);
+                        ptx::prefetch_tile_3d(&tmQ, 64 * kb, qh, nx.c0);
+                        ptx::prefetch_tile_3d(&tmV, 64 * kb, nx.h, nx.c0);
+                    }
+                }
+            }
         }
     } else {
         // ===================== workers (256 threads)
@@ -604,34 +615,38 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                                 tc::idesc_f16(64, 128, false, true), s > 0);
                 tc::commit(bar3);
             }
+            // the copies of Kt and P have read their tiles (Q' goes into the Kt tile)
+            if (tid == 0) ptx::bulk_wait_read_all_but_last();
             ok = ptx::named_bar_and(3, PR_WORK, ptx::mbar_wait_sleep(bar3, ph));
             if (!ok) break;
             tc::fence_after();
             {
-                // Q' = scale e^{G_r} q_r / |q_r| + (P Wn)_r, in place over the query rows
+                // Q' = scale e^{G_r} q_r / |q_r| + (P Wn)_r into the Kt tile, in image layout
                 // (columns [64 hh, 64 hh + 64) of i)
                 const float fa = F[fQF + ra], fb = F[fQF + rb];
                 float v[32];
                 tc::ld16x256<8>(tmem + lane_off + 128 + 64 * hh, v);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    __half2 *pa = reinterpret_cast<__half2 *>(sm + rKQ + hh * 16384 + 8192 + sw(ra, k) + 2 * cp);
-                    __half2 *pb = reinterpret_cast<__half2 *>(sm + rKQ + hh * 16384 + 8192 + sw(rb, k) + 2 * cp);
-                    const float2 xa = __half22float2(*pa), xb = __half22float2(*pb);
-                    *pa = __floats2half2_rn(fmaf(fa, xa.x, v[4 * k]), fmaf(fa, xa.y, v[4 * k + 1]));
-                    *pb = __floats2half2_rn(fmaf(fb, xb.x, v[4 * k + 2]), fmaf(fb, xb.y, v[4 * k + 3]));
+                    const float2 xa = __half22float2(
+                        *reinterpret_cast<const __half2 *>(sm + rKQ + hh * 16384 + 8192 + sw(ra, k) + 2 * cp));
+                    const float2 xb = __half22float2(
+                        *reinterpret_cast<const __half2 *>(sm + rKQ + hh * 16384 + 8192 + sw(rb, k) + 2 * cp));
+                    *reinterpret_cast<__half2 *>(sm + rKt + hh * 8192 + sw(ra, k) + 2 * cp) =
+                        __floats2half2_rn(fmaf(fa, xa.x, v[4 * k]), fmaf(fa, xa.y, v[4 * k + 1]));
+                    *reinterpret_cast<__half2 *>(sm + rKt + hh * 8192 + sw(rb, k) + 2 * cp) =
+                        __floats2half2_rn(fmaf(fb, xb.x, v[4 * k + 2]), fmaf(fb, xb.y, v[4 * k + 3]));
                 }
             }
             tc::fence_async_smem();
             ptx::named_bar_sync(3, PR_WORK);
             if (tid == 0) {
-                ptx::bulk_s2g(dst + IM_Q, sm + rKQ + 8192, 8192);
-                ptx::bulk_s2g(dst + IM_Q + 8192, sm + rKQ + 16384 + 8192, 8192);
-                ptx::bulk_commit();
-                // the key, query and value tiles are free for the producer's next loads once
-                // the copies have read them
+                // the key, query and value tiles are free for the producer's next loads once the
+                // copy of U has read the value tile
                 ptx::bulk_wait_read();
                 ptx::mbar_arrive(tfree);
+                ptx::bulk_s2g(dst + IM_Q, sm + rKt, 16384);
+                ptx::bulk_commit();
             }
             {
                 // E = Wn^T Kt + (e^{G_C} - 1) I: row i = 32 q + lane, columns [64 hh, 64 hh + 64),
@@ -875,6 +890,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 const unsigned char *src = img + ((size_t)(slot0 + c) * p.Hv + h) * IM_BYTES;
                 unsigned char *dstb = sm + cImg + bf * IM_BYTES;
                 ptx::mbar_arrive_expect_tx(&land[bf], IM_BYTES - skip);
+                // the image two chunks ahead into L2, so that its load from there is short
+                if (c + 2 < nch)
+                    ptx::prefetch_l2(src + 2 * (size_t)p.Hv * IM_BYTES + skip, IM_BYTES - skip);
                 if (STEP == kStepE) ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);  // E and Q'
                 else ptx::bulk_g2s(dstb + IM_Q, src + IM_Q, IM_U - IM_Q, &land[bf]);
                 ptx::bulk_g2s(dstb + IM_U, src + IM_U, IM_BYTES - IM_U, &land[bf]);  // U, P, Kt

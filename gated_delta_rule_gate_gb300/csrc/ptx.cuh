@@ -86,6 +86,10 @@ __device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t by
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until the sources of this thread's committed bulk groups have been read.
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until the sources of all but this thread's most recent committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_read_all_but_last() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Waits until this thread's committed bulk groups have completed.
 __device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -329,6 +333,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
         "[%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+// Brings `bytes` of global memory into L2 ahead of a later load (no shared memory,
+// no completion to wait for).  Address 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// The same for one box of a tensor map.
+__device__ __forceinline__ void prefetch_tile_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 // Named barrier over `nthreads` threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool pred) {
