@@ -274,7 +274,9 @@ def kernel_name(p, path):
     if per_key:
         return "recurrent_long_kernel<%d>" % p["dk"]
     if p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16" and p["rule"] != "gdn2":
-        return "chunk_chain_kernel<%d>" % {"linear": 0, "gated": 1}.get(p["rule"], 2)
+        retr = p["rule"] in ("delta", "gated_delta")
+        return "chunk_prepare_kernel<%d>+chunk_chain_kernel<%d>" % (
+            int(retr), {"linear": 0, "gated": 1}.get(p["rule"], 2))
     return "chunked_mma_kernel<%d,%s>" % (p["dk"], "true" if p["rule"] == "gdn2" else "false")
 
 
@@ -283,7 +285,7 @@ def launches_per_call(p, path):
     chunk-offset scan and the per-chunk operand pass (with the triangular
     solves for the delta rules) before the chain."""
     k = kernel_name(p, path)
-    return 3 if k.startswith("chunk_chain_kernel") else 1
+    return 3 if "chunk_chain_kernel" in k else 1
 
 
 def kernel_source_digest(path, kernel=""):
