@@ -271,9 +271,14 @@ def kernel_name(p, path):
         L = p.get("seq_len") or p["total_tokens"] // max(p["batch"], 1)
         return ("recurrent_long_kernel<%d>" if L > 32 else "recurrent_pipe_kernel<%d>") % p["dk"]
     per_key = p.get("decay_per_key") and p["rule"] in ("gated", "gated_delta", "gdn2")
+    tc_shape = p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16"
+    f32_gates = (p.get("decay") is None or p["decay"].dtype == torch.float32 or not per_key) and \
+        (p["rule"] != "gdn2" or p["beta"].dtype == torch.float32)
+    if tc_shape and f32_gates and (p["rule"] == "gdn2" or (per_key and p["rule"] == "gated_delta")):
+        return "chunk_prepare_perkey_kernel<%d>+chunk_chain_kernel<2>" % int(p["rule"] == "gdn2")
     if per_key:
         return "recurrent_long_kernel<%d>" % p["dk"]
-    if p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16" and p["rule"] != "gdn2":
+    if tc_shape and p["rule"] != "gdn2":
         retr = p["rule"] in ("delta", "gated_delta")
         return "chunk_prepare_kernel<%d>+chunk_chain_kernel<%d>" % (
             int(retr), {"linear": 0, "gated": 1}.get(p["rule"], 2))
@@ -289,11 +294,19 @@ def launches_per_call(p, path):
 
 
 def kernel_source_digest(path, kernel=""):
-    name = "recurrent.cu" if kernel.startswith("recurrent") else (
-        "chunked_tc.cu" if kernel.startswith(("chunk_chain", "chunk_prepare")) else "chunked.cu")
-    f = os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc", name)
-    with open(f, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+    """SHA-256 prefix of the sources the dispatched kernels are built from."""
+    if kernel.startswith("recurrent"):
+        names = ["recurrent.cu"]
+    elif kernel.startswith(("chunk_chain", "chunk_prepare")):
+        names = ["chunked_tc.cu", "chunk_image.cuh"] + (
+            ["chunked_tc_perkey.cu"] if "perkey" in kernel else [])
+    else:
+        names = ["chunked.cu"]
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload, path, kernel=""):

@@ -608,12 +608,13 @@ bool chunked_supported(const Problem &p, int, const char **why) {
 
 cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_bytes, cudaStream_t stream) {
     (void)chunk;
+    if (chunked_tc_eligible(p)) return launch_chunked_tc(p, ws, ws_bytes, stream);
     if ((p.flags & kPerKey) && rule_has_decay(p.rule)) {
-        // Per-key decay does not factor through the key contraction; this
-        // build runs it through the token-serial kernel (same result).
+        // Per-key decay outside the tcgen05 path's shapes and rules (the gated
+        // rule, other head sizes, fp32 activations) runs through the
+        // token-serial kernel (same result).
         return launch_recurrent(p, stream);
     }
-    if (chunked_tc_eligible(p)) return launch_chunked_tc(p, ws, ws_bytes, stream);
     const bool g2 = p.rule == kGdn2;
     switch (p.dk) {
         case 16: return g2 ? launch_mma<16, true>(p, stream) : launch_mma<16, false>(p, stream);

@@ -31,6 +31,7 @@
 #include <cuda.h>  // CUtensorMap (the encoder is fetched through the runtime)
 #include <cuda_fp16.h>
 
+#include "chunk_image.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -38,53 +39,7 @@
 namespace gdn {
 namespace {
 
-constexpr int TC_C = 64;  // tokens per chunk
-
-// ---------------------------------------------------------------------------
-// Chunk operand image: the state-independent operands of one (chunk, value
-// head), in shared-memory layout (128-byte swizzle; 64 fp16 per 128-byte row;
-// 16-byte chunk c of row r stored at chunk position c ^ (r % 8)):
-//   E   [2 j-blocks][128 i][64 j]   B operand, N-major (row = K index i)
-//   Q'  [2 i-blocks][64 t][64 i]    B operand, K-major (row = N index t)
-//   U   [2 v-blocks][64 t][64 v]    A operand of U^T, M-major (row = K index t)
-//   P   [64 r][64 t]                B operand, K-major (row = N index r)
-//   Kt  [2 j-blocks][64 t][64 j]    B operand, N-major (row = K index t)
-constexpr int IM_E = 0, IM_Q = 32768, IM_U = 49152, IM_P = 65536, IM_KT = 73728;
-constexpr int IM_BYTES = 90112;
-
-// writes 8 consecutive fp16 values (one 16-byte chunk) of row `row`, chunk
-// `ch` (0..7) of a 64-column block
-__device__ __forceinline__ void st_chunk(unsigned char *tile, int row, int ch, const float *x) {
-    uint4 u;
-    u.x = ptx::pack_h2(x[0], x[1]);
-    u.y = ptx::pack_h2(x[2], x[3]);
-    u.z = ptx::pack_h2(x[4], x[5]);
-    u.w = ptx::pack_h2(x[6], x[7]);
-    *reinterpret_cast<uint4 *>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) = u;
-}
-
-// byte offset of 16-byte chunk `ch` of row `r` in a 128-byte-swizzled block
-__device__ __forceinline__ int sw(int r, int ch) { return r * 128 + ((ch ^ (r & 7)) << 4); }
-
-// Scales the eight fp16 values of one 16-byte chunk by f: fp16 products while
-// the factor is well inside the fp16 range, fp32 products beyond it (the
-// factor 1 / |x| of an all-zero padding row is 1e6: 0 x 1e6 must stay 0).
-constexpr float kHalfSafe = 8192.f;
-__device__ __forceinline__ uint4 scale_chunk(uint4 u, float f) {
-    __half2 *hp = reinterpret_cast<__half2 *>(&u);
-    if (fabsf(f) <= kHalfSafe) {
-        const __half2 f2 = __float2half2_rn(f);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) hp[w] = __hmul2(hp[w], f2);
-    } else {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float2 x = __half22float2(hp[w]);
-            hp[w] = __floats2half2_rn(x.x * f, x.y * f);
-        }
-    }
-    return u;
-}
+using namespace img;
 
 // number of chunks of request b
 __device__ __forceinline__ int request_chunks(const Problem &p, int b) {
@@ -200,6 +155,7 @@ constexpr int rHdr = rGin + 2 * 128 * 4; // 2 x {slot, head, first token, tokens
 constexpr int rBar = rHdr + 32;          // land, tiles free, three MMA barriers, TMEM address
 constexpr int PR_SMEM = rBar + 64 + 1024;
 static_assert(rTf + 64 * FT * 4 <= rKt, "prepare layout");
+static_assert(FA == kSolveStride && FT == kSolveStride && PR_WORK == kSolveThreads, "prepare layout: solve");
 static_assert(rAt + 32768 <= rKt, "prepare layout: E staging");
 static_assert(rKt % 1024 == 0 && rP % 1024 == 0, "prepare layout: swizzled tiles");
 static_assert(2 * (PR_SMEM + 1024) <= 228 * 1024, "prepare: two CTAs per SM");
@@ -223,7 +179,6 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
     const long long ntasks = (long long)total * p.Hv;
     float *At = reinterpret_cast<float *>(sm + rAt);
     float *Tf = reinterpret_cast<float *>(sm + rTf);
-    float *Y = Tf + 32;  // [32][FT]: rows 0..31, columns 32..63 of T, never part of T
     float *F = reinterpret_cast<float *>(sm + rSc);
     uint64_t *land = reinterpret_cast<uint64_t *>(sm + rBar);
     uint64_t *tfree = land + 1, *bar1 = land + 2, *bar2 = land + 3, *bar3 = land + 4;
@@ -464,79 +419,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 ph ^= 1u;
                 continue;
             }
-            {
-                // diagonal blocks: column c of the inverse of block b, rows 4 s .. 4 s + 3 of it,
-                // right-looking (once x[j] is final it updates every later row at once)
-                const int b = tid >> 6, c = (tid >> 2) & 15, s4 = 4 * (tid & 3);
-                float x[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) x[e] = (s4 + e == c) ? 1.f : 0.f;
-#pragma unroll
-                for (int j = 0; j < 15; ++j) {
-                    const float xj = __shfl_sync(0xffffffffu, x[j & 3], (lane & ~3) | (j >> 2));
-                    const float4 a = *reinterpret_cast<const float4 *>(At + (16 * b + j) * FA + 16 * b + s4);
-                    x[0] = s4 > j ? fmaf(-a.x, xj, x[0]) : x[0];
-                    x[1] = s4 + 1 > j ? fmaf(-a.y, xj, x[1]) : x[1];
-                    x[2] = s4 + 2 > j ? fmaf(-a.z, xj, x[2]) : x[2];
-                    x[3] = s4 + 3 > j ? fmaf(-a.w, xj, x[3]) : x[3];
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) Tf[(16 * b + s4 + e) * FT + 16 * b + c] = x[e];
-                // the strictly upper blocks (0,1) and (2,3) that the 32x32 products read are zero
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int idx = 2 * tid + e, blk = idx >> 8, rr = (idx >> 4) & 15, cc = idx & 15;
-                    Tf[(32 * blk + rr) * FT + 32 * blk + 16 + cc] = 0.f;
-                }
-            }
-            ptx::named_bar_sync(3, PR_WORK);
-            {
-                // level 1: blocks (1,0) and (3,2): Y = A_{b,b-1} T_{b-1}, then L = -T_b Y
-                const int blk = tid >> 7, r = (tid >> 3) & 15, c = 2 * (tid & 7), o0 = 32 * blk;
-                float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float a = At[(o0 + k) * FA + o0 + 16 + r];
-                    const float2 tv = *reinterpret_cast<const float2 *>(Tf + (o0 + k) * FT + o0 + c);
-                    y0 = fmaf(a, tv.x, y0);
-                    y1 = fmaf(a, tv.y, y1);
-                }
-                *reinterpret_cast<float2 *>(Y + (16 * blk + r) * FT + c) = make_float2(y0, y1);
-                ptx::named_bar_sync(3, PR_WORK);
-                float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float tv = Tf[(o0 + 16 + r) * FT + o0 + 16 + k];
-                    const float2 yy = *reinterpret_cast<const float2 *>(Y + (16 * blk + k) * FT + c);
-                    l0 = fmaf(tv, yy.x, l0);
-                    l1 = fmaf(tv, yy.y, l1);
-                }
-                *reinterpret_cast<float2 *>(Tf + (o0 + 16 + r) * FT + o0 + c) = make_float2(-l0, -l1);
-            }
-            ptx::named_bar_sync(3, PR_WORK);
-            {
-                // level 2: Y = A_10 T_0 (32 x 32), then L = -T_1 Y; thread = (row, 4 columns).
-                // T_0 and T_1 are lower triangular: Y[r][c] sums k >= c, L[r][c] sums k <= r.
-                const int r = tid >> 3, c = 4 * (tid & 7);
-                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                for (int k = c; k < 32; ++k) {
-                    const float a = At[k * FA + 32 + r];
-                    const float4 tv = *reinterpret_cast<const float4 *>(Tf + k * FT + c);
-                    y.x = fmaf(a, tv.x, y.x), y.y = fmaf(a, tv.y, y.y), y.z = fmaf(a, tv.z, y.z), y.w = fmaf(a, tv.w, y.w);
-                }
-                *reinterpret_cast<float4 *>(Y + r * FT + c) = y;
-                ptx::named_bar_sync(3, PR_WORK);
-                float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                for (int k = 0; k <= r; ++k) {
-                    const float tv = Tf[(32 + r) * FT + 32 + k];
-                    const float4 yy = *reinterpret_cast<const float4 *>(Y + k * FT + c);
-                    l.x = fmaf(tv, yy.x, l.x), l.y = fmaf(tv, yy.y, l.y), l.z = fmaf(tv, yy.z, l.z), l.w = fmaf(tv, yy.w, l.w);
-                }
-                *reinterpret_cast<float4 *>(Tf + (32 + r) * FT + c) = make_float4(-l.x, -l.y, -l.z, -l.w);
-            }
-            ptx::named_bar_sync(3, PR_WORK);
+            solve_unit_lower64(At, Tf, tid);
             {
                 // Tb[r][j] = T[r][j] beta_j and Ta'[r][j] = -T[r][j] beta_j e^{G_j} / |k_j| (j <= r),
                 // fp16, K-major (the At rows are no longer read); thread = (row, 16 columns)
@@ -969,8 +852,11 @@ size_t head_bytes(const Problem &p) {
 }  // namespace
 
 bool chunked_tc_eligible(const Problem &p) {
+    // scalar decay, v1 rules: the scalar prepare kernel; per-key decay of gated_delta and
+    // GDN-2: the per-key prepare kernel.  Both feed the same chain kernel.
     const bool rule_ok = p.rule == kLinear || p.rule == kGated || p.rule == kDelta || p.rule == kGatedDelta;
-    return rule_ok && p.dk == 128 && p.dv == 128 && p.act_f16 && !((p.flags & kPerKey) && rule_has_decay(p.rule)) &&
+    const bool scalar_ok = rule_ok && !((p.flags & kPerKey) && rule_has_decay(p.rule));
+    return (scalar_ok || chunk_prepare_perkey_eligible(p)) && p.dk == 128 && p.dv == 128 && p.act_f16 &&
            al16(p.q) && al16(p.k) && al16(p.v) && al16(p.fin) && (p.init == nullptr || al16(p.init));
 }
 
@@ -997,8 +883,7 @@ static EncodeTiledFn encoder() {
     return fn;
 }
 
-// [T, H, 128] fp16 rows -> boxes of 64 channels x 1 head x 64 tokens, 128-byte swizzle.
-static bool make_map(CUtensorMap *m, const void *base, int heads, int tokens) {
+bool make_kqv_map(CUtensorMap *m, const void *base, int heads, int tokens) {
     EncodeTiledFn enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)tokens};
@@ -1029,7 +914,8 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         if (dev < 64) attr_done[dev] = 1;
     }
     CUtensorMap tk, tq, tv;
-    if (!make_map(&tk, p.k, p.Hq, p.T) || !make_map(&tq, p.q, p.Hq, p.T) || !make_map(&tv, p.v, p.Hv, p.T))
+    if (!make_kqv_map(&tk, p.k, p.Hq, p.T) || !make_kqv_map(&tq, p.q, p.Hq, p.T) ||
+        !make_kqv_map(&tv, p.v, p.Hv, p.T))
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)((long long)p.B * p.Hv);
     if (grid == 0) return cudaSuccess;
@@ -1046,13 +932,17 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     // persistent prepare CTAs: two per SM (shared and tensor memory), at most one per task
     const long long tasks = (long long)cap * p.Hv;
     const long long pgrid = std::min<long long>(tasks, 2LL * sm_count());
-    if (retr)
-        chunk_prepare_kernel<true><<<(unsigned)pgrid, PR_THREADS, PR_SMEM, stream>>>(p, tk, tq, tv, offs, slot_req, img,
-                                                                                   cap);
-    else
-        chunk_prepare_kernel<false><<<(unsigned)pgrid, PR_THREADS, PR_SMEM, stream>>>(p, tk, tq, tv, offs, slot_req,
-                                                                                    img, cap);
-    e = cudaGetLastError();
+    if (chunk_prepare_perkey_eligible(p)) {
+        e = launch_chunk_prepare_perkey(p, tk, tq, tv, offs, slot_req, img, cap, stream);
+    } else {
+        if (retr)
+            chunk_prepare_kernel<true><<<(unsigned)pgrid, PR_THREADS, PR_SMEM, stream>>>(p, tk, tq, tv, offs, slot_req,
+                                                                                       img, cap);
+        else
+            chunk_prepare_kernel<false><<<(unsigned)pgrid, PR_THREADS, PR_SMEM, stream>>>(p, tk, tq, tv, offs, slot_req,
+                                                                                        img, cap);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     if (p.rule == kLinear)
         chunk_chain_kernel<kStepPlain><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);

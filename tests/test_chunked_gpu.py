@@ -47,6 +47,17 @@ CASES += [
          l2norm_q=True),
     dict(rule="gated_delta", act="f16", dk=64, dv=64, hq=1, hv=2, decay_per_key=True),
     dict(rule="gdn2", act="f16", dk=64, dv=64, hq=1, hv=1, decay_per_key=True, write_gate=True),
+    # per-key decay on the tensor-core path (fp32 per-key gates, dk = dv = 128)
+    dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=2, decay_per_key=True, gate_dtype="f32"),
+    dict(rule="gdn2", act="f16", dk=128, dv=128, hq=2, hv=4, decay_per_key=True, gate_dtype="f32",
+         write_gate=True),
+    dict(rule="gdn2", act="f16", dk=128, dv=128, hq=1, hv=2, decay_per_key=True, gate="log",
+         logdecay_range=(-6.0, 0.0), beta_mode="direct", l2norm_q=True),
+    dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=2, decay_per_key=True, gate="log",
+         logdecay_range=(-3.0, 0.0), l2norm_q=True),
+    # per-key decay in fp16 and the gated rule with per-key decay take the token-serial kernel
+    dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True),
+    dict(rule="gated", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True, gate_dtype="f32"),
 ]
 
 
