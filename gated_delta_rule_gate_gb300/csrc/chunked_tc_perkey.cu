@@ -82,6 +82,22 @@ __device__ __forceinline__ int kq_at(int r, int ch, bool query) {
 // the same for a [2 c-blocks][64 t][64 c] tile (value, Kt, Qh, X', b .* k)
 __device__ __forceinline__ int t64(int r, int ch) { return (ch >> 3) * 8192 + sw(r, ch & 7); }
 
+// ln(1 + e^x) for the per-key raw gate, 8192 of them per task: x itself above
+// 15 (the correction, below 3.1e-7, is under fp32 resolution of x);
+// y (1 - y / 2) with y = e^x below y = 1e-3 (the dropped terms are below
+// 3.4e-7 relative); otherwise the fast logarithm of 1 + y, whose error stays
+// below 2e-4 relative near y = 1e-3 and near fp32 resolution for y ~ 1.  The
+// log decay it feeds is then exact to a few 1e-7 absolute.
+__device__ __forceinline__ float softplus_fast(float x) {
+    const float y = __expf(x);
+    const float r = y < 1e-3f ? y * fmaf(-0.5f, y, 1.f) : __logf(1.f + y);
+    return x > 15.f ? x : r;
+}
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+
+__device__ __forceinline__ float2 h2f(const unsigned char *p) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(p));
+}
 __device__ __forceinline__ void unpack8(uint4 u, float *x) {
     const __half2 *h = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
@@ -295,21 +311,27 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             // Gamma of the log decays per channel, in place
             const int gc = tid & 127, ghf = tid >> 7;
             {
-                const float gb = (perkey && p.raw_gate) ? p.gate_bias[(size_t)h * 128 + gc] : 0.f;
-                float run = 0.f;
-#pragma unroll 4
-                for (int tt = 0; tt < 32; ++tt) {
-                    const int tk = 32 * ghf + tt;
-                    float g;
-                    if (perkey) {
-                        g = G[tk * 128 + gc];
-                        if (p.raw_gate) g = gs * softplus_f(g + gb);
-                        if (tk >= n) g = 0.f;
-                    } else {
-                        g = gin[tk];
+                float gv[32];
+                if (perkey) {
+                    const float gb = p.raw_gate ? p.gate_bias[(size_t)h * 128 + gc] : 0.f;
+#pragma unroll
+                    for (int tt = 0; tt < 32; ++tt) gv[tt] = G[(32 * ghf + tt) * 128 + gc];
+                    if (p.raw_gate) {
+#pragma unroll
+                        for (int tt = 0; tt < 32; ++tt) gv[tt] = gs * softplus_fast(gv[tt] + gb);
                     }
-                    run += g;
-                    G[tk * 128 + gc] = run;
+#pragma unroll
+                    for (int tt = 0; tt < 32; ++tt)
+                        if (32 * ghf + tt >= n) gv[tt] = 0.f;
+                } else {
+#pragma unroll
+                    for (int tt = 0; tt < 32; ++tt) gv[tt] = gin[32 * ghf + tt];
+                }
+                float run = 0.f;
+#pragma unroll
+                for (int tt = 0; tt < 32; ++tt) {
+                    run += gv[tt];
+                    G[(32 * ghf + tt) * 128 + gc] = run;
                 }
                 if (warp == 0) {
                     F[fB + lane] = gin[64 + lane];
@@ -318,7 +340,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             }
             // 1 / |k| and 1 / |q| per row (warp = 16 of the 128 key and query rows, lane = 4
             // channels); for GDN-2 also b .* k of the key rows (raw keys), fp16
-#pragma unroll 2
+#pragma unroll
             for (int k8 = 0; k8 < 16; ++k8) {
                 const int rr = 16 * warp + k8, r = rr & 63;
                 const bool qrow = rr >= 64;
@@ -331,8 +353,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 if (GDN2 && !qrow) {
                     float4 bb = *reinterpret_cast<const float4 *>(sm + pXp + r * 512 + lane * 16);
                     if (p.flags & kBetaSigmoid) {
-                        bb.x = sigmoid_f(bb.x), bb.y = sigmoid_f(bb.y);
-                        bb.z = sigmoid_f(bb.z), bb.w = sigmoid_f(bb.w);
+                        bb.x = sigmoid_fast(bb.x), bb.y = sigmoid_fast(bb.y);
+                        bb.z = sigmoid_fast(bb.z), bb.w = sigmoid_fast(bb.w);
                     }
                     uint2 o;
                     o.x = ptx::pack_h2(bb.x * x0.x, bb.y * x0.y);
@@ -437,41 +459,65 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 for (int tt = 0; tt < 32; ++tt) G[(32 * ghf + tt) * 128 + gc] = __expf(gv[tt + 1] - gv[tt]);
                 ptx::named_bar_sync(3, PK_WORK);
             }
-            // diagonal blocks of A and P: thread = (block s, row R of it, channel quarter cq); the
-            // factor e^{Gamma_R - Gamma_J} runs down J from R as a product of per-token decays
-            const int ds = warp >> 1, drl = 8 * (warp & 1) + (lane >> 2), dcq = lane & 3, dR = 16 * ds + drl;
-            float Ad[16], Pd[16];
+            // diagonal blocks of A and P: thread = (block s, rows rp and rp + 8 of it, channel group
+            // cg: the pairs 16 m + 2 cg, + 1 for m = 0..7), so every thread has one short and one
+            // long row; the factor e^{Gamma_R - Gamma_J} runs down J from R as a product of
+            // per-token decays, two channels at a time (packed fp32x2)
+            const int ds = warp >> 1, drp = 4 * (warp & 1) + (lane >> 3), dcg = lane & 7;
+            const int dR1 = 16 * ds + drp, dR2 = dR1 + 8;
+            float2 A1[8], P1[8], A2[16], P2[16];
             {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) Ad[e] = Pd[e] = 0.f;
-                const int bo = 4 * dcq;
+                for (int e = 0; e < 8; ++e) A1[e] = P1[e] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) A2[e] = P2[e] = make_float2(0.f, 0.f);
+                const int bo = 4 * (dcg & 3);
 #pragma unroll 1
-                for (int ic = 0; ic < 16; ++ic) {
-                    const int xoff = GDN2 ? pKap + t64(dR, ic) : pKQ + kq_at(dR, ic, false);
-                    const float2 xk = __half22float2(*reinterpret_cast<const __half2 *>(sm + xoff + bo));
-                    const float2 xq =
-                        __half22float2(*reinterpret_cast<const __half2 *>(sm + pKQ + kq_at(dR, ic, true) + bo));
-                    float e0 = 1.f, e1 = 1.f;
+                for (int m = 0; m < 8; ++m) {
+                    const int ic = 2 * m + (dcg >> 2);  // the 16-byte chunk of channels 16 m + 2 cg, + 1
+                    const int xo1 = GDN2 ? pKap + t64(dR1, ic) : pKQ + kq_at(dR1, ic, false);
+                    const int xo2 = GDN2 ? pKap + t64(dR2, ic) : pKQ + kq_at(dR2, ic, false);
+                    const float2 xk1 = h2f(sm + xo1 + bo), xk2 = h2f(sm + xo2 + bo);
+                    const float2 xq1 = h2f(sm + pKQ + kq_at(dR1, ic, true) + bo);
+                    const float2 xq2 = h2f(sm + pKQ + kq_at(dR2, ic, true) + bo);
+                    float2 e1 = make_float2(1.f, 1.f), e2 = e1;
 #pragma unroll
                     for (int jl = 15; jl >= 0; --jl) {
-                        if (jl <= drl) {
+                        if (jl <= drp + 8) {
                             const int J = 16 * ds + jl;
-                            const float2 kk =
-                                __half22float2(*reinterpret_cast<const __half2 *>(sm + pKQ + kq_at(J, ic, false) + bo));
-                            const float t0 = kk.x * e0, t1 = kk.y * e1;
-                            Ad[jl] = fmaf(xk.x, t0, fmaf(xk.y, t1, Ad[jl]));
-                            Pd[jl] = fmaf(xq.x, t0, fmaf(xq.y, t1, Pd[jl]));
-                            const float2 a2 = *reinterpret_cast<const float2 *>(G + J * 128 + 8 * ic + 2 * dcq);
-                            e0 *= a2.x, e1 *= a2.y;
+                            const float2 kk = h2f(sm + pKQ + kq_at(J, ic, false) + bo);
+                            const float2 a2 = *reinterpret_cast<const float2 *>(G + J * 128 + 16 * m + 2 * dcg);
+                            const float2 t2 = __fmul2_rn(kk, e2);
+                            A2[jl] = __ffma2_rn(xk2, t2, A2[jl]);
+                            P2[jl] = __ffma2_rn(xq2, t2, P2[jl]);
+                            e2 = __fmul2_rn(e2, a2);
+                            if (jl < 8 && jl <= drp) {
+                                const float2 t1 = __fmul2_rn(kk, e1);
+                                A1[jl & 7] = __ffma2_rn(xk1, t1, A1[jl & 7]);
+                                P1[jl & 7] = __ffma2_rn(xq1, t1, P1[jl & 7]);
+                                e1 = __fmul2_rn(e1, a2);
+                            }
                         }
                     }
                 }
+            }
+            // sums over the channel pair and the eight channel groups
+            float a1[8], p1[8], a2s[16], p2s[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a1[e] = A1[e].x + A1[e].y, p1[e] = P1[e].x + P1[e].y;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) a2s[e] = A2[e].x + A2[e].y, p2s[e] = P2[e].x + P2[e].y;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    a1[e] += __shfl_xor_sync(0xffffffffu, a1[e], o);
+                    p1[e] += __shfl_xor_sync(0xffffffffu, p1[e], o);
+                }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    Ad[e] += __shfl_xor_sync(0xffffffffu, Ad[e], 1);
-                    Ad[e] += __shfl_xor_sync(0xffffffffu, Ad[e], 2);
-                    Pd[e] += __shfl_xor_sync(0xffffffffu, Pd[e], 1);
-                    Pd[e] += __shfl_xor_sync(0xffffffffu, Pd[e], 2);
+                    a2s[e] += __shfl_xor_sync(0xffffffffu, a2s[e], o);
+                    p2s[e] += __shfl_xor_sync(0xffffffffu, p2s[e], o);
                 }
             }
             // the off-block products are done: their operand area takes A
@@ -479,27 +525,37 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             if (!ok) break;
             tc::fence_after();
             {
-                const float bR = F[fB + dR], ikR = F[fIK + dR], iqR = F[fIQ + dR], sc = p.scale;
-                // A[R][J] of this block, stored transposed; lane dcq takes columns 4 dcq .. 4 dcq + 3
+                const float sc = p.scale;
+                const float f1 = F[fB + dR1] * F[fIK + dR1], f2 = F[fB + dR2] * F[fIK + dR2];
+                const float g1 = sc * F[fIQ + dR1], g2 = sc * F[fIQ + dR2];
+                // A[R][J] of this block for both rows, stored transposed: lane cg takes columns 2 cg, + 1
 #pragma unroll
                 for (int jl = 0; jl < 16; ++jl)
-                    if ((jl >> 2) == dcq) {
+                    if ((jl >> 1) == dcg) {
                         const int J = 16 * ds + jl;
-                        At[J * kFA + dR] = jl < drl ? bR * ikR * F[fIK + J] * Ad[jl] : 0.f;
+                        const float ikJ = F[fIK + J];
+                        At[J * kFA + dR1] = (jl < 8 && jl < drp) ? f1 * ikJ * a1[jl & 7] : 0.f;
+                        At[J * kFA + dR2] = jl < drp + 8 ? f2 * ikJ * a2s[jl] : 0.f;
                     }
-                // P row R: this block's two chunks (lanes 0, 1), the zero chunks right of it (lanes 2, 3)
-                if (dcq < 2) {
+                // P rows: this block's two chunks of each row (lanes 0-3), the zero chunks right of
+                // the block (lanes 4-7)
+                if (dcg < 4) {
+                    const bool second = dcg >= 2;
+                    const int c = dcg & 1;
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float v = dcq == 0 ? Pd[e] : Pd[8 + e];
-                        const int jl = 8 * dcq + e;
-                        x[e] = jl <= drl ? sc * iqR * F[fIK + 16 * ds + jl] * v : 0.f;
+                        const int jl = 8 * c + e;
+                        const float ikJ = F[fIK + 16 * ds + jl];
+                        const float v1 = (c == 0 && e <= drp) ? g1 * ikJ * p1[e] : 0.f;
+                        const float v2 = c == 0 ? p2s[e] : p2s[8 + e];
+                        x[e] = second ? (jl <= drp + 8 ? g2 * ikJ * v2 : 0.f) : v1;
                     }
-                    st_chunk(sm + pP, dR, 2 * ds + dcq, x);
+                    st_chunk(sm + pP, second ? dR2 : dR1, 2 * ds + c, x);
                 } else {
                     const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    for (int ch = 2 * ds + dcq; ch < 8; ch += 2) st_chunk(sm + pP, dR, ch, z);
+                    const int row = (dcg & 1) ? dR2 : dR1;
+                    for (int ch = 2 * ds + 2 + ((dcg >> 1) & 1); ch < 8; ch += 2) st_chunk(sm + pP, row, ch, z);
                 }
             }
             if (warp < 4) {
