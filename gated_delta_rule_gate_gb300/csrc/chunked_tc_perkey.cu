@@ -61,8 +61,8 @@ constexpr int pKap = pP + 8192;        // 16 KB: b .* k (raw keys), GDN-2; [2 c-
 constexpr int pSc = pKap + 16384;      // per-token and per-channel factors
 constexpr int pGin = pSc + 320 * 4;    // 2 x (scalar log decay, beta) of 64 tokens, from the producer
 constexpr int pHdr = pGin + 2 * 128 * 4;  // 2 x {slot, head, first token, tokens, gate scale}
-constexpr int pBar = pHdr + 2 * 8 * 4;    // land, tiles free, three MMA barriers, off-block MMA, TMEM address
-constexpr int PK_SMEM = pBar + 64 + 1024;
+constexpr int pBar = pHdr + 2 * 8 * 4;    // seven mbarriers, TMEM address
+constexpr int PK_SMEM = pBar + 96 + 1024;
 constexpr int pAt = pXo, pTf = pXo + 64 * kFA * 4, pTb = pXo, pTa = pXo + 8192;
 static_assert(pTf + 64 * kFA * 4 <= pXp, "perkey layout: solve area");
 static_assert(pYo % 1024 == 0 && pXp % 1024 == 0 && pKt % 1024 == 0 && pQh % 1024 == 0 && pP % 1024 == 0 &&
@@ -95,6 +95,10 @@ __device__ __forceinline__ float softplus_fast(float x) {
 }
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    return make_uint4(ptx::pack_h2(x[0], x[1]), ptx::pack_h2(x[2], x[3]), ptx::pack_h2(x[4], x[5]),
+                      ptx::pack_h2(x[6], x[7]));
+}
 __device__ __forceinline__ float2 h2f(const unsigned char *p) {
     return __half22float2(*reinterpret_cast<const __half2 *>(p));
 }
@@ -145,11 +149,14 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
     const bool perkey = (p.flags & kPerKey) != 0;
     float *F = reinterpret_cast<float *>(sm + pSc);
     float *G = reinterpret_cast<float *>(sm + pG);
+    // land / tfree: key, query, value tiles and erase-gate rows landed / free again;
+    // landG / gfree: the same for the log-decay rows; MMA completions bar2, bar3, barO
     uint64_t *land = reinterpret_cast<uint64_t *>(sm + pBar);
     uint64_t *tfree = land + 1, *bar2 = land + 2, *bar3 = land + 3, *barO = land + 4;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + pBar + 48);
+    uint64_t *landG = land + 5, *gfree = land + 6;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + pBar + 64);
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) ptx::mbar_init(&land[i], 1);
+        for (int i = 0; i < 7; ++i) ptx::mbar_init(&land[i], 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(tslot, 256);
@@ -212,7 +219,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         if (blockIdx.x < ntasks) nx = fetch(blockIdx.x);
         int i = 0;
         for (long long t = blockIdx.x; t < ntasks; t += NG, ++i) {
-            if (i > 0 && !ptx::mbar_wait_sleep(tfree, (i - 1) & 1)) {
+            // the log-decay rows land once the previous task has finished its diagonal blocks
+            if (i > 0 && !ptx::mbar_wait_sleep(gfree, (i - 1) & 1)) {
                 if (p.err && lane == 0) atomicOr(p.err, 2);
                 break;
             }
@@ -228,10 +236,26 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 hdr[4] = __float_as_int(nx.gs);
             }
             __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_expect_tx(landG, perkey ? (uint32_t)nx.n * 512u : 0u);
+            __syncwarp();
+            if (perkey) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int rr = lane + 32 * e;
+                    if (rr < nx.n) {
+                        const size_t th = (size_t)(nx.c0 + rr) * p.Hv + nx.h;
+                        ptx::bulk_g2s(sm + pG + rr * 512, static_cast<const float *>(p.decay) + th * 128, 512, landG);
+                    }
+                }
+            }
+            // the other tiles once the previous task's last products have read them
+            if (i > 0 && !ptx::mbar_wait_sleep(tfree, (i - 1) & 1)) {
+                if (p.err && lane == 0) atomicOr(p.err, 2);
+                break;
+            }
             if (lane == 0) {
                 const int qh = (int)((long long)nx.h * p.Hq / p.Hv);
-                const uint32_t rows = (uint32_t)nx.n * 512u * ((perkey ? 1u : 0u) + (GDN2 ? 1u : 0u));
-                ptx::mbar_arrive_expect_tx(land, 3 * 16384 + rows);
+                ptx::mbar_arrive_expect_tx(land, 3 * 16384 + (GDN2 ? (uint32_t)nx.n * 512u : 0u));
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     ptx::tma_load_3d(sm + pKQ + kb * 16384, &tmK, 64 * kb, qh, nx.c0, land);
@@ -240,15 +264,14 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 }
             }
             __syncwarp();
+            if (GDN2) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int rr = lane + 32 * e;
-                if (rr < nx.n) {
-                    const size_t th = (size_t)(nx.c0 + rr) * p.Hv + nx.h;
-                    if (perkey)
-                        ptx::bulk_g2s(sm + pG + rr * 512, static_cast<const float *>(p.decay) + th * 128, 512, land);
-                    if (GDN2)
+                for (int e = 0; e < 2; ++e) {
+                    const int rr = lane + 32 * e;
+                    if (rr < nx.n) {
+                        const size_t th = (size_t)(nx.c0 + rr) * p.Hv + nx.h;
                         ptx::bulk_g2s(sm + pXp + rr * 512, static_cast<const float *>(p.beta) + th * 128, 512, land);
+                    }
                 }
             }
             if (t + NG < ntasks) {
@@ -283,7 +306,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         uint32_t ph = 0;
         int i = 0;
         for (long long t = blockIdx.x; t < ntasks; t += NG, ++i) {
-            ok = ptx::named_bar_and(3, PK_WORK, ptx::mbar_wait_sleep(land, i & 1));
+            // the previous task's last image copies (Q', E) have read their staging areas
+            if (tid == 0) ptx::bulk_wait_read();
+            ok = ptx::named_bar_and(3, PK_WORK,
+                                    ptx::mbar_wait_sleep(landG, i & 1) && ptx::mbar_wait_sleep(land, i & 1));
             if (!ok) break;
             const float *gin = reinterpret_cast<const float *>(sm + pGin) + (i & 1) * 128;
             const int *hdr = reinterpret_cast<const int *>(sm + pHdr) + (i & 1) * 8;
@@ -338,28 +364,56 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                     F[fB + 32 + lane] = gin[96 + lane];
                 }
             }
-            // 1 / |k| and 1 / |q| per row (warp = 16 of the 128 key and query rows, lane = 4
-            // channels); for GDN-2 also b .* k of the key rows (raw keys), fp16
+            // 1 / |k| and 1 / |q| per row (warp = 16 of the 128 key and query rows: warps 0-3 keys,
+            // 4-7 queries; lane = 4 channels); for GDN-2 also b .* k of the key rows (raw keys),
+            // fp16.  All loads first, then the sums, then the stores.
+            {
+                const bool qrow = warp >= 4;
+                uint2 u[16];
 #pragma unroll
-            for (int k8 = 0; k8 < 16; ++k8) {
-                const int rr = 16 * warp + k8, r = rr & 63;
-                const bool qrow = rr >= 64;
-                const uint2 u =
-                    *reinterpret_cast<const uint2 *>(sm + pKQ + kq_at(r, lane >> 1, qrow) + (lane & 1) * 8);
-                const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
-                const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
-                const float ss = warp_sum(x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y);
-                if (lane == 0) F[(qrow ? fIQ : fIK) + r] = (qrow ? nq : nk) ? rsqrtf(ss + 1e-12f) : 1.f;
+                for (int k8 = 0; k8 < 16; ++k8) {
+                    const int r = (16 * warp + k8) & 63;
+                    u[k8] = *reinterpret_cast<const uint2 *>(sm + pKQ + kq_at(r, lane >> 1, qrow) + (lane & 1) * 8);
+                }
+                float inv[16];
+#pragma unroll
+                for (int k8 = 0; k8 < 16; ++k8) {
+                    const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&u[k8].x));
+                    const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&u[k8].y));
+                    inv[k8] = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int k8 = 0; k8 < 16; ++k8) inv[k8] += __shfl_xor_sync(0xffffffffu, inv[k8], o);
                 if (GDN2 && !qrow) {
-                    float4 bb = *reinterpret_cast<const float4 *>(sm + pXp + r * 512 + lane * 16);
-                    if (p.flags & kBetaSigmoid) {
-                        bb.x = sigmoid_fast(bb.x), bb.y = sigmoid_fast(bb.y);
-                        bb.z = sigmoid_fast(bb.z), bb.w = sigmoid_fast(bb.w);
+                    float4 bb[16];
+#pragma unroll
+                    for (int k8 = 0; k8 < 16; ++k8)
+                        bb[k8] = *reinterpret_cast<const float4 *>(sm + pXp + (16 * warp + k8) * 512 + lane * 16);
+                    const bool sg = (p.flags & kBetaSigmoid) != 0;
+#pragma unroll
+                    for (int k8 = 0; k8 < 16; ++k8) {
+                        float4 c = bb[k8];
+                        if (sg) {
+                            c.x = sigmoid_fast(c.x), c.y = sigmoid_fast(c.y);
+                            c.z = sigmoid_fast(c.z), c.w = sigmoid_fast(c.w);
+                        }
+                        const float2 x0 = __half22float2(*reinterpret_cast<const __half2 *>(&u[k8].x));
+                        const float2 x1 = __half22float2(*reinterpret_cast<const __half2 *>(&u[k8].y));
+                        u[k8].x = ptx::pack_h2(c.x * x0.x, c.y * x0.y);
+                        u[k8].y = ptx::pack_h2(c.z * x1.x, c.w * x1.y);
                     }
-                    uint2 o;
-                    o.x = ptx::pack_h2(bb.x * x0.x, bb.y * x0.y);
-                    o.y = ptx::pack_h2(bb.z * x1.x, bb.w * x1.y);
-                    *reinterpret_cast<uint2 *>(sm + pKap + t64(r, lane >> 1) + (lane & 1) * 8) = o;
+#pragma unroll
+                    for (int k8 = 0; k8 < 16; ++k8)
+                        *reinterpret_cast<uint2 *>(sm + pKap + t64(16 * warp + k8, lane >> 1) + (lane & 1) * 8) = u[k8];
+                }
+                const bool nrm = qrow ? nq : nk;
+                if (lane < 16) {
+                    float x = inv[0];
+#pragma unroll
+                    for (int k8 = 1; k8 < 16; ++k8) x = lane == k8 ? inv[k8] : x;
+                    F[(qrow ? fIQ : fIK) + ((16 * warp + lane) & 63)] = nrm ? rsqrtf(x + 1e-12f) : 1.f;
                 }
             }
             ptx::named_bar_sync(3, PK_WORK);
@@ -480,23 +534,26 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                     const float2 xk1 = h2f(sm + xo1 + bo), xk2 = h2f(sm + xo2 + bo);
                     const float2 xq1 = h2f(sm + pKQ + kq_at(dR1, ic, true) + bo);
                     const float2 xq2 = h2f(sm + pKQ + kq_at(dR2, ic, true) + bo);
-                    float2 e1 = make_float2(1.f, 1.f), e2 = e1;
+                    // e = 0 above the row's diagonal, 1 on it, then the running product: no branches,
+                    // so the loads of every step can run ahead of the product chain
+                    float2 e1 = make_float2(0.f, 0.f), e2 = e1;
+                    const float2 one = make_float2(1.f, 1.f);
 #pragma unroll
                     for (int jl = 15; jl >= 0; --jl) {
-                        if (jl <= drp + 8) {
-                            const int J = 16 * ds + jl;
-                            const float2 kk = h2f(sm + pKQ + kq_at(J, ic, false) + bo);
-                            const float2 a2 = *reinterpret_cast<const float2 *>(G + J * 128 + 16 * m + 2 * dcg);
-                            const float2 t2 = __fmul2_rn(kk, e2);
-                            A2[jl] = __ffma2_rn(xk2, t2, A2[jl]);
-                            P2[jl] = __ffma2_rn(xq2, t2, P2[jl]);
-                            e2 = __fmul2_rn(e2, a2);
-                            if (jl < 8 && jl <= drp) {
-                                const float2 t1 = __fmul2_rn(kk, e1);
-                                A1[jl & 7] = __ffma2_rn(xk1, t1, A1[jl & 7]);
-                                P1[jl & 7] = __ffma2_rn(xq1, t1, P1[jl & 7]);
-                                e1 = __fmul2_rn(e1, a2);
-                            }
+                        const int J = 16 * ds + jl;
+                        const float2 kk = h2f(sm + pKQ + kq_at(J, ic, false) + bo);
+                        const float2 a2 = *reinterpret_cast<const float2 *>(G + J * 128 + 16 * m + 2 * dcg);
+                        e2 = jl == drp + 8 ? one : e2;
+                        const float2 t2 = __fmul2_rn(kk, e2);
+                        A2[jl] = __ffma2_rn(xk2, t2, A2[jl]);
+                        P2[jl] = __ffma2_rn(xq2, t2, P2[jl]);
+                        e2 = __fmul2_rn(e2, a2);
+                        if (jl < 8) {
+                            e1 = jl == drp ? one : e1;
+                            const float2 t1 = __fmul2_rn(kk, e1);
+                            A1[jl & 7] = __ffma2_rn(xk1, t1, A1[jl & 7]);
+                            P1[jl & 7] = __ffma2_rn(xq1, t1, P1[jl & 7]);
+                            e1 = __fmul2_rn(e1, a2);
                         }
                     }
                 }
@@ -523,17 +580,21 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             // the off-block products are done: their operand area takes A
             ok = ptx::named_bar_and(3, PK_WORK, ptx::mbar_wait_sleep(barO, ph));
             if (!ok) break;
+            if (tid == 0) ptx::mbar_arrive(gfree);  // nothing reads the decays of this task any more
             tc::fence_after();
             {
                 const float sc = p.scale;
                 const float f1 = F[fB + dR1] * F[fIK + dR1], f2 = F[fB + dR2] * F[fIK + dR2];
                 const float g1 = sc * F[fIQ + dR1], g2 = sc * F[fIQ + dR2];
+                float ikb[16];  // 1 / |k_J| of this block's columns, read before any store below
+#pragma unroll
+                for (int jl = 0; jl < 16; ++jl) ikb[jl] = F[fIK + 16 * ds + jl];
                 // A[R][J] of this block for both rows, stored transposed: lane cg takes columns 2 cg, + 1
 #pragma unroll
                 for (int jl = 0; jl < 16; ++jl)
                     if ((jl >> 1) == dcg) {
                         const int J = 16 * ds + jl;
-                        const float ikJ = F[fIK + J];
+                        const float ikJ = ikb[jl];
                         At[J * kFA + dR1] = (jl < 8 && jl < drp) ? f1 * ikJ * a1[jl & 7] : 0.f;
                         At[J * kFA + dR2] = jl < drp + 8 ? f2 * ikJ * a2s[jl] : 0.f;
                     }
@@ -546,7 +607,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int jl = 8 * c + e;
-                        const float ikJ = F[fIK + 16 * ds + jl];
+                        const float ikJ = c == 0 ? ikb[e] : ikb[8 + e];
                         const float v1 = (c == 0 && e <= drp) ? g1 * ikJ * p1[e] : 0.f;
                         const float v2 = c == 0 ? p2s[e] : p2s[8 + e];
                         x[e] = second ? (jl <= drp + 8 ? g2 * ikJ * v2 : 0.f) : v1;
@@ -670,6 +731,12 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             }
             ok = ptx::named_bar_and(3, PK_WORK, ptx::mbar_wait_sleep(bar3, ph));
             if (!ok) break;
+            if (tid == 0) {
+                // the last products have read the key rows (Wn), X' and Kt, and the copies of U, P
+                // and Kt their staging areas: the next task's tiles may land
+                ptx::bulk_wait_read();
+                ptx::mbar_arrive(tfree);
+            }
             tc::fence_after();
 
             // ---- 5. Q' = Qh + P Wn in place (columns [64 hh, 64 hh + 64) of i), and
@@ -712,9 +779,6 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 ptx::bulk_s2g(dst + IM_Q, sm + pQh, 16384);
                 ptx::bulk_s2g(dst + IM_E, sm + pXo, 32768);
                 ptx::bulk_commit();
-                // every staging area has been read: the next task's tiles may land
-                ptx::bulk_wait_read();
-                ptx::mbar_arrive(tfree);
             }
             ph ^= 1u;
         }
