@@ -62,7 +62,8 @@ constexpr int pSc = pKap + 16384;      // per-token and per-channel factors
 constexpr int pGin = pSc + 320 * 4;    // 2 x (scalar log decay, beta) of 64 tokens, from the producer
 constexpr int pHdr = pGin + 2 * 128 * 4;  // 2 x {slot, head, first token, tokens, gate scale}
 constexpr int pBar = pHdr + 2 * 8 * 4;    // seven mbarriers, TMEM address
-constexpr int PK_SMEM = pBar + 96 + 1024;
+constexpr int pGb = pBar + 96;            // the head's per-key gate bias (raw arm), 128 floats
+constexpr int PK_SMEM = pGb + 512 + 1024;
 constexpr int pAt = pXo, pTf = pXo + 64 * kFA * 4, pTb = pXo, pTa = pXo + 8192;
 static_assert(pTf + 64 * kFA * 4 <= pXp, "perkey layout: solve area");
 static_assert(pYo % 1024 == 0 && pXp % 1024 == 0 && pKt % 1024 == 0 && pQh % 1024 == 0 && pP % 1024 == 0 &&
@@ -95,9 +96,9 @@ __device__ __forceinline__ float softplus_fast(float x) {
 }
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
-__device__ __forceinline__ uint4 pack8(const float *x) {
-    return make_uint4(ptx::pack_h2(x[0], x[1]), ptx::pack_h2(x[2], x[3]), ptx::pack_h2(x[4], x[5]),
-                      ptx::pack_h2(x[6], x[7]));
+__device__ __forceinline__ void ld8f(const float *p, float *x) {
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
 }
 __device__ __forceinline__ float2 h2f(const unsigned char *p) {
     return __half22float2(*reinterpret_cast<const __half2 *>(p));
@@ -109,10 +110,6 @@ __device__ __forceinline__ void unpack8(uint4 u, float *x) {
         const float2 f = __half22float2(h[w]);
         x[2 * w] = f.x, x[2 * w + 1] = f.y;
     }
-}
-__device__ __forceinline__ void ld8f(const float *p, float *x) {
-    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
-    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
 }
 
 // ---------------------------------------------------------------------------
@@ -236,7 +233,11 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 hdr[4] = __float_as_int(nx.gs);
             }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_expect_tx(landG, perkey ? (uint32_t)nx.n * 512u : 0u);
+            const bool gbias = perkey && p.raw_gate;
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(landG, (perkey ? (uint32_t)nx.n * 512u : 0u) + (gbias ? 512u : 0u));
+                if (gbias) ptx::bulk_g2s(sm + pGb, p.gate_bias + (size_t)nx.h * 128, 512, landG);
+            }
             __syncwarp();
             if (perkey) {
 #pragma unroll
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             {
                 float gv[32];
                 if (perkey) {
-                    const float gb = p.raw_gate ? p.gate_bias[(size_t)h * 128 + gc] : 0.f;
+                    const float gb = p.raw_gate ? reinterpret_cast<const float *>(sm + pGb)[gc] : 0.f;
 #pragma unroll
                     for (int tt = 0; tt < 32; ++tt) gv[tt] = G[(32 * ghf + tt) * 128 + gc];
                     if (p.raw_gate) {
@@ -801,7 +802,7 @@ bool chunk_prepare_perkey_eligible(const Problem &p) {
     const bool rule_ok = p.rule == kGdn2 || (p.rule == kGatedDelta && perkey);
     auto al = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
     return rule_ok && p.dk == 128 && p.dv == 128 && p.act_f16 && (!perkey || (!p.decay_f16 && al(p.decay))) &&
-           (p.rule != kGdn2 || (!p.beta_f16 && al(p.beta)));
+           (!perkey || !p.raw_gate || al(p.gate_bias)) && (p.rule != kGdn2 || (!p.beta_f16 && al(p.beta)));
 }
 
 cudaError_t launch_chunk_prepare_perkey(const Problem &p, const CUtensorMap &tk, const CUtensorMap &tq,
