@@ -591,6 +591,14 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
 // SMs the chain streams about 60 GB/s of images per SM: the loads, not the
 // tensor cores, set its pace.  Hand-overs are mbarriers with bounded,
 // sleeping waits; each role makes a failed wait uniform before leaving.
+//
+// Value rows never mix (S <- S + U^T Kt + S E and O^T = U^T P^T + S Q'^T act
+// row by row), so with ROWS = 64 a chain is split over two CTAs, each with
+// half the value rows: every product has M = 64 (row m of an M = 64 result
+// sits on tensor-memory lane 32 (m / 16) + m % 16, so lanes 16-31 of each
+// quarter carry nothing), each CTA loads only its half of U, and twice as
+// many SMs work on the same chains.  The launcher splits when there are fewer
+// chains than SMs.
 constexpr int CH_THREADS = 448;
 constexpr int cImg = 0;                       // 2 x IM_BYTES
 constexpr int cS = 2 * IM_BYTES;              // 32 KB: Sh, 2 blocks [128 v][64 i]
@@ -601,9 +609,11 @@ constexpr uint32_t tS = 0, tO = 128;          // tensor-memory columns: S, two O
 // what the state step of a rule needs beyond U^T Kt
 enum : int { kStepPlain = 0, kStepDecay = 1, kStepE = 2 };
 
-template <int STEP>
+template <int STEP, int ROWS>
 __global__ void __launch_bounds__(CH_THREADS, 1)
     chunk_chain_kernel(Problem p, const int *offs, const int *order, const unsigned char *img, int cap) {
+    constexpr bool HALF = ROWS == 64;
+    constexpr int SHB = ROWS * 128;  // bytes per 64-column block of Sh
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
     unsigned char *sm = smraw + (((sb0 + 1023u) & ~1023u) - sb0);
@@ -619,8 +629,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     unsigned char *sS = sm + cS;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % p.Hv, b = order[blockIdx.x / p.Hv];
-    const int row = state_row(p, b, h == 0 && tid == 0);
+    const int vh = HALF ? (int)(blockIdx.x & 1) : 0;  // which half of the value rows (ROWS = 64)
+    const int cid = HALF ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int h = cid % p.Hv, b = order[cid / p.Hv];
+    const int row = state_row(p, b, h == 0 && vh == 0 && tid == 0);
     if (row < 0) return;
     int t0, t1;
     request_range(p, b, t0, t1);
@@ -634,10 +646,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             return;
         }
     }
-    const size_t sbase = ((size_t)row * p.Hv + h) * 128 * 128;
+    const size_t sbase = ((size_t)row * p.Hv + h) * 128 * 128 + (size_t)64 * vh * 128;  // this CTA's rows
     if (nch == 0) {  // empty request: copy the incoming state through
         if (p.fin != p.init) {
-            for (int idx = tid; idx < 128 * 32; idx += CH_THREADS)
+            for (int idx = tid; idx < ROWS * 32; idx += CH_THREADS)
                 reinterpret_cast<float4 *>(p.fin + sbase)[idx] =
                     p.init ? reinterpret_cast<const float4 *>(p.init + sbase)[idx] : make_float4(0, 0, 0, 0);
         }
@@ -656,7 +668,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 
     if (warp < 8) {
         // ===================== state: S_c -> Sh after every chunk (256 threads)
-        const int q4 = warp & 3, hc = warp >> 2, i = 32 * q4 + lane;
+        const int q4 = warp & 3, hc = warp >> 2, i = (HALF ? 16 : 32) * q4 + lane;
+        const bool live = !HALF || lane < 16;  // lanes that hold a row of this CTA's state
         const uint32_t lo = tmem + ((uint32_t)(32 * q4) << 16) + tS + 64 * hc;
         const size_t srow = sbase + (size_t)i * 128 + 64 * hc;
         // e^{G_C} of chunk c, as the prepare kernel left it in the chunk's image
@@ -670,12 +683,15 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             for (int pc = 0; pc < 2; ++pc) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float4 f = p.init ? *reinterpret_cast<const float4 *>(p.init + srow + 32 * pc + 4 * j)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 f = (p.init && live)
+                                         ? *reinterpret_cast<const float4 *>(p.init + srow + 32 * pc + 4 * j)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                     v[4 * j] = f.x, v[4 * j + 1] = f.y, v[4 * j + 2] = f.z, v[4 * j + 3] = f.w;
                 }
+                if (live) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * 16384, i, 4 * pc + cc, v + 8 * cc);
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * SHB, i, 4 * pc + cc, v + 8 * cc);
+                }
                 if (STEP == kStepDecay) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] *= g0;
@@ -715,14 +731,16 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             ptx::named_bar_sync(1, 256);
             if (tid == 0) ptx::mbar_arrive(rsread);
             if (c + 1 < nch) {
+                if (live) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * 16384, i, cc, v0 + 8 * cc);
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * SHB, i, cc, v0 + 8 * cc);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * 16384, i, 4 + cc, v1 + 8 * cc);
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * SHB, i, 4 + cc, v1 + 8 * cc);
+                }
                 tc::fence_async_smem();
                 ptx::named_bar_sync(1, 256);
                 if (tid == 0) ptx::mbar_arrive(shready);
-            } else {
+            } else if (live) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     *reinterpret_cast<float4 *>(p.fin + srow + 4 * j) =
@@ -735,7 +753,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         if (!ok && p.err && tid == 0) atomicOr(p.err, 2);
     } else if (warp < 12) {
         // ===================== outputs (128 threads): O^T[i][t] -> O[t][h][i]
-        const int q4 = warp & 3, i = 32 * q4 + lane, ot = tid - 256;
+        const int q4 = warp & 3, i = (HALF ? 16 : 32) * q4 + lane, ot = tid - 256;
+        const bool live = !HALF || lane < 16;
         const uint32_t lo = tmem + ((uint32_t)(32 * q4) << 16) + tO;
         const size_t rstride = (size_t)p.Hv * 128;
         bool ok = true;
@@ -750,8 +769,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             tc::fence_before();
             ptx::named_bar_sync(2, 128);
             if (ot == 0) ptx::mbar_arrive(&ofree[bf]);
-            const int n = min(TC_C, t1 - (t0 + TC_C * c));
-            __half *orow = static_cast<__half *>(p.o) + ((size_t)(t0 + TC_C * c) * p.Hv + h) * 128 + i;
+            const int n = live ? min(TC_C, t1 - (t0 + TC_C * c)) : 0;
+            __half *orow = static_cast<__half *>(p.o) + ((size_t)(t0 + TC_C * c) * p.Hv + h) * 128 + 64 * vh + i;
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj)
                 if (jj < n) orow[jj * rstride] = __float2half_rn(o0[jj]);
@@ -764,6 +783,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         // ===================== image loads, two buffers
         if (lane == 0) {
             const uint32_t skip = STEP == kStepE ? 0u : (uint32_t)IM_Q;  // only the delta rules load E
+            const uint32_t ubytes = HALF ? 8192u : 16384u;               // U: this CTA's value rows
             for (int c = 0; c < nch; ++c) {
                 const int bf = c & 1;
                 if (c >= 2 && !ptx::mbar_wait_sleep(&freeb[bf], ((c - 2) >> 1) & 1)) {
@@ -772,13 +792,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 }
                 const unsigned char *src = img + ((size_t)(slot0 + c) * p.Hv + h) * IM_BYTES;
                 unsigned char *dstb = sm + cImg + bf * IM_BYTES;
-                ptx::mbar_arrive_expect_tx(&land[bf], IM_BYTES - skip);
+                ptx::mbar_arrive_expect_tx(&land[bf], IM_BYTES - skip - (16384u - ubytes));
                 // the image two chunks ahead into L2, so that its load from there is short
                 if (c + 2 < nch)
                     ptx::prefetch_l2(src + 2 * (size_t)p.Hv * IM_BYTES + skip, IM_BYTES - skip);
                 if (STEP == kStepE) ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);  // E and Q'
                 else ptx::bulk_g2s(dstb + IM_Q, src + IM_Q, IM_U - IM_Q, &land[bf]);
-                ptx::bulk_g2s(dstb + IM_U, src + IM_U, IM_BYTES - IM_U, &land[bf]);  // U, P, Kt
+                ptx::bulk_g2s(dstb + IM_U, src + IM_U + 8192 * vh, ubytes, &land[bf]);  // U (its rows)
+                ptx::bulk_g2s(dstb + IM_P, src + IM_P, IM_BYTES - IM_P, &land[bf]);      // P, Kt
             }
         }
     } else {
@@ -796,7 +817,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     tc::mma_f16(tmem + tS, tc::desc_sw128(base + IM_U + s * 2048, 8192),
-                                tc::desc_sw128(base + IM_KT + s * 2048, 8192), tc::idesc_f16(128, 128, true, true), true);
+                                tc::desc_sw128(base + IM_KT + s * 2048, 8192), tc::idesc_f16(ROWS, 128, true, true), true);
 
                 if (c >= 2) {
                     ok = ptx::mbar_wait_sleep(&ofree[bf], ((c - 2) >> 1) & 1);
@@ -807,23 +828,23 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     tc::mma_f16(tmem + tO + 64 * bf, tc::desc_sw128(base + IM_U + s * 2048, 8192),
-                                tc::desc_sw128(base + IM_P + s * 32), tc::idesc_f16(128, 64, true, false), s > 0);
+                                tc::desc_sw128(base + IM_P + s * 32), tc::idesc_f16(ROWS, 64, true, false), s > 0);
                 ok = ptx::mbar_wait_sleep(shready, c & 1);
                 if (!ok) break;
                 tc::fence_after();
                 // SQ: O^T += Sh Q'^T (N = 64 t, K = 128 i; both K-major)
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    tc::mma_f16(tmem + tO + 64 * bf, tc::desc_sw128(aS + (s >> 2) * 16384 + (s & 3) * 32),
-                                tc::desc_sw128(base + IM_Q + (s >> 2) * 8192 + (s & 3) * 32), tc::idesc_f16(128, 64),
+                    tc::mma_f16(tmem + tO + 64 * bf, tc::desc_sw128(aS + (s >> 2) * SHB + (s & 3) * 32),
+                                tc::desc_sw128(base + IM_Q + (s >> 2) * 8192 + (s & 3) * 32), tc::idesc_f16(ROWS, 64),
                                 true);
                 tc::commit(&barO[bf]);
                 if (STEP == kStepE) {
                     // SE: S += Sh E (N = 128 j, K = 128 i; B N-major)
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        tc::mma_f16(tmem + tS, tc::desc_sw128(aS + (s >> 2) * 16384 + (s & 3) * 32),
-                                    tc::desc_sw128(base + IM_E + s * 2048, 16384), tc::idesc_f16(128, 128, false, true),
+                        tc::mma_f16(tmem + tS, tc::desc_sw128(aS + (s >> 2) * SHB + (s & 3) * 32),
+                                    tc::desc_sw128(base + IM_E + s * 2048, 16384), tc::idesc_f16(ROWS, 128, false, true),
                                     true);
                 }
                 // every product of chunk c is done: S_{c+1} is complete and Sh is free
@@ -905,12 +926,16 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(chunk_prepare_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_chain_kernel<kStepPlain>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_chain_kernel<kStepDecay>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_chain_kernel<kStepE>, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
-        if (e != cudaSuccess) return e;
+        const void *chains[6] = {(const void *)chunk_chain_kernel<kStepPlain, 128>,
+                                 (const void *)chunk_chain_kernel<kStepDecay, 128>,
+                                 (const void *)chunk_chain_kernel<kStepE, 128>,
+                                 (const void *)chunk_chain_kernel<kStepPlain, 64>,
+                                 (const void *)chunk_chain_kernel<kStepDecay, 64>,
+                                 (const void *)chunk_chain_kernel<kStepE, 64>};
+        for (const void *fn : chains) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
+            if (e != cudaSuccess) return e;
+        }
         if (dev < 64) attr_done[dev] = 1;
     }
     CUtensorMap tk, tq, tv;
@@ -944,12 +969,22 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    if (p.rule == kLinear)
-        chunk_chain_kernel<kStepPlain><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
-    else if (p.rule == kGated)
-        chunk_chain_kernel<kStepDecay><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
-    else
-        chunk_chain_kernel<kStepE><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+    // fewer chains than SMs: two CTAs per chain, one per half of the value rows
+    if ((long long)grid < sm_count()) {
+        if (p.rule == kLinear)
+            chunk_chain_kernel<kStepPlain, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+        else if (p.rule == kGated)
+            chunk_chain_kernel<kStepDecay, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+        else
+            chunk_chain_kernel<kStepE, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+    } else {
+        if (p.rule == kLinear)
+            chunk_chain_kernel<kStepPlain, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+        else if (p.rule == kGated)
+            chunk_chain_kernel<kStepDecay, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+        else
+            chunk_chain_kernel<kStepE, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+    }
     return cudaGetLastError();
 }
 

@@ -217,3 +217,20 @@ def test_long_prefill_full_size_sampled(rule):
 def test_gdn2_full_size_sampled():
     """GDN-2 extension, B = 2, S = 4096, H = 16, per-key decay and erase gate."""
     _full(workloads.gdn2(), [1])
+
+
+@pytest.mark.parametrize("rule,per_key", [("linear", False), ("gated", False), ("delta", False),
+                                          ("gated_delta", False), ("gdn2", True)])
+def test_chunked_many_chains(rule, per_key):
+    """160 (request, head) chains, more than the GPU has SMs: the chain kernel
+    keeps one CTA per chain (fewer chains are split over two CTAs by value
+    rows, which the other parity cases cover)."""
+    kw = dict(seed=31, B=10, lengths=[70, 1, 64, 130, 5, 65, 0, 127, 33, 64], hq=8, hv=16, dk=128, dv=128,
+              act="f16", rule=rule, state="random", state_std=0.3)
+    if per_key:
+        kw.update(decay_per_key=True, gate_dtype="f32", write_gate=True)
+    p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
