@@ -214,14 +214,19 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  * accepted and none changes the result beyond rounding; <= 0 selects 64.)
  * Extra constraints (GDN_ERR_UNSUPPORTED otherwise): dk in {16, 32, 64, 128},
  * dv a multiple of 16 (<= 256), q, k, v, o and the state 16-byte aligned.
- * fp32 activations are rounded to fp16 for the products.  Per-key decay runs
- * the token-serial form (same result).
+ * fp32 activations are rounded to fp16 for the products.  Per-key decay
+ * (gated_delta) and GDN2 run on the tensor cores when dk = dv = 128, the
+ * activations are fp16 and the per-key gates (log decay, erase gate) are fp32
+ * and 16-byte aligned; per-key log decays are expected <= 0 there (decays in
+ * (0, 1], as the raw-gate arm always gives).  Other per-key problems (the
+ * gated rule, fp16 per-key gates, other head sizes) run the token-serial
+ * form (same result).
  *
  * Workspace: owned by the caller, device memory of at least
  * gdn_chunked_prefill_workspace_size() bytes, 256-byte aligned (NULL allowed
- * when that is 0); GDN_ERR_WORKSPACE otherwise.  It is non-zero for every rule
- * with dk = dv = 128, fp16 activations and no per-key decay (the tensor-core
- * path), and 0 otherwise.  Layout, for T / 64 + B + 1 chunk slots:
+ * when that is 0); GDN_ERR_WORKSPACE otherwise.  It is non-zero whenever the
+ * tensor-core path runs (every rule with dk = dv = 128 and fp16 activations,
+ * per-key problems as above), and 0 otherwise.  Layout, for T / 64 + B + 1 chunk slots:
  * per-request chunk offsets, a chunk-slot -> request table and the requests
  * ordered by length (rounded up to 1 KB); then one 88 KB image per (chunk
  * slot, value head) of the chunk's state-independent operands (fp16).
