@@ -131,11 +131,13 @@ __device__ __forceinline__ void solve_unit_lower64(const float *At, float *Tf, i
     ptx::named_bar_sync(3, kSolveThreads);
     {
         // level 2: Y = A_10 T_0 (32 x 32), then L = -T_1 Y; thread = (row, 4 columns).
-        // T_0 and T_1 are lower triangular: Y[r][c] sums k >= c, L[r][c] sums k <= r.
+        // T_0 and T_1 are lower triangular and their upper parts are stored as zeros, so
+        // both sums run over every k: the same k in every lane (broadcast loads, no bank
+        // conflicts) and no divergent trip counts.
         const int r = tid >> 3, c = 4 * (tid & 7);
         float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int k = c; k < 32; ++k) {
+        for (int k = 0; k < 32; ++k) {
             const float a = At[k * kSolveStride + 32 + r];
             const float4 tv = *reinterpret_cast<const float4 *>(Tf + k * kSolveStride + c);
             y.x = fmaf(a, tv.x, y.x), y.y = fmaf(a, tv.y, y.y), y.z = fmaf(a, tv.z, y.z), y.w = fmaf(a, tv.w, y.w);
@@ -144,7 +146,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float *At, float *Tf, i
         ptx::named_bar_sync(3, kSolveThreads);
         float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int k = 0; k <= r; ++k) {
+        for (int k = 0; k < 32; ++k) {
             const float tv = Tf[(32 + r) * kSolveStride + 32 + k];
             const float4 yy = *reinterpret_cast<const float4 *>(Y + k * kSolveStride + c);
             l.x = fmaf(tv, yy.x, l.x), l.y = fmaf(tv, yy.y, l.y), l.z = fmaf(tv, yy.z, l.z), l.w = fmaf(tv, yy.w, l.w);

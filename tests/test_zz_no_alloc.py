@@ -49,32 +49,47 @@ def test_oversize_rejected_on_the_host():
     assert lib.gdn_chunked_prefill_noalloc(ctypes.byref(bad), 64, None) == N.GDN_ERR_UNSUPPORTED
 
 
-@pytest.mark.gpu
-@pytest.mark.parametrize("rule", ["gated_delta", "delta", "linear"])
-def test_same_result_as_the_workspace_entry_point(rule):
-    import oracle
-    import workloads
-    from gpu_helpers import o_flat, rel_err, run, to_dev
-    p = workloads.make(seed=81, B=3, lengths=[130, 0, 75], hq=2, hv=4, dk=128, dv=128, act="f16",
-                       rule=rule, state="random", state_std=0.3)
-    o1, f1, d = run(p, path="chunked")
-    # the same problem through the no-alloc entry point
-    q, k, v = d["q"], d["k"], d["v"]
+def _noalloc_like(p, d, o1, f1, rule):
+    """Runs the problem already run through the workspace entry point (o1, f1)
+    through the no-alloc entry point into fresh outputs."""
     o2 = torch.full_like(o1, float("nan"))
     f2 = torch.full_like(f1, float("nan"))
-    prob = api.make_problem(q=q, k=k, v=v, o=o2, final_state=f2, rule=rule, decay=d.get("decay"),
-                            beta=d.get("beta"), gate_bias=d.get("gate_bias"),
+    prob = api.make_problem(q=d["q"], k=d["k"], v=d["v"], o=o2, final_state=f2, rule=rule,
+                            decay=d.get("decay"), beta=d.get("beta"), gate_bias=d.get("gate_bias"),
                             gate_scale=d.get("gate_scale"), cu_seqlens=d.get("cu_seqlens"),
                             initial_state=d.get("initial_state"), batch=p["batch"],
-                            l2norm_k=p.get("l2norm_k", False), beta_sigmoid=p.get("beta_sigmoid", False))
+                            l2norm_k=p.get("l2norm_k", False), beta_sigmoid=p.get("beta_sigmoid", False),
+                            decay_per_key=p.get("decay_per_key", False))
     api.gdn_chunked_prefill_noalloc(prob)
+    return o2, f2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rule,per_key", [("gated_delta", False), ("delta", False), ("linear", False),
+                                          ("gdn2", True)])
+def test_same_result_as_the_workspace_entry_point(rule, per_key):
+    """Two no-alloc calls in a row (different problems, the second reusing the
+    scratch the first left behind), each bit-exact against the workspace entry
+    point; the first also against the oracle."""
+    import oracle
+    import workloads
+    from gpu_helpers import o_flat, rel_err, run
+    extra = dict(decay_per_key=True, gate_dtype="f32", write_gate=True) if per_key else {}
+    pa = workloads.make(seed=81, B=3, lengths=[130, 0, 75], hq=2, hv=4, dk=128, dv=128, act="f16",
+                        rule=rule, state="random", state_std=0.3, **extra)
+    pb = workloads.make(seed=82, B=2, lengths=[64, 257], hq=1, hv=2, dk=128, dv=128, act="f16",
+                        rule=rule, state="random", state_std=0.3, **extra)
+    oa, fa, da = run(pa, path="chunked")
+    ob, fb, db = run(pb, path="chunked")
+    oa2, fa2 = _noalloc_like(pa, da, oa, fa, rule)
+    ob2, fb2 = _noalloc_like(pb, db, ob, fb, rule)
     torch.cuda.synchronize()
-    assert torch.equal(o1.nan_to_num(7.0), o2.nan_to_num(7.0))
-    assert torch.equal(f1, f2)
-    ref_o, ref_fin, _ = oracle.run_problem(p)
+    for x1, x2 in ((oa, oa2), (fa, fa2), (ob, ob2), (fb, fb2)):
+        assert torch.equal(x1.nan_to_num(7.0), x2.nan_to_num(7.0))
+    ref_o, ref_fin, _ = oracle.run_problem(pa)
     covered = ~np.isnan(ref_o)
-    assert rel_err(o_flat(o2, p)[covered], ref_o[covered]) <= 5e-3
-    assert rel_err(f2.double().cpu().numpy(), ref_fin) <= 5e-3
+    assert rel_err(o_flat(oa2, pa)[covered], ref_o[covered]) <= 5e-3
+    assert rel_err(fa2.double().cpu().numpy(), ref_fin) <= 5e-3
 
 
 @pytest.mark.gpu
