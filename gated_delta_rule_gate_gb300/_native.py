@@ -36,7 +36,7 @@ class GdnProblem(ctypes.Structure):
         ("q", _vp), ("k", _vp), ("v", _vp), ("o", _vp), ("decay", _vp),
         ("gate_bias", _vp), ("gate_scale", _vp), ("beta", _vp),
         ("cu_seqlens", _vp), ("slot_ids", _vp), ("initial_state", _vp),
-        ("final_state", _vp), ("error_word", _vp),
+        ("final_state", _vp), ("error_word", _vp), ("seq_lens", _vp),
     ]
 
 

@@ -42,13 +42,14 @@ def make_problem(q, k, v, o, final_state, *, rule="gated_delta", decay=None, bet
                  gate_bias=None, gate_scale=None, cu_seqlens=None, slot_ids=None,
                  initial_state=None, batch=None, scale=0.0, l2norm_q=False, l2norm_k=False,
                  beta_sigmoid=False, decay_per_key=False, error_word=None,
-                 state_update_capacity=0):
+                 state_update_capacity=0, seq_lens=None):
     """Builds the ``gdn_problem`` struct.  q/k are [T, Hq, dk] (rank-3, packed)
     or [B, S, Hq, dk] (rank-4); v/o follow with Hv, dv; states are
-    [rows, Hv, dv, dk] fp32.  Keeps references to the tensors alive on the
-    returned struct."""
+    [rows, Hv, dv, dk] fp32.  ``seq_lens`` ([B] int32, rank-4 only) bounds each
+    row to its first seq_lens[b] tokens.  Keeps references to the tensors alive
+    on the returned struct."""
     _need_cuda(q, k, v, o, final_state, decay, beta, gate_bias, gate_scale, cu_seqlens,
-               slot_ids, initial_state, error_word)
+               slot_ids, initial_state, error_word, seq_lens)
     if q.dim() == 4:
         B, S, hq, dk = q.shape
         T, seq_len = B * S, S
@@ -82,9 +83,10 @@ def make_problem(q, k, v, o, final_state, *, rule="gated_delta", decay=None, bet
                     ("gate_bias", gate_bias), ("gate_scale", gate_scale), ("beta", beta),
                     ("cu_seqlens", cu_seqlens), ("slot_ids", slot_ids),
                     ("initial_state", initial_state), ("final_state", final_state),
-                    ("error_word", error_word)):
+                    ("error_word", error_word), ("seq_lens", seq_lens)):
         setattr(p, name, None if t is None else t.data_ptr())
     for t, name, dt in ((cu_seqlens, "cu_seqlens", torch.int32), (slot_ids, "slot_ids", torch.int32),
+                        (seq_lens, "seq_lens", torch.int32),
                         (error_word, "error_word", torch.int32), (gate_bias, "gate_bias", torch.float32),
                         (gate_scale, "gate_scale", torch.float32),
                         (initial_state, "initial_state", torch.float32),
@@ -92,7 +94,7 @@ def make_problem(q, k, v, o, final_state, *, rule="gated_delta", decay=None, bet
         if t is not None and t.dtype != dt:
             raise TypeError("%s must be %s" % (name, dt))
     p._keep = (q, k, v, o, final_state, decay, beta, gate_bias, gate_scale, cu_seqlens, slot_ids,
-               initial_state, error_word)
+               initial_state, error_word, seq_lens)
     return p
 
 

@@ -34,7 +34,7 @@ struct Problem {
     const void *decay;
     const float *gate_bias, *gate_scale;
     const void *beta;
-    const int32_t *cu, *slots;
+    const int32_t *cu, *slots, *seqlens;
     const float *init;
     float *fin;
     int32_t *err;
@@ -50,7 +50,8 @@ __device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
 
 // Token range [t0, t1) of request b: cu_seqlens clamped to [0, T] (a
-// decreasing pair gives an empty request), or uniform packing.
+// decreasing pair gives an empty request), or uniform packing, whose rows
+// seq_lens (clamped to [0, seq_len]) can shorten.
 __device__ __forceinline__ void request_range(const Problem &p, int b, int &t0, int &t1) {
     if (p.cu) {
         int a = p.cu[b], c = p.cu[b + 1];
@@ -61,7 +62,12 @@ __device__ __forceinline__ void request_range(const Problem &p, int b, int &t0, 
     } else {
         int L = p.seq_len ? p.seq_len : p.T / p.B;
         t0 = b * L;
-        t1 = t0 + L;
+        int n = L;
+        if (p.seqlens) {
+            n = p.seqlens[b];
+            n = n < 0 ? 0 : (n > L ? L : n);
+        }
+        t1 = t0 + n;
     }
 }
 

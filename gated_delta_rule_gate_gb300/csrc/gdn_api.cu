@@ -103,6 +103,8 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
         if ((long long)p->batch * p->seq_len != p->total_tokens)
             return fail(GDN_ERR_INVALID, "rank-4 form: total_tokens (%d) != batch * seq_len (%d * %d)",
                         p->total_tokens, p->batch, p->seq_len);
+    } else if (p->seq_lens) {
+        return fail(GDN_ERR_INVALID, "seq_lens requires the rank-4 (padded) form; seq_len must be > 0");
     } else if (!p->cu_seqlens && p->batch > 0 && p->total_tokens % p->batch != 0) {
         return fail(GDN_ERR_INVALID, "uniform packing: total_tokens (%d) is not a multiple of batch (%d)",
                     p->total_tokens, p->batch);
@@ -141,7 +143,7 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
         !aligned(p->decay, dtype_size(p->decay_dtype)) || !aligned(p->beta, dtype_size(p->beta_dtype)) ||
         !aligned(p->gate_bias, 4) || !aligned(p->gate_scale, 4) || !aligned(p->cu_seqlens, 4) ||
         !aligned(p->slot_ids, 4) || !aligned(p->initial_state, 4) || !aligned(p->final_state, 4) ||
-        !aligned(p->error_word, 4))
+        !aligned(p->error_word, 4) || !aligned(p->seq_lens, 4))
         return fail(GDN_ERR_INVALID, "a pointer is not aligned to its element size");
     const long long grid_bound = (long long)p->batch * p->num_heads_v * p->head_dim_v;
     if (grid_bound > (1LL << 31) - 1) return fail(GDN_ERR_UNSUPPORTED, "batch * Hv * dv exceeds 2^31 - 1");
@@ -171,6 +173,7 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
     d.gate_scale = p->gate_scale;
     d.beta = p->beta;
     d.cu = p->cu_seqlens;
+    d.seqlens = p->seq_lens;
     d.slots = p->slot_ids;
     d.init = p->initial_state;
     d.fin = p->final_state;

@@ -96,7 +96,12 @@ typedef enum gdn_rule {
  * that no request covers are not written.
  * Rank-4 form (seq_len > 0): q, k are [batch, seq_len, Hq, dk] (the same
  * memory layout), total_tokens must equal batch * seq_len, and cu_seqlens must
- * be NULL (the op allows cu_seqlens with the rank-3 spelling only).
+ * be NULL (the op allows cu_seqlens with the rank-3 spelling only).  seq_lens
+ * (rank-4 form only; "gatedDeltaUpdate", seq_lens bounds the rows of a ragged
+ * prefill) makes the batch padded-ragged: request b owns the first
+ * clamp(seq_lens[b], 0, seq_len) tokens of its row, [b * seq_len,
+ * b * seq_len + that); the padding tokens are neither read nor written.
+ * seq_lens NULL means every row is full.
  *
  * Heads.  num_heads_v is a positive multiple of num_heads_q; value head h
  * reads query/key head h * Hq / Hv.
@@ -158,6 +163,7 @@ typedef struct gdn_problem {
     const float *initial_state;
     float *final_state;
     int32_t *error_word; /* optional device int32 */
+    const int32_t *seq_lens; /* [batch] or NULL: rank-4 form only (see Token layout) */
 } gdn_problem;
 
 /*

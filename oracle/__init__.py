@@ -40,7 +40,7 @@ class _Problem(ctypes.Structure):
         ("decay", _dp), ("gate_bias", _dp), ("gate_scale", _dp), ("beta", _dp),
         ("cu_seqlens", _ip), ("slot_ids", _ip),
         ("initial_state", _dp), ("final_state", _dp), ("o", _dp),
-        ("error_word", _ip),
+        ("error_word", _ip), ("seq_lens", _ip),
     ]
 
 
@@ -110,7 +110,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         gate_scale=None, cu_seqlens=None, batch=None, slot_ids=None,
         initial_state=None, final_state=None, num_state_rows=None, scale=0.0,
         l2norm_q=False, l2norm_k=False, beta_sigmoid=False, decay_per_key=False,
-        threads=1):
+        threads=1, seq_lens=None):
     """Runs the recurrence token by token in float64.
 
     q, k: [T, Hq, dk]; v: [T, Hv, dv] (rank-4 callers flatten [B, S] to T and
@@ -118,6 +118,8 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
     error_word).  ``final_state`` (if given) is the buffer the update lands in
     (copied, so the caller's array is not modified); rows that no request
     names keep its values.  Output tokens outside every request are NaN.
+    ``seq_lens`` ([batch], uniform layout only) shortens request b to the first
+    seq_lens[b] tokens of its row.
     """
     lib = _load()
     q64, k64, v64 = _f64(q), _f64(k), _f64(v)
@@ -125,6 +127,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
     hv, dv = v64.shape[1], v64.shape[2]
     cu = _i32(cu_seqlens)
     slots = _i32(slot_ids)
+    sl = _i32(seq_lens)
     if batch is None:
         batch = (len(cu) - 1) if cu is not None else 1
     init = _f64(initial_state)
@@ -157,7 +160,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         decay=_ptr(dec, _dp), gate_bias=_ptr(gb, _dp), gate_scale=_ptr(gs, _dp),
         beta=_ptr(bet, _dp), cu_seqlens=_ptr(cu, _ip), slot_ids=_ptr(slots, _ip),
         initial_state=_ptr(init, _dp), final_state=_ptr(fin, _dp), o=_ptr(o, _dp),
-        error_word=_ptr(err, _ip),
+        error_word=_ptr(err, _ip), seq_lens=_ptr(sl, _ip),
     )
     rc = lib.oracle_gdn(ctypes.byref(prob))
     if rc != 0:
@@ -199,11 +202,19 @@ def run_problem(p, threads=1, requests=None):
     cu = p.get("cu_seqlens")
     slots = p.get("slot_ids")
     batch = p["batch"]
+    sl = p.get("seq_lens")
     if cu is None:
         L = T // batch
         cu_np = np.arange(batch + 1, dtype=np.int64) * L
     else:
         cu_np = np.asarray(cu.numpy() if hasattr(cu, "numpy") else cu, dtype=np.int64)
+    ranges = []
+    for b in range(batch):
+        t0 = min(max(int(cu_np[b]), 0), T)
+        t1 = max(min(max(int(cu_np[b + 1]), 0), T), t0)
+        if sl is not None:
+            t1 = t0 + min(max(int(sl[b]), 0), t1 - t0)
+        ranges.append((t0, t1))
     if requests is not None:
         # Sub-problem: the chosen requests keep their own token ranges; their
         # state rows are gathered into a compact slab (row j = request j), so
@@ -213,8 +224,7 @@ def run_problem(p, threads=1, requests=None):
         rows = []
         T_, idx = 0, []
         for j, b in enumerate(req):
-            t0 = min(max(int(cu_np[b]), 0), T)
-            t1 = max(min(max(int(cu_np[b + 1]), 0), T), t0)
+            t0, t1 = ranges[b]
             idx.extend(range(t0, t1))
             T_ += t1 - t0
             sub_cu[j + 1] = T_
@@ -254,4 +264,4 @@ def run_problem(p, threads=1, requests=None):
                num_state_rows=p.get("num_slots") or batch, scale=p.get("scale", 0.0),
                l2norm_q=p.get("l2norm_q", False), l2norm_k=p.get("l2norm_k", False),
                beta_sigmoid=p.get("beta_sigmoid", False),
-               decay_per_key=p.get("decay_per_key", False), threads=threads)
+               decay_per_key=p.get("decay_per_key", False), threads=threads, seq_lens=sl)

@@ -22,6 +22,10 @@
  *    means uniform packing.  initial_state absent means zeros.
  *  - same page, Outputs table: a request with no tokens copies its incoming
  *    state through.
+ *  - "gatedDeltaUpdate": seq_lens [B] bounds the rows of a ragged prefill in
+ *    the [B, T, ...] layout: request b takes the first seq_lens[b] tokens of
+ *    its row (clamped to [0, row length]; the rest is padding, neither read
+ *    nor written).
  *  - same page, Attributes: beta_activation (sigmoid in float), qk_l2_norm
  *    (eps 1e-12), scale (0 selects 1/sqrt(head_size_qk)), update_rule
  *    (linear drops decay and retrieval, gated keeps only decay, delta keeps
@@ -89,6 +93,7 @@ typedef struct {
     double *final_state;         /* [rows,Hv,dv,dk] */
     double *o;                   /* [T,Hv,dv] */
     int32_t *error_word;         /* may be NULL */
+    const int32_t *seq_lens;     /* [B] or NULL: rows of the uniform layout shortened */
 } oracle_problem;
 
 /* softplus(x) = ln(1 + e^x), evaluated without overflow. */
@@ -120,7 +125,8 @@ static int32_t clamp_i32(int32_t x, int32_t lo, int32_t hi) {
     return x < lo ? lo : (x > hi ? hi : x);
 }
 
-/* Token range of request b: clamped exclusive prefix sums, or uniform. */
+/* Token range of request b: clamped exclusive prefix sums, or uniform rows,
+ * each shortened to its clamped seq_lens entry when those are given. */
 static void request_range(const oracle_problem *p, int32_t b, int32_t *t0, int32_t *t1) {
     if (p->cu_seqlens) {
         *t0 = clamp_i32(p->cu_seqlens[b], 0, p->total_tokens);
@@ -129,7 +135,7 @@ static void request_range(const oracle_problem *p, int32_t b, int32_t *t0, int32
     } else {
         int32_t len = p->total_tokens / p->batch;
         *t0 = b * len;
-        *t1 = *t0 + len;
+        *t1 = *t0 + (p->seq_lens ? clamp_i32(p->seq_lens[b], 0, len) : len);
     }
 }
 
@@ -250,6 +256,7 @@ int oracle_gdn(const oracle_problem *p) {
     if (rule_has_retrieval(p->rule) && !p->beta) return 1;
     if (p->raw_gate && (!p->gate_bias || !p->gate_scale)) return 1;
     if (!p->cu_seqlens && p->total_tokens % p->batch != 0) return 1;
+    if (p->cu_seqlens && p->seq_lens) return 1;
 
     const int64_t pairs = (int64_t)p->batch * p->hv;
     const size_t per = (size_t)p->dv * p->dk + 4 * (size_t)p->dk + 2 * (size_t)p->dv;

@@ -83,6 +83,8 @@ def _call_chunked(p, chunk=64, ws=None, nbytes=0):
     (dict(gate_scale=FAKE), N.GDN_ERR_INVALID, "together"),
     (dict(state_update_capacity=4), N.GDN_ERR_INVALID, "state_update_capacity"),
     (dict(seq_len=4, cu_seqlens=FAKE), N.GDN_ERR_INVALID, "rank-3"),
+    (dict(seq_lens=FAKE), N.GDN_ERR_INVALID, "rank-4"),
+    (dict(seq_len=4, seq_lens=FAKE + 2), N.GDN_ERR_INVALID, "aligned"),
     (dict(seq_len=3), N.GDN_ERR_INVALID, "batch * seq_len"),
     (dict(total_tokens=7), N.GDN_ERR_INVALID, "multiple of batch"),
     (dict(final_state=None), N.GDN_ERR_INVALID, "final_state"),

@@ -234,3 +234,24 @@ def test_chunked_many_chains(rule, per_key):
     assert err == 0
     o, fin, _ = run(p, path="chunked")
     _check(p, o, fin, ref_o, ref_fin)
+
+
+@pytest.mark.parametrize("case", [
+    dict(rule="gated_delta"),
+    dict(rule="linear"),
+    dict(rule="gdn2", decay_per_key=True, gate_dtype="f32", write_gate=True),
+    dict(rule="gated_delta", dk=64, dv=64),
+    dict(rule="gated", decay_per_key=True, gate_dtype="f32"),
+], ids=["tc-gated_delta", "tc-linear", "tc-perkey-gdn2", "mma", "token-serial"])
+def test_chunked_seq_lens_padded_rows(case):
+    """Rank-4 batch whose rows are bounded by seq_lens ("gatedDeltaUpdate"):
+    request b takes the first clamp(seq_lens[b], 0, S) tokens of its row, over
+    every chunked path; padding tokens keep the sentinel."""
+    kw = dict(seed=41, B=4, seq_len=100, seq_lens=[100, 0, 37, 250], hq=1, hv=2, dk=128, dv=128,
+              act="f16", state="random", state_std=0.3)
+    kw.update(case)
+    p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)

@@ -328,6 +328,36 @@ def test_empty_request_copies_state_and_clamps():
     np.testing.assert_array_equal(fin[2], ref2[1][0])
 
 
+def test_seq_lens_rows_equal_separate_requests():
+    """Padded rank-4 rows bounded by seq_lens ("gatedDeltaUpdate"): request b
+    is exactly the recurrence over the first clamp(seq_lens[b], 0, S) tokens of
+    its row, run on its own; padding outputs stay NaN; an empty row copies its
+    state through."""
+    S, lens = 6, [6, 0, 2, 9, -1]
+    p = workloads.make(seed=24, B=5, seq_len=S, seq_lens=lens, hq=1, hv=2, dk=4, dv=3, act="f32",
+                       rule="gated_delta", state="random", state_std=0.5)
+    o, fin, err = oracle.run_problem(p)
+    S0 = _np(p["initial_state"])
+    assert err == 0
+    for b, n in enumerate(lens):
+        n = min(max(n, 0), S)
+        lo = b * S
+        assert np.isnan(o[lo + n:lo + S]).all()
+        if n == 0:
+            assert np.array_equal(fin[b], S0[b])
+            continue
+        ref = oracle.gdn(p["q"][lo:lo + n], p["k"][lo:lo + n], p["v"][lo:lo + n],
+                         decay=p["decay"][lo:lo + n], beta=p["beta"][lo:lo + n],
+                         gate_bias=p["gate_bias"], gate_scale=p["gate_scale"],
+                         initial_state=S0[b:b + 1], l2norm_k=True, beta_sigmoid=True)
+        np.testing.assert_array_equal(o[lo:lo + n], ref[0])
+        np.testing.assert_array_equal(fin[b], ref[1][0])
+    with pytest.raises(ValueError):  # seq_lens bound the uniform layout only
+        oracle.gdn(p["q"], p["k"], p["v"], decay=p["decay"], beta=p["beta"], gate_bias=p["gate_bias"],
+                   gate_scale=p["gate_scale"], cu_seqlens=np.arange(6, dtype=np.int32) * S, batch=5,
+                   seq_lens=np.asarray(lens, dtype=np.int32))
+
+
 def test_uncovered_tokens_and_untouched_slots():
     p = _small(21, 8, B=2, cu_seqlens=[1, 4, 6], num_slots=5)
     p["slot_ids"] = np.array([3, 0], dtype=np.int32)

@@ -265,3 +265,20 @@ def test_recurrent_long_requests(case):
     assert err == 0
     o, fin, _ = run(p)
     _check(p, o, fin, ref_o, ref_fin)
+
+
+@pytest.mark.parametrize("case", [
+    dict(seq_len=4, seq_lens=[4, 1, 0, 3, 7], dk=128, dv=128),   # decode kernel
+    dict(seq_len=150, seq_lens=[150, 0, 37, 400, 1], dk=128, dv=128),  # long-request kernel
+    dict(seq_len=9, seq_lens=[2, 9, 0, 5, -3], dk=48, dv=24),     # any-dk kernel
+], ids=["decode", "long", "generic"])
+def test_seq_lens_padded_rows(case):
+    """Rank-4 batch whose rows are bounded by seq_lens ("gatedDeltaUpdate"):
+    each request takes the first clamp(seq_lens[b], 0, S) tokens of its row;
+    padding tokens keep the sentinel; slots in place."""
+    p = workloads.make(seed=43, B=5, hq=2, hv=4, act="f16", rule="gated_delta", state="random",
+                       num_slots=8, slot_mode="perm", **case)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p)
+    _check(p, o, fin, ref_o, ref_fin)

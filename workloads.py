@@ -52,7 +52,7 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
          a_log_range=(0.0, 2.0), dt_bias_range=(-2.0, 2.0), gate_dtype=None,
          beta_dtype=None, logdecay_range=(-1.0, 0.0), beta_mode="sigmoid",
          state="zero", state_std=0.02, num_slots=None, slot_mode=None,
-         write_gate=False, l2norm_q=False, l2norm_k=True, scale=0.0, qk_std=1.0):
+         write_gate=False, l2norm_q=False, l2norm_k=True, scale=0.0, qk_std=1.0, seq_lens=None):
     """Draws one problem.  ``gate`` is 'raw' (raw projection + gate_bias +
     gate_scale), 'log' (log-space decay drawn U(logdecay_range)) or ignored
     for rules without decay.  ``beta_mode`` is 'sigmoid' (raw N(0,1) logits +
@@ -111,6 +111,8 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
         else:
             p["beta"] = torch.rand(*bshape, generator=gen).to(bd)
     p["cu_seqlens"] = cu_seqlens
+    # padded-ragged rank-4 batch: request b uses the first seq_lens[b] tokens of its row
+    p["seq_lens"] = torch.as_tensor(seq_lens, dtype=torch.int32) if seq_lens is not None else None
     rows = num_slots if num_slots else B
     p["num_slots"] = rows
     if slot_mode == "perm":
@@ -172,8 +174,9 @@ def gdn2(seed=5, B=2, S=4096, h=16, dk=128, dv=128):
 
 
 def token_ranges(p):
-    """Per-request [t0, t1) after the cu_seqlens clamp, as python ints (host
-    bookkeeping for samplers and sentinel checks)."""
+    """Per-request [t0, t1) after the cu_seqlens clamp (or the seq_lens bound
+    of the padded rank-4 layout), as python ints (host bookkeeping for samplers
+    and sentinel checks)."""
     T, B = p["total_tokens"], p["batch"]
     out = []
     cu = p.get("cu_seqlens")
@@ -185,5 +188,7 @@ def token_ranges(p):
         else:
             L = T // B
             t0, t1 = b * L, (b + 1) * L
+            if p.get("seq_lens") is not None:
+                t1 = t0 + min(max(int(p["seq_lens"][b]), 0), L)
         out.append((t0, t1))
     return out
