@@ -14,6 +14,7 @@ GDN_OK, GDN_ERR_INVALID, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_ERR_CUDA = 
 DTYPE_F32, DTYPE_F16, DTYPE_BF16 = 0, 1, 2
 RULES = {"linear": 0, "gated": 1, "delta": 2, "gated_delta": 3, "gdn2": 4}
 FLAG_L2NORM_Q, FLAG_L2NORM_K, FLAG_BETA_SIGMOID, FLAG_DECAY_PER_KEY = 0x1, 0x2, 0x4, 0x8
+FLAG_BETA_SHARED = 0x10
 DEVERR_BAD_SLOT = 0x1
 
 EXPORTS = ("gdn_gate", "gdn_recurrent_step", "gdn_chunked_prefill_workspace_size",

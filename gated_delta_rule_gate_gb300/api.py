@@ -42,12 +42,13 @@ def make_problem(q, k, v, o, final_state, *, rule="gated_delta", decay=None, bet
                  gate_bias=None, gate_scale=None, cu_seqlens=None, slot_ids=None,
                  initial_state=None, batch=None, scale=0.0, l2norm_q=False, l2norm_k=False,
                  beta_sigmoid=False, decay_per_key=False, error_word=None,
-                 state_update_capacity=0, seq_lens=None):
+                 state_update_capacity=0, seq_lens=None, beta_shared=False):
     """Builds the ``gdn_problem`` struct.  q/k are [T, Hq, dk] (rank-3, packed)
     or [B, S, Hq, dk] (rank-4); v/o follow with Hv, dv; states are
     [rows, Hv, dv, dk] fp32.  ``seq_lens`` ([B] int32, rank-4 only) bounds each
-    row to its first seq_lens[b] tokens.  Keeps references to the tensors alive
-    on the returned struct."""
+    row to its first seq_lens[b] tokens.  ``beta_shared``: beta is [T] (one
+    per token for every value head).  Keeps references to the tensors alive on
+    the returned struct."""
     _need_cuda(q, k, v, o, final_state, decay, beta, gate_bias, gate_scale, cu_seqlens,
                slot_ids, initial_state, error_word, seq_lens)
     if q.dim() == 4:
@@ -76,7 +77,7 @@ def make_problem(q, k, v, o, final_state, *, rule="gated_delta", decay=None, bet
     p.rule = N.RULES[rule] if isinstance(rule, str) else int(rule)
     p.flags = ((N.FLAG_L2NORM_Q if l2norm_q else 0) | (N.FLAG_L2NORM_K if l2norm_k else 0) |
                (N.FLAG_BETA_SIGMOID if beta_sigmoid else 0) |
-               (N.FLAG_DECAY_PER_KEY if decay_per_key else 0))
+               (N.FLAG_DECAY_PER_KEY if decay_per_key else 0) | (N.FLAG_BETA_SHARED if beta_shared else 0))
     p.scale = float(scale)
     p.state_update_capacity = int(state_update_capacity)
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("decay", decay),

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(NTH, 2) chunked_mma_kernel(Problem p, int slic
                 }
                 br = 1.f;
                 if (beta_scalar) {
-                    br = ld_any(p.beta, th, p.beta_f16);
+                    br = ld_any(p.beta, beta_at(p, c0 + r, h), p.beta_f16);
                     if (sig) br = sigmoid_f(br);
                 }
             }

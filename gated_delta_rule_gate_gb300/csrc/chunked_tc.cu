@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 const int tt = lane + 32 * e;
                 const size_t th = (size_t)(x.c0 + tt) * p.Hv + x.h;
                 x.g[e] = (rule_has_decay(p.rule) && tt < x.n) ? ld_any(p.decay, th, p.decay_f16) : 0.f;
-                x.bt[e] = (RETR && tt < x.n) ? ld_any(p.beta, th, p.beta_f16) : 0.f;
+                x.bt[e] = (RETR && tt < x.n) ? ld_any(p.beta, beta_at(p, x.c0 + tt, x.h), p.beta_f16) : 0.f;
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                     if (GDN2) {
                         bt = 1.f;
                     } else {
-                        bt = ld_any(p.beta, th, p.beta_f16);
+                        bt = ld_any(p.beta, beta_at(p, x.c0 + tt, x.h), p.beta_f16);
                         if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
                     }
                 }

@@ -12,7 +12,7 @@ namespace gdn {
 
 // Rules and flags, mirrored from include/gdn.h for device code.
 enum : int { kLinear = 0, kGated = 1, kDelta = 2, kGatedDelta = 3, kGdn2 = 4 };
-enum : unsigned { kL2q = 0x1u, kL2k = 0x2u, kBetaSigmoid = 0x4u, kPerKey = 0x8u };
+enum : unsigned { kL2q = 0x1u, kL2k = 0x2u, kBetaSigmoid = 0x4u, kPerKey = 0x8u, kBetaShared = 0x10u };
 
 __host__ __device__ inline bool rule_has_decay(int r) {
     return r == kGated || r == kGatedDelta || r == kGdn2;
@@ -39,6 +39,12 @@ struct Problem {
     float *fin;
     int32_t *err;
 };
+
+// Element index of the scalar beta of token t and value head h: [T, Hv], or
+// [T] when one beta per token serves every value head (kBetaShared).
+__device__ __forceinline__ size_t beta_at(const Problem &p, size_t t, int h) {
+    return (p.flags & kBetaShared) ? t : t * p.Hv + h;
+}
 
 __device__ __forceinline__ float ld_any(const void *p, size_t i, int f16) {
     return f16 ? __half2float(static_cast<const __half *>(p)[i]) : static_cast<const float *>(p)[i];

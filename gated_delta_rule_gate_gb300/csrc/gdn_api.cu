@@ -91,8 +91,15 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
     if ((st = check_dtype(p->act_dtype, "act_dtype")) != GDN_OK) return st;
     if (p->rule < GDN_RULE_LINEAR || p->rule > GDN_RULE_GDN2)
         return fail(GDN_ERR_INVALID, "unknown update rule %d", p->rule);
-    if (p->flags & ~(GDN_FLAG_L2NORM_Q | GDN_FLAG_L2NORM_K | GDN_FLAG_BETA_SIGMOID | GDN_FLAG_DECAY_PER_KEY))
+    static_assert(GDN_FLAG_L2NORM_Q == gdn::kL2q && GDN_FLAG_L2NORM_K == gdn::kL2k &&
+                      GDN_FLAG_BETA_SIGMOID == gdn::kBetaSigmoid && GDN_FLAG_DECAY_PER_KEY == gdn::kPerKey &&
+                      GDN_FLAG_BETA_SHARED == gdn::kBetaShared,
+                  "flag mirror");
+    if (p->flags &
+        ~(GDN_FLAG_L2NORM_Q | GDN_FLAG_L2NORM_K | GDN_FLAG_BETA_SIGMOID | GDN_FLAG_DECAY_PER_KEY | GDN_FLAG_BETA_SHARED))
         return fail(GDN_ERR_INVALID, "unknown flag bits 0x%x", p->flags);
+    if ((p->flags & GDN_FLAG_BETA_SHARED) && p->rule != GDN_RULE_DELTA && p->rule != GDN_RULE_GATED_DELTA)
+        return fail(GDN_ERR_INVALID, "GDN_FLAG_BETA_SHARED applies to the scalar beta of rules DELTA and GATED_DELTA");
     if (p->state_update_capacity != 0)
         return fail(GDN_ERR_INVALID, "state_update_capacity must be 0 (compact capture is not provided)");
     if (!isfinite(p->scale)) return fail(GDN_ERR_INVALID, "scale must be finite");

@@ -126,7 +126,7 @@ __device__ void stage_tokens(const Problem &p, const Stage &s, int h, int qh, in
                 alpha = expf(g);
             }
             if (beta_scalar) {
-                beta = ld_any(p.beta, th, p.beta_f16);
+                beta = ld_any(p.beta, beta_at(p, t, h), p.beta_f16);
                 if (sig) beta = sigmoid_f(beta);
             }
             s.alpha[tt] = alpha;
@@ -467,7 +467,7 @@ __device__ __forceinline__ void issue_pair(const Problem &p, const PipeLayout &L
                 ts.gb = p.gate_bias[h];
             }
         }
-        if (p.rule == kDelta || p.rule == kGatedDelta) ts.b = ld_bits(p.beta, th, p.beta_f16);
+        if (p.rule == kDelta || p.rule == kGatedDelta) ts.b = ld_bits(p.beta, beta_at(p, t0 + lane, h), p.beta_f16);
     }
 }
 
@@ -887,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, 
         if (tid < nt) {
             const size_t th = (size_t)(tb + tid) * p.Hv + h;
             if (has_decay && !Ly.has_a) g = ld_any(p.decay, th, p.decay_f16);
-            if (beta_scalar) bb = ld_any(p.beta, th, p.beta_f16);
+            if (beta_scalar) bb = ld_any(p.beta, beta_at(p, tb + tid, h), p.beta_f16);
         }
     };
     float sg, sb;

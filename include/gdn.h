@@ -77,6 +77,7 @@ typedef enum gdn_rule {
 #define GDN_FLAG_L2NORM_K 0x2u      /* same for k */
 #define GDN_FLAG_BETA_SIGMOID 0x4u  /* beta <- sigmoid(beta) in fp32 (beta_activation) */
 #define GDN_FLAG_DECAY_PER_KEY 0x8u /* decay is [.., Hv, dk]: one log-decay per key channel */
+#define GDN_FLAG_BETA_SHARED 0x10u  /* beta is [total_tokens]: one per token, shared by every value head */
 
 /* Bits OR-ed into *error_word by the device (never reset by the library). */
 #define GDN_DEVERR_BAD_SLOT 0x1 /* a slot id outside [0, num_state_rows): request skipped */
@@ -117,8 +118,11 @@ typedef enum gdn_rule {
  *  GDN_FLAG_DECAY_PER_KEY; decay_dtype is F32 or act_dtype.
  *
  * Beta.  Present exactly for rules DELTA, GATED_DELTA (shape [total_tokens,
- * Hv]) and GDN2 (the erase gate b, [total_tokens, Hv, dk]); beta_dtype is F32
- * or act_dtype; GDN_FLAG_BETA_SIGMOID applies the logistic sigmoid first.
+ * Hv], or [total_tokens] with GDN_FLAG_BETA_SHARED: beta's last dimension 1,
+ * broadcast over the value heads, as the LinearAttention schema allows) and
+ * GDN2 (the erase gate b, [total_tokens, Hv, dk]; GDN_FLAG_BETA_SHARED is
+ * rejected there); beta_dtype is F32 or act_dtype; GDN_FLAG_BETA_SIGMOID
+ * applies the logistic sigmoid first.
  * For GDN2 the write gate w is folded into v by the caller.
  *
  * State.  initial_state and final_state are fp32, value-major

@@ -40,7 +40,7 @@ class _Problem(ctypes.Structure):
         ("decay", _dp), ("gate_bias", _dp), ("gate_scale", _dp), ("beta", _dp),
         ("cu_seqlens", _ip), ("slot_ids", _ip),
         ("initial_state", _dp), ("final_state", _dp), ("o", _dp),
-        ("error_word", _ip), ("seq_lens", _ip),
+        ("error_word", _ip), ("seq_lens", _ip), ("beta_shared", ctypes.c_int32),
     ]
 
 
@@ -110,7 +110,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         gate_scale=None, cu_seqlens=None, batch=None, slot_ids=None,
         initial_state=None, final_state=None, num_state_rows=None, scale=0.0,
         l2norm_q=False, l2norm_k=False, beta_sigmoid=False, decay_per_key=False,
-        threads=1, seq_lens=None):
+        threads=1, seq_lens=None, beta_shared=False):
     """Runs the recurrence token by token in float64.
 
     q, k: [T, Hq, dk]; v: [T, Hv, dv] (rank-4 callers flatten [B, S] to T and
@@ -119,7 +119,8 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
     (copied, so the caller's array is not modified); rows that no request
     names keep its values.  Output tokens outside every request are NaN.
     ``seq_lens`` ([batch], uniform layout only) shortens request b to the first
-    seq_lens[b] tokens of its row.
+    seq_lens[b] tokens of its row.  ``beta_shared``: the scalar beta is [T],
+    one per token for every value head.
     """
     lib = _load()
     q64, k64, v64 = _f64(q), _f64(k), _f64(v)
@@ -160,7 +161,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         decay=_ptr(dec, _dp), gate_bias=_ptr(gb, _dp), gate_scale=_ptr(gs, _dp),
         beta=_ptr(bet, _dp), cu_seqlens=_ptr(cu, _ip), slot_ids=_ptr(slots, _ip),
         initial_state=_ptr(init, _dp), final_state=_ptr(fin, _dp), o=_ptr(o, _dp),
-        error_word=_ptr(err, _ip), seq_lens=_ptr(sl, _ip),
+        error_word=_ptr(err, _ip), seq_lens=_ptr(sl, _ip), beta_shared=int(beta_shared),
     )
     rc = lib.oracle_gdn(ctypes.byref(prob))
     if rc != 0:
@@ -252,7 +253,8 @@ def run_problem(p, threads=1, requests=None):
                             scale=p.get("scale", 0.0),
                             l2norm_q=p.get("l2norm_q", False), l2norm_k=p.get("l2norm_k", False),
                             beta_sigmoid=p.get("beta_sigmoid", False),
-                            decay_per_key=p.get("decay_per_key", False), threads=threads)
+                            decay_per_key=p.get("decay_per_key", False), threads=threads,
+                            beta_shared=p.get("beta_shared", False))
         o = np.full((T, p["hv"], p["dv"]), np.nan)
         if len(idx):
             o[idx] = o_s
@@ -264,4 +266,5 @@ def run_problem(p, threads=1, requests=None):
                num_state_rows=p.get("num_slots") or batch, scale=p.get("scale", 0.0),
                l2norm_q=p.get("l2norm_q", False), l2norm_k=p.get("l2norm_k", False),
                beta_sigmoid=p.get("beta_sigmoid", False),
-               decay_per_key=p.get("decay_per_key", False), threads=threads, seq_lens=sl)
+               decay_per_key=p.get("decay_per_key", False), threads=threads, seq_lens=sl,
+               beta_shared=p.get("beta_shared", False))

@@ -22,6 +22,9 @@
  *    means uniform packing.  initial_state absent means zeros.
  *  - same page, Outputs table: a request with no tokens copies its incoming
  *    state through.
+ *  - ONNX issue "Spec gap ... Gated DeltaNet-2", "What LinearAttention
+ *    currently does": beta's last dimension is kv_num_heads or 1; with 1,
+ *    one beta per token serves every value head.
  *  - "gatedDeltaUpdate": seq_lens [B] bounds the rows of a ragged prefill in
  *    the [B, T, ...] layout: request b takes the first seq_lens[b] tokens of
  *    its row (clamped to [0, row length]; the rest is padding, neither read
@@ -94,6 +97,7 @@ typedef struct {
     double *o;                   /* [T,Hv,dv] */
     int32_t *error_word;         /* may be NULL */
     const int32_t *seq_lens;     /* [B] or NULL: rows of the uniform layout shortened */
+    int32_t beta_shared;         /* scalar beta is [T]: one per token for every value head */
 } oracle_problem;
 
 /* softplus(x) = ln(1 + e^x), evaluated without overflow. */
@@ -219,7 +223,7 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
                     kappa[c] = bc * kv[c];
                 }
             } else {
-                beta = p->beta[(size_t)t * hv + h];
+                beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];
                 if (p->beta_sigmoid) beta = sigmoid(beta);
                 memcpy(kappa, kv, sizeof(double) * dk);
             }
@@ -257,6 +261,7 @@ int oracle_gdn(const oracle_problem *p) {
     if (p->raw_gate && (!p->gate_bias || !p->gate_scale)) return 1;
     if (!p->cu_seqlens && p->total_tokens % p->batch != 0) return 1;
     if (p->cu_seqlens && p->seq_lens) return 1;
+    if (p->beta_shared && p->rule != ORACLE_RULE_DELTA && p->rule != ORACLE_RULE_GATED_DELTA) return 1;
 
     const int64_t pairs = (int64_t)p->batch * p->hv;
     const size_t per = (size_t)p->dv * p->dk + 4 * (size_t)p->dk + 2 * (size_t)p->dv;

@@ -65,7 +65,7 @@ def run(p, path="recurrent", chunk=64, in_place=None, sentinel=float("nan"), err
     kw = dict(q=q, k=k, v=v, o=o, final_state=fin, rule=p["rule"], decay=d.get("decay"),
               beta=d.get("beta"), gate_bias=d.get("gate_bias"), gate_scale=d.get("gate_scale"),
               cu_seqlens=d.get("cu_seqlens"), slot_ids=d.get("slot_ids"), initial_state=init,
-              seq_lens=d.get("seq_lens"),
+              seq_lens=d.get("seq_lens"), beta_shared=p.get("beta_shared", False),
               batch=p["batch"], scale=p.get("scale", 0.0), l2norm_q=p.get("l2norm_q", False),
               l2norm_k=p.get("l2norm_k", False), beta_sigmoid=p.get("beta_sigmoid", False),
               decay_per_key=p.get("decay_per_key", False), error_word=error_word)

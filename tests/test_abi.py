@@ -84,6 +84,7 @@ def _call_chunked(p, chunk=64, ws=None, nbytes=0):
     (dict(state_update_capacity=4), N.GDN_ERR_INVALID, "state_update_capacity"),
     (dict(seq_len=4, cu_seqlens=FAKE), N.GDN_ERR_INVALID, "rank-3"),
     (dict(seq_lens=FAKE), N.GDN_ERR_INVALID, "rank-4"),
+    (dict(flags=N.FLAG_BETA_SHARED, rule=N.RULES["gdn2"]), N.GDN_ERR_INVALID, "BETA_SHARED"),
     (dict(seq_len=4, seq_lens=FAKE + 2), N.GDN_ERR_INVALID, "aligned"),
     (dict(seq_len=3), N.GDN_ERR_INVALID, "batch * seq_len"),
     (dict(total_tokens=7), N.GDN_ERR_INVALID, "multiple of batch"),

@@ -255,3 +255,22 @@ def test_chunked_seq_lens_padded_rows(case):
     assert err == 0
     o, fin, _ = run(p, path="chunked")
     _check(p, o, fin, ref_o, ref_fin)
+
+
+@pytest.mark.parametrize("case", [dict(), dict(dk=64, dv=64),
+                                  dict(decay_per_key=True, gate_dtype="f32")],
+                         ids=["tc", "mma", "tc-perkey"])
+@pytest.mark.parametrize("rule", ["delta", "gated_delta"])
+def test_chunked_shared_beta(case, rule):
+    """beta [T]: one per token, broadcast over the value heads, on every
+    chunked path."""
+    if rule == "delta" and case.get("decay_per_key"):
+        pytest.skip("the delta rule has no decay")
+    kw = dict(seed=45, B=3, lengths=[70, 0, 130], hq=1, hv=2, dk=128, dv=128, act="f16", rule=rule,
+              state="random", state_std=0.3, beta_shared=True)
+    kw.update(case)
+    p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)

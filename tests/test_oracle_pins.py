@@ -9,6 +9,7 @@ import math
 from fractions import Fraction
 
 import numpy as np
+import torch
 import pytest
 
 import oracle
@@ -356,6 +357,28 @@ def test_seq_lens_rows_equal_separate_requests():
         oracle.gdn(p["q"], p["k"], p["v"], decay=p["decay"], beta=p["beta"], gate_bias=p["gate_bias"],
                    gate_scale=p["gate_scale"], cu_seqlens=np.arange(6, dtype=np.int32) * S, batch=5,
                    seq_lens=np.asarray(lens, dtype=np.int32))
+
+
+@pytest.mark.parametrize("rule", ["delta", "gated_delta"])
+def test_shared_beta_equals_repeated_per_head_beta(rule):
+    """beta with last dimension 1 (the LinearAttention schema's broadcast, per
+    the GDN-2 issue) is the per-head form with the token's beta repeated over
+    the value heads."""
+    p = workloads.make(seed=25, B=2, lengths=[5, 4], hq=1, hv=3, dk=4, dv=3, act="f32", rule=rule,
+                       state="random", state_std=0.5, beta_shared=True)
+    assert tuple(p["beta"].shape) == (9,) and p["beta_shared"]
+    o, fin, err = oracle.run_problem(p)
+    q = dict(p)
+    q["beta"] = p["beta"][:, None].repeat(1, 3)
+    q["beta_shared"] = False
+    o2, fin2, err2 = oracle.run_problem(q)
+    assert err == err2 == 0
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(fin, fin2)
+    # and a shared beta is not the same as the first head's beta everywhere else
+    q["beta"] = p["beta"][:, None].repeat(1, 3) * torch.tensor([1.0, 0.5, 0.25])
+    o3, _, _ = oracle.run_problem(q)
+    assert not np.allclose(o[:, 1:], o3[:, 1:])
 
 
 def test_uncovered_tokens_and_untouched_slots():

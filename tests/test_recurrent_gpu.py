@@ -282,3 +282,19 @@ def test_seq_lens_padded_rows(case):
     assert err == 0
     o, fin, _ = run(p)
     _check(p, o, fin, ref_o, ref_fin)
+
+
+@pytest.mark.parametrize("case", [
+    dict(lengths=[1, 4, 0, 2], dk=128, dv=128),        # decode kernel
+    dict(lengths=[120, 3, 77], dk=128, dv=128),        # long-request kernel
+    dict(lengths=[3, 0, 5], dk=48, dv=24),             # any-dk kernel
+], ids=["decode", "long", "generic"])
+@pytest.mark.parametrize("rule", ["delta", "gated_delta"])
+def test_shared_beta(case, rule):
+    """beta [T]: one per token, broadcast over the value heads."""
+    p = workloads.make(seed=44, B=len(case["lengths"]), hq=2, hv=4, act="f16", rule=rule,
+                       state="random", beta_shared=True, **case)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p)
+    _check(p, o, fin, ref_o, ref_fin)

@@ -52,7 +52,8 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
          a_log_range=(0.0, 2.0), dt_bias_range=(-2.0, 2.0), gate_dtype=None,
          beta_dtype=None, logdecay_range=(-1.0, 0.0), beta_mode="sigmoid",
          state="zero", state_std=0.02, num_slots=None, slot_mode=None,
-         write_gate=False, l2norm_q=False, l2norm_k=True, scale=0.0, qk_std=1.0, seq_lens=None):
+         write_gate=False, l2norm_q=False, l2norm_k=True, scale=0.0, qk_std=1.0, seq_lens=None,
+         beta_shared=False):
     """Draws one problem.  ``gate`` is 'raw' (raw projection + gate_bias +
     gate_scale), 'log' (log-space decay drawn U(logdecay_range)) or ignored
     for rules without decay.  ``beta_mode`` is 'sigmoid' (raw N(0,1) logits +
@@ -103,7 +104,8 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
         else:
             raise ValueError(gate)
     if has_beta:
-        bshape = (T, hv, dk) if rule == "gdn2" else (T, hv)
+        bshape = (T, hv, dk) if rule == "gdn2" else ((T,) if beta_shared else (T, hv))
+        p["beta_shared"] = bool(beta_shared) and rule != "gdn2"
         bd = ACT[beta_dtype] if beta_dtype else torch.float32
         if beta_mode == "sigmoid":
             p["beta"] = torch.randn(*bshape, generator=gen).to(bd)
