@@ -587,10 +587,12 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
 // 32 (warp % 4) + lane, column half warp / 4), write Sh and, after the last
 // chunk, the final state; warps 8-11 read O^T and store the outputs; warp 12
 // loads the images; warp 13 issues the products, SQ before SE, so that the
-// completion of a chunk's last product also frees Sh.  With 64 chains on 64
-// SMs the chain streams about 60 GB/s of images per SM: the loads, not the
-// tensor cores, set its pace.  Hand-overs are mbarriers with bounded,
-// sleeping waits; each role makes a failed wait uniform before leaving.
+// completion of a chunk's last product also frees Sh.  A chunk takes about
+// 2.7 K cycles whatever the product sizes (M = 128 or 64) and whether E is
+// streamed or not: the round trip S -> Sh -> products -> commit sets the
+// pace, not the tensor cores or the image stream.  Hand-overs are mbarriers
+// with bounded, sleeping waits; each role makes a failed wait uniform before
+// leaving.
 //
 // Value rows never mix (S <- S + U^T Kt + S E and O^T = U^T P^T + S Q'^T act
 // row by row), so with ROWS = 64 a chain is split over two CTAs, each with
