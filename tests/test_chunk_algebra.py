@@ -77,3 +77,81 @@ def test_chunk_form_equals_token_loop(rule, C):
                     rule in ("delta", "gated_delta", "gdn2"))
     np.testing.assert_allclose(o, ref_o[:, 0], rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(M, ref_f[0, 0], rtol=1e-10, atol=1e-12)
+
+
+def _chunked_perkey(q, k, v, g, beta, kappa, M0, scale, C, blk=16):
+    """The per-key-decay chunk step in the form the tensor-core prepare pass and
+    the chain kernel compute it.  g is [T, dk] (one log decay per key channel),
+    Gamma its in-chunk cumulants.  A and P: entries whose column lies in an
+    earlier block of `blk` tokens are products of two scaled operands about the
+    reference token rho = (first token of the row's block) - 1, both factors at
+    most 1; entries inside a block come from a running product of per-token
+    decays.  Then the affine chunk map
+        S <- S + U^T Kt + S E,   O^T = U^T P^T + S Q'^T,
+        E = Diag(e^{Gamma_C}) - I + Wn^T Kt,   Q' = Qh + P Wn,   Wn = -W."""
+    T, dk = k.shape
+    S = M0.copy()
+    out = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, C):
+        sl = slice(c0, min(T, c0 + C))
+        Q, K, V, X, bt = q[sl], k[sl], v[sl], kappa[sl], beta[sl]
+        G = np.cumsum(g[sl], axis=0)  # [n, dk]
+        alpha = np.exp(g[sl])
+        n = len(G)
+        A = np.zeros((n, n))
+        P = np.zeros((n, n))
+        for r in range(n):
+            s = r // blk
+            if s > 0:
+                rho = blk * s - 1
+                xr = X[r] * np.exp(G[r] - G[rho])
+                qr = Q[r] * np.exp(G[r] - G[rho])
+                for j in range(blk * s):
+                    yj = K[j] * np.exp(G[rho] - G[j])
+                    A[r, j] = bt[r] * xr @ yj
+                    P[r, j] = qr @ yj
+            e = np.ones(dk)
+            for j in range(r, blk * s - 1, -1):  # down from the diagonal inside the block
+                if j < r:
+                    A[r, j] = bt[r] * np.sum(X[r] * K[j] * e)
+                P[r, j] = np.sum(Q[r] * K[j] * e)
+                e = e * alpha[j]
+        Tm = np.linalg.inv(np.eye(n) + A)
+        U = Tm @ (bt[:, None] * V)
+        Wn = -Tm @ (bt[:, None] * (np.exp(G) * X))
+        Kt = np.exp(G[-1] - G) * K
+        Qh = scale * np.exp(G) * Q
+        E = np.diag(np.exp(G[-1])) - np.eye(dk) + Wn.T @ Kt
+        Qp = Qh + scale * P @ Wn
+        out[sl] = (U.T @ (scale * P).T + S @ Qp.T).T
+        S = S + U.T @ Kt + S @ E
+    return out, S
+
+
+@pytest.mark.parametrize("rule", ["gated_delta", "gdn2"])
+@pytest.mark.parametrize("C", [16, 64])
+@pytest.mark.parametrize("lo", [-1.0, -6.0])
+def test_per_key_chunk_form_equals_token_loop(rule, C, lo):
+    """Per-key decay (GDN-2 issue; "gatedDeltaUpdate" per-key gate): the block
+    factorisation and the affine chunk map equal the token loop, including
+    strong decays whose in-chunk cumulants reach -380."""
+    T, dk, dv = 150, 8, 6
+    p = workloads.make(seed=62, B=1, cu_seqlens=[0, T], hq=1, hv=1, dk=dk, dv=dv, act="f32",
+                       rule=rule, gate="log", logdecay_range=(lo, 0.0), decay_per_key=True,
+                       beta_mode="direct", state="random", state_std=0.3, l2norm_k=False)
+    k = p["k"].double().numpy()[:, 0]
+    k = k / np.linalg.norm(k, axis=1, keepdims=True)
+    p["k"] = p["k"].double().new_tensor(k[:, None, :]).float()
+    k = p["k"].double().numpy()[:, 0]
+    q = p["q"].double().numpy()[:, 0]
+    v = p["v"].double().numpy()[:, 0]
+    g = p["decay"].double().numpy()[:, 0]  # [T, dk]
+    if rule == "gdn2":
+        kappa, beta = p["beta"].double().numpy()[:, 0] * k, np.ones(T)
+    else:
+        kappa, beta = k, p["beta"].double().numpy()[:, 0]
+    M0 = p["initial_state"].double().numpy()[0, 0]
+    ref_o, ref_f, _ = oracle.run_problem(p)
+    o, M = _chunked_perkey(q, k, v, g, beta, kappa, M0, 1 / np.sqrt(dk), C)
+    np.testing.assert_allclose(o, ref_o[:, 0], rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(M, ref_f[0, 0], rtol=1e-9, atol=1e-11)
