@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *off
 //   6. U to the image, Wn over the key rows;
 //   7. products Wn^T Kt and P Wn;
 //   8. Q' = Qh + P Wn (staged over Kt) and E = Wn^T Kt + (e^{G_C} - 1) I to the image.
-// The rules without retrieval stop after step 3, with U = V and Q' = Qh; for
+// The rules without retrieval stop after step 3, with Q' = Qh (U = V, which the
+// chain loads from the value input itself); for
 // the gated rule the image's E area holds only e^{G_C}.  Padding tokens of a short last chunk get
 // zero keys, queries, values, log decay and beta, so every operand row or
 // column that belongs to them is zero.
@@ -350,15 +351,14 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             }
             ptx::named_bar_sync(3, PR_WORK);
             // Kt rows = e^{G_C - G_t} k_t / |k_t| into their tile (image layout; the operand of E);
-            // without retrieval also U = V and Q' = Qh straight to the image
+            // without retrieval also Q' = Qh straight to the image
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 const int idx = tid + PR_WORK * w, tr = idx >> 4, ch = idx & 15;
                 const int io = (ch >> 3) * 8192 + sw(tr, ch & 7);  // image (and Kt / V tile) offset
                 *reinterpret_cast<uint4 *>(sm + rKt + io) =
                     scale_chunk(*reinterpret_cast<const uint4 *>(sm + kq_off(tr, ch, false)), F[fKF + tr]);
-                if (!RETR) {
-                    *reinterpret_cast<uint4 *>(dst + IM_U + io) = *reinterpret_cast<const uint4 *>(sm + rV + io);
+                if (!RETR) {  // (U = V: the chain loads it from the value input)
                     *reinterpret_cast<uint4 *>(dst + IM_Q + io) =
                         scale_chunk(*reinterpret_cast<const uint4 *>(sm + kq_off(tr, ch, true)), F[fQF + tr]);
                 }
@@ -613,7 +613,8 @@ enum : int { kStepPlain = 0, kStepDecay = 1, kStepE = 2 };
 
 template <int STEP, int ROWS>
 __global__ void __launch_bounds__(CH_THREADS, 1)
-    chunk_chain_kernel(Problem p, const int *offs, const int *order, const unsigned char *img, int cap) {
+    chunk_chain_kernel(Problem p, const __grid_constant__ CUtensorMap tmV, const int *offs, const int *order,
+                       const unsigned char *img, int cap) {
     constexpr bool HALF = ROWS == 64;
     constexpr int SHB = ROWS * 128;  // bytes per 64-column block of Sh
     extern __shared__ unsigned char smraw[];
@@ -796,12 +797,33 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 unsigned char *dstb = sm + cImg + bf * IM_BYTES;
                 ptx::mbar_arrive_expect_tx(&land[bf], IM_BYTES - skip - (16384u - ubytes));
                 // the image two chunks ahead into L2, so that its load from there is short
-                if (c + 2 < nch)
-                    ptx::prefetch_l2(src + 2 * (size_t)p.Hv * IM_BYTES + skip, IM_BYTES - skip);
-                if (STEP == kStepE) ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);  // E and Q'
-                else ptx::bulk_g2s(dstb + IM_Q, src + IM_Q, IM_U - IM_Q, &land[bf]);
-                ptx::bulk_g2s(dstb + IM_U, src + IM_U + 8192 * vh, ubytes, &land[bf]);  // U (its rows)
-                ptx::bulk_g2s(dstb + IM_P, src + IM_P, IM_BYTES - IM_P, &land[bf]);      // P, Kt
+                if (c + 2 < nch) {
+                    const unsigned char *nxt = src + 2 * (size_t)p.Hv * IM_BYTES;
+                    if (STEP == kStepE) {
+                        ptx::prefetch_l2(nxt, IM_BYTES);
+                    } else {
+                        ptx::prefetch_l2(nxt + IM_Q, IM_U - IM_Q);
+                        ptx::prefetch_l2(nxt + IM_P, IM_BYTES - IM_P);
+#pragma unroll
+                        for (int kb = 0; kb < 2; ++kb)
+                            if (!HALF || kb == vh) ptx::prefetch_tile_3d(&tmV, 64 * kb, h, t0 + TC_C * (c + 2));
+                    }
+                }
+                if (STEP == kStepE) {
+                    ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);                                // E and Q'
+                    ptx::bulk_g2s(dstb + IM_U, src + IM_U + 8192 * vh, ubytes, &land[bf]);  // U (its rows)
+                } else {
+                    ptx::bulk_g2s(dstb + IM_Q, src + IM_Q, IM_U - IM_Q, &land[bf]);  // Q'
+                    // without retrieval U = V: its rows straight from the value input (the box
+                    // lands in the image's U layout; rows past the request meet zero Kt rows and
+                    // causally masked P entries only)
+#pragma unroll
+                    for (int kb = 0; kb < 2; ++kb)
+                        if (!HALF || kb == vh)
+                            ptx::tma_load_3d(dstb + IM_U + (HALF ? 0 : 8192 * kb), &tmV, 64 * kb, h, t0 + TC_C * c,
+                                             &land[bf]);
+                }
+                ptx::bulk_g2s(dstb + IM_P, src + IM_P, IM_BYTES - IM_P, &land[bf]);  // P, Kt
             }
         }
     } else {
@@ -815,6 +837,21 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 ok = ptx::mbar_wait_sleep(&land[bf], (c >> 1) & 1) && ptx::mbar_wait_sleep(rsread, c & 1);
                 if (!ok) break;
                 tc::fence_after();
+                if (STEP != kStepE && c == nch - 1) {
+                    // U came straight from the value input: in a short last chunk its rows past the
+                    // request hold other tokens (or whatever the caller keeps there) and are cleared
+                    const int n = t1 - (t0 + TC_C * c);
+                    if (n < TC_C) {
+                        unsigned char *ub = sm + cImg + bf * IM_BYTES + IM_U;
+                        for (int r = n; r < TC_C; ++r)
+#pragma unroll
+                            for (int kb = 0; kb < (HALF ? 1 : 2); ++kb)
+#pragma unroll
+                                for (int q16 = 0; q16 < 8; ++q16)
+                                    *reinterpret_cast<uint4 *>(ub + kb * 8192 + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+                        tc::fence_async_smem();
+                    }
+                }
                 // UK: S += U^T Kt (M = 128 v, N = 128 j, K = 64 t; A and B M/N-major)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
@@ -974,18 +1011,18 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     // fewer chains than SMs: two CTAs per chain, one per half of the value rows
     if ((long long)grid < sm_count()) {
         if (p.rule == kLinear)
-            chunk_chain_kernel<kStepPlain, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+            chunk_chain_kernel<kStepPlain, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
         else if (p.rule == kGated)
-            chunk_chain_kernel<kStepDecay, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+            chunk_chain_kernel<kStepDecay, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
         else
-            chunk_chain_kernel<kStepE, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+            chunk_chain_kernel<kStepE, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
     } else {
         if (p.rule == kLinear)
-            chunk_chain_kernel<kStepPlain, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+            chunk_chain_kernel<kStepPlain, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
         else if (p.rule == kGated)
-            chunk_chain_kernel<kStepDecay, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+            chunk_chain_kernel<kStepDecay, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
         else
-            chunk_chain_kernel<kStepE, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, offs, order, img, cap);
+            chunk_chain_kernel<kStepE, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
     }
     return cudaGetLastError();
 }

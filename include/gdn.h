@@ -101,7 +101,8 @@ typedef enum gdn_rule {
  * (rank-4 form only; "gatedDeltaUpdate", seq_lens bounds the rows of a ragged
  * prefill) makes the batch padded-ragged: request b owns the first
  * clamp(seq_lens[b], 0, seq_len) tokens of its row, [b * seq_len,
- * b * seq_len + that); the padding tokens are neither read nor written.
+ * b * seq_len + that); the padding tokens take no part in any result and
+ * are not written (their contents may be anything, NaN included).
  * seq_lens NULL means every row is full.
  *
  * Heads.  num_heads_v is a positive multiple of num_heads_q; value head h

@@ -12,6 +12,25 @@ from gated_delta_rule_gate_gb300 import api
 DEV = "cuda"
 
 
+def poison_uncovered(p):
+    """Fills every token that no request covers (gaps between requests, the
+    padding of seq_lens rows) with NaN in q, k, v and the gates: no result may
+    depend on them."""
+    import workloads
+    T = p["total_tokens"]
+    covered = np.zeros(T, dtype=bool)
+    for t0, t1 in workloads.token_ranges(p):
+        covered[t0:t1] = True
+    idx = torch.as_tensor(np.nonzero(~covered)[0])
+    for key in ("q", "k", "v", "decay", "beta"):
+        t = p.get(key)
+        if t is not None and len(idx):
+            t = t.clone()
+            t.reshape((T,) + tuple(t.shape[1:]) if t.dim() > 1 else (T,))[idx] = float("nan")
+            p[key] = t
+    return p
+
+
 def to_dev(p):
     d = dict(p)
     for key in ("q", "k", "v", "decay", "gate_bias", "gate_scale", "beta", "cu_seqlens",

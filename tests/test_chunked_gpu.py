@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_helpers import DEV, o_flat, rel_err, run, to_dev
+from gpu_helpers import DEV, o_flat, poison_uncovered, rel_err, run, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -250,7 +250,7 @@ def test_chunked_seq_lens_padded_rows(case):
     kw = dict(seed=41, B=4, seq_len=100, seq_lens=[100, 0, 37, 250], hq=1, hv=2, dk=128, dv=128,
               act="f16", state="random", state_std=0.3)
     kw.update(case)
-    p = workloads.make(**kw)
+    p = poison_uncovered(workloads.make(**kw))  # NaN in every padding token
     ref_o, ref_fin, err = oracle.run_problem(p)
     assert err == 0
     o, fin, _ = run(p, path="chunked")
@@ -270,6 +270,24 @@ def test_chunked_shared_beta(case, rule):
               state="random", state_std=0.3, beta_shared=True)
     kw.update(case)
     p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
+
+
+@pytest.mark.parametrize("case", [dict(rule="linear"), dict(rule="gated"), dict(rule="gated_delta"),
+                                  dict(rule="gdn2", decay_per_key=True, gate_dtype="f32", write_gate=True),
+                                  dict(rule="gated", dk=64, dv=64)],
+                         ids=["tc-linear", "tc-gated", "tc-gated_delta", "tc-perkey-gdn2", "mma-gated"])
+def test_chunked_ignores_uncovered_tokens(case):
+    """Tokens outside every request (before the first, between clamped
+    requests, after the last) hold NaN in q, k, v and the gates: outputs and
+    states match the oracle, and uncovered outputs keep the sentinel."""
+    kw = dict(seed=46, B=3, T=260, cu_seqlens=[3, 70, 70, 200], hq=1, hv=2, dk=128, dv=128, act="f16",
+              state="random", state_std=0.3)
+    kw.update(case)
+    p = poison_uncovered(workloads.make(**kw))
     ref_o, ref_fin, err = oracle.run_problem(p)
     assert err == 0
     o, fin, _ = run(p, path="chunked")

@@ -15,7 +15,7 @@ import torch
 import oracle
 import workloads
 from gated_delta_rule_gate_gb300 import api
-from gpu_helpers import DEV, o_flat, rel_err, run, to_dev
+from gpu_helpers import DEV, o_flat, poison_uncovered, rel_err, run, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -278,6 +278,7 @@ def test_seq_lens_padded_rows(case):
     padding tokens keep the sentinel; slots in place."""
     p = workloads.make(seed=43, B=5, hq=2, hv=4, act="f16", rule="gated_delta", state="random",
                        num_slots=8, slot_mode="perm", **case)
+    p = poison_uncovered(p)  # NaN in every padding token
     ref_o, ref_fin, err = oracle.run_problem(p)
     assert err == 0
     o, fin, _ = run(p)
