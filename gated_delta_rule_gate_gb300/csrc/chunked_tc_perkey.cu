@@ -114,11 +114,14 @@ __device__ __forceinline__ void unpack8(uint4 u, float *x) {
 
 // ---------------------------------------------------------------------------
 // chunk_prepare_perkey_kernel: the operand image of every (chunk slot, value
-// head).  Persistent CTAs, one per SM: a producer warp (task lookup and the
-// scalar gates one task ahead; key, query and value tiles by TMA and the
-// per-key log decay and erase-gate rows by bulk copies once the previous task
-// has released shared memory; the next task's rows prefetched into L2) and
-// eight worker warps.  Per task the workers
+// head).  Persistent CTAs, one per SM: a producer warp and eight worker warps.
+// The producer looks up the next task and loads its scalar gates one task
+// ahead.  It lands the per-key log-decay rows and the head's gate bias as soon
+// as the previous task has finished its diagonal blocks (gfree).  The key,
+// query and value tiles (TMA) and the erase-gate rows follow once that task's
+// last products have read their buffers (tfree), and the task after that is
+// prefetched into L2.  So the next task's loads overlap the solve and the
+// epilogues of the current one.  Per task the workers
 //   1. zero the rows past a short last chunk, apply the raw gate and take the
 //      per-channel cumulants Gamma, 1/|k|, 1/|q| and b .* k;
 //   2. write Kt, Qh, X' and the scaled operands of the off-block products;
