@@ -52,3 +52,36 @@ def test_reference_arm_two_ranks_gloo():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_line(lines[0], 2)
+
+
+def test_kernel_names_mirror_the_dispatch():
+    """The bench names the kernels the library dispatches: the tcgen05 prefill
+    for every rule at dk = dv = 128 with fp16 activations (per-key decay and
+    GDN-2 through the per-key prepare pass when their gates are fp32), the
+    warp-level MMA kernel for other shapes, the token-serial kernels otherwise."""
+    import importlib.util
+    sys.path.insert(0, ROOT)
+    import workloads
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    base = dict(seed=1, B=1, lengths=[8], hq=1, hv=1, dk=128, dv=128, act="f16")
+    cases = [
+        (dict(rule="gated_delta"), "chunk_prepare_kernel<1>+chunk_chain_kernel<2>"),
+        (dict(rule="linear"), "chunk_prepare_kernel<0>+chunk_chain_kernel<0>"),
+        (dict(rule="gated"), "chunk_prepare_kernel<0>+chunk_chain_kernel<1>"),
+        (dict(rule="gdn2", decay_per_key=True, gate_dtype="f32"),
+         "chunk_prepare_perkey_kernel<1>+chunk_chain_kernel<2>"),
+        (dict(rule="gated_delta", decay_per_key=True, gate_dtype="f32"),
+         "chunk_prepare_perkey_kernel<0>+chunk_chain_kernel<2>"),
+        (dict(rule="gated_delta", decay_per_key=True, lengths=[200]), "recurrent_long_kernel<128>"),
+        (dict(rule="gated_delta", dk=64, dv=64), "chunked_mma_kernel<64,false>"),
+    ]
+    for over, name in cases:
+        kw = dict(base)
+        kw.update(over)
+        p = workloads.make(**kw)
+        assert b.kernel_name(p, "chunked") == name, (over, b.kernel_name(p, "chunked"))
+        assert b.launches_per_call(p, "chunked") == (3 if "chain" in name else 1)
+    p = workloads.decode(1, B=4, num_slots=8)
+    assert b.kernel_name(p, "recurrent") == "recurrent_pipe_kernel<128>"
