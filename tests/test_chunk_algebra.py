@@ -15,8 +15,12 @@ for a chunk with incoming state M0 and in-chunk log-decay cumulants G,
     M_C  = e^{G_C} M0 + Delta^T diag(e^{G_C - G}) K
 
 (kappa = k for the v1 rules, b .* k with beta = 1 for GDN-2; rules without
-retrieval use Delta = V).  This test is the derivation's check: it is not
-the oracle and the oracle does not use it.
+retrieval use Delta = V).  The same file checks the per-key-decay form of the
+chunk step (block factorisation about reference tokens, running products on
+the diagonal blocks, the affine chunk map the chain kernel applies) and the
+decode kernel's token step with a lazy scalar decay factor.  These tests are
+the derivations' checks: they are not the oracle and the oracle does not use
+them.
 """
 import numpy as np
 import pytest
@@ -155,3 +159,55 @@ def test_per_key_chunk_form_equals_token_loop(rule, C, lo):
     o, M = _chunked_perkey(q, k, v, g, beta, kappa, M0, 1 / np.sqrt(dk), C)
     np.testing.assert_allclose(o, ref_o[:, 0], rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(M, ref_f[0, 0], rtol=1e-9, atol=1e-11)
+
+
+def _lazy_decay_loop(q, k, v, g, beta, kappa, M0, scale, retrieval, floor=1e-20):
+    """The token step of the decode kernel with a scalar decay kept as a lazy
+    factor, S = c * S~, so that each token touches the state once:
+        c' = c alpha,  u = c' (S~ kappa),  d = beta (v - u)  (v without retrieval),
+        o = scale (c' (S~ q) + d (k . q)),  S~ += (d / c') k^T,
+    with c' folded into S~ before it underflows (c' < floor)."""
+    S = M0.copy()
+    c = 1.0
+    out = np.zeros((len(k), v.shape[1]))
+    for t in range(len(k)):
+        cn = c * np.exp(g[t])
+        u = cn * (S @ kappa[t])
+        d = beta[t] * (v[t] - u) if retrieval else v[t]
+        out[t] = scale * (cn * (S @ q[t]) + d * (k[t] @ q[t]))
+        if cn < floor:
+            S *= cn
+            cn = 1.0
+        S += np.outer(d / cn, k[t])
+        c = cn
+    return out, c * S
+
+
+@pytest.mark.parametrize("rule", ["gated", "gated_delta", "gdn2"])
+@pytest.mark.parametrize("lo", [-1.0, -30.0])
+def test_lazy_decay_form_equals_token_loop(rule, lo):
+    """The lazy-factor decode step equals the token loop, also when the decay
+    is strong enough (log decays down to -30 per token) that the factor is
+    folded back into the state several times."""
+    T, dk, dv = 40, 8, 6
+    p = workloads.make(seed=63, B=1, cu_seqlens=[0, T], hq=1, hv=1, dk=dk, dv=dv, act="f32",
+                       rule=rule, gate="log", logdecay_range=(lo, 0.0), beta_mode="direct",
+                       state="random", state_std=0.3, l2norm_k=False)
+    k = p["k"].double().numpy()[:, 0]
+    k = k / np.linalg.norm(k, axis=1, keepdims=True)
+    p["k"] = p["k"].double().new_tensor(k[:, None, :]).float()
+    k = p["k"].double().numpy()[:, 0]
+    q = p["q"].double().numpy()[:, 0]
+    v = p["v"].double().numpy()[:, 0]
+    g = p["decay"].double().numpy()[:, 0]
+    if rule == "gdn2":
+        kappa, beta = p["beta"].double().numpy()[:, 0] * k, np.ones(T)
+    elif rule == "gated_delta":
+        kappa, beta = k, p["beta"].double().numpy()[:, 0]
+    else:
+        kappa, beta = k, np.ones(T)
+    M0 = p["initial_state"].double().numpy()[0, 0]
+    ref_o, ref_f, _ = oracle.run_problem(p)
+    o, M = _lazy_decay_loop(q, k, v, g, beta, kappa, M0, 1 / np.sqrt(dk), rule != "gated")
+    np.testing.assert_allclose(o, ref_o[:, 0], rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(M, ref_f[0, 0], rtol=1e-9, atol=1e-12)
