@@ -643,7 +643,6 @@ __device__ __forceinline__ void consume_slices(const Problem &p, const Stage &st
 
 template <int DK>
 __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Problem p, int slices, int pairs) {
-    constexpr int NV = DK / 32;  // float4s per lane per row
     constexpr int kSlice = kFastRows * DK;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const PipeLayout Ly = pipe_layout(p);
@@ -881,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, 
     const bool has_decay = rule_has_decay(p.rule);
     const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
     const bool sig = (p.flags & kBetaSigmoid) != 0;
-    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4;
     auto prefetch_scalars = [&](int tb, int nt, float &g, float &bb) {
         g = 0.f, bb = 1.f;
         if (tid < nt) {
