@@ -267,9 +267,12 @@ def time_e2e(api, p, d, prob, path, steps, warmup, stream, dev):
 def kernel_name(p, path):
     """The kernel the library dispatches for this workload (mirrors the host
     dispatch in the CUDA sources)."""
-    if path == "recurrent":
+    def token_serial():
+        # average request length above four staged token blocks (of 8): the long-request kernel
         L = p.get("seq_len") or p["total_tokens"] // max(p["batch"], 1)
         return ("recurrent_long_kernel<%d>" if L > 32 else "recurrent_pipe_kernel<%d>") % p["dk"]
+    if path == "recurrent":
+        return token_serial()
     per_key = p.get("decay_per_key") and p["rule"] in ("gated", "gated_delta", "gdn2")
     tc_shape = p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16"
     f32_gates = (p.get("decay") is None or p["decay"].dtype == torch.float32 or not per_key) and \
@@ -277,7 +280,7 @@ def kernel_name(p, path):
     if tc_shape and f32_gates and (p["rule"] == "gdn2" or (per_key and p["rule"] == "gated_delta")):
         return "chunk_prepare_perkey_kernel<%d>+chunk_chain_kernel<2>" % int(p["rule"] == "gdn2")
     if per_key:
-        return "recurrent_long_kernel<%d>" % p["dk"]
+        return token_serial()
     if tc_shape and p["rule"] != "gdn2":
         retr = p["rule"] in ("delta", "gated_delta")
         return "chunk_prepare_kernel<%d>+chunk_chain_kernel<%d>" % (
