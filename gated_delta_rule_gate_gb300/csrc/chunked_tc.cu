@@ -591,11 +591,12 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
 // chunk, the final state; warps 8-11 read O^T and store the outputs; warp 12
 // loads the images; warp 13 issues the products, SQ before SE, so that the
 // completion of a chunk's last product also frees Sh.  A chunk takes about
-// 2.7 K cycles whatever the product sizes (M = 128 or 64) and whether E is
-// streamed or not: the round trip S -> Sh -> products -> commit sets the
-// pace, not the tensor cores or the image stream.  Hand-overs are mbarriers
-// with bounded, sleeping waits; each role makes a failed wait uniform before
-// leaving.
+// 2.7 K cycles whether the products have M = 128 or 64 and whether E is
+// streamed or not: an M = 64 instruction holds the tensor pipe about as long
+// as an M = 128 one, so the 24 instructions on the serial path, with the
+// round trip S -> Sh -> products -> commit around them, set the pace.
+// Hand-overs are mbarriers with bounded, sleeping waits; each role makes a
+// failed wait uniform before leaving.
 //
 // Value rows never mix (S <- S + U^T Kt + S E and O^T = U^T P^T + S Q'^T act
 // row by row), so with ROWS = 64 a chain is split over two CTAs, each with
