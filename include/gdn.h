@@ -131,8 +131,8 @@ typedef enum gdn_rule {
  * slot_ids[b] if slot_ids is non-NULL (the slab of gatedDeltaUpdate), else
  * row b.  initial_state NULL means a zero state.  final_state may equal
  * initial_state (in-place update); otherwise the two must not overlap.  Rows
- * no request names are not touched.  A request with no tokens copies its
- * incoming state through.  Slot ids must be distinct (caller's contract); a
+ * no request names are not touched.  An empty request leaves its final
+ * state equal to its initial state ("com.microsoft.GatedDeltaNet", Outputs).  Slot ids must be distinct (caller's contract); a
  * slot id outside [0, num_state_rows) makes every CTA of that request skip it
  * and OR GDN_DEVERR_BAD_SLOT into *error_word (if error_word is non-NULL).
  *

@@ -41,6 +41,7 @@ class _Problem(ctypes.Structure):
         ("cu_seqlens", _ip), ("slot_ids", _ip),
         ("initial_state", _dp), ("final_state", _dp), ("o", _dp),
         ("error_word", _ip), ("seq_lens", _ip), ("beta_shared", ctypes.c_int32),
+        ("state_kmajor", ctypes.c_int32), ("erase_gate", _dp), ("write_gate", _dp),
     ]
 
 
@@ -110,7 +111,8 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         gate_scale=None, cu_seqlens=None, batch=None, slot_ids=None,
         initial_state=None, final_state=None, num_state_rows=None, scale=0.0,
         l2norm_q=False, l2norm_k=False, beta_sigmoid=False, decay_per_key=False,
-        threads=1, seq_lens=None, beta_shared=False):
+        threads=1, seq_lens=None, beta_shared=False, state_kmajor=False, erase_gate=None,
+        write_gate=None):
     """Runs the recurrence token by token in float64.
 
     q, k: [T, Hq, dk]; v: [T, Hv, dv] (rank-4 callers flatten [B, S] to T and
@@ -120,7 +122,11 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
     names keep its values.  Output tokens outside every request are NaN.
     ``seq_lens`` ([batch], uniform layout only) shortens request b to the first
     seq_lens[b] tokens of its row.  ``beta_shared``: the scalar beta is [T],
-    one per token for every value head.
+    one per token for every value head.  ``state_kmajor``: states are
+    [rows, Hv, dk, dv] ("gatedDeltaUpdate") instead of [rows, Hv, dv, dk].
+    ``erase_gate`` ([T, Hv, dk], rule gdn2): the GDN-2 erase gate as its own
+    input, beta then being the scalar write rate; ``write_gate`` ([T, Hv, dv],
+    rule gdn2): the GDN-2 write gate, applied to v here.
     """
     lib = _load()
     q64, k64, v64 = _f64(q), _f64(k), _f64(v)
@@ -144,13 +150,16 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
     elif init is not None:
         fin = init.copy()
     else:
-        fin = np.zeros((num_state_rows, hv, dv, dk), np.float64)
+        fin = np.zeros((num_state_rows, hv, dk, dv) if state_kmajor else (num_state_rows, hv, dv, dk),
+                       np.float64)
     o = np.full((T, hv, dv), np.nan, np.float64)
     err = np.zeros(1, np.int32)
     dec = _f64(decay)
     bet = _f64(beta)
     gb = _f64(gate_bias)
     gs = _f64(gate_scale)
+    eg = _f64(erase_gate)
+    wg = _f64(write_gate)
     raw = gb is not None or gs is not None
     prob = _Problem(
         batch=batch, total_tokens=T, hq=hq, hv=hv, dk=dk, dv=dv, rule=RULES[rule],
@@ -162,6 +171,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         beta=_ptr(bet, _dp), cu_seqlens=_ptr(cu, _ip), slot_ids=_ptr(slots, _ip),
         initial_state=_ptr(init, _dp), final_state=_ptr(fin, _dp), o=_ptr(o, _dp),
         error_word=_ptr(err, _ip), seq_lens=_ptr(sl, _ip), beta_shared=int(beta_shared),
+        state_kmajor=int(bool(state_kmajor)), erase_gate=_ptr(eg, _dp), write_gate=_ptr(wg, _dp),
     )
     rc = lib.oracle_gdn(ctypes.byref(prob))
     if rc != 0:
@@ -254,7 +264,9 @@ def run_problem(p, threads=1, requests=None):
                             l2norm_q=p.get("l2norm_q", False), l2norm_k=p.get("l2norm_k", False),
                             beta_sigmoid=p.get("beta_sigmoid", False),
                             decay_per_key=p.get("decay_per_key", False), threads=threads,
-                            beta_shared=p.get("beta_shared", False))
+                            beta_shared=p.get("beta_shared", False),
+                            state_kmajor=p.get("state_kmajor", False),
+                            erase_gate=take(p.get("erase_gate")), write_gate=take(p.get("write_gate")))
         o = np.full((T, p["hv"], p["dv"]), np.nan)
         if len(idx):
             o[idx] = o_s
@@ -267,4 +279,5 @@ def run_problem(p, threads=1, requests=None):
                l2norm_q=p.get("l2norm_q", False), l2norm_k=p.get("l2norm_k", False),
                beta_sigmoid=p.get("beta_sigmoid", False),
                decay_per_key=p.get("decay_per_key", False), threads=threads, seq_lens=sl,
-               beta_shared=p.get("beta_shared", False))
+               beta_shared=p.get("beta_shared", False), state_kmajor=p.get("state_kmajor", False),
+               erase_gate=p.get("erase_gate"), write_gate=p.get("write_gate"))

@@ -20,8 +20,8 @@
  *  - same page, Inputs table: cu_seqlens are exclusive prefix sums clamped to
  *    [0, total_tokens]; a decreasing entry yields an empty request; absent
  *    means uniform packing.  initial_state absent means zeros.
- *  - same page, Outputs table: a request with no tokens copies its incoming
- *    state through.
+ *  - same page, Outputs table (final_state row): when a request is empty,
+ *    its final state equals its initial state.
  *  - ONNX issue "Spec gap ... Gated DeltaNet-2", "What LinearAttention
  *    currently does": beta's last dimension is kv_num_heads or 1; with 1,
  *    one beta per token serves every value head.
@@ -44,6 +44,15 @@
  *    DeltaNet-2 channel-wise erase gate", proposal (A): decay first, then the
  *    erase with retrieval key (b_t .* k_t) on the key side, then the write
  *    k_t v_t^T; the write gate w_t is folded into v by the caller.
+ *  - same issue, proposal (B): the erase gate b_t is an input of its own,
+ *    [T, Hv * dk], beside the scalar beta; with b_t = beta_t * 1 the update is
+ *    gated_delta again.  Reading taken here: beta keeps the write role, so
+ *    delta = beta (w .* v) - D S (b .* k); the write gate w_t of the first
+ *    display of that issue may be passed in (w .* v formed here) instead of
+ *    being folded into v by the caller.
+ *  - "gatedDeltaUpdate": the state may be stored key-major, [B, HV, K, V]
+ *    (slab [num_slots, HV, K, V]); the recurrence is the same, only the
+ *    layout of initial_state and final_state changes.
  *
  * Storage here is value-major: M (dv x dk) is the transpose of the key-major
  * state of the first page, row i = value channel i, contiguous over dk.  With
@@ -54,7 +63,9 @@
  *     delta = v               (linear, gated)
  *     M    <- M + delta k^T
  *     o     = scale * M q                     (readout of the updated state)
- * where kappa = k for the v1 rules and kappa = b .* k for GDN-2.
+ * where kappa = k for the v1 rules and kappa = b .* k for GDN-2.  For GDN-2,
+ * delta = beta (w .* v) - u, with beta == 1 when the erase gate rides in
+ * beta (proposal A) and w == 1 when no write gate is passed.
  */
 #include <math.h>
 #include <stddef.h>
@@ -98,6 +109,9 @@ typedef struct {
     int32_t *error_word;         /* may be NULL */
     const int32_t *seq_lens;     /* [B] or NULL: rows of the uniform layout shortened */
     int32_t beta_shared;         /* scalar beta is [T]: one per token for every value head */
+    int32_t state_kmajor;        /* states are [rows,Hv,dk,dv] (key-major) instead of [rows,Hv,dv,dk] */
+    const double *erase_gate;    /* GDN-2 proposal (B): [T,Hv,dk]; beta is then scalar */
+    const double *write_gate;    /* GDN-2: [T,Hv,dv] or NULL (w == 1) */
 } oracle_problem;
 
 /* softplus(x) = ln(1 + e^x), evaluated without overflow. */
@@ -178,10 +192,13 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
     double *delta = u + dv;           /* dv */
 
     const size_t state_off = (((size_t)row * hv) + h) * (size_t)dv * dk;
-    if (p->initial_state)
-        memcpy(M, p->initial_state + state_off, sizeof(double) * (size_t)dv * dk);
-    else
+    if (!p->initial_state)
         memset(M, 0, sizeof(double) * (size_t)dv * dk);
+    else if (p->state_kmajor) /* stored [dk][dv]: element (i, c) of M at c * dv + i */
+        for (int32_t i = 0; i < dv; ++i)
+            for (int32_t c = 0; c < dk; ++c) M[(size_t)i * dk + c] = p->initial_state[state_off + (size_t)c * dv + i];
+    else
+        memcpy(M, p->initial_state + state_off, sizeof(double) * (size_t)dv * dk);
 
     const double scale = p->scale != 0.0 ? p->scale : 1.0 / sqrt((double)dk);
     int32_t t0, t1;
@@ -214,19 +231,38 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
                 for (int32_t c = 0; c < dk; ++c) M[(size_t)i * dk + c] *= alpha[c];
         }
 
-        if (rule_has_retrieval(p->rule)) {
-            double beta = 1.0;
-            if (p->rule == ORACLE_RULE_GDN2) {
-                for (int32_t c = 0; c < dk; ++c) {
-                    double bc = p->beta[((size_t)t * hv + h) * dk + c];
+        if (p->rule == ORACLE_RULE_GDN2) {
+            /* erase gate b: its own input (proposal B, taken as given) or the
+             * per-key beta (proposal A, through the sigmoid when asked) */
+            for (int32_t c = 0; c < dk; ++c) {
+                double bc;
+                if (p->erase_gate) {
+                    bc = p->erase_gate[((size_t)t * hv + h) * dk + c];
+                } else {
+                    bc = p->beta[((size_t)t * hv + h) * dk + c];
                     if (p->beta_sigmoid) bc = sigmoid(bc);
-                    kappa[c] = bc * kv[c];
                 }
-            } else {
+                kappa[c] = bc * kv[c];
+            }
+            /* the write's scalar: beta under proposal B, 1 under proposal A */
+            double beta = 1.0;
+            if (p->erase_gate) {
                 beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];
                 if (p->beta_sigmoid) beta = sigmoid(beta);
-                memcpy(kappa, kv, sizeof(double) * dk);
             }
+            for (int32_t i = 0; i < dv; ++i) {
+                double s = 0.0;
+                for (int32_t c = 0; c < dk; ++c) s += M[(size_t)i * dk + c] * kappa[c];
+                u[i] = s;
+            }
+            for (int32_t i = 0; i < dv; ++i) {
+                const double w = p->write_gate ? p->write_gate[((size_t)t * hv + h) * dv + i] : 1.0;
+                delta[i] = beta * (w * vin[i]) - u[i];
+            }
+        } else if (rule_has_retrieval(p->rule)) {
+            double beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];
+            if (p->beta_sigmoid) beta = sigmoid(beta);
+            memcpy(kappa, kv, sizeof(double) * dk);
             for (int32_t i = 0; i < dv; ++i) {
                 double s = 0.0;
                 for (int32_t c = 0; c < dk; ++c) s += M[(size_t)i * dk + c] * kappa[c];
@@ -247,7 +283,11 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
             out[i] = scale * s;
         }
     }
-    memcpy(p->final_state + state_off, M, sizeof(double) * (size_t)dv * dk);
+    if (p->state_kmajor)
+        for (int32_t i = 0; i < dv; ++i)
+            for (int32_t c = 0; c < dk; ++c) p->final_state[state_off + (size_t)c * dv + i] = M[(size_t)i * dk + c];
+    else
+        memcpy(p->final_state + state_off, M, sizeof(double) * (size_t)dv * dk);
 }
 
 /* Runs every (request, value head) pair.  Returns 0, or 1 on bad arguments. */
@@ -261,7 +301,10 @@ int oracle_gdn(const oracle_problem *p) {
     if (p->raw_gate && (!p->gate_bias || !p->gate_scale)) return 1;
     if (!p->cu_seqlens && p->total_tokens % p->batch != 0) return 1;
     if (p->cu_seqlens && p->seq_lens) return 1;
-    if (p->beta_shared && p->rule != ORACLE_RULE_DELTA && p->rule != ORACLE_RULE_GATED_DELTA) return 1;
+    if (p->beta_shared && p->rule != ORACLE_RULE_DELTA && p->rule != ORACLE_RULE_GATED_DELTA &&
+        !(p->rule == ORACLE_RULE_GDN2 && p->erase_gate))
+        return 1;
+    if ((p->erase_gate || p->write_gate) && p->rule != ORACLE_RULE_GDN2) return 1;
 
     const int64_t pairs = (int64_t)p->batch * p->hv;
     const size_t per = (size_t)p->dv * p->dk + 4 * (size_t)p->dk + 2 * (size_t)p->dv;

@@ -485,3 +485,170 @@ def test_threads_do_not_change_results():
     o4, f4, _ = oracle.run_problem(p, threads=4)
     np.testing.assert_array_equal(o1, o4)
     np.testing.assert_array_equal(f1, f4)
+
+
+# --------------------------------------------------------------------------
+# Per-key raw-gate arm ("gatedDeltaUpdate": gate_bias [HV, K] beside a
+# [B, T, HV, K] gate, gate_scale [HV]): each key channel c of head h takes
+# g = gate_scale[h] * softplus(raw + gate_bias[h, c]).  The log decays are
+# formed here with the Python math library and fed to the oracle directly.
+# A bias taken per head, per channel only, or a scale taken per channel fails.
+# --------------------------------------------------------------------------
+def test_per_key_raw_gate_arm():
+    rng = np.random.default_rng(31)
+    T, hv, dk, dv = 7, 2, 5, 3
+    q = rng.standard_normal((T, 1, dk))
+    k = _unit(rng.standard_normal((T, 1, dk)))
+    v = rng.standard_normal((T, hv, dv))
+    raw = rng.standard_normal((T, hv, dk)) * 2.0
+    bias = rng.uniform(-2.0, 2.0, (hv, dk))
+    gscale = -np.exp(rng.uniform(0.0, 2.0, hv))
+    beta = rng.random((T, hv))
+    S0 = rng.standard_normal((1, hv, dv, dk)) * 0.3
+    g = np.empty((T, hv, dk))
+    for t in range(T):
+        for h in range(hv):
+            for c in range(dk):
+                g[t, h, c] = gscale[h] * math.log1p(math.exp(raw[t, h, c] + bias[h, c]))
+    o1, f1, _ = oracle.gdn(q, k, v, rule="gated_delta", decay=raw, gate_bias=bias, gate_scale=gscale,
+                           beta=beta, initial_state=S0, decay_per_key=True)
+    o2, f2, _ = oracle.gdn(q, k, v, rule="gated_delta", decay=g, beta=beta, initial_state=S0,
+                           decay_per_key=True)
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(f1, f2, rtol=1e-13, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# The GDN-2 erase gate through beta_activation: with BETA_SIGMOID the
+# per-key beta logits x give b = 1 / (1 + e^-x) (GDN-2 issue: b_t in
+# [0, 1]^{d_k}); b is formed here with the Python math library.
+# --------------------------------------------------------------------------
+def test_gdn2_erase_gate_sigmoid():
+    rng = np.random.default_rng(32)
+    T, hv, dk, dv = 6, 2, 4, 3
+    q = rng.standard_normal((T, 1, dk))
+    k = _unit(rng.standard_normal((T, 1, dk)))
+    v = rng.standard_normal((T, hv, dv))
+    x = rng.standard_normal((T, hv, dk)) * 3.0
+    b = np.vectorize(lambda z: 1.0 / (1.0 + math.exp(-z)))(x)
+    g = -rng.random((T, hv, dk))
+    S0 = rng.standard_normal((1, hv, dv, dk)) * 0.3
+    o1, f1, _ = oracle.gdn(q, k, v, rule="gdn2", decay=g, beta=x, beta_sigmoid=True, initial_state=S0,
+                           decay_per_key=True)
+    o2, f2, _ = oracle.gdn(q, k, v, rule="gdn2", decay=g, beta=b, initial_state=S0, decay_per_key=True)
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(f1, f2, rtol=1e-13, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# Key-major state ("gatedDeltaUpdate": the [B, HV, K, V] state decays by
+# exp(g), takes the rank-1 update (beta k) (x) (v - S^T k) and emits
+# o = (scale q)^T S).  That loop is written here in its own key-major form
+# with numpy; the oracle run with key-major states must match it, and must
+# equal the transpose of its value-major run exactly.
+# --------------------------------------------------------------------------
+def test_key_major_state_follows_the_clika_form():
+    rng = np.random.default_rng(33)
+    T, hq, hv, dk, dv, rows = 8, 1, 2, 5, 3, 4
+    q = rng.standard_normal((T, hq, dk))
+    k = _unit(rng.standard_normal((T, hq, dk)))
+    v = rng.standard_normal((T, hv, dv))
+    g = -rng.random((T, hv))
+    beta = rng.random((T, hv))
+    SK = rng.standard_normal((rows, hv, dk, dv)) * 0.3      # key-major slab
+    cu = [0, 5, 8]
+    slots = np.array([3, 1], dtype=np.int32)
+    o, fin, err = oracle.gdn(q, k, v, rule="gated_delta", decay=g, beta=beta, initial_state=SK,
+                             cu_seqlens=cu, slot_ids=slots, scale=0.6, state_kmajor=True)
+    assert err == 0 and fin.shape == SK.shape
+    want = SK.copy()
+    for b in range(2):
+        for h in range(hv):
+            S = SK[slots[b], h].copy()                      # dk x dv
+            for t in range(cu[b], cu[b + 1]):
+                kt, qt = k[t, 0], q[t, 0]
+                S = math.exp(g[t, h]) * S
+                S = S + np.outer(beta[t, h] * kt, v[t, h] - S.T @ kt)
+                np.testing.assert_allclose(o[t, h], (0.6 * qt) @ S, rtol=1e-12, atol=1e-12)
+            want[slots[b], h] = S
+    np.testing.assert_allclose(fin, want, rtol=1e-12, atol=1e-12)
+    # the same run with value-major states gives the transposed states bit for bit
+    o_v, fin_v, _ = oracle.gdn(q, k, v, rule="gated_delta", decay=g, beta=beta,
+                               initial_state=np.ascontiguousarray(SK.transpose(0, 1, 3, 2)),
+                               cu_seqlens=cu, slot_ids=slots, scale=0.6)
+    assert np.array_equal(o_v, o)
+    assert np.array_equal(fin_v.transpose(0, 1, 3, 2), fin)
+
+
+# --------------------------------------------------------------------------
+# GDN-2 proposal (B): the erase gate is an input of its own beside the scalar
+# beta.  (1) b = beta * 1 gives gated_delta back ("old beta_t = b_t * 1 is the
+# strict-generalization fallback").  (2) Against the issue's first display
+# with the write term carrying beta and the write gate,
+#   S_K = (I - k (b .* k)^T) D S_K + beta k (w .* v)^T,  written densely here.
+# --------------------------------------------------------------------------
+def test_gdn2_erase_gate_input_with_b_equal_beta_is_gated_delta():
+    rng = np.random.default_rng(34)
+    T, hv, dk, dv = 9, 2, 6, 4
+    q = rng.standard_normal((T, 1, dk))
+    k = _unit(rng.standard_normal((T, 1, dk)))
+    v = rng.standard_normal((T, hv, dv))
+    g = -rng.random((T, hv))
+    x = rng.standard_normal((T, hv))
+    beta = 1.0 / (1.0 + np.exp(-x))
+    S0 = rng.standard_normal((1, hv, dv, dk)) * 0.3
+    o1, f1, _ = oracle.gdn(q, k, v, rule="gated_delta", decay=g, beta=x, beta_sigmoid=True, initial_state=S0)
+    b = np.repeat(beta[:, :, None], dk, axis=2)
+    o2, f2, _ = oracle.gdn(q, k, v, rule="gdn2", decay=g, beta=x, beta_sigmoid=True, erase_gate=b,
+                           initial_state=S0)
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(f2, f1, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_gdn2_erase_gate_input_dense_form(shared):
+    rng = np.random.default_rng(35)
+    T, hv, dk, dv = 7, 2, 4, 3
+    q = rng.standard_normal((T, 1, dk))
+    k = rng.standard_normal((T, 1, dk))
+    v = rng.standard_normal((T, hv, dv))
+    b = rng.random((T, hv, dk))
+    w = rng.random((T, hv, dv))
+    beta = rng.random((T,) if shared else (T, hv))
+    g = -rng.random((T, hv, dk))
+    S0 = rng.standard_normal((1, hv, dv, dk))
+    o, fin, _ = oracle.gdn(q, k, v, rule="gdn2", decay=g, beta=beta, erase_gate=b, write_gate=w,
+                           initial_state=S0, decay_per_key=True, scale=1.0, beta_shared=shared)
+    for h in range(hv):
+        SK = S0[0, h].T.copy()
+        for t in range(T):
+            bt = beta[t] if shared else beta[t, h]
+            kt = k[t, 0][:, None]
+            bk = (b[t, h] * k[t, 0])[:, None]
+            SK = (np.eye(dk) - kt @ bk.T) @ np.diag(np.exp(g[t, h])) @ SK + bt * kt @ (w[t, h] * v[t, h])[None, :]
+            np.testing.assert_allclose(o[t, h], SK.T @ q[t, 0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(fin[0, h], SK.T, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn2_write_gate_input_equals_folded():
+    """Proposal (A) keeps the write gate outside the op (v <- w .* v by the
+    caller); passed to the op it must give the same result, and proposal (B)
+    with beta = 1 must equal proposal (A)."""
+    rng = np.random.default_rng(36)
+    T, hv, dk, dv = 8, 2, 5, 4
+    q = rng.standard_normal((T, 1, dk))
+    k = _unit(rng.standard_normal((T, 1, dk)))
+    v = rng.standard_normal((T, hv, dv))
+    w = rng.random((T, hv, dv))
+    b = rng.random((T, hv, dk))
+    g = -rng.random((T, hv, dk))
+    S0 = rng.standard_normal((1, hv, dv, dk)) * 0.3
+    o1, f1, _ = oracle.gdn(q, k, v * w, rule="gdn2", decay=g, beta=b, initial_state=S0, decay_per_key=True)
+    o2, f2, _ = oracle.gdn(q, k, v, rule="gdn2", decay=g, beta=b, write_gate=w, initial_state=S0,
+                           decay_per_key=True)
+    np.testing.assert_allclose(o2, o1, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(f2, f1, rtol=1e-14, atol=1e-15)
+    o3, f3, _ = oracle.gdn(q, k, v, rule="gdn2", decay=g, beta=np.ones((T, hv)), erase_gate=b, write_gate=w,
+                           initial_state=S0, decay_per_key=True)
+    np.testing.assert_allclose(o3, o1, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(f3, f1, rtol=1e-14, atol=1e-15)

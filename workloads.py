@@ -14,6 +14,11 @@ A problem is a plain dict:
     gate_bias       [Hv] or [Hv, dk] fp32, or None (log-space decay given)
     gate_scale      [Hv] fp32, the once-folded -exp(A_log), or None
     beta            [T, Hv] (or [T, Hv, dk] erase gate for gdn2), or None
+    erase_gate      gdn2 with the erase gate as its own input: [T, Hv, dk] fp32
+                    (beta is then the scalar [T, Hv] write rate), or None
+    write_gate      gdn2 write gate passed to the op: [T, Hv, dv] fp32, or None
+                    (folded into v by the caller, or absent)
+    state_kmajor    states are [rows, Hv, dk, dv] instead of [rows, Hv, dv, dk]
     cu_seqlens      [B+1] int32 or None
     slot_ids        [B] int32 or None
     initial_state   [rows, Hv, dv, dk] fp32 or None (zeros)
@@ -53,11 +58,16 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
          beta_dtype=None, logdecay_range=(-1.0, 0.0), beta_mode="sigmoid",
          state="zero", state_std=0.02, num_slots=None, slot_mode=None,
          write_gate=False, l2norm_q=False, l2norm_k=True, scale=0.0, qk_std=1.0, seq_lens=None,
-         beta_shared=False):
+         beta_shared=False, erase="beta", state_kmajor=False):
     """Draws one problem.  ``gate`` is 'raw' (raw projection + gate_bias +
     gate_scale), 'log' (log-space decay drawn U(logdecay_range)) or ignored
     for rules without decay.  ``beta_mode`` is 'sigmoid' (raw N(0,1) logits +
-    BETA_SIGMOID flag) or 'direct' (beta drawn U(0,1), used as given)."""
+    BETA_SIGMOID flag) or 'direct' (beta drawn U(0,1), used as given).
+    GDN-2 only: ``erase`` is 'beta' (the erase gate is the per-key beta) or
+    'input' (a scalar beta as for gated_delta, and the erase gate
+    sigmoid(N(0,1)) as its own input); ``write_gate`` is False, True / 'fold'
+    (w = sigmoid(N(0,1)) multiplied into v here) or 'input' (w kept apart).
+    ``state_kmajor`` draws the state key-major, [rows, Hv, dk, dv]."""
     gen = _gen(seed)
     dt = ACT[act]
     if seq_len:
@@ -77,11 +87,16 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
     p["q"] = (torch.randn(T, hq, dk, generator=gen) * qk_std).to(dt)
     p["k"] = (torch.randn(T, hq, dk, generator=gen) * qk_std).to(dt)
     v = torch.randn(T, hv, dv, generator=gen)
+    p["write_gate"] = p["erase_gate"] = None
+    p["state_kmajor"] = bool(state_kmajor)
     if write_gate:
-        # GDN-2 write gate w ~ sigmoid(N(0,1)) on the value axis, folded into v
-        # by the caller (a graph-level Mul, outside the op).
+        # GDN-2 write gate w ~ sigmoid(N(0,1)) on the value axis: folded into v
+        # by the caller (a graph-level Mul, outside the op), or passed to the op
         w = torch.sigmoid(torch.randn(T, hv, dv, generator=gen))
-        v = v * w
+        if write_gate == "input":
+            p["write_gate"] = w.float()
+        else:
+            v = v * w
     p["v"] = v.to(dt)
     has_decay = rule in ("gated", "gated_delta", "gdn2")
     has_beta = rule in ("delta", "gated_delta", "gdn2")
@@ -104,14 +119,17 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
         else:
             raise ValueError(gate)
     if has_beta:
-        bshape = (T, hv, dk) if rule == "gdn2" else ((T,) if beta_shared else (T, hv))
-        p["beta_shared"] = bool(beta_shared) and rule != "gdn2"
+        per_key_beta = rule == "gdn2" and erase == "beta"
+        bshape = (T, hv, dk) if per_key_beta else ((T,) if beta_shared else (T, hv))
+        p["beta_shared"] = bool(beta_shared) and not per_key_beta
         bd = ACT[beta_dtype] if beta_dtype else torch.float32
         if beta_mode == "sigmoid":
             p["beta"] = torch.randn(*bshape, generator=gen).to(bd)
             p["beta_sigmoid"] = True
         else:
             p["beta"] = torch.rand(*bshape, generator=gen).to(bd)
+        if rule == "gdn2" and erase == "input":
+            p["erase_gate"] = torch.sigmoid(torch.randn(T, hv, dk, generator=gen)).float()
     p["cu_seqlens"] = cu_seqlens
     # padded-ragged rank-4 batch: request b uses the first seq_lens[b] tokens of its row
     p["seq_lens"] = torch.as_tensor(seq_lens, dtype=torch.int32) if seq_lens is not None else None
@@ -122,7 +140,8 @@ def make(*, seed, B, T=None, seq_len=0, lengths=None, cu_seqlens=None, hq, hv, d
     else:
         p["slot_ids"] = None
     if state == "random":
-        p["initial_state"] = torch.randn(rows, hv, dv, dk, generator=gen) * state_std
+        sshape = (rows, hv, dk, dv) if state_kmajor else (rows, hv, dv, dk)
+        p["initial_state"] = torch.randn(*sshape, generator=gen) * state_std
     else:
         p["initial_state"] = None
     return p
