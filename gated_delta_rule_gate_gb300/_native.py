@@ -15,7 +15,8 @@ DTYPE_F32, DTYPE_F16, DTYPE_BF16 = 0, 1, 2
 RULES = {"linear": 0, "gated": 1, "delta": 2, "gated_delta": 3, "gdn2": 4}
 FLAG_L2NORM_Q, FLAG_L2NORM_K, FLAG_BETA_SIGMOID, FLAG_DECAY_PER_KEY = 0x1, 0x2, 0x4, 0x8
 FLAG_BETA_SHARED = 0x10
-DEVERR_BAD_SLOT = 0x1
+FLAG_STATE_KMAJOR = 0x20
+DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_OVERLAP, DEVERR_DECAY_RANGE = 0x1, 0x2, 0x4, 0x8
 
 EXPORTS = ("gdn_gate", "gdn_recurrent_step", "gdn_chunked_prefill_workspace_size",
            "gdn_chunked_prefill", "gdn_chunked_prefill_noalloc", "gdn_status_string",
@@ -38,6 +39,7 @@ class GdnProblem(ctypes.Structure):
         ("gate_bias", _vp), ("gate_scale", _vp), ("beta", _vp),
         ("cu_seqlens", _vp), ("slot_ids", _vp), ("initial_state", _vp),
         ("final_state", _vp), ("error_word", _vp), ("seq_lens", _vp),
+        ("erase_gate", _vp), ("write_gate", _vp),
     ]
 
 

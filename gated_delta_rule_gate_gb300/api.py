@@ -42,15 +42,19 @@ def make_problem(q, k, v, o, final_state, *, rule="gated_delta", decay=None, bet
                  gate_bias=None, gate_scale=None, cu_seqlens=None, slot_ids=None,
                  initial_state=None, batch=None, scale=0.0, l2norm_q=False, l2norm_k=False,
                  beta_sigmoid=False, decay_per_key=False, error_word=None,
-                 state_update_capacity=0, seq_lens=None, beta_shared=False):
+                 state_update_capacity=0, seq_lens=None, beta_shared=False, erase_gate=None,
+                 write_gate=None, state_kmajor=False):
     """Builds the ``gdn_problem`` struct.  q/k are [T, Hq, dk] (rank-3, packed)
     or [B, S, Hq, dk] (rank-4); v/o follow with Hv, dv; states are
     [rows, Hv, dv, dk] fp32.  ``seq_lens`` ([B] int32, rank-4 only) bounds each
     row to its first seq_lens[b] tokens.  ``beta_shared``: beta is [T] (one
-    per token for every value head).  Keeps references to the tensors alive on
-    the returned struct."""
+    per token for every value head).  GDN2: ``erase_gate`` ([T, Hv, dk] fp32)
+    is the erase gate as its own input, beta then being the scalar write
+    rate; ``write_gate`` ([T, Hv, dv] fp32) is multiplied into v by the
+    kernels.  ``state_kmajor``: states are [rows, Hv, dk, dv].  Keeps
+    references to the tensors alive on the returned struct."""
     _need_cuda(q, k, v, o, final_state, decay, beta, gate_bias, gate_scale, cu_seqlens,
-               slot_ids, initial_state, error_word, seq_lens)
+               slot_ids, initial_state, error_word, seq_lens, erase_gate, write_gate)
     if q.dim() == 4:
         B, S, hq, dk = q.shape
         T, seq_len = B * S, S
@@ -77,25 +81,28 @@ def make_problem(q, k, v, o, final_state, *, rule="gated_delta", decay=None, bet
     p.rule = N.RULES[rule] if isinstance(rule, str) else int(rule)
     p.flags = ((N.FLAG_L2NORM_Q if l2norm_q else 0) | (N.FLAG_L2NORM_K if l2norm_k else 0) |
                (N.FLAG_BETA_SIGMOID if beta_sigmoid else 0) |
-               (N.FLAG_DECAY_PER_KEY if decay_per_key else 0) | (N.FLAG_BETA_SHARED if beta_shared else 0))
+               (N.FLAG_DECAY_PER_KEY if decay_per_key else 0) | (N.FLAG_BETA_SHARED if beta_shared else 0) |
+               (N.FLAG_STATE_KMAJOR if state_kmajor else 0))
     p.scale = float(scale)
     p.state_update_capacity = int(state_update_capacity)
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("decay", decay),
                     ("gate_bias", gate_bias), ("gate_scale", gate_scale), ("beta", beta),
                     ("cu_seqlens", cu_seqlens), ("slot_ids", slot_ids),
                     ("initial_state", initial_state), ("final_state", final_state),
-                    ("error_word", error_word), ("seq_lens", seq_lens)):
+                    ("error_word", error_word), ("seq_lens", seq_lens), ("erase_gate", erase_gate),
+                    ("write_gate", write_gate)):
         setattr(p, name, None if t is None else t.data_ptr())
     for t, name, dt in ((cu_seqlens, "cu_seqlens", torch.int32), (slot_ids, "slot_ids", torch.int32),
                         (seq_lens, "seq_lens", torch.int32),
                         (error_word, "error_word", torch.int32), (gate_bias, "gate_bias", torch.float32),
                         (gate_scale, "gate_scale", torch.float32),
                         (initial_state, "initial_state", torch.float32),
-                        (final_state, "final_state", torch.float32)):
+                        (final_state, "final_state", torch.float32), (erase_gate, "erase_gate", torch.float32),
+                        (write_gate, "write_gate", torch.float32)):
         if t is not None and t.dtype != dt:
             raise TypeError("%s must be %s" % (name, dt))
     p._keep = (q, k, v, o, final_state, decay, beta, gate_bias, gate_scale, cu_seqlens, slot_ids,
-               initial_state, error_word, seq_lens)
+               initial_state, error_word, seq_lens, erase_gate, write_gate)
     return p
 
 

@@ -65,7 +65,8 @@ struct Lay {
     static constexpr int oEGC = oEG + C * 4;
     static constexpr int oX16 = oEGC + C * 4;
     static constexpr int oKap = oX16 + NW * 16 * 17 * 4;
-    static constexpr int total = oKap + (GDN2 ? bK : 0);
+    static constexpr int oVB = oKap + (GDN2 ? bK : 0);  // GDN-2: beta of the write, per token
+    static constexpr int total = oVB + (GDN2 ? C * 4 : 0);
 };
 
 __device__ __forceinline__ float2 ld_f2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(NTH, 2) chunked_mma_kernel(Problem p, int slic
     float *sEGC = reinterpret_cast<float *>(sm + Ly::oEGC);
     float *sX16 = reinterpret_cast<float *>(sm + Ly::oX16);
     __half *sKap = reinterpret_cast<__half *>(sm + Ly::oKap);
+    float *sVB = reinterpret_cast<float *>(sm + Ly::oVB);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
@@ -115,24 +117,38 @@ __global__ void __launch_bounds__(NTH, 2) chunked_mma_kernel(Problem p, int slic
 
     // ---- the state: rows rlo = wrow0 + g and rhi = rlo + 8, columns 8 nt + 2 t4 + {0,1}
     float S[NT8][4];
-    const size_t sbase = ((size_t)row * p.Hv + h) * p.dv;
+    // element (r, c) of the state tile: value-major at r * DK + c, key-major at c * dv + r
+    const bool km = (p.flags & kKMajor) != 0;
+    const size_t tile = ((size_t)row * p.Hv + h) * p.dv * DK;
     const int rlo = wrow0 + g, rhi = rlo + 8;
     const bool lo_ok = rlo < p.dv, hi_ok = rhi < p.dv;
+    auto ld_pair = [&](int r, int col) {
+        return km ? make_float2(p.init[tile + (size_t)col * p.dv + r], p.init[tile + (size_t)(col + 1) * p.dv + r])
+                  : ld_f2(p.init + tile + (size_t)r * DK + col);
+    };
+    auto st_pair = [&](int r, int col, float x, float y) {
+        if (km) {
+            p.fin[tile + (size_t)col * p.dv + r] = x;
+            p.fin[tile + (size_t)(col + 1) * p.dv + r] = y;
+        } else {
+            *reinterpret_cast<float2 *>(p.fin + tile + (size_t)r * DK + col) = make_float2(x, y);
+        }
+    };
 #pragma unroll
     for (int nt = 0; nt < NT8; ++nt) {
         const int col = 8 * nt + 2 * t4;
         float2 a = make_float2(0.f, 0.f), c = make_float2(0.f, 0.f);
-        if (p.init && lo_ok) a = ld_f2(p.init + (sbase + rlo) * DK + col);
-        if (p.init && hi_ok) c = ld_f2(p.init + (sbase + rhi) * DK + col);
+        if (p.init && lo_ok) a = ld_pair(rlo, col);
+        if (p.init && hi_ok) c = ld_pair(rhi, col);
         S[nt][0] = a.x, S[nt][1] = a.y, S[nt][2] = c.x, S[nt][3] = c.y;
     }
-    if (t1 == t0) {  // empty request: copy the incoming state through
+    if (t1 == t0) {  // empty request: the final state is the initial one
         if (p.fin != p.init) {
 #pragma unroll
             for (int nt = 0; nt < NT8; ++nt) {
                 const int col = 8 * nt + 2 * t4;
-                if (lo_ok) *reinterpret_cast<float2 *>(p.fin + (sbase + rlo) * DK + col) = make_float2(S[nt][0], S[nt][1]);
-                if (hi_ok) *reinterpret_cast<float2 *>(p.fin + (sbase + rhi) * DK + col) = make_float2(S[nt][2], S[nt][3]);
+                if (lo_ok) st_pair(rlo, col, S[nt][0], S[nt][1]);
+                if (hi_ok) st_pair(rhi, col, S[nt][2], S[nt][3]);
             }
         }
         return;
@@ -189,13 +205,15 @@ __global__ void __launch_bounds__(NTH, 2) chunked_mma_kernel(Problem p, int slic
                     if (p.raw_gate) gr = p.gate_scale[h] * softplus_f(gr + p.gate_bias[h]);
                 }
                 br = 1.f;
-                if (beta_scalar) {
+                if (beta_scalar || (GDN2 && p.erase_gate)) {
                     br = ld_any(p.beta, beta_at(p, c0 + r, h), p.beta_f16);
                     if (sig) br = sigmoid_f(br);
                 }
             }
             sG[r] = gr;
-            sBt[r] = br;
+            // GDN-2: beta (its own erase gate given) scales the value rows, not the system
+            sBt[r] = GDN2 ? 1.f : br;
+            if (GDN2) sVB[r] = br;
         }
         ptx::cp_async_wait_all();
         __syncthreads();
@@ -228,12 +246,28 @@ __global__ void __launch_bounds__(NTH, 2) chunked_mma_kernel(Problem p, int slic
                             if (GDN2) {
                                 float bb = 0.f;
                                 if (r < n) {
-                                    bb = ld_any(p.beta, ((size_t)(c0 + r) * p.Hv + h) * DK + c, p.beta_f16);
-                                    if (sig) bb = sigmoid_f(bb);
+                                    const size_t e = ((size_t)(c0 + r) * p.Hv + h) * DK + c;
+                                    if (p.erase_gate) {
+                                        bb = p.erase_gate[e];
+                                    } else {
+                                        bb = ld_any(p.beta, e, p.beta_f16);
+                                        if (sig) bb = sigmoid_f(bb);
+                                    }
                                 }
                                 sKap[r * KS + c] = __float2half_rn(bb * kn);
                             }
                         }
+                    }
+                }
+            }
+            if (GDN2 && scales_v(p)) {
+                // v' = beta w .* v (beta of the write when the erase gate is its own input)
+                for (int idx = tid; idx < n * VS; idx += NTH) {
+                    const int r = idx / VS, c = idx % VS, col = vs0 + c;
+                    if (col < p.dv) {
+                        float f = sVB[r];
+                        if (p.write_gate) f *= p.write_gate[((size_t)(c0 + r) * p.Hv + h) * p.dv + col];
+                        sV[r * VSS + c] = __float2half_rn(__half2float(sV[r * VSS + c]) * f);
                     }
                 }
             }
@@ -559,8 +593,8 @@ __global__ void __launch_bounds__(NTH, 2) chunked_mma_kernel(Problem p, int slic
 #pragma unroll
     for (int nt = 0; nt < NT8; ++nt) {
         const int col = 8 * nt + 2 * t4;
-        if (lo_ok) *reinterpret_cast<float2 *>(p.fin + (sbase + rlo) * DK + col) = make_float2(S[nt][0], S[nt][1]);
-        if (hi_ok) *reinterpret_cast<float2 *>(p.fin + (sbase + rhi) * DK + col) = make_float2(S[nt][2], S[nt][3]);
+        if (lo_ok) st_pair(rlo, col, S[nt][0], S[nt][1]);
+        if (hi_ok) st_pair(rhi, col, S[nt][2], S[nt][3]);
     }
 }
 
@@ -569,15 +603,8 @@ cudaError_t launch_mma(const Problem &p, cudaStream_t stream) {
     using Ly = Lay<DK, GDN2>;
     const int slices = (p.dv + VS - 1) / VS;
     const long long grid = (long long)p.B * p.Hv * slices;
-    static int attr_done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const cudaError_t e = smem_attr((const void *)chunked_mma_kernel<DK, GDN2>, Ly::total);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(chunked_mma_kernel<DK, GDN2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::total);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_done[dev] = 1;
-    }
     chunked_mma_kernel<DK, GDN2><<<(unsigned)grid, NTH, Ly::total, stream>>>(p, slices);
     return cudaGetLastError();
 }

@@ -653,12 +653,20 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             return;
         }
     }
-    const size_t sbase = ((size_t)row * p.Hv + h) * 128 * 128 + (size_t)64 * vh * 128;  // this CTA's rows
-    if (nch == 0) {  // empty request: copy the incoming state through
+    // the state tile; value row i_g, key column c at i_g * 128 + c (value-major) or
+    // c * 128 + i_g (key-major, GDN_FLAG_STATE_KMAJOR)
+    const bool km = (p.flags & kKMajor) != 0;
+    const size_t tile = ((size_t)row * p.Hv + h) * 128 * 128;
+    const size_t sbase = tile + (size_t)64 * vh * 128;  // this CTA's rows (value-major)
+    if (nch == 0) {  // empty request: the final state is the initial one
         if (p.fin != p.init) {
-            for (int idx = tid; idx < ROWS * 32; idx += CH_THREADS)
-                reinterpret_cast<float4 *>(p.fin + sbase)[idx] =
-                    p.init ? reinterpret_cast<const float4 *>(p.init + sbase)[idx] : make_float4(0, 0, 0, 0);
+            for (int idx = tid; idx < ROWS * 32; idx += CH_THREADS) {
+                // key-major: key row c, four of this CTA's value columns
+                const size_t off = km ? tile + (size_t)(idx / (ROWS / 4)) * 128 + 64 * vh + 4 * (idx % (ROWS / 4))
+                                      : sbase + 4 * (size_t)idx;
+                *reinterpret_cast<float4 *>(p.fin + off) =
+                    p.init ? *reinterpret_cast<const float4 *>(p.init + off) : make_float4(0, 0, 0, 0);
+            }
         }
         return;
     }
@@ -679,6 +687,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         const bool live = !HALF || lane < 16;  // lanes that hold a row of this CTA's state
         const uint32_t lo = tmem + ((uint32_t)(32 * q4) << 16) + tS + 64 * hc;
         const size_t srow = sbase + (size_t)i * 128 + 64 * hc;
+        // key-major: element (value row 64 vh + i, key column 64 hc + c) at kcol + c * 128
+        const size_t kcol = tile + (size_t)(64 * hc) * 128 + 64 * vh + i;
         // e^{G_C} of chunk c, as the prepare kernel left it in the chunk's image
         auto gamma = [&](int c) {
             return *reinterpret_cast<const float *>(img + ((size_t)(slot0 + c) * p.Hv + h) * IM_BYTES + IM_E);
@@ -690,9 +700,15 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             for (int pc = 0; pc < 2; ++pc) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float4 f = (p.init && live)
-                                         ? *reinterpret_cast<const float4 *>(p.init + srow + 32 * pc + 4 * j)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (p.init && live) {
+                        if (km) {
+                            const float *b = p.init + kcol + (size_t)(32 * pc + 4 * j) * 128;
+                            f = make_float4(b[0], b[128], b[256], b[384]);
+                        } else {
+                            f = *reinterpret_cast<const float4 *>(p.init + srow + 32 * pc + 4 * j);
+                        }
+                    }
                     v[4 * j] = f.x, v[4 * j + 1] = f.y, v[4 * j + 2] = f.z, v[4 * j + 3] = f.w;
                 }
                 if (live) {
@@ -747,6 +763,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 tc::fence_async_smem();
                 ptx::named_bar_sync(1, 256);
                 if (tid == 0) ptx::mbar_arrive(shready);
+            } else if (live && km) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    p.fin[kcol + (size_t)j * 128] = v0[j];
+                    p.fin[kcol + (size_t)(32 + j) * 128] = v1[j];
+                }
             } else if (live) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -960,26 +982,18 @@ bool make_kqv_map(CUtensorMap *m, const void *base, int heads, int tokens) {
 }
 
 cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream) {
-    static int attr_done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(chunk_prepare_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
+    const void *fns[8] = {(const void *)chunk_prepare_kernel<true>,
+                          (const void *)chunk_prepare_kernel<false>,
+                          (const void *)chunk_chain_kernel<kStepPlain, 128>,
+                          (const void *)chunk_chain_kernel<kStepDecay, 128>,
+                          (const void *)chunk_chain_kernel<kStepE, 128>,
+                          (const void *)chunk_chain_kernel<kStepPlain, 64>,
+                          (const void *)chunk_chain_kernel<kStepDecay, 64>,
+                          (const void *)chunk_chain_kernel<kStepE, 64>};
+    cudaError_t e;
+    for (int f = 0; f < 8; ++f) {
+        e = smem_attr(fns[f], f < 2 ? PR_SMEM : CH_SMEM);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_prepare_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PR_SMEM);
-        if (e != cudaSuccess) return e;
-        const void *chains[6] = {(const void *)chunk_chain_kernel<kStepPlain, 128>,
-                                 (const void *)chunk_chain_kernel<kStepDecay, 128>,
-                                 (const void *)chunk_chain_kernel<kStepE, 128>,
-                                 (const void *)chunk_chain_kernel<kStepPlain, 64>,
-                                 (const void *)chunk_chain_kernel<kStepDecay, 64>,
-                                 (const void *)chunk_chain_kernel<kStepE, 64>};
-        for (const void *fn : chains) {
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM);
-            if (e != cudaSuccess) return e;
-        }
-        if (dev < 64) attr_done[dev] = 1;
     }
     CUtensorMap tk, tq, tv;
     if (!make_kqv_map(&tk, p.k, p.Hq, p.T) || !make_kqv_map(&tq, p.q, p.Hq, p.T) ||

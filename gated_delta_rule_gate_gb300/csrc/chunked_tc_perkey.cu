@@ -2,7 +2,10 @@
 // decay per key channel ("aclnnRecurrentGatedDeltaRule" Formula, second form;
 // "gatedDeltaUpdate" per-key gate) and for the GDN-2 key-channel erase gate
 // (ONNX issue "Spec gap: LinearAttention ... Gated DeltaNet-2", section "The
-// GDN-2 recurrence", option A of "Proposed extension").
+// GDN-2 recurrence", options A and B of "Proposed extension").  Under option
+// B (the erase gate as its own input beside a scalar beta) and with a write
+// gate w, GDN-2 is option A on the value rows beta_r w_r .* v_r, which this
+// kernel scales in shared memory before the U product.
 //
 // With per-channel log decay g_t[c], in-chunk cumulants Gamma_t[c] (one per
 // key channel), retrieval key kappa_t (= k_t for gated_delta, = b_t .* k_t
@@ -59,8 +62,8 @@ constexpr int pQh = pKt + 16384;       // 16 KB: Qh, then Q' (image layout)
 constexpr int pP = pQh + 16384;        //  8 KB: P (image layout)
 constexpr int pKap = pP + 8192;        // 16 KB: b .* k (raw keys), GDN-2; [2 c-blocks][64 t][64 c]
 constexpr int pSc = pKap + 16384;      // per-token and per-channel factors
-constexpr int pGin = pSc + 320 * 4;    // 2 x (scalar log decay, beta) of 64 tokens, from the producer
-constexpr int pHdr = pGin + 2 * 128 * 4;  // 2 x {slot, head, first token, tokens, gate scale}
+constexpr int pGin = pSc + 320 * 4;    // 2 x (scalar log decay, beta, value-row factor) of 64 tokens
+constexpr int pHdr = pGin + 2 * 192 * 4;  // 2 x {slot, head, first token, tokens, gate scale}
 constexpr int pBar = pHdr + 2 * 8 * 4;    // seven mbarriers, TMEM address
 constexpr int pGb = pBar + 96;            // the head's per-key gate bias (raw arm), 128 floats
 constexpr int PK_SMEM = pGb + 512 + 1024;
@@ -165,12 +168,14 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
     tc::fence_after();
     const uint32_t tmem = *tslot;
     const long long NG = gridDim.x;
+    // the GDN-2 erase gate rows (fp32): its own input, or the per-key beta
+    const float *erase_rows = p.erase_gate ? p.erase_gate : static_cast<const float *>(p.beta);
 
     if (warp == 8) {
         // ===================== producer
         struct Next {
             int slot, h, c0, n;
-            float gs, g[2], bt[2];
+            float gs, g[2], bt[2], bv[2];
         };
         auto fetch = [&](long long t) {
             Next x;
@@ -186,20 +191,22 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             for (int e = 0; e < 2; ++e) {
                 const int tt = lane + 32 * e;
                 const size_t th = (size_t)(x.c0 + tt) * p.Hv + x.h;
-                float g = 0.f, bt = 0.f;
+                float g = 0.f, bt = 0.f, bv = 1.f;
                 if (tt < x.n) {
                     if (!perkey) {
                         g = ld_any(p.decay, th, p.decay_f16);
                         if (p.raw_gate) g = x.gs * softplus_f(g + gb);
                     }
-                    if (GDN2) {
+                    if (GDN2 && !p.erase_gate) {
                         bt = 1.f;
                     } else {
                         bt = ld_any(p.beta, beta_at(p, x.c0 + tt, x.h), p.beta_f16);
                         if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
                     }
+                    // GDN-2 with its own erase gate: beta scales the value row, not the system
+                    if (GDN2) bv = bt, bt = 1.f;
                 }
-                x.g[e] = g, x.bt[e] = bt;
+                x.g[e] = g, x.bt[e] = bt, x.bv[e] = bv;
             }
             return x;
         };
@@ -211,12 +218,14 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 if (rr < x.n) {
                     const size_t th = (size_t)(x.c0 + rr) * p.Hv + x.h;
                     if (perkey) ptx::prefetch_l2(static_cast<const float *>(p.decay) + th * 128, 512);
-                    if (GDN2) ptx::prefetch_l2(static_cast<const float *>(p.beta) + th * 128, 512);
+                    if (GDN2) ptx::prefetch_l2(erase_rows + th * 128, 512);
+                    if (GDN2 && p.write_gate) ptx::prefetch_l2(p.write_gate + th * 128, 512);
                 }
             }
         };
         Next nx;
         if (blockIdx.x < ntasks) nx = fetch(blockIdx.x);
+        if (blockIdx.x < ntasks) prefetch_rows(nx);
         int i = 0;
         for (long long t = blockIdx.x; t < ntasks; t += NG, ++i) {
             // the log-decay rows land once the previous task has finished its diagonal blocks
@@ -224,12 +233,13 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 if (p.err && lane == 0) atomicOr(p.err, 2);
                 break;
             }
-            float *gin = reinterpret_cast<float *>(sm + pGin) + (i & 1) * 128;
+            float *gin = reinterpret_cast<float *>(sm + pGin) + (i & 1) * 192;
             int *hdr = reinterpret_cast<int *>(sm + pHdr) + (i & 1) * 8;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 gin[lane + 32 * e] = nx.g[e];
                 gin[64 + lane + 32 * e] = nx.bt[e];
+                gin[128 + lane + 32 * e] = nx.bv[e];
             }
             if (lane == 0) {
                 hdr[0] = nx.slot, hdr[1] = nx.h, hdr[2] = nx.c0, hdr[3] = nx.n;
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                     const int rr = lane + 32 * e;
                     if (rr < nx.n) {
                         const size_t th = (size_t)(nx.c0 + rr) * p.Hv + nx.h;
-                        ptx::bulk_g2s(sm + pXp + rr * 512, static_cast<const float *>(p.beta) + th * 128, 512, land);
+                        ptx::bulk_g2s(sm + pXp + rr * 512, erase_rows + th * 128, 512, land);
                     }
                 }
             }
@@ -315,7 +325,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             ok = ptx::named_bar_and(3, PK_WORK,
                                     ptx::mbar_wait_sleep(landG, i & 1) && ptx::mbar_wait_sleep(land, i & 1));
             if (!ok) break;
-            const float *gin = reinterpret_cast<const float *>(sm + pGin) + (i & 1) * 128;
+            const float *gin = reinterpret_cast<const float *>(sm + pGin) + (i & 1) * 192;
             const int *hdr = reinterpret_cast<const int *>(sm + pHdr) + (i & 1) * 8;
             const int slot = hdr[0], h = hdr[1], n = hdr[3];
             const float gs = __int_as_float(hdr[4]);
@@ -337,6 +347,32 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 }
                 ptx::named_bar_sync(3, PK_WORK);
             }
+            if (GDN2 && scales_v(p)) {
+                // v' = beta_r w_r .* v_r in the value tile (fp16, image layout); thread = four
+                // 16-byte chunks (8 value channels each) of the rows below n
+                const int c0 = hdr[2];
+                for (int idx = tid; idx < n * 16; idx += PK_WORK) {
+                    const int r = idx >> 4, ch = idx & 15;
+                    const float f = gin[128 + r];
+                    float x[8];
+                    uint4 *cell = reinterpret_cast<uint4 *>(sm + pV + t64(r, ch));
+                    unpack8(*cell, x);
+                    if (p.write_gate) {
+                        float w[8];
+                        ld8f(p.write_gate + ((size_t)(c0 + r) * p.Hv + h) * 128 + 8 * ch, w);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] *= f * w[e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] *= f;
+                    }
+                    uint4 u;
+                    u.x = ptx::pack_h2(x[0], x[1]), u.y = ptx::pack_h2(x[2], x[3]);
+                    u.z = ptx::pack_h2(x[4], x[5]), u.w = ptx::pack_h2(x[6], x[7]);
+                    *cell = u;
+                }
+                // (the U product reads the tile after several barriers of the workers)
+            }
             // gates: thread = (channel c, half of the tokens); the inclusive cumulative sum
             // Gamma of the log decays per channel, in place
             const int gc = tid & 127, ghf = tid >> 7;
@@ -353,6 +389,13 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
 #pragma unroll
                     for (int tt = 0; tt < 32; ++tt)
                         if (32 * ghf + tt >= n) gv[tt] = 0.f;
+                    if (!p.raw_gate && p.err) {
+                        // this path needs log decays <= 0 (its operand factors are then at most 1)
+                        bool bad = false;
+#pragma unroll
+                        for (int tt = 0; tt < 32; ++tt) bad |= gv[tt] > 0.f;
+                        if (bad) atomicOr(p.err, kErrDecayRange);
+                    }
                 } else {
 #pragma unroll
                     for (int tt = 0; tt < 32; ++tt) gv[tt] = gin[32 * ghf + tt];
@@ -395,7 +438,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
 #pragma unroll
                     for (int k8 = 0; k8 < 16; ++k8)
                         bb[k8] = *reinterpret_cast<const float4 *>(sm + pXp + (16 * warp + k8) * 512 + lane * 16);
-                    const bool sg = (p.flags & kBetaSigmoid) != 0;
+                    const bool sg = (p.flags & kBetaSigmoid) != 0 && !p.erase_gate;
 #pragma unroll
                     for (int k8 = 0; k8 < 16; ++k8) {
                         float4 c = bb[k8];
@@ -804,26 +847,20 @@ bool chunk_prepare_perkey_eligible(const Problem &p) {
     const bool perkey = (p.flags & kPerKey) != 0;
     const bool rule_ok = p.rule == kGdn2 || (p.rule == kGatedDelta && perkey);
     auto al = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    // GDN-2's erase-gate rows land by 512-byte bulk copies: fp32, 16-byte aligned
+    const bool erase_ok = p.erase_gate ? al(p.erase_gate) : (!p.beta_f16 && al(p.beta));
     return rule_ok && p.dk == 128 && p.dv == 128 && p.act_f16 && (!perkey || (!p.decay_f16 && al(p.decay))) &&
-           (!perkey || !p.raw_gate || al(p.gate_bias)) && (p.rule != kGdn2 || (!p.beta_f16 && al(p.beta)));
+           (!perkey || !p.raw_gate || al(p.gate_bias)) && (p.rule != kGdn2 || erase_ok) &&
+           (p.write_gate == nullptr || al(p.write_gate));
 }
 
 cudaError_t launch_chunk_prepare_perkey(const Problem &p, const CUtensorMap &tk, const CUtensorMap &tq,
                                         const CUtensorMap &tv, const int *offs, const int *slot_req,
                                         unsigned char *img, int cap, cudaStream_t stream) {
-    static int attr_done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = smem_attr((const void *)chunk_prepare_perkey_kernel<true>, PK_SMEM);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(chunk_prepare_perkey_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PK_SMEM);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(chunk_prepare_perkey_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 PK_SMEM);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_done[dev] = 1;
-    }
+    e = smem_attr((const void *)chunk_prepare_perkey_kernel<false>, PK_SMEM);
+    if (e != cudaSuccess) return e;
     // persistent CTAs, one per SM (shared memory), at most one per task
     const long long tasks = (long long)cap * p.Hv;
     const unsigned grid = (unsigned)std::min<long long>(tasks, sm_count());

@@ -12,7 +12,9 @@ namespace gdn {
 
 // Rules and flags, mirrored from include/gdn.h for device code.
 enum : int { kLinear = 0, kGated = 1, kDelta = 2, kGatedDelta = 3, kGdn2 = 4 };
-enum : unsigned { kL2q = 0x1u, kL2k = 0x2u, kBetaSigmoid = 0x4u, kPerKey = 0x8u, kBetaShared = 0x10u };
+enum : unsigned { kL2q = 0x1u, kL2k = 0x2u, kBetaSigmoid = 0x4u, kPerKey = 0x8u, kBetaShared = 0x10u, kKMajor = 0x20u };
+// Device error bits, mirrored from include/gdn.h.
+enum : int { kErrBadSlot = 0x1, kErrTimeout = 0x2, kErrOverlap = 0x4, kErrDecayRange = 0x8 };
 
 __host__ __device__ inline bool rule_has_decay(int r) {
     return r == kGated || r == kGatedDelta || r == kGdn2;
@@ -38,7 +40,21 @@ struct Problem {
     const float *init;
     float *fin;
     int32_t *err;
+    const float *erase_gate;  // GDN-2 erase gate as its own input [T, Hv, dk], or null
+    const float *write_gate;  // GDN-2 write gate [T, Hv, dv], or null
 };
+
+// GDN-2 with the erase gate in its own input: beta is then a scalar per
+// (token, head) that scales the write, d = beta (w .* v) - u.
+__host__ __device__ inline bool erase_input(const Problem &p) { return p.erase_gate != nullptr; }
+// Rules whose beta is one scalar per (token, head) (or per token, shared).
+__host__ __device__ inline bool beta_is_scalar(const Problem &p) {
+    return p.rule == kDelta || p.rule == kGatedDelta || (p.rule == kGdn2 && p.erase_gate != nullptr);
+}
+// GDN-2 with its value rows scaled inside the kernel (v' = beta w .* v).
+__host__ __device__ inline bool scales_v(const Problem &p) {
+    return p.rule == kGdn2 && (p.erase_gate != nullptr || p.write_gate != nullptr);
+}
 
 // Element index of the scalar beta of token t and value head h: [T, Hv], or
 // [T] when one beta per token serves every value head (kBetaShared).

@@ -12,7 +12,9 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "../../include/gdn.h"
@@ -43,22 +45,12 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 constexpr size_t kNoAllocBytes = (size_t)768 << 20;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-// Its address on the current device, looked up once per device (the first
-// call must not be inside a stream capture).
+// Its address on the current device, looked up on every call: after a
+// device reset the module is loaded again and the array may move, so a
+// cached address could be stale.
 cudaError_t noalloc_scratch(void **ptr) {
-    static std::mutex mu;
-    static void *addr[64] = {nullptr};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        e = cudaGetSymbolAddress(&addr[dev], g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-    }
-    *ptr = addr[dev];
-    return cudaSuccess;
+    *ptr = nullptr;
+    return cudaGetSymbolAddress(ptr, g_noalloc_scratch);
 }
 
 size_t dtype_size(int dt) { return dt == GDN_DTYPE_F16 || dt == GDN_DTYPE_BF16 ? 2 : 4; }
@@ -93,13 +85,20 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
         return fail(GDN_ERR_INVALID, "unknown update rule %d", p->rule);
     static_assert(GDN_FLAG_L2NORM_Q == gdn::kL2q && GDN_FLAG_L2NORM_K == gdn::kL2k &&
                       GDN_FLAG_BETA_SIGMOID == gdn::kBetaSigmoid && GDN_FLAG_DECAY_PER_KEY == gdn::kPerKey &&
-                      GDN_FLAG_BETA_SHARED == gdn::kBetaShared,
+                      GDN_FLAG_BETA_SHARED == gdn::kBetaShared && GDN_FLAG_STATE_KMAJOR == gdn::kKMajor,
                   "flag mirror");
-    if (p->flags &
-        ~(GDN_FLAG_L2NORM_Q | GDN_FLAG_L2NORM_K | GDN_FLAG_BETA_SIGMOID | GDN_FLAG_DECAY_PER_KEY | GDN_FLAG_BETA_SHARED))
+    static_assert(GDN_DEVERR_BAD_SLOT == gdn::kErrBadSlot && GDN_DEVERR_TIMEOUT == gdn::kErrTimeout &&
+                      GDN_DEVERR_OVERLAP == gdn::kErrOverlap && GDN_DEVERR_DECAY_RANGE == gdn::kErrDecayRange,
+                  "error bit mirror");
+    if (p->flags & ~(GDN_FLAG_L2NORM_Q | GDN_FLAG_L2NORM_K | GDN_FLAG_BETA_SIGMOID | GDN_FLAG_DECAY_PER_KEY |
+                     GDN_FLAG_BETA_SHARED | GDN_FLAG_STATE_KMAJOR))
         return fail(GDN_ERR_INVALID, "unknown flag bits 0x%x", p->flags);
-    if ((p->flags & GDN_FLAG_BETA_SHARED) && p->rule != GDN_RULE_DELTA && p->rule != GDN_RULE_GATED_DELTA)
-        return fail(GDN_ERR_INVALID, "GDN_FLAG_BETA_SHARED applies to the scalar beta of rules DELTA and GATED_DELTA");
+    if ((p->erase_gate || p->write_gate) && p->rule != GDN_RULE_GDN2)
+        return fail(GDN_ERR_INVALID, "erase_gate and write_gate belong to rule GDN2");
+    if ((p->flags & GDN_FLAG_BETA_SHARED) && p->rule != GDN_RULE_DELTA && p->rule != GDN_RULE_GATED_DELTA &&
+        !(p->rule == GDN_RULE_GDN2 && p->erase_gate))
+        return fail(GDN_ERR_INVALID,
+                    "GDN_FLAG_BETA_SHARED applies to a scalar beta (rules DELTA, GATED_DELTA, GDN2 with erase_gate)");
     if (p->state_update_capacity != 0)
         return fail(GDN_ERR_INVALID, "state_update_capacity must be 0 (compact capture is not provided)");
     if (!isfinite(p->scale)) return fail(GDN_ERR_INVALID, "scale must be finite");
@@ -150,7 +149,8 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
         !aligned(p->decay, dtype_size(p->decay_dtype)) || !aligned(p->beta, dtype_size(p->beta_dtype)) ||
         !aligned(p->gate_bias, 4) || !aligned(p->gate_scale, 4) || !aligned(p->cu_seqlens, 4) ||
         !aligned(p->slot_ids, 4) || !aligned(p->initial_state, 4) || !aligned(p->final_state, 4) ||
-        !aligned(p->error_word, 4) || !aligned(p->seq_lens, 4))
+        !aligned(p->error_word, 4) || !aligned(p->seq_lens, 4) || !aligned(p->erase_gate, 4) ||
+        !aligned(p->write_gate, 4))
         return fail(GDN_ERR_INVALID, "a pointer is not aligned to its element size");
     const long long grid_bound = (long long)p->batch * p->num_heads_v * p->head_dim_v;
     if (grid_bound > (1LL << 31) - 1) return fail(GDN_ERR_UNSUPPORTED, "batch * Hv * dv exceeds 2^31 - 1");
@@ -185,6 +185,8 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
     d.init = p->initial_state;
     d.fin = p->final_state;
     d.err = p->error_word;
+    d.erase_gate = p->erase_gate;
+    d.write_gate = p->write_gate;
     return GDN_OK;
 }
 
@@ -196,6 +198,46 @@ gdn_status cuda_status(cudaError_t e) {
 }  // namespace
 
 namespace gdn {
+
+// Kernel attributes and occupancy, set or queried once per (device, kernel,
+// size) under a lock, so that threads making their first calls at the same
+// time do not race on the caches.
+namespace {
+std::mutex g_attr_mu;
+std::map<std::tuple<int, const void *, size_t>, int> g_attr;  // value: blocks per SM (0: attribute only)
+}  // namespace
+
+cudaError_t smem_attr(const void *fn, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    const auto key = std::make_tuple(dev, fn, (size_t)bytes | ((size_t)1 << 62));
+    if (g_attr.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_attr[key] = 0;
+    return e;
+}
+
+cudaError_t blocks_per_sm(const void *fn, int threads, size_t smem, int *n) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    const auto key = std::make_tuple(dev, fn, smem * 4096 + (size_t)threads);
+    auto it = g_attr.find(key);
+    if (it != g_attr.end()) {
+        *n = it->second;
+        return cudaSuccess;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    g_attr[key] = per_sm;
+    *n = per_sm;
+    return cudaSuccess;
+}
 
 int sm_count() {
     static std::mutex mu;

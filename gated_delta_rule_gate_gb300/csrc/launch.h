@@ -23,6 +23,10 @@ struct GateLaunch {
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+// Sets a kernel's dynamic shared-memory limit once per (device, kernel, size).
+cudaError_t smem_attr(const void *fn, int bytes);
+// Resident blocks per SM of a kernel at a launch shape (at least 1; cached).
+cudaError_t blocks_per_sm(const void *fn, int threads, size_t smem, int *n);
 
 cudaError_t launch_gate(const GateLaunch &g, cudaStream_t stream);
 cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream);

@@ -60,6 +60,26 @@ __host__ __device__ constexpr size_t stage_bytes(int dkp, int vrows) {
     return sizeof(float) * ((size_t)4 * kTB * dkp + (size_t)kTB * vrows + 3 * kTB);
 }
 
+// GDN-2 erase gate b of element e = (token, head) * dk + channel: its own
+// input (taken as given) or the per-key beta (through the sigmoid if asked).
+__device__ __forceinline__ float erase_at(const Problem &p, size_t e) {
+    if (p.erase_gate) return p.erase_gate[e];
+    const float b = ld_any(p.beta, e, p.beta_f16);
+    return (p.flags & kBetaSigmoid) ? sigmoid_f(b) : b;
+}
+
+// GDN-2 factor on value entry vi = (token t, head h) * dv + i: the scalar
+// beta of the write when the erase gate is its own input, times the write gate.
+__device__ __forceinline__ float write_scale(const Problem &p, int t, int h, size_t vi) {
+    float f = 1.f;
+    if (p.erase_gate) {
+        f = ld_any(p.beta, beta_at(p, t, h), p.beta_f16);
+        if (p.flags & kBetaSigmoid) f = sigmoid_f(f);
+    }
+    if (p.write_gate) f *= p.write_gate[vi];
+    return f;
+}
+
 // Stages tokens [tb, tb + nt) of value head h (key head qh) and the v entries
 // of rows [r0, r0 + s.vrows).  Threads [0, nthreads) of the CTA take part.
 __device__ void stage_tokens(const Problem &p, const Stage &s, int h, int qh, int tb, int nt,
@@ -70,11 +90,15 @@ __device__ void stage_tokens(const Problem &p, const Stage &s, int h, int qh, in
     const bool gdn2 = p.rule == kGdn2;
     const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
     const bool sig = (p.flags & kBetaSigmoid) != 0;
+    const bool vscale = scales_v(p);
     const int rows = s.vrows;
     for (int idx = tid; idx < nt * rows; idx += nthreads) {
         const int tt = idx / rows, r = idx % rows;
         const int i = r0 + r;
-        s.v[tt * rows + r] = i < p.dv ? ld_any(p.v, ((size_t)(tb + tt) * p.Hv + h) * p.dv + i, p.act_f16) : 0.f;
+        const size_t vi = ((size_t)(tb + tt) * p.Hv + h) * p.dv + i;
+        float x = i < p.dv ? ld_any(p.v, vi, p.act_f16) : 0.f;
+        if (vscale && i < p.dv) x *= write_scale(p, tb + tt, h, vi);
+        s.v[tt * rows + r] = x;
     }
     for (int tt = warp; tt < nt; tt += nw) {
         const int t = tb + tt;
@@ -111,11 +135,7 @@ __device__ void stage_tokens(const Problem &p, const Stage &s, int h, int qh, in
                     if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[(size_t)h * p.dk + c]);
                     s.a[tt * s.dkp + c] = expf(g);
                 }
-                if (gdn2) {
-                    float bb = ld_any(p.beta, th * p.dk + c, p.beta_f16);
-                    if (sig) bb = sigmoid_f(bb);
-                    s.x[tt * s.dkp + c] = bb * kv[i];
-                }
+                if (gdn2) s.x[tt * s.dkp + c] = erase_at(p, th * p.dk + c) * kv[i];
             }
         }
         if (lane == 0) {
@@ -356,22 +376,35 @@ struct PipeLayout {
     int stage_floats; // floats per staging buffer
     int raw_bytes;    // cp.async landing area of the stager
     int ring_bytes;
+    int red_bytes;    // key-major consumers: per-warp partial sums, two buffers
+    int stages;       // state slices in flight
     int total_bytes;
-    bool has_a, has_x;
+    int xes;          // bytes per element of the GDN-2 erase-gate rows
+    bool has_a, has_x, has_w;
 };
+
+// Key-major state in the decode kernel: one CTA per SM with twice the ring.
+constexpr int kStagesKM = 8;
 
 __host__ __device__ inline PipeLayout pipe_layout(const Problem &p) {
     PipeLayout L;
+    const bool km = (p.flags & kKMajor) != 0;
     L.has_a = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
     L.has_x = p.rule == kGdn2;
+    L.has_w = p.rule == kGdn2 && p.write_gate != nullptr;
+    L.xes = p.erase_gate ? 4 : (p.beta_f16 ? 2 : 4);
     L.dvp = (p.dv + 3) & ~3;
     L.stage_floats = kTB * p.dk * (2 + (L.has_a ? 1 : 0) + (L.has_x ? 1 : 0)) + kTB * L.dvp + 3 * kTB + 4;
     const int es = p.act_f16 ? 2 : 4;
-    const int des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
-    L.raw_bytes = kTB * (2 * p.dk * es + p.dv * es + (L.has_a ? p.dk * des : 0) + (L.has_x ? p.dk * bes : 0));
+    const int des = p.decay_f16 ? 2 : 4;
+    L.raw_bytes = kTB * (2 * p.dk * es + p.dv * es + (L.has_a ? p.dk * des : 0) + (L.has_x ? p.dk * L.xes : 0) +
+                         (L.has_w ? p.dv * 4 : 0));
     L.raw_bytes = (L.raw_bytes + 15) & ~15;
-    L.ring_bytes = kStages * kFastRows * p.dk * 4;
-    L.total_bytes = L.ring_bytes + 2 * L.stage_floats * 4 + L.raw_bytes + (2 * kStages + 4) * 8;
+    L.stages = km ? kStagesKM : kStages;
+    // a slice is 32 stored rows: value rows of dk floats, or key rows of dv floats (key-major)
+    L.ring_bytes = L.stages * kFastRows * (km ? p.dv : p.dk) * 4;
+    L.red_bytes = km ? 2 * (kThreads / 32) * 32 * 32 : 0;
+    L.total_bytes = L.ring_bytes + 2 * L.stage_floats * 4 + L.raw_bytes + L.red_bytes + (2 * L.stages + 4) * 8;
     return L;
 }
 
@@ -415,6 +448,18 @@ __device__ __forceinline__ float bits_to_f(uint32_t x, int f16) {
     return f16 ? __half2float(__ushort_as_half((unsigned short)x)) : __uint_as_float(x);
 }
 
+// cp.async of L token rows of row_bytes each (a multiple of 16): row tt comes
+// from row first + tt * step of src and lands at dst + tt * row_bytes.
+__device__ __forceinline__ void copy_token_rows(unsigned char *dst, const void *src, size_t first, size_t step,
+                                                int row_bytes, int L, int lane) {
+    const int ch = row_bytes / 16;
+    const unsigned char *s0 = static_cast<const unsigned char *>(src);
+    for (int idx = lane; idx < L * ch; idx += 32) {
+        const int tt = idx / ch, c = idx % ch;
+        ptx::cp_async16(dst + tt * row_bytes + 16 * c, s0 + (first + (size_t)tt * step) * row_bytes + 16 * c, 16);
+    }
+}
+
 // The stager's copies for one pair with 0 < L <= kTB tokens starting at t0:
 // raw key/query/value rows (and per-key decay, erase gate) land in `raw` by
 // cp.async; the per-token scalars come back in `ts`.
@@ -422,40 +467,20 @@ template <int DK>
 __device__ __forceinline__ void issue_pair(const Problem &p, const PipeLayout &Ly, unsigned char *raw, int h, int qh,
                                            int t0, int L, int lane, TokScalars &ts) {
     const int es = p.act_f16 ? 2 : 4;
-    const int des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    const int des = p.decay_f16 ? 2 : 4;
     unsigned char *rk = raw;
     unsigned char *rq = rk + kTB * DK * es;
     unsigned char *rv = rq + kTB * DK * es;
     unsigned char *ra = rv + kTB * p.dv * es;
     unsigned char *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
-    const int kch = DK * es / 16, vch = p.dv * es / 16;
-    for (int idx = lane; idx < L * kch; idx += 32) {
-        const int tt = idx / kch, c = idx % kch;
-        const size_t off = (((size_t)(t0 + tt) * p.Hq + qh) * DK) * es + 16 * c;
-        ptx::cp_async16(rk + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.k) + off, 16);
-        ptx::cp_async16(rq + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.q) + off, 16);
-    }
-    for (int idx = lane; idx < L * vch; idx += 32) {
-        const int tt = idx / vch, c = idx % vch;
-        const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * p.dv) * es + 16 * c;
-        ptx::cp_async16(rv + tt * p.dv * es + 16 * c, static_cast<const unsigned char *>(p.v) + off, 16);
-    }
-    if (Ly.has_a) {
-        const int ach = DK * des / 16;
-        for (int idx = lane; idx < L * ach; idx += 32) {
-            const int tt = idx / ach, c = idx % ach;
-            const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * DK) * des + 16 * c;
-            ptx::cp_async16(ra + tt * DK * des + 16 * c, static_cast<const unsigned char *>(p.decay) + off, 16);
-        }
-    }
-    if (Ly.has_x) {
-        const int xch = DK * bes / 16;
-        for (int idx = lane; idx < L * xch; idx += 32) {
-            const int tt = idx / xch, c = idx % xch;
-            const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * DK) * bes + 16 * c;
-            ptx::cp_async16(rx + tt * DK * bes + 16 * c, static_cast<const unsigned char *>(p.beta) + off, 16);
-        }
-    }
+    const size_t kv0 = (size_t)t0 * p.Hq + qh, hv0 = (size_t)t0 * p.Hv + h;
+    copy_token_rows(rk, p.k, kv0, p.Hq, DK * es, L, lane);
+    copy_token_rows(rq, p.q, kv0, p.Hq, DK * es, L, lane);
+    copy_token_rows(rv, p.v, hv0, p.Hv, p.dv * es, L, lane);
+    if (Ly.has_a) copy_token_rows(ra, p.decay, hv0, p.Hv, DK * des, L, lane);
+    // the GDN-2 erase gate (its own input, or the per-key beta) and write gate
+    if (Ly.has_x) copy_token_rows(rx, p.erase_gate ? (const void *)p.erase_gate : p.beta, hv0, p.Hv, DK * Ly.xes, L, lane);
+    if (Ly.has_w) copy_token_rows(rx + kTB * DK * Ly.xes, p.write_gate, hv0, p.Hv, p.dv * 4, L, lane);
     ts.g = ts.b = 0u;
     ts.gs = ts.gb = 0.f;
     if (lane < L) {
@@ -467,7 +492,7 @@ __device__ __forceinline__ void issue_pair(const Problem &p, const PipeLayout &L
                 ts.gb = p.gate_bias[h];
             }
         }
-        if (p.rule == kDelta || p.rule == kGatedDelta) ts.b = ld_bits(p.beta, beta_at(p, t0 + lane, h), p.beta_f16);
+        if (beta_is_scalar(p)) ts.b = ld_bits(p.beta, beta_at(p, t0 + lane, h), p.beta_f16);
     }
 }
 
@@ -523,8 +548,8 @@ __device__ __forceinline__ void stage_token_group(const Problem &p, const Stage 
                 st.a[tt * DK + c] = expf(g);
             }
             if (Ly.has_x) {
-                float bb = ld_raw(rx, tt * DK + c, p.beta_f16);
-                if (sig) bb = sigmoid_f(bb);
+                float bb = ld_raw(rx, tt * DK + c, p.erase_gate ? 0 : p.beta_f16);
+                if (sig && !p.erase_gate) bb = sigmoid_f(bb);
                 st.x[tt * DK + c] = bb * kn;
             }
         }
@@ -540,13 +565,15 @@ __device__ void finish_pair(const Problem &p, const Stage &st, const PipeLayout 
                             int L, int lane, const TokScalars &ts) {
     const int es = p.act_f16 ? 2 : 4;
     const int des = p.decay_f16 ? 2 : 4;
-    const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;
+    const bool beta_scalar = p.rule == kDelta || p.rule == kGatedDelta;  // d = beta (v - alpha u)
+    const bool vscale = scales_v(p);  // GDN-2: v' = beta w .* v, d = v' - alpha u
     const bool sig = (p.flags & kBetaSigmoid) != 0;
     const unsigned char *rk = raw;
     const unsigned char *rq = rk + kTB * DK * es;
     const unsigned char *rv = rq + kTB * DK * es;
     const unsigned char *ra = rv + kTB * p.dv * es;
     const unsigned char *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
+    const unsigned char *rw = rx + (Ly.has_x ? kTB * DK * Ly.xes : 0);
     int g0 = 0;
     for (; g0 + 4 <= L; g0 += 4) stage_token_group<DK, 4>(p, st, Ly, rk, rq, ra, rx, h, g0, L, lane);
     if (L - g0 == 1)
@@ -555,22 +582,8 @@ __device__ void finish_pair(const Problem &p, const Stage &st, const PipeLayout 
         stage_token_group<DK, 2>(p, st, Ly, rk, rq, ra, rx, h, g0, L, lane);
     else if (L - g0 == 3)
         stage_token_group<DK, 4>(p, st, Ly, rk, rq, ra, rx, h, g0, L, lane);
-    // value rows: 16-byte chunks (dv * element size is a multiple of 16)
-    const int vch = p.dv * es / 16;
-    for (int idx = lane; idx < L * vch; idx += 32) {
-        const int tt = idx / vch, c = idx % vch;
-        const uint4 w = *reinterpret_cast<const uint4 *>(rv + tt * p.dv * es + 16 * c);
-        float *dst = st.v + tt * st.vrows;
-        if (p.act_f16) {
-            const __half2 *hp = reinterpret_cast<const __half2 *>(&w);
-            const float2 f0 = __half22float2(hp[0]), f1 = __half22float2(hp[1]);
-            const float2 f2 = __half22float2(hp[2]), f3 = __half22float2(hp[3]);
-            *reinterpret_cast<float4 *>(dst + 8 * c) = make_float4(f0.x, f0.y, f1.x, f1.y);
-            *reinterpret_cast<float4 *>(dst + 8 * c + 4) = make_float4(f2.x, f2.y, f3.x, f3.y);
-        } else {
-            *reinterpret_cast<uint4 *>(dst + 4 * c) = w;
-        }
-    }
+    // per-token scalars (lane tt holds token tt's)
+    float vb = 1.f;  // GDN-2 with its own erase gate: beta scales the value row
     if (lane < L) {
         float alpha = 1.f;
         if (rule_has_decay(p.rule) && !Ly.has_a) {
@@ -579,8 +592,56 @@ __device__ void finish_pair(const Problem &p, const Stage &st, const PipeLayout 
             alpha = expf(g);
         }
         const float b0 = bits_to_f(ts.b, p.beta_f16);
+        const float bs = sig ? sigmoid_f(b0) : b0;
         st.alpha[lane] = alpha;
-        st.beta[lane] = beta_scalar ? (sig ? sigmoid_f(b0) : b0) : 1.f;
+        st.beta[lane] = beta_scalar ? bs : 1.f;
+        if (p.erase_gate) vb = bs;
+    }
+    // value rows: 16-byte chunks (dv * element size is a multiple of 16)
+    const int vch = p.dv * es / 16;
+    if (!vscale) {
+        for (int idx = lane; idx < L * vch; idx += 32) {
+            const int tt = idx / vch, c = idx % vch;
+            const uint4 w = *reinterpret_cast<const uint4 *>(rv + tt * p.dv * es + 16 * c);
+            float *dst = st.v + tt * st.vrows;
+            if (p.act_f16) {
+                const __half2 *hp = reinterpret_cast<const __half2 *>(&w);
+                const float2 f0 = __half22float2(hp[0]), f1 = __half22float2(hp[1]);
+                const float2 f2 = __half22float2(hp[2]), f3 = __half22float2(hp[3]);
+                *reinterpret_cast<float4 *>(dst + 8 * c) = make_float4(f0.x, f0.y, f1.x, f1.y);
+                *reinterpret_cast<float4 *>(dst + 8 * c + 4) = make_float4(f2.x, f2.y, f3.x, f3.y);
+            } else {
+                *reinterpret_cast<uint4 *>(dst + 4 * c) = w;
+            }
+        }
+        return;
+    }
+    // GDN-2: v' = beta w .* v.  The trip count is the same in every lane so that
+    // the shuffle (beta of token tt from lane tt) sees all of them.
+    for (int base = 0; base < L * vch; base += 32) {
+        const int idx = base + lane;
+        const int tt = idx / vch, c = idx % vch;
+        const float f = __shfl_sync(0xffffffffu, vb, min(tt, 31));
+        if (idx < L * vch) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(rv + tt * p.dv * es + 16 * c);
+            float *dst = st.v + tt * st.vrows;
+            const float *wr = reinterpret_cast<const float *>(rw + tt * p.dv * 4);
+            if (p.act_f16) {
+                const __half2 *hp = reinterpret_cast<const __half2 *>(&w);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = __half22float2(hp[e]);
+                    const int col = 8 * c + 2 * e;
+                    dst[col] = x.x * (Ly.has_w ? f * wr[col] : f);
+                    dst[col + 1] = x.y * (Ly.has_w ? f * wr[col + 1] : f);
+                }
+            } else {
+                const float x[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                                    __uint_as_float(w.w)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dst[4 * c + e] = x[e] * (Ly.has_w ? f * wr[4 * c + e] : f);
+            }
+        }
     }
 }
 
@@ -641,22 +702,182 @@ __device__ __forceinline__ void consume_slices(const Problem &p, const Stage &st
     }
 }
 
-template <int DK>
-__global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Problem p, int slices, int pairs) {
+
+// ---------------------------------------------------------------------------
+// Key-major state ("gatedDeltaUpdate": [rows, Hv, dk, dv]; dk = dv = 128).
+// The stored rows are key rows, so a slice is 32 key rows of 128 value
+// columns, and the dot products S^T kappa and S^T q of a value column run
+// over all four slices.  The consumers hold the whole tile in registers:
+// thread (warp w, lane l) keeps key rows 32 s + 4 w + m (s, m = 0..3) of the
+// value columns 4 l .. 4 l + 3 (every ring load is a 512-byte row per warp).
+// Per token each warp's partial sums go through shared memory (two buffers,
+// one barrier of the consumer warps per token) and every thread adds the
+// eight partials of its four columns.  The scalar decay is kept as a lazy
+// factor as in apply_tokens_multi.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 f4_fma(float a, const float4 &x, const float4 &y) {
+    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
+}
+__device__ __forceinline__ float4 f4_add(const float4 &x, const float4 &y) {
+    return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+}
+__device__ __forceinline__ float4 f4_scale(float a, const float4 &x) {
+    return make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
+}
+
+// `tok` counts the tokens this thread has applied (it picks the buffer of red).
+__device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s, float4 (&S)[4][4], float4 *red,
+                                                int nt, int tb, int h, int warp, int lane, int &tok) {
+    constexpr int DK = 128;
+    const bool perkey = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
+    const bool retrieval = rule_has_retrieval(p.rule);
+    const float *kap = p.rule == kGdn2 ? s.x : s.k;
+    float c = 1.f;
+    for (int tt = 0; tt < nt; ++tt, ++tok) {
+        const int ro = tt * DK + 4 * warp;  // staged entry of key row 4 warp (+ 32 s + m)
+        if (perkey) {
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+                const float4 a4 = ld_f4(s.a + ro + 32 * sl);
+                S[sl][0] = f4_scale(a4.x, S[sl][0]);
+                S[sl][1] = f4_scale(a4.y, S[sl][1]);
+                S[sl][2] = f4_scale(a4.z, S[sl][2]);
+                S[sl][3] = f4_scale(a4.w, S[sl][3]);
+            }
+        }
+        float4 ua = make_float4(0.f, 0.f, 0.f, 0.f), ub = ua, wa = ua, wb = ua;
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+            const float4 x4 = ld_f4(kap + ro + 32 * sl), q4 = ld_f4(s.q + ro + 32 * sl);
+            ua = f4_fma(x4.x, S[sl][0], ua), ub = f4_fma(x4.y, S[sl][1], ub);
+            ua = f4_fma(x4.z, S[sl][2], ua), ub = f4_fma(x4.w, S[sl][3], ub);
+            wa = f4_fma(q4.x, S[sl][0], wa), wb = f4_fma(q4.y, S[sl][1], wb);
+            wa = f4_fma(q4.z, S[sl][2], wa), wb = f4_fma(q4.w, S[sl][3], wb);
+        }
+        float4 *rb = red + (tok & 1) * (2 * kThreads);
+        rb[2 * (warp * 32 + lane)] = f4_add(ua, ub);
+        rb[2 * (warp * 32 + lane) + 1] = f4_add(wa, wb);
+        ptx::named_bar_sync(2, kThreads);
+        float4 U = rb[2 * lane], W = rb[2 * lane + 1];
+#pragma unroll
+        for (int w2 = 1; w2 < kThreads / 32; ++w2) {
+            U = f4_add(U, rb[2 * (w2 * 32 + lane)]);
+            W = f4_add(W, rb[2 * (w2 * 32 + lane) + 1]);
+        }
+        float cn = c * s.alpha[tt];  // alpha is 1 without scalar decay
+        const float bt = s.beta[tt], kq = s.kq[tt];
+        const float4 v4 = ld_f4(s.v + tt * s.vrows + 4 * lane);
+        float4 d;
+        if (retrieval) {
+            d.x = bt * (v4.x - cn * U.x), d.y = bt * (v4.y - cn * U.y);
+            d.z = bt * (v4.z - cn * U.z), d.w = bt * (v4.w - cn * U.w);
+        } else {
+            d = v4;
+        }
+        if (warp == 0) {
+            const float4 ov = make_float4(p.scale * fmaf(cn, W.x, d.x * kq), p.scale * fmaf(cn, W.y, d.y * kq),
+                                          p.scale * fmaf(cn, W.z, d.z * kq), p.scale * fmaf(cn, W.w, d.w * kq));
+            const size_t oi = ((size_t)(tb + tt) * p.Hv + h) * p.dv + 4 * lane;
+            if (p.act_f16) {
+                __half2 *o2 = reinterpret_cast<__half2 *>(static_cast<__half *>(p.o) + oi);
+                o2[0] = __floats2half2_rn(ov.x, ov.y);
+                o2[1] = __floats2half2_rn(ov.z, ov.w);
+            } else {
+                *reinterpret_cast<float4 *>(static_cast<float *>(p.o) + oi) = ov;
+            }
+        }
+        if (cn < 1e-20f) {  // fold the factor in before it underflows (uniform across the CTA)
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) S[sl][m] = f4_scale(cn, S[sl][m]);
+            cn = 1.f;
+        }
+        const float rc = __frcp_rn(cn);
+        const float4 e = f4_scale(rc, d);
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl) {
+            const float4 k4 = ld_f4(s.k + ro + 32 * sl);
+            S[sl][0] = f4_fma(k4.x, e, S[sl][0]);
+            S[sl][1] = f4_fma(k4.y, e, S[sl][1]);
+            S[sl][2] = f4_fma(k4.z, e, S[sl][2]);
+            S[sl][3] = f4_fma(k4.w, e, S[sl][3]);
+        }
+        c = cn;
+    }
+    if (c != 1.f) {
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) S[sl][m] = f4_scale(c, S[sl][m]);
+    }
+}
+
+// The key-major consumer side of one (request, head) pair.  `j` counts ring
+// uses (set to -1 if a wait runs out); `tok` as in apply_tokens_km.
+template <int NST>
+__device__ __forceinline__ void consume_tile_km(const Problem &p, const Stage &st, const float *ring, uint64_t *full,
+                                                uint64_t *empty, float4 *red, int &j, int &tok, int row, int h,
+                                                int qh, int t0, int t1, int tid, int warp, int lane) {
+    constexpr int kSlice = kFastRows * 128;
+    float4 S[4][4];
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl) {
+        const int slot = j % NST;
+        if (!ptx::mbar_wait(&full[slot], (j / NST) & 1)) {
+            if (p.err && tid == 0) atomicOr(p.err, kErrTimeout);
+            j = -1;
+            return;
+        }
+        ++j;
+        const bool have = row >= 0 && p.init != nullptr;
+        const float *src = ring + slot * kSlice + 4 * warp * 128 + 4 * lane;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) S[sl][m] = have ? ld_f4(src + m * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&empty[slot]);
+    }
+    if (row < 0) return;
+    const int L = t1 - t0;
+    if (L > 0) {
+        for (int tb = t0; tb < t1; tb += kTB) {
+            const int nt = min(kTB, t1 - tb);
+            if (L > kTB) {  // long request: stage kTB tokens at a time ourselves
+                ptx::named_bar_sync(1, kThreads);
+                stage_tokens(p, st, h, qh, tb, nt, 0, tid, kThreads);
+                ptx::named_bar_sync(1, kThreads);
+            }
+            apply_tokens_km(p, st, S, red, nt, tb, h, warp, lane, tok);
+        }
+    } else if (p.fin == p.init) {
+        return;  // empty request, in place: nothing changes
+    }
+    float *dst = p.fin + ((size_t)row * p.Hv + h) * 128 * 128 + 4 * warp * 128 + 4 * lane;
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) __stcs(reinterpret_cast<float4 *>(dst + (32 * sl + m) * 128), S[sl][m]);
+}
+
+template <int DK, bool KM>
+__global__ void __launch_bounds__(kThreads + 64, KM ? 1 : 2) recurrent_pipe_kernel(Problem p, int slices, int pairs) {
+    // KM: key-major state (dk = dv = DK = 128); a slice is 32 key rows
+    constexpr int NST = KM ? kStagesKM : kStages;
     constexpr int kSlice = kFastRows * DK;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const PipeLayout Ly = pipe_layout(p);
     float *ring = reinterpret_cast<float *>(smem_raw);
     float *stage_base = reinterpret_cast<float *>(smem_raw + Ly.ring_bytes);
     unsigned char *raw = smem_raw + Ly.ring_bytes + 2 * Ly.stage_floats * 4;
-    uint64_t *full = reinterpret_cast<uint64_t *>(raw + Ly.raw_bytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *tok_full = empty + kStages;
+    float4 *red = reinterpret_cast<float4 *>(raw + Ly.raw_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw + Ly.raw_bytes + Ly.red_bytes);
+    uint64_t *empty = full + NST;
+    uint64_t *tok_full = empty + NST;
     uint64_t *tok_empty = tok_full + 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kCW = kThreads / 32;  // consumer warps
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], kCW);
         }
@@ -676,13 +897,14 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
                 const int row = p.slots ? p.slots[b] : b;
                 const bool valid = row >= 0 && row < p.rows && p.init != nullptr;
                 for (int sl = 0; sl < slices; ++sl, ++j) {
-                    const int s = j % kStages;
-                    if (!ptx::mbar_wait(&empty[s], ((j / kStages) & 1) ^ 1)) {
+                    const int s = j % NST;
+                    if (!ptx::mbar_wait(&empty[s], ((j / NST) & 1) ^ 1)) {
                         if (p.err) atomicOr(p.err, 2);
                         return;
                     }
                     const int r0 = sl * kFastRows;
-                    const int nrows = min(kFastRows, p.dv - r0);
+                    // stored rows: value rows of DK floats (or key rows of dv = DK floats)
+                    const int nrows = min(kFastRows, (KM ? p.dk : p.dv) - r0);
                     if (valid) {
                         const uint32_t bytes = (uint32_t)nrows * DK * 4u;
                         ptx::mbar_arrive_expect_tx(&full[s], bytes);
@@ -738,7 +960,7 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
     // ---- consumer warps
     const int cg = lane & 7;
     const int rloc = warp * 4 + (lane >> 3);
-    int j = 0, k = 0;
+    int j = 0, k = 0, tok = 0;
     for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x, ++k) {
         const int buf = k & 1;
         if (!ptx::mbar_wait(&tok_full[buf], (k >> 1) & 1)) {
@@ -754,7 +976,9 @@ __global__ void __launch_bounds__(kThreads + 64, 2) recurrent_pipe_kernel(Proble
         const bool one_block = L <= kTB;
         // R state slices per pass (2 when the slice count is even): the staged
         // key/query loads are shared and the rows' reduction chains interleave
-        if ((slices & 1) == 0)
+        if (KM)
+            consume_tile_km<NST>(p, st, ring, full, empty, red, j, tok, row, h, qh, t0, t1, tid, warp, lane);
+        else if ((slices & 1) == 0)
             consume_slices<DK, 2>(p, st, ring, full, empty, j, slices, row, h, qh, t0, t1, tid, lane, cg, rloc);
         else
             consume_slices<DK, 1>(p, st, ring, full, empty, j, slices, row, h, qh, t0, t1, tid, lane, cg, rloc);
@@ -783,8 +1007,8 @@ __host__ __device__ inline LongLayout long_layout(const Problem &p) {
     L.has_a = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
     L.has_x = p.rule == kGdn2;
     L.stage_floats = kTB * p.dk * (2 + (L.has_a ? 1 : 0) + (L.has_x ? 1 : 0)) + kTB * kFastRows + 3 * kTB + 4;
-    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
-    L.raw_bytes = kTB * (2 * p.dk * es + kFastRows * es + (L.has_a ? p.dk * des : 0) + (L.has_x ? p.dk * bes : 0));
+    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, xes = p.erase_gate ? 4 : (p.beta_f16 ? 2 : 4);
+    L.raw_bytes = kTB * (2 * p.dk * es + kFastRows * es + (L.has_a ? p.dk * des : 0) + (L.has_x ? p.dk * xes : 0));
     L.raw_bytes = (L.raw_bytes + 15) & ~15;
     L.total_bytes = L.stage_floats * 4 + 2 * L.raw_bytes;
     return L;
@@ -793,7 +1017,7 @@ __host__ __device__ inline LongLayout long_layout(const Problem &p) {
 template <int DK>
 __device__ void issue_block_raw(const Problem &p, const LongLayout &Ly, unsigned char *raw, int h, int qh, int r0,
                                 int tb, int nt) {
-    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, bes = p.beta_f16 ? 2 : 4;
+    const int es = p.act_f16 ? 2 : 4, des = p.decay_f16 ? 2 : 4, xes = p.erase_gate ? 4 : (p.beta_f16 ? 2 : 4);
     unsigned char *rk = raw, *rq = rk + kTB * DK * es, *rv = rq + kTB * DK * es;
     unsigned char *ra = rv + kTB * kFastRows * es, *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
     const int kch = DK * es / 16;
@@ -817,12 +1041,13 @@ __device__ void issue_block_raw(const Problem &p, const LongLayout &Ly, unsigned
             ptx::cp_async16(ra + tt * DK * des + 16 * c, static_cast<const unsigned char *>(p.decay) + off, 16);
         }
     }
-    if (Ly.has_x) {
-        const int xch = DK * bes / 16;
+    if (Ly.has_x) {  // the GDN-2 erase gate: its own input, or the per-key beta
+        const int xch = DK * xes / 16;
+        const unsigned char *xsrc = static_cast<const unsigned char *>(p.erase_gate ? (const void *)p.erase_gate : p.beta);
         for (int idx = threadIdx.x; idx < nt * xch; idx += blockDim.x) {
             const int tt = idx / xch, c = idx % xch;
-            const size_t off = (((size_t)(tb + tt) * p.Hv + h) * DK) * bes + 16 * c;
-            ptx::cp_async16(rx + tt * DK * bes + 16 * c, static_cast<const unsigned char *>(p.beta) + off, 16);
+            const size_t off = (((size_t)(tb + tt) * p.Hv + h) * DK) * xes + 16 * c;
+            ptx::cp_async16(rx + tt * DK * xes + 16 * c, xsrc + off, 16);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -847,16 +1072,39 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, 
     if (row < 0) return;
     int t0, t1;
     request_range(p, b, t0, t1);
-    const size_t soff = (((size_t)row * p.Hv + h) * p.dv + i_row) * DK + 4 * cg;
-    float4 S[NV];
+    // value-major: row i_row is contiguous; key-major: element (i, c) sits at c * dv + i
+    const bool km = (p.flags & kKMajor) != 0;
+    const size_t tbase = ((size_t)row * p.Hv + h) * p.dv * DK;
+    const size_t soff = tbase + (size_t)i_row * DK + 4 * cg;
+    auto load_state = [&](float4(&S)[NV]) {
 #pragma unroll
-    for (int j = 0; j < NV; ++j)
-        S[j] = (active && p.init) ? *reinterpret_cast<const float4 *>(p.init + soff + 32 * j) : make_float4(0, 0, 0, 0);
-    if (t1 == t0) {
-        if (active && p.fin != p.init) {
-#pragma unroll
-            for (int j = 0; j < NV; ++j) *reinterpret_cast<float4 *>(p.fin + soff + 32 * j) = S[j];
+        for (int j = 0; j < NV; ++j) {
+            if (!active || !p.init) {
+                S[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else if (km) {
+                const float *b = p.init + tbase + (size_t)(4 * cg + 32 * j) * p.dv + i_row;
+                S[j] = make_float4(b[0], b[p.dv], b[2 * p.dv], b[3 * p.dv]);
+            } else {
+                S[j] = *reinterpret_cast<const float4 *>(p.init + soff + 32 * j);
+            }
         }
+    };
+    auto store_state = [&](const float4(&S)[NV]) {
+        if (!active) return;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if (km) {
+                float *b = p.fin + tbase + (size_t)(4 * cg + 32 * j) * p.dv + i_row;
+                b[0] = S[j].x, b[p.dv] = S[j].y, b[2 * p.dv] = S[j].z, b[3 * p.dv] = S[j].w;
+            } else {
+                *reinterpret_cast<float4 *>(p.fin + soff + 32 * j) = S[j];
+            }
+        }
+    };
+    float4 S[NV];
+    load_state(S);
+    if (t1 == t0) {
+        if (p.fin != p.init) store_state(S);
         return;
     }
     Stage st;
@@ -941,8 +1189,8 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, 
                     st.a[tt * DK + c] = expf(g);
                 }
                 if (Ly.has_x) {
-                    float bb = ld_raw(rx, tt * DK + c, p.beta_f16);
-                    if (sig) bb = sigmoid_f(bb);
+                    float bb = ld_raw(rx, tt * DK + c, p.erase_gate ? 0 : p.beta_f16);
+                    if (sig && !p.erase_gate) bb = sigmoid_f(bb);
                     st.x[tt * DK + c] = bb * kv[i];
                 }
             }
@@ -951,9 +1199,12 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, 
         {
             const unsigned char *rv = raw + 2 * kTB * DK * es;
             const int vrows = min(kFastRows, p.dv - r0);
+            const bool vscale = scales_v(p);
             for (int idx = tid; idx < nt * kFastRows; idx += kThreads) {
                 const int tt = idx / kFastRows, r = idx % kFastRows;
-                st.v[tt * kFastRows + r] = r < vrows ? ld_raw(rv, tt * kFastRows + r, p.act_f16) : 0.f;
+                float x = r < vrows ? ld_raw(rv, tt * kFastRows + r, p.act_f16) : 0.f;
+                if (vscale && r < vrows) x *= write_scale(p, tb + tt, h, ((size_t)(tb + tt) * p.Hv + h) * p.dv + r0 + r);
+                st.v[tt * kFastRows + r] = x;
             }
         }
         if (tid < nt) {
@@ -965,10 +1216,7 @@ __global__ void __launch_bounds__(kThreads, 2) recurrent_long_kernel(Problem p, 
         __syncthreads();
         apply_tokens<NV>(p, st, S, nt, tb, h, i_row, rloc, cg, active);
     }
-    if (active) {
-#pragma unroll
-        for (int j = 0; j < NV; ++j) *reinterpret_cast<float4 *>(p.fin + soff + 32 * j) = S[j];
-    }
+    store_state(S);
 }
 
 // Any dk, dv <= 256: one warp per value row, lane c holds columns c + 32 i.
@@ -985,19 +1233,22 @@ __global__ void __launch_bounds__(kThreads) recurrent_generic_kernel(Problem p, 
     if (row < 0) return;
     int t0, t1;
     request_range(p, b, t0, t1);
-    const size_t soff = (((size_t)row * p.Hv + h) * p.dv + i_row) * p.dk;
+    // element (i_row, c) of the state tile: value-major at i_row * dk + c, key-major at c * dv + i_row
+    const bool km = (p.flags & kKMajor) != 0;
+    const size_t tbase = ((size_t)row * p.Hv + h) * p.dv * p.dk;
+    auto sat = [&](int c) { return tbase + (km ? (size_t)c * p.dv + i_row : (size_t)i_row * p.dk + c); };
     float S[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int c = lane + 32 * i;
-        S[i] = (active && p.init && c < p.dk) ? p.init[soff + c] : 0.f;
+        S[i] = (active && p.init && c < p.dk) ? p.init[sat(c)] : 0.f;
     }
     if (t1 == t0) {
         if (active && p.fin != p.init) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int c = lane + 32 * i;
-                if (c < p.dk) p.fin[soff + c] = S[i];
+                if (c < p.dk) p.fin[sat(c)] = S[i];
             }
         }
         return;
@@ -1043,38 +1294,27 @@ __global__ void __launch_bounds__(kThreads) recurrent_generic_kernel(Problem p, 
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int c = lane + 32 * i;
-            if (c < p.dk) p.fin[soff + c] = S[i];
+            if (c < p.dk) p.fin[sat(c)] = S[i];
         }
     }
 }
 
 static bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-template <int DK>
+template <int DK, bool KM>
 static cudaError_t launch_pipe(const Problem &p, cudaStream_t stream) {
-    const int slices = (p.dv + kFastRows - 1) / kFastRows;
+    const int slices = ((KM ? p.dk : p.dv) + kFastRows - 1) / kFastRows;
     const int pairs = p.B * p.Hv;
     const size_t smem = (size_t)pipe_layout(p).total_bytes;
-    // Dynamic shared memory above 48 KB must be enabled per device; the
-    // occupancy depends on the size, so both are redone when it changes.
-    static int cached_smem[64] = {0}, cached_per_sm[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    const void *fn = (const void *)recurrent_pipe_kernel<DK, KM>;
+    cudaError_t e = smem_attr(fn, 220 * 1024);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    if (dev < 64 && cached_smem[dev] == (int)smem) {
-        per_sm = cached_per_sm[dev];
-    } else {
-        e = cudaFuncSetAttribute(recurrent_pipe_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, recurrent_pipe_kernel<DK>, kThreads + 64, smem);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) per_sm = 1;
-        if (dev < 64) cached_smem[dev] = (int)smem, cached_per_sm[dev] = per_sm;
-    }
+    int per_sm = 1;
+    e = blocks_per_sm(fn, kThreads + 64, smem, &per_sm);
+    if (e != cudaSuccess) return e;
     long long grid = (long long)sm_count() * per_sm;
     if (grid > pairs) grid = pairs;
-    recurrent_pipe_kernel<DK><<<(unsigned)grid, kThreads + 64, smem, stream>>>(p, slices, pairs);
+    recurrent_pipe_kernel<DK, KM><<<(unsigned)grid, kThreads + 64, smem, stream>>>(p, slices, pairs);
     return cudaGetLastError();
 }
 
@@ -1083,15 +1323,8 @@ static cudaError_t launch_long(const Problem &p, cudaStream_t stream) {
     const int slices = (p.dv + kFastRows - 1) / kFastRows;
     const long long grid = (long long)p.B * p.Hv * slices;
     const size_t smem = (size_t)long_layout(p).total_bytes;
-    static int attr_done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = smem_attr((const void *)recurrent_long_kernel<DK>, 120 * 1024);
     if (e != cudaSuccess) return e;
-    if (dev >= 64 || !attr_done[dev]) {
-        e = cudaFuncSetAttribute(recurrent_long_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize, 120 * 1024);
-        if (e != cudaSuccess) return e;
-        if (dev < 64) attr_done[dev] = 1;
-    }
     recurrent_long_kernel<DK><<<(unsigned)grid, kThreads, smem, stream>>>(p, slices);
     return cudaGetLastError();
 }
@@ -1101,15 +1334,19 @@ cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream) {
     const int es = p.act_f16 ? 2 : 4;
     const bool per_key = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
     // the stager's cp.async copies need 16-byte aligned rows
-    const bool rows16 = aligned16(p.q) && aligned16(p.k) && aligned16(p.v) && (p.dv * es) % 16 == 0 &&
-                        (!per_key || aligned16(p.decay)) && (p.rule != kGdn2 || aligned16(p.beta));
+    // the GDN-2 erase-gate rows: the erase-gate input, or the per-key beta
+    const void *xrows = p.erase_gate ? (const void *)p.erase_gate : p.beta;
+    const bool gates16 = (!per_key || aligned16(p.decay)) && (p.rule != kGdn2 || aligned16(xrows)) &&
+                         (p.write_gate == nullptr || aligned16(p.write_gate));
+    const bool rows16 = aligned16(p.q) && aligned16(p.k) && aligned16(p.v) && (p.dv * es) % 16 == 0 && gates16;
+    const bool km = (p.flags & kKMajor) != 0;
+    // key-major state: the decode kernel's consumers hold whole 128 x 128 tiles
     const bool fast = fast_dk && rows16 && aligned16(p.fin) && (p.init == nullptr || aligned16(p.init)) &&
-                      pipe_layout(p).total_bytes <= 200 * 1024;
+                      pipe_layout(p).total_bytes <= 200 * 1024 && (!km || (p.dk == 128 && p.dv == 128));
     // Requests longer than a few token blocks on average: spread the slices of
     // each (request, head) over their own CTAs instead of one persistent CTA.
     const long long avg_len = p.seq_len ? p.seq_len : (p.B ? (long long)p.T / p.B : 0);
-    const bool long_rows = (p.dv * es) % 16 == 0 && aligned16(p.q) && aligned16(p.k) && aligned16(p.v) &&
-                           (!per_key || aligned16(p.decay)) && (p.rule != kGdn2 || aligned16(p.beta));
+    const bool long_rows = (p.dv * es) % 16 == 0 && aligned16(p.q) && aligned16(p.k) && aligned16(p.v) && gates16;
     if (fast_dk && long_rows && avg_len > 4 * kTB && aligned16(p.fin) && (p.init == nullptr || aligned16(p.init))) {
         switch (p.dk) {
             case 32: return launch_long<32>(p, stream);
@@ -1118,12 +1355,13 @@ cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream) {
             default: return launch_long<256>(p, stream);
         }
     }
+    if (fast && km) return launch_pipe<128, true>(p, stream);
     if (fast) {
         switch (p.dk) {
-            case 32: return launch_pipe<32>(p, stream);
-            case 64: return launch_pipe<64>(p, stream);
-            case 128: return launch_pipe<128>(p, stream);
-            default: return launch_pipe<256>(p, stream);
+            case 32: return launch_pipe<32, false>(p, stream);
+            case 64: return launch_pipe<64, false>(p, stream);
+            case 128: return launch_pipe<128, false>(p, stream);
+            default: return launch_pipe<256, false>(p, stream);
         }
     }
     const long long pairs = (long long)p.B * p.Hv;

@@ -9,7 +9,9 @@
  *     S     = S * Diag(alpha)               (decay; rules gated, gated_delta, gdn2)
  *     u     = S kappa                       (retrieval; rules delta, gated_delta, gdn2)
  *     d     = beta_t (v_t - u)              (delta, gated_delta)
- *     d     = v_t - u                       (gdn2; kappa = b_t .* k_t)
+ *     d     = beta_t (w_t .* v_t) - u       (gdn2; kappa = b_t .* k_t; beta_t = 1
+ *                                            when the erase gate rides in beta,
+ *                                            w_t = 1 without a write gate)
  *     d     = v_t                           (linear, gated)
  *     S     = S + d k_t^T
  *     o_t   = scale * S q_t
@@ -18,8 +20,9 @@
  * Outputs, Attributes); "com.microsoft.LinearAttentionGate" (Description);
  * "aclnnRecurrentGatedDeltaRule" (Formula; two-phase workspace query);
  * "gatedDeltaUpdate" (CLIKA runtime: slot_ids slab, raw-gate arm, per-key
- * gate); ONNX issue "Spec gap: LinearAttention (opset 27) cannot represent
- * Gated DeltaNet-2 channel-wise erase gate" (proposal A).
+ * gate, key-major state slab); ONNX issue "Spec gap: LinearAttention
+ * (opset 27) cannot represent Gated DeltaNet-2 channel-wise erase gate"
+ * (proposals A and B, and the write gate of its first display).
  *
  * Conventions for every entry point:
  *  - Every tensor pointer is DEVICE memory owned by the caller, row-major and
@@ -62,8 +65,9 @@ typedef enum gdn_dtype {
     GDN_DTYPE_BF16 = 2 /* named so it can be declined: GDN_ERR_UNSUPPORTED */
 } gdn_dtype;
 
-/* "com.microsoft.GatedDeltaNet", Attributes, update_rule; GDN2 is proposal
- * (A) of the ONNX "Spec gap ... Gated DeltaNet-2" issue. */
+/* "com.microsoft.GatedDeltaNet", Attributes, update_rule; GDN2 is the rule
+ * of the ONNX "Spec gap ... Gated DeltaNet-2" issue (its erase gate in beta,
+ * proposal A, or in erase_gate, proposal B). */
 typedef enum gdn_rule {
     GDN_RULE_LINEAR = 0,      /* no decay, no retrieval: S += v k^T */
     GDN_RULE_GATED = 1,       /* decay only */
@@ -78,12 +82,16 @@ typedef enum gdn_rule {
 #define GDN_FLAG_BETA_SIGMOID 0x4u  /* beta <- sigmoid(beta) in fp32 (beta_activation) */
 #define GDN_FLAG_DECAY_PER_KEY 0x8u /* decay is [.., Hv, dk]: one log-decay per key channel */
 #define GDN_FLAG_BETA_SHARED 0x10u  /* beta is [total_tokens]: one per token, shared by every value head */
+#define GDN_FLAG_STATE_KMAJOR 0x20u /* states are key-major [num_state_rows, Hv, dk, dv] ("gatedDeltaUpdate") */
 
 /* Bits OR-ed into *error_word by the device (never reset by the library). */
 #define GDN_DEVERR_BAD_SLOT 0x1 /* a slot id outside [0, num_state_rows): request skipped */
 #define GDN_DEVERR_TIMEOUT 0x2  /* a bounded wait on an asynchronous copy ran out: the CTA gave up */
 #define GDN_DEVERR_OVERLAP 0x4  /* chunked prefill: the requests' chunks outgrew the workspace, which only
                                    requests sharing tokens can do; the requests past it were skipped */
+#define GDN_DEVERR_DECAY_RANGE 0x8 /* chunked prefill, per-key decay on the tensor cores: a log decay above 0
+                                      (a decay above 1) was given; that path needs decays in (0, 1] and the
+                                      results of the chunks concerned are not valid */
 
 /*
  * One call of the recurrence over a batch of requests.
@@ -121,19 +129,29 @@ typedef enum gdn_rule {
  * Beta.  Present exactly for rules DELTA, GATED_DELTA (shape [total_tokens,
  * Hv], or [total_tokens] with GDN_FLAG_BETA_SHARED: beta's last dimension 1,
  * broadcast over the value heads, as the LinearAttention schema allows) and
- * GDN2 (the erase gate b, [total_tokens, Hv, dk]; GDN_FLAG_BETA_SHARED is
- * rejected there); beta_dtype is F32 or act_dtype; GDN_FLAG_BETA_SIGMOID
- * applies the logistic sigmoid first.
- * For GDN2 the write gate w is folded into v by the caller.
+ * GDN2 (the erase gate b, [total_tokens, Hv, dk], when erase_gate is NULL;
+ * GDN_FLAG_BETA_SHARED is then rejected); beta_dtype is F32 or act_dtype;
+ * GDN_FLAG_BETA_SIGMOID applies the logistic sigmoid first.
+ *
+ * GDN2 gates (ONNX GDN-2 issue).  erase_gate (proposal B) is the erase gate b
+ * as an input of its own, fp32 [total_tokens, Hv, dk], taken as given (no
+ * activation); beta is then the scalar write rate of DELTA / GATED_DELTA
+ * ([total_tokens, Hv], or [total_tokens] with GDN_FLAG_BETA_SHARED; the
+ * sigmoid flag applies to it), so erase_gate = beta * 1 gives GATED_DELTA.
+ * write_gate is the write gate w, fp32 [total_tokens, Hv, dv], multiplied
+ * into v inside the kernels (NULL: w = 1, or already folded into v by the
+ * caller).  Both are GDN2 only (GDN_ERR_INVALID otherwise).
  *
  * State.  initial_state and final_state are fp32, value-major
- * [num_state_rows, Hv, dv, dk].  Request b reads and writes row
+ * [num_state_rows, Hv, dv, dk], or key-major [num_state_rows, Hv, dk, dv]
+ * with GDN_FLAG_STATE_KMAJOR (the slab layout of "gatedDeltaUpdate"; the
+ * recurrence is the same).  Request b reads and writes row
  * slot_ids[b] if slot_ids is non-NULL (the slab of gatedDeltaUpdate), else
  * row b.  initial_state NULL means a zero state.  final_state may equal
  * initial_state (in-place update); otherwise the two must not overlap.  Rows
  * no request names are not touched.  An empty request leaves its final
- * state equal to its initial state ("com.microsoft.GatedDeltaNet", Outputs).  Slot ids must be distinct (caller's contract); a
- * slot id outside [0, num_state_rows) makes every CTA of that request skip it
+ * state equal to its initial state ("com.microsoft.GatedDeltaNet",
+ * Outputs).  Slot ids must be distinct (caller's contract); a slot id outside [0, num_state_rows) makes every CTA of that request skip it
  * and OR GDN_DEVERR_BAD_SLOT into *error_word (if error_word is non-NULL).
  *
  * scale == 0 selects 1/sqrt(dk).  state_update_capacity must be 0 (compact
@@ -169,6 +187,8 @@ typedef struct gdn_problem {
     float *final_state;
     int32_t *error_word; /* optional device int32 */
     const int32_t *seq_lens; /* [batch] or NULL: rank-4 form only (see Token layout) */
+    const float *erase_gate; /* GDN2 only: [total_tokens, Hv, dk] fp32, or NULL (see GDN2 gates) */
+    const float *write_gate; /* GDN2 only: [total_tokens, Hv, dv] fp32, or NULL (see GDN2 gates) */
 } gdn_problem;
 
 /*
@@ -256,16 +276,19 @@ gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *w
  * device memory around the call.
  *
  * The scratch is one static device array of 768 MiB per device (set aside
- * when libgdn loads; this entry point allocates nothing).  Problems whose
+ * when libgdn loads; this entry point allocates nothing).  Each process that
+ * loads libgdn reserves its own 768 MiB on every device it uses, so calls
+ * from different processes never share it.  Problems whose
  * gdn_chunked_prefill_workspace_size() exceeds it are rejected on the host
  * with GDN_ERR_WORKSPACE before anything is enqueued (the long and ragged
- * prefill configurations, about 745-765 MB, fit).  Every call on a device
- * shares the array: two calls in flight at the same time on that device
- * (different streams, threads or processes sharing the context) race on it,
- * so the caller serialises them.  The first call on each device looks the
- * array's address up (cudaGetSymbolAddress) and sets kernel attributes: make
- * it outside any stream capture; later calls can be captured in a CUDA graph.
- * Same arguments, constraints, results and error bits as gdn_chunked_prefill.
+ * prefill configurations, about 745-765 MB, fit).  Within a process, every
+ * call on a device shares the array: two calls in flight at the same time on
+ * that device (different streams or threads) race on it, so the caller
+ * serialises them.  Every call looks the array's address up on the current
+ * device (cudaGetSymbolAddress), so the address stays right after a device
+ * reset; the first call on each device also sets kernel attributes: make it
+ * outside any stream capture.  Same arguments, constraints, results and
+ * error bits as gdn_chunked_prefill.
  */
 gdn_status gdn_chunked_prefill_noalloc(const gdn_problem *p, int32_t chunk_size, gdn_stream stream);
 

@@ -22,7 +22,7 @@ def poison_uncovered(p):
     for t0, t1 in workloads.token_ranges(p):
         covered[t0:t1] = True
     idx = torch.as_tensor(np.nonzero(~covered)[0])
-    for key in ("q", "k", "v", "decay", "beta"):
+    for key in ("q", "k", "v", "decay", "beta", "erase_gate", "write_gate"):
         t = p.get(key)
         if t is not None and len(idx):
             t = t.clone()
@@ -34,7 +34,7 @@ def poison_uncovered(p):
 def to_dev(p):
     d = dict(p)
     for key in ("q", "k", "v", "decay", "gate_bias", "gate_scale", "beta", "cu_seqlens",
-                "slot_ids", "initial_state", "seq_lens"):
+                "slot_ids", "initial_state", "seq_lens", "erase_gate", "write_gate"):
         t = p.get(key)
         if t is not None:
             d[key] = torch.as_tensor(t).to(DEV).contiguous()
@@ -74,20 +74,23 @@ def run(p, path="recurrent", chunk=64, in_place=None, sentinel=float("nan"), err
     if in_place is None:
         in_place = p.get("slot_ids") is not None
     init = d.get("initial_state")
+    sshape = (rows, p["hv"], p["dk"], p["dv"]) if p.get("state_kmajor") else (rows, p["hv"], p["dv"], p["dk"])
     if in_place:
         if init is None:
-            init = torch.zeros(rows, p["hv"], p["dv"], p["dk"], device=DEV)
+            init = torch.zeros(*sshape, device=DEV)
         init = init.clone()
         fin = init
     else:
-        fin = torch.full((rows, p["hv"], p["dv"], p["dk"]), sentinel, dtype=torch.float32, device=DEV)
+        fin = torch.full(sshape, sentinel, dtype=torch.float32, device=DEV)
     kw = dict(q=q, k=k, v=v, o=o, final_state=fin, rule=p["rule"], decay=d.get("decay"),
               beta=d.get("beta"), gate_bias=d.get("gate_bias"), gate_scale=d.get("gate_scale"),
               cu_seqlens=d.get("cu_seqlens"), slot_ids=d.get("slot_ids"), initial_state=init,
               seq_lens=d.get("seq_lens"), beta_shared=p.get("beta_shared", False),
               batch=p["batch"], scale=p.get("scale", 0.0), l2norm_q=p.get("l2norm_q", False),
               l2norm_k=p.get("l2norm_k", False), beta_sigmoid=p.get("beta_sigmoid", False),
-              decay_per_key=p.get("decay_per_key", False), error_word=error_word)
+              decay_per_key=p.get("decay_per_key", False), error_word=error_word,
+              erase_gate=d.get("erase_gate"), write_gate=d.get("write_gate"),
+              state_kmajor=p.get("state_kmajor", False))
     prob = api.make_problem(**kw)
     if path == "recurrent":
         api.gdn_recurrent_step(prob, stream=stream)

@@ -98,6 +98,11 @@ def _call_chunked(p, chunk=64, ws=None, nbytes=0):
      "PER_KEY"),
     (dict(num_state_rows=1), N.GDN_ERR_INVALID, "num_state_rows"),
     (dict(scale=float("inf")), N.GDN_ERR_INVALID, "finite"),
+    (dict(erase_gate=FAKE), N.GDN_ERR_INVALID, "GDN2"),
+    (dict(write_gate=FAKE), N.GDN_ERR_INVALID, "GDN2"),
+    (dict(rule=N.RULES["gdn2"], erase_gate=FAKE + 2), N.GDN_ERR_INVALID, "aligned"),
+    (dict(rule=N.RULES["gdn2"], write_gate=FAKE + 1), N.GDN_ERR_INVALID, "aligned"),
+    (dict(flags=N.FLAG_STATE_KMAJOR << 1), N.GDN_ERR_INVALID, "flag"),
 ])
 def test_recurrent_rejects(over, status, msg):
     p = _problem(**over)

@@ -217,28 +217,32 @@ def test_tiny_fp32_workload():
     _check(p, o, fin, ref_o, ref_fin)
 
 
+@pytest.mark.parametrize("kmajor", [False, True], ids=["vmajor", "kmajor"])
 @pytest.mark.parametrize("L", [1, 4])
-def test_decode_full_size_sampled(L):
+def test_decode_full_size(L, kmajor):
     """256 requests x 32 heads, dk = dv = 128, slab [1024, 32, 128, 128] in place,
-    in the launch configuration the benchmark times; the oracle checks a
-    sample of 24 requests (all heads) and the untouched slab rows."""
+    in the launch configuration the benchmark times: every request against the
+    oracle, every untouched slab row bit for bit.  kmajor: the same slab
+    stored key-major ([1024, 32, dk, dv], "gatedDeltaUpdate")."""
     p = workloads.decode(L)
+    if kmajor:
+        p = dict(p, state_kmajor=True,
+                 initial_state=p["initial_state"].transpose(2, 3).contiguous())
     o, fin, d = run(p)
     torch.cuda.synchronize()
-    sample = list(range(0, 256, 11))
-    ref_o, ref_fin, _ = oracle.run_problem(p, requests=sample, threads=8)
+    # every request, its state row gathered into a compact slab (row j = request j)
+    ref_o, ref_fin, err = oracle.run_problem(p, requests=range(p["batch"]), threads=16)
+    assert err == 0
     og = o_flat(o, p)
-    idx = ~np.isnan(ref_o[:, 0, 0])
-    assert rel_err(og[idx], ref_o[idx]) <= TOL_O["f16"]
-    slots = p["slot_ids"]
-    rows = [int(slots[b]) for b in sample]
-    fg = fin[torch.tensor(rows, device=DEV)].double().cpu().numpy()
-    assert rel_err(fg, ref_fin) <= TOL_STATE
-    touched = set(int(s) for s in slots)
-    untouched = [r for r in range(0, 1024, 7) if r not in touched][:40]
-    ui = torch.tensor(untouched)
-    assert torch.equal(fin[ui.to(DEV)].cpu(), p["initial_state"][ui])
     assert not np.isnan(og).any()
+    assert rel_err(og, ref_o) <= TOL_O["f16"]
+    slots = p["slot_ids"]
+    rows = torch.as_tensor([int(x) for x in slots])
+    fg = fin[rows.to(DEV)].double().cpu().numpy()
+    assert rel_err(fg, ref_fin) <= TOL_STATE
+    touched = set(int(x) for x in slots)
+    untouched = torch.as_tensor([r for r in range(1024) if r not in touched])
+    assert torch.equal(fin[untouched.to(DEV)].cpu(), p["initial_state"][untouched])
 
 
 LONG_CASES = []

@@ -185,13 +185,15 @@ def long_prefill(rule, seed=4, B=4, S=8192, h=16, dk=128, dv=128):
                 gate="raw", beta_dtype="f16")
 
 
-def gdn2(seed=5, B=2, S=4096, h=16, dk=128, dv=128):
+def gdn2(seed=5, B=2, S=4096, h=16, dk=128, dv=128, erase="beta", write_gate="fold"):
     """GDN-2: per-key log decay -softplus(N(0,1)) (raw arm, gate_scale = -1,
     gate_bias = 0), erase gate sigmoid(N(0,1)) per key channel, write gate
-    sigmoid(N(0,1)) folded into v, unit keys, zero state."""
+    sigmoid(N(0,1)) folded into v, unit keys, zero state.  ``erase='input'``
+    passes the erase gate as its own input beside a scalar beta =
+    sigmoid(N(0,1)); ``write_gate='input'`` passes w to the op."""
     return make(seed=seed, B=B, seq_len=S, hq=h, hv=h, dk=dk, dv=dv, act="f16", rule="gdn2",
                 gate="raw", decay_per_key=True, gate_dtype="f32", a_log_range=(0.0, 0.0),
-                dt_bias_range=(0.0, 0.0), write_gate=True)
+                dt_bias_range=(0.0, 0.0), write_gate=write_gate, erase=erase)
 
 
 def token_ranges(p):
