@@ -1,7 +1,8 @@
 """Benchmark of the gated delta rule library on one node.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
-                    [--workload decode-L1|decode-L4|ragged-prefill|long-prefill-<rule>|gdn2]
+                    [--workload decode-L1|decode-L4|decode-L1-kmajor|decode-L4-kmajor|
+                                ragged-prefill|long-prefill-<rule>|gdn2|gdn2-gates]
                     [--no-extra]
 
 A step is one call of the library on one batch of the workload (the decode
@@ -48,8 +49,12 @@ def make_workload(name, seed_offset=0, shrink=1):
     """The named workload; ``shrink`` > 1 divides its request count or
     sequence length (a smaller case of the same kernel, for profiling)."""
     if name.startswith("decode-L"):
-        L = int(name[len("decode-L"):])
-        return workloads.decode(L, seed=2 + seed_offset, B=256 // shrink, num_slots=1024 // shrink), "recurrent"
+        km = name.endswith("-kmajor")
+        L = int(name[len("decode-L"):].split("-")[0])
+        p = workloads.decode(L, seed=2 + seed_offset, B=256 // shrink, num_slots=1024 // shrink)
+        if km:  # the same slab stored key-major, [rows, Hv, dk, dv]
+            p = dict(p, state_kmajor=True, initial_state=p["initial_state"].transpose(2, 3).contiguous())
+        return p, "recurrent"
     if name == "ragged-prefill":
         return workloads.ragged_prefill(seed=3 + seed_offset, total=16384 // shrink,
                                         max_len=4096 // shrink), "chunked"
@@ -58,6 +63,8 @@ def make_workload(name, seed_offset=0, shrink=1):
                                       S=8192 // shrink), "chunked"
     if name == "gdn2":
         return workloads.gdn2(seed=5 + seed_offset, S=4096 // shrink), "chunked"
+    if name == "gdn2-gates":  # erase gate as its own input beside a scalar beta, write gate passed in
+        return workloads.gdn2(seed=5 + seed_offset, S=4096 // shrink, erase="input", write_gate="input"), "chunked"
     raise SystemExit("unknown workload " + name)
 
 
@@ -69,7 +76,7 @@ def algorithmic_bytes(p):
     """Each input read once, each output written once, the touched state rows
     read (if an initial state is given) and written once."""
     b = sum(_nbytes(p.get(k)) for k in ("q", "k", "v", "decay", "gate_bias", "gate_scale", "beta",
-                                         "cu_seqlens", "slot_ids"))
+                                         "erase_gate", "write_gate", "cu_seqlens", "slot_ids"))
     b += _nbytes(p["v"])  # o, same shape and dtype as v
     tile = p["batch"] * p["hv"] * p["dv"] * p["dk"] * 4
     b += tile * (2 if p.get("initial_state") is not None else 1)
@@ -92,7 +99,68 @@ def tokens(p):
 
 
 # ------------------------------------------------------------------ clocks
-class ClockSampler:
+class NvmlClocks:
+    """Samples the SM clock and the clock event reasons through NVML (ctypes,
+    read-only queries) every millisecond in a thread, so that even a timed
+    region of a few milliseconds holds several samples."""
+    # nvmlClocksEventReason* bits of the NVML API
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, device_index=0):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle for " + uuid)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.samples = []
+        self.run = False
+
+    def _one(self):
+        ct = self.ct
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(mhz)) != 0:  # NVML_CLOCK_SM
+            return None
+        if self.reasons_fn(self.dev, ct.byref(rs)) != 0:
+            rs.value = 0
+        return mhz.value, rs.value
+
+    def _loop(self):
+        while self.run:
+            x = self._one()
+            if x:
+                self.samples.append(x)
+            time.sleep(0.001)
+
+    def start(self):
+        self.samples = []
+        self.run = True
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 1.0:
+            time.sleep(0.0005)
+
+    def stop(self):
+        self.run = False
+        self.thread.join(timeout=2)
+        mx = self.ct.c_uint()
+        smax = mx.value if self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, self.ct.byref(mx)) == 0 else None
+        sm = [m for m, _ in self.samples]
+        reasons = sorted(nm for nm, bit in self.REASONS.items() if any(r & bit for _, r in self.samples))
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(sm), "source": "nvml, 1 ms"}
+
+
+class SmiClocks:
+    """The same from nvidia-smi (20 ms samples), where NVML cannot be loaded."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -156,14 +224,23 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, 20 ms"}
+
+
+
+
+def clock_sampler(device_index=0):
+    try:
+        return NvmlClocks(device_index)
+    except Exception:
+        return SmiClocks(device_index)
 
 
 # ------------------------------------------------------------------ device runs
 def to_dev(p, dev):
     d = dict(p)
-    for k in ("q", "k", "v", "decay", "gate_bias", "gate_scale", "beta", "cu_seqlens", "slot_ids",
-              "initial_state"):
+    for k in ("q", "k", "v", "decay", "gate_bias", "gate_scale", "beta", "erase_gate", "write_gate",
+              "cu_seqlens", "slot_ids", "initial_state"):
         if p.get(k) is not None:
             d[k] = p[k].to(dev).contiguous()
     return d
@@ -185,7 +262,9 @@ def build_problem(api, p, d, o, fin):
                             scale=p.get("scale", 0.0), l2norm_q=p.get("l2norm_q", False),
                             l2norm_k=p.get("l2norm_k", False),
                             beta_sigmoid=p.get("beta_sigmoid", False),
-                            decay_per_key=p.get("decay_per_key", False))
+                            decay_per_key=p.get("decay_per_key", False),
+                            erase_gate=d.get("erase_gate"), write_gate=d.get("write_gate"),
+                            state_kmajor=p.get("state_kmajor", False))
 
 
 def launch(api, prob, path, stream):
@@ -202,7 +281,8 @@ def prepare(api, p, path, dev):
     if p.get("slot_ids") is not None:
         fin = d["initial_state"]  # the slab, updated in place
     else:
-        fin = torch.empty(rows, p["hv"], p["dv"], p["dk"], dtype=torch.float32, device=dev)
+        shape = (rows, p["hv"], p["dk"], p["dv"]) if p.get("state_kmajor") else (rows, p["hv"], p["dv"], p["dk"])
+        fin = torch.empty(*shape, dtype=torch.float32, device=dev)
     prob = build_problem(api, p, d, o, fin)
     prob._ws_buf = None
     if path == "chunked":
@@ -236,7 +316,7 @@ def time_device(api, prob, path, steps, warmup, stream, barrier):
 def time_e2e(api, p, d, prob, path, steps, warmup, stream, dev):
     """Every step: pinned host -> device copies of the step's inputs, the call,
     and a device -> host copy of the output."""
-    names = [k for k in ("q", "k", "v", "decay", "beta", "cu_seqlens", "slot_ids")
+    names = [k for k in ("q", "k", "v", "decay", "beta", "erase_gate", "write_gate", "cu_seqlens", "slot_ids")
              if p.get(k) is not None]
     host = {k: p[k].contiguous().pin_memory() for k in names}
     o_host = torch.empty(p["v"].shape, dtype=p["v"].dtype).pin_memory()
@@ -270,13 +350,16 @@ def kernel_name(p, path):
     def token_serial():
         # average request length above four staged token blocks (of 8): the long-request kernel
         L = p.get("seq_len") or p["total_tokens"] // max(p["batch"], 1)
-        return ("recurrent_long_kernel<%d>" if L > 32 else "recurrent_pipe_kernel<%d>") % p["dk"]
+        if L > 32:
+            return "recurrent_long_kernel<%d>" % p["dk"]
+        return "recurrent_pipe_kernel<%d,%s>" % (p["dk"], "true" if p.get("state_kmajor") else "false")
     if path == "recurrent":
         return token_serial()
     per_key = p.get("decay_per_key") and p["rule"] in ("gated", "gated_delta", "gdn2")
     tc_shape = p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16"
+    erase = p.get("erase_gate") if p.get("erase_gate") is not None else p.get("beta")
     f32_gates = (p.get("decay") is None or p["decay"].dtype == torch.float32 or not per_key) and \
-        (p["rule"] != "gdn2" or p["beta"].dtype == torch.float32)
+        (p["rule"] != "gdn2" or erase.dtype == torch.float32)
     if tc_shape and f32_gates and (p["rule"] == "gdn2" or (per_key and p["rule"] == "gated_delta")):
         return "chunk_prepare_perkey_kernel<%d>+chunk_chain_kernel<2>" % int(p["rule"] == "gdn2")
     if per_key:
@@ -408,7 +491,7 @@ def workload_config(p, args, note=None):
     cfg = {"workload": args.workload, "batch": p["batch"], "total_tokens": p["total_tokens"],
            "seq_len": p.get("seq_len") or None, "Hq": p["hq"], "Hv": p["hv"], "dk": p["dk"],
            "dv": p["dv"], "rule": p["rule"], "act_dtype": p["act_dtype"],
-           "state": "fp32 V-major", "parallelism": "replicas" if args.gpus > 1 else "single-gpu",
+           "state": "fp32 " + ("K-major" if p.get("state_kmajor") else "V-major"), "parallelism": "replicas" if args.gpus > 1 else "single-gpu",
            "l2_policy": "inputs larger than L2 (touched state > 129 MB)"}
     if p.get("num_slots") and p.get("slot_ids") is not None:
         cfg["slab_rows"] = p["num_slots"]
@@ -417,10 +500,43 @@ def workload_config(p, args, note=None):
     return cfg
 
 
-def extra_workloads(api, dev, stream, names, steps=20, warmup=5):
-    """Device throughput of the other workloads (one pass each), for context."""
+def roofline(p, path, workload, kern_ms):
+    """Algorithmic bytes (and flops) per launch over the mean launch time,
+    against the measured peaks."""
+    hbm, tc, tc_s, src = peaks()
+    ab = algorithmic_bytes(p)
+    achieved = ab / (kern_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": ncu_traffic(workload, path, kernel_name(p, path)), "kernel": kernel_name(p, path),
+            "algorithmic_bytes_per_launch": ab, "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)"}
+    if path == "chunked":
+        af = algorithmic_flops(p)
+        roof["tensor_achieved_tflops"] = af / (kern_ms * 1e-3) / 1e12
+        roof["tensor_frac"] = roof["tensor_achieved_tflops"] / tc
+        roof["algorithmic_flops_per_launch"] = af
+    return roof
+
+
+def cpu_baseline(p, budget_s, single_thread_budget=None):
+    cores = cpu_cores()
+    rate, sample, stoks, sdt = oracle_rate(p, budget_s, cores)
+    out = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": "%d of %d requests, all %d value heads (%d tokens, %.1f s), fp64"
+                     % (len(sample), p["batch"], p["hv"], stoks, sdt)}
+    if single_thread_budget:
+        r1, s1, t1, d1 = oracle_rate(p, single_thread_budget, 1)
+        out["single_thread"] = {"value": r1, "unit": "tokens/s", "cores": 1,
+                                "sample": "%d of %d requests, all %d value heads (%d tokens, %.1f s), fp64"
+                                          % (len(s1), p["batch"], p["hv"], t1, d1)}
+    return out
+
+
+def extra_workloads(api, dev, stream, names, with_cpu=True, region_s=0.2, warmup=5):
+    """Each other workload measured like the headline one: device time of a
+    timed region of about region_s seconds with clocks sampled inside it, its
+    roofline, an end-to-end figure with host copies, and the CPU oracle on a
+    bounded sample of it."""
     out = {}
-    hbm, tc, tc_s, _ = peaks()
     for name in names:
         p, path = make_workload(name)
         try:
@@ -428,17 +544,22 @@ def extra_workloads(api, dev, stream, names, steps=20, warmup=5):
         except Exception as e:  # an unsupported configuration is reported, not hidden
             out[name] = {"error": str(e)[:200]}
             continue
-        total, per = time_device(api, prob, path, steps, warmup, stream, lambda: None)
+        est, _ = time_device(api, prob, path, 5, warmup, stream, lambda: None)
+        steps = int(min(2000, max(20, math.ceil(region_s * 1e3 / max(est / 5, 1e-3)))))
+        clocks = clock_sampler(dev.index or 0)
+        clocks.start()
+        total, per = time_device(api, prob, path, steps, 3, stream, lambda: None)
+        clk = clocks.stop()
         ms = total / steps
         toks = tokens(p)
-        ab = algorithmic_bytes(p)
-        ent = {"tokens_per_s": toks / (ms * 1e-3), "ms_per_call": ms,
-               "hbm_frac_of_measured": ab / (ms * 1e-3) / 1e9 / hbm,
-               "algorithmic_bytes": ab, "path": path}
-        if path == "chunked":
-            af = algorithmic_flops(p)
-            ent["tensor_frac_of_measured"] = af / (ms * 1e-3) / 1e12 / tc
-            ent["algorithmic_flops"] = af
+        ent = {"tokens_per_s": toks / (ms * 1e-3), "ms_per_call": ms, "steps": steps, "path": path,
+               "roofline": roofline(p, path, name, statistics.fmean(per)), "clocks": clk,
+               "gpu_launches": steps * launches_per_call(p, path)}
+        e2e_ms, h2d, d2h = time_e2e(api, p, d, prob, path, 10, 3, stream, dev)
+        ent["e2e"] = {"value": toks / (e2e_ms / 10 * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h}
+        if with_cpu:
+            ent["cpu_baseline"] = cpu_baseline(p, 1.0)
         out[name] = ent
         del d, o, fin, prob
         torch.cuda.empty_cache()
@@ -487,7 +608,7 @@ def main():
     d, o, fin, prob = prepare(api, p, path, dev)
     stream = torch.cuda.current_stream(dev)
 
-    clocks = ClockSampler(local)
+    clocks = clock_sampler(local)
     clocks.start()
     total_ms, per_launch = time_device(api, prob, path, args.steps, args.warmup, stream, barrier)
     clk = clocks.stop()
@@ -508,18 +629,7 @@ def main():
         e2e = {"value": toks * world / (e2e_ms / e2e_steps * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
-    hbm, tc, tc_s, src = peaks()
-    kern_ms = statistics.fmean(per_launch)
-    ab = algorithmic_bytes(p)
-    achieved = ab / (kern_ms * 1e-3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "traffic": ncu_traffic(args.workload, path, kernel_name(p, path)),
-            "kernel": kernel_name(p, path),
-            "algorithmic_bytes_per_launch": ab, "peak_source": src + " (MEASURED_PEAKS.json hbm_gbs)"}
-    if path == "chunked":
-        af = algorithmic_flops(p)
-        roof["tensor_achieved_tflops"] = af / (kern_ms * 1e-3) / 1e12
-        roof["tensor_frac"] = roof["tensor_achieved_tflops"] / tc
+    roof = roofline(p, path, args.workload, statistics.fmean(per_launch))
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -534,19 +644,16 @@ def main():
         if args.shrink > 1:
             line["config"]["shrink"] = args.shrink
     if rank == 0 and not args.no_cpu:
-        cores = cpu_cores()
-        rate, sample, stoks, sdt = oracle_rate(p, 3.0, cores)
-        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                "sample": "%d of %d requests, all %d value heads (%d tokens, %.1f s)"
-                                          % (len(sample), p["batch"], p["hv"], stoks, sdt)}
+        line["cpu_baseline"] = cpu_baseline(p, 3.0, single_thread_budget=2.0)
     if rank == 0:
         if not args.no_extra and world == 1:
-            names = [n for n in ("decode-L1", "decode-L4", "ragged-prefill", "long-prefill-linear",
-                                 "long-prefill-gated", "long-prefill-delta",
-                                 "long-prefill-gated_delta", "gdn2") if n != args.workload]
+            names = [n for n in ("decode-L1", "decode-L4", "decode-L1-kmajor", "decode-L4-kmajor",
+                                 "ragged-prefill", "long-prefill-linear", "long-prefill-gated",
+                                 "long-prefill-delta", "long-prefill-gated_delta", "gdn2", "gdn2-gates")
+                     if n != args.workload]
             del d, o, fin, prob
             torch.cuda.empty_cache()
-            line["other_workloads"] = extra_workloads(api, dev, stream, names)
+            line["other_workloads"] = extra_workloads(api, dev, stream, names, with_cpu=not args.no_cpu)
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

@@ -378,13 +378,20 @@ struct PipeLayout {
     int ring_bytes;
     int red_bytes;    // key-major consumers: per-warp partial sums, two buffers
     int stages;       // state slices in flight
+    int nbuf;         // staging buffers
+    int nstg;         // stager warps (each with its own landing area)
     int total_bytes;
     int xes;          // bytes per element of the GDN-2 erase-gate rows
     bool has_a, has_x, has_w;
 };
 
-// Key-major state in the decode kernel: one CTA per SM with twice the ring.
+// Key-major state in the decode kernel: one CTA per SM with twice the ring
+// (when the staging area leaves room for it), two stager warps taking
+// alternate pairs and three staging buffers, so that one CTA stages pairs as
+// fast as the two CTAs per SM of the value-major kernel.
 constexpr int kStagesKM = 8;
+constexpr int kMaxStagers = 2;
+constexpr int kMaxStageBufs = 3;
 
 __host__ __device__ inline PipeLayout pipe_layout(const Problem &p) {
     PipeLayout L;
@@ -400,11 +407,18 @@ __host__ __device__ inline PipeLayout pipe_layout(const Problem &p) {
     L.raw_bytes = kTB * (2 * p.dk * es + p.dv * es + (L.has_a ? p.dk * des : 0) + (L.has_x ? p.dk * L.xes : 0) +
                          (L.has_w ? p.dv * 4 : 0));
     L.raw_bytes = (L.raw_bytes + 15) & ~15;
-    L.stages = km ? kStagesKM : kStages;
-    // a slice is 32 stored rows: value rows of dk floats, or key rows of dv floats (key-major)
-    L.ring_bytes = L.stages * kFastRows * (km ? p.dv : p.dk) * 4;
+    L.nbuf = km ? kMaxStageBufs : 2;
+    L.nstg = km ? kMaxStagers : 1;
     L.red_bytes = km ? 2 * (kThreads / 32) * 32 * 32 : 0;
-    L.total_bytes = L.ring_bytes + 2 * L.stage_floats * 4 + L.raw_bytes + L.red_bytes + (2 * L.stages + 4) * 8;
+    // a slice is 32 stored rows: value rows of dk floats, or key rows of dv floats (key-major)
+    const int slice_bytes = kFastRows * (km ? p.dv : p.dk) * 4;
+    auto total = [&](int stages) {
+        return stages * slice_bytes + L.nbuf * L.stage_floats * 4 + L.nstg * L.raw_bytes + L.red_bytes +
+               (2 * stages + 2 * L.nbuf) * 8;
+    };
+    L.stages = km && total(kStagesKM) <= 200 * 1024 ? kStagesKM : kStages;
+    L.ring_bytes = L.stages * slice_bytes;
+    L.total_bytes = total(L.stages);
     return L;
 }
 
@@ -453,11 +467,10 @@ __device__ __forceinline__ float bits_to_f(uint32_t x, int f16) {
 __device__ __forceinline__ void copy_token_rows(unsigned char *dst, const void *src, size_t first, size_t step,
                                                 int row_bytes, int L, int lane) {
     const int ch = row_bytes / 16;
-    const unsigned char *s0 = static_cast<const unsigned char *>(src);
-    for (int idx = lane; idx < L * ch; idx += 32) {
-        const int tt = idx / ch, c = idx % ch;
-        ptx::cp_async16(dst + tt * row_bytes + 16 * c, s0 + (first + (size_t)tt * step) * row_bytes + 16 * c, 16);
-    }
+    const unsigned char *s0 = static_cast<const unsigned char *>(src) + first * row_bytes;
+    const size_t sstep = step * row_bytes;
+    for (int tt = 0; tt < L; ++tt, dst += row_bytes, s0 += sstep)
+        for (int c = lane; c < ch; c += 32) ptx::cp_async16(dst + 16 * c, s0 + 16 * c, 16);
 }
 
 // The stager's copies for one pair with 0 < L <= kTB tokens starting at t0:
@@ -754,15 +767,16 @@ __device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s
             wa = f4_fma(q4.x, S[sl][0], wa), wb = f4_fma(q4.y, S[sl][1], wb);
             wa = f4_fma(q4.z, S[sl][2], wa), wb = f4_fma(q4.w, S[sl][3], wb);
         }
+        // [u partials of the 8 warps][w partials]: a warp's loads are 512 contiguous bytes
         float4 *rb = red + (tok & 1) * (2 * kThreads);
-        rb[2 * (warp * 32 + lane)] = f4_add(ua, ub);
-        rb[2 * (warp * 32 + lane) + 1] = f4_add(wa, wb);
+        rb[warp * 32 + lane] = f4_add(ua, ub);
+        rb[kThreads + warp * 32 + lane] = f4_add(wa, wb);
         ptx::named_bar_sync(2, kThreads);
-        float4 U = rb[2 * lane], W = rb[2 * lane + 1];
+        float4 U = rb[lane], W = rb[kThreads + lane];
 #pragma unroll
         for (int w2 = 1; w2 < kThreads / 32; ++w2) {
-            U = f4_add(U, rb[2 * (w2 * 32 + lane)]);
-            W = f4_add(W, rb[2 * (w2 * 32 + lane) + 1]);
+            U = f4_add(U, rb[w2 * 32 + lane]);
+            W = f4_add(W, rb[kThreads + w2 * 32 + lane]);
         }
         float cn = c * s.alpha[tt];  // alpha is 1 without scalar decay
         const float bt = s.beta[tt], kq = s.kq[tt];
@@ -815,10 +829,9 @@ __device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s
 
 // The key-major consumer side of one (request, head) pair.  `j` counts ring
 // uses (set to -1 if a wait runs out); `tok` as in apply_tokens_km.
-template <int NST>
 __device__ __forceinline__ void consume_tile_km(const Problem &p, const Stage &st, const float *ring, uint64_t *full,
                                                 uint64_t *empty, float4 *red, int &j, int &tok, int row, int h,
-                                                int qh, int t0, int t1, int tid, int warp, int lane) {
+                                                int qh, int t0, int t1, int tid, int warp, int lane, int NST) {
     constexpr int kSlice = kFastRows * 128;
     float4 S[4][4];
 #pragma unroll
@@ -860,20 +873,23 @@ __device__ __forceinline__ void consume_tile_km(const Problem &p, const Stage &s
 }
 
 template <int DK, bool KM>
-__global__ void __launch_bounds__(kThreads + 64, KM ? 1 : 2) recurrent_pipe_kernel(Problem p, int slices, int pairs) {
+__global__ void __launch_bounds__(kThreads + 32 + 32 * (KM ? kMaxStagers : 1), KM ? 1 : 2)
+    recurrent_pipe_kernel(Problem p, int slices, int pairs) {
     // KM: key-major state (dk = dv = DK = 128); a slice is 32 key rows
-    constexpr int NST = KM ? kStagesKM : kStages;
+    constexpr int NSTG = KM ? kMaxStagers : 1;   // stager warps
+    constexpr int NBUF = KM ? kMaxStageBufs : 2; // staging buffers
     constexpr int kSlice = kFastRows * DK;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const PipeLayout Ly = pipe_layout(p);
+    const int NST = Ly.stages;
     float *ring = reinterpret_cast<float *>(smem_raw);
     float *stage_base = reinterpret_cast<float *>(smem_raw + Ly.ring_bytes);
-    unsigned char *raw = smem_raw + Ly.ring_bytes + 2 * Ly.stage_floats * 4;
-    float4 *red = reinterpret_cast<float4 *>(raw + Ly.raw_bytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(raw + Ly.raw_bytes + Ly.red_bytes);
+    unsigned char *raw0 = smem_raw + Ly.ring_bytes + NBUF * Ly.stage_floats * 4;
+    float4 *red = reinterpret_cast<float4 *>(raw0 + NSTG * Ly.raw_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw0 + NSTG * Ly.raw_bytes + Ly.red_bytes);
     uint64_t *empty = full + NST;
     uint64_t *tok_full = empty + NST;
-    uint64_t *tok_empty = tok_full + 2;
+    uint64_t *tok_empty = tok_full + NBUF;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kCW = kThreads / 32;  // consumer warps
     if (tid == 0) {
@@ -881,7 +897,7 @@ __global__ void __launch_bounds__(kThreads + 64, KM ? 1 : 2) recurrent_pipe_kern
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], kCW);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NBUF; ++s) {
             ptx::mbar_init(&tok_full[s], 1);
             ptx::mbar_init(&tok_empty[s], kCW);
         }
@@ -918,7 +934,10 @@ __global__ void __launch_bounds__(kThreads + 64, KM ? 1 : 2) recurrent_pipe_kern
         }
         return;
     }
-    if (warp == kCW + 1) {  // ---- token stager
+    if (warp > kCW) {  // ---- token stagers: stager s takes the CTA's pairs k = s, s + NSTG, ...
+        const int sid = warp - kCW - 1;
+        unsigned char *raw = raw0 + sid * Ly.raw_bytes;
+        const int gstep = NSTG * (int)gridDim.x;
         // request range and slot of the next pair are read one pair ahead
         auto header = [&](int pair, int &row, int &t0, int &t1) {
             const int b = pair / p.Hv, h = pair % p.Hv;
@@ -926,13 +945,15 @@ __global__ void __launch_bounds__(kThreads + 64, KM ? 1 : 2) recurrent_pipe_kern
             request_range(p, b, t0, t1);
         };
         int nrow = -1, nt0 = 0, nt1 = 0;
-        if (blockIdx.x < pairs) header(blockIdx.x, nrow, nt0, nt1);
-        int k = 0;
-        for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x, ++k) {
-            const int buf = k & 1;
+        const int first = blockIdx.x + sid * (int)gridDim.x;
+        if (first < pairs) header(first, nrow, nt0, nt1);
+        int k = sid;
+        for (int pair = first; pair < pairs; pair += gstep, k += NSTG) {
+            // buffer k % NBUF, used for the (k / NBUF)-th time
+            const int buf = k % NBUF;
             const int row = nrow, t0 = nt0, t1 = nt1;
-            if (pair + (int)gridDim.x < pairs) header(pair + gridDim.x, nrow, nt0, nt1);
-            if (!ptx::mbar_wait(&tok_empty[buf], ((k >> 1) & 1) ^ 1)) {
+            if (pair + gstep < pairs) header(pair + gstep, nrow, nt0, nt1);
+            if (!ptx::mbar_wait(&tok_empty[buf], ((k / NBUF) & 1) ^ 1)) {
                 if (p.err && lane == 0) atomicOr(p.err, 2);
                 return;
             }
@@ -962,8 +983,8 @@ __global__ void __launch_bounds__(kThreads + 64, KM ? 1 : 2) recurrent_pipe_kern
     const int rloc = warp * 4 + (lane >> 3);
     int j = 0, k = 0, tok = 0;
     for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x, ++k) {
-        const int buf = k & 1;
-        if (!ptx::mbar_wait(&tok_full[buf], (k >> 1) & 1)) {
+        const int buf = k % NBUF;
+        if (!ptx::mbar_wait(&tok_full[buf], (k / NBUF) & 1)) {
             if (p.err && tid == 0) atomicOr(p.err, 2);
             return;
         }
@@ -977,7 +998,7 @@ __global__ void __launch_bounds__(kThreads + 64, KM ? 1 : 2) recurrent_pipe_kern
         // R state slices per pass (2 when the slice count is even): the staged
         // key/query loads are shared and the rows' reduction chains interleave
         if (KM)
-            consume_tile_km<NST>(p, st, ring, full, empty, red, j, tok, row, h, qh, t0, t1, tid, warp, lane);
+            consume_tile_km(p, st, ring, full, empty, red, j, tok, row, h, qh, t0, t1, tid, warp, lane, NST);
         else if ((slices & 1) == 0)
             consume_slices<DK, 2>(p, st, ring, full, empty, j, slices, row, h, qh, t0, t1, tid, lane, cg, rloc);
         else
@@ -1310,11 +1331,12 @@ static cudaError_t launch_pipe(const Problem &p, cudaStream_t stream) {
     cudaError_t e = smem_attr(fn, 220 * 1024);
     if (e != cudaSuccess) return e;
     int per_sm = 1;
-    e = blocks_per_sm(fn, kThreads + 64, smem, &per_sm);
+    const int threads = kThreads + 32 + 32 * (KM ? kMaxStagers : 1);
+    e = blocks_per_sm(fn, threads, smem, &per_sm);
     if (e != cudaSuccess) return e;
     long long grid = (long long)sm_count() * per_sm;
     if (grid > pairs) grid = pairs;
-    recurrent_pipe_kernel<DK, KM><<<(unsigned)grid, kThreads + 64, smem, stream>>>(p, slices, pairs);
+    recurrent_pipe_kernel<DK, KM><<<(unsigned)grid, threads, smem, stream>>>(p, slices, pairs);
     return cudaGetLastError();
 }
 
