@@ -23,13 +23,20 @@ constexpr int TC_C = 64;  // tokens per chunk
 // Chunk operand image: the state-independent operands of one (chunk, value
 // head), in shared-memory layout (128-byte swizzle; 64 fp16 per 128-byte row;
 // 16-byte chunk c of row r stored at chunk position c ^ (r % 8)):
-//   E   [2 j-blocks][128 i][64 j]   B operand, N-major (row = K index i)
-//   Q'  [2 i-blocks][64 t][64 i]    B operand, K-major (row = N index t)
-//   U   [2 v-blocks][64 t][64 v]    A operand of U^T, M-major (row = K index t)
-//   P   [64 r][64 t]                B operand, K-major (row = N index r)
-//   Kt  [2 j-blocks][64 t][64 j]    B operand, N-major (row = K index t)
-constexpr int IM_E = 0, IM_Q = 32768, IM_U = 49152, IM_P = 65536, IM_KT = 73728;
+//   EQ  [2 i-blocks][192 rows][64 i] B operand, K-major: rows 0-127 hold E^T
+//                                    (row = N index j), rows 128-191 hold Q'
+//                                    (row = N index t), so that S E and S Q'^T
+//                                    are one N = 192 product over the shared A
+//   U   [2 v-blocks][64 t][64 v]     A operand of U^T, M-major (row = K index t)
+//   P   [64 r][64 t]                 B operand, K-major (row = N index r)
+//   Kt  [2 j-blocks][64 t][64 j]     B operand, N-major (row = K index t)
+// (The gated rule keeps e^{G_C}, one float, at the start of the EQ area.)
+constexpr int IM_EQ = 0, IM_EQ_BLK = 24576, IM_EQ_Q = 16384;
+constexpr int IM_U = 49152, IM_P = 65536, IM_KT = 73728;
 constexpr int IM_BYTES = 90112;
+// byte offsets of i-block b of E^T and of Q'
+__host__ __device__ constexpr int im_e(int b) { return IM_EQ + b * IM_EQ_BLK; }
+__host__ __device__ constexpr int im_q(int b) { return IM_EQ + b * IM_EQ_BLK + IM_EQ_Q; }
 
 // writes 8 consecutive fp16 values (one 16-byte chunk) of row `row`, chunk
 // `ch` (0..7) of a 64-column block

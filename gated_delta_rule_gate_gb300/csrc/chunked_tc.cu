@@ -281,6 +281,14 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
         const uint32_t aKQ = ptx::smem_u32(sm + rKQ), aV = ptx::smem_u32(sm + rV);
         const uint32_t aKt = ptx::smem_u32(sm + rKt), aP = ptx::smem_u32(sm + rP);
         const uint32_t aTb = ptx::smem_u32(sm + rTb), aTa = ptx::smem_u32(sm + rTa);
+        // shared-memory descriptors built once; each product advances them (desc_adv)
+        const uint64_t d_aKQ = tc::desc_sw128(aKQ);
+        const uint64_t d_aKQ_16384 = tc::desc_sw128(aKQ, 16384);
+        const uint64_t d_aKt_8192 = tc::desc_sw128(aKt, 8192);
+        const uint64_t d_aP = tc::desc_sw128(aP);
+        const uint64_t d_aTa = tc::desc_sw128(aTa);
+        const uint64_t d_aTb = tc::desc_sw128(aTb);
+        const uint64_t d_aV_8192 = tc::desc_sw128(aV, 8192);
         bool ok = true;
         uint32_t ph = 0;
         int i = 0;
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t o = (s >> 2) * 16384 + (s & 3) * 32;
-                    tc::mma_f16(tmem, tc::desc_sw128(aKQ + o), tc::desc_sw128(aKQ + o), tc::idesc_f16(128, 128), s > 0);
+                    tc::mma_f16(tmem, tc::desc_adv(d_aKQ, o), tc::desc_adv(d_aKQ, o), tc::idesc_f16(128, 128), s > 0);
                 }
                 tc::commit(bar1);
             }
@@ -362,14 +370,14 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 *reinterpret_cast<uint4 *>(sm + rKt + io) =
                     scale_chunk(*reinterpret_cast<const uint4 *>(sm + kq_off(tr, ch, false)), F[fKF + tr]);
                 if (!RETR) {  // (U = V: the chain loads it from the value input)
-                    *reinterpret_cast<uint4 *>(dst + IM_Q + io) =
+                    *reinterpret_cast<uint4 *>(dst + im_q(ch >> 3) + sw(tr, ch & 7)) =
                         scale_chunk(*reinterpret_cast<const uint4 *>(sm + kq_off(tr, ch, true)), F[fQF + tr]);
                 }
             }
             tc::fence_async_smem();
             if (!RETR) {
                 // the gated rule's chain scales the state by e^{G_C} itself: only that goes to the image
-                if (decay && tid == 0) *reinterpret_cast<float *>(dst + IM_E) = __expf(F[fG + TC_C - 1]);
+                if (decay && tid == 0) *reinterpret_cast<float *>(dst + IM_EQ) = __expf(F[fG + TC_C - 1]);
                 ptx::named_bar_sync(3, PR_WORK);
                 if (tid == 0) {
                     ptx::bulk_s2g(dst + IM_KT, sm + rKt, 16384);
@@ -455,9 +463,9 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 // U = Tb V -> [0, 128) and Wn = Ta' K -> [128, 256): M = 64, N = 128, K = 64
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
-                    tc::mma_f16(tmem, tc::desc_sw128(aTb + s * 32), tc::desc_sw128(aV + s * 2048, 8192),
+                    tc::mma_f16(tmem, tc::desc_adv(d_aTb, s * 32), tc::desc_adv(d_aV_8192, s * 2048),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
-                    tc::mma_f16(tmem + 128, tc::desc_sw128(aTa + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
+                    tc::mma_f16(tmem + 128, tc::desc_adv(d_aTa, s * 32), tc::desc_adv(d_aKQ_16384, s * 2048),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
                 }
                 tc::commit(bar2);
@@ -489,15 +497,16 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 ptx::bulk_s2g(dst + IM_U, sm + rV, 16384);
                 ptx::bulk_commit();
                 tc::fence_after();
-                // Wn^T Kt -> [0, 128): M = 128 (i), N = 128 (j), K = 64 (t), both operands M/N-major
+                // Kt^T Wn = (Wn^T Kt)^T -> [0, 128): M = 128 (j), N = 128 (i), K = 64 (t), both
+                // operands M/N-major (E^T, the K-major B operand of the chain's S E)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem, tc::desc_sw128(aKQ + s * 2048, 16384), tc::desc_sw128(aKt + s * 2048, 8192),
+                    tc::mma_f16(tmem, tc::desc_adv(d_aKt_8192, s * 2048), tc::desc_adv(d_aKQ_16384, s * 2048),
                                 tc::idesc_f16(128, 128, true, true), s > 0);
                 // P Wn -> [128, 256): M = 64 (r), N = 128 (i), K = 64 (t)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem + 128, tc::desc_sw128(aP + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
+                    tc::mma_f16(tmem + 128, tc::desc_adv(d_aP, s * 32), tc::desc_adv(d_aKQ_16384, s * 2048),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
                 tc::commit(bar3);
             }
@@ -531,12 +540,13 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 // copy of U has read the value tile
                 ptx::bulk_wait_read();
                 ptx::mbar_arrive(tfree);
-                ptx::bulk_s2g(dst + IM_Q, sm + rKt, 16384);
+                ptx::bulk_s2g(dst + im_q(0), sm + rKt, 8192);
+                ptx::bulk_s2g(dst + im_q(1), sm + rKt + 8192, 8192);
                 ptx::bulk_commit();
             }
             {
-                // E = Wn^T Kt + (e^{G_C} - 1) I: row i = 32 q + lane, columns [64 hh, 64 hh + 64),
-                // staged in the At region
+                // E^T = Kt^T Wn + (e^{G_C} - 1) I: row j = 32 q + lane, columns i in
+                // [64 hh, 64 hh + 64), staged in the At region as [2 i-blocks][128 j][64 i]
                 const int ii = 32 * q + lane;
                 float v[64];
                 tc::ld64(tmem + lane_off + 64 * hh, v);
@@ -559,7 +569,8 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             tc::fence_before();
             ptx::named_bar_sync(3, PR_WORK);
             if (tid == 0) {
-                ptx::bulk_s2g(dst + IM_E, sm + rAt, 32768);
+                ptx::bulk_s2g(dst + im_e(0), sm + rAt, 16384);
+                ptx::bulk_s2g(dst + im_e(1), sm + rAt + 16384, 16384);
                 ptx::bulk_commit();
             }
             ph ^= 1u;
@@ -579,24 +590,28 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
 // columns) is accumulated in tensor memory; its fp16 copy Sh (K-major, shared
 // memory) is the A operand.  Per chunk c, with the chunk's image landed by
 // bulk copies (two buffers):
-//   UK:  S   += U^T Kt    (state-independent; issued once S_c has been read)
-//   UP:  O^T  = U^T P^T   (state-independent; into one of two O buffers)
-//   SQ:  O^T += Sh Q'^T   (once Sh = S_c is in shared memory)
-//   SE:  S   += Sh E      (the only product on the chain; delta rules only)
-// The gated rule has E = (e^{G_C} - 1) I: instead of a product, the state
-// warps scale S by e^{G_C} in tensor memory when they read it (the prepare
-// kernel leaves e^{G_C} at the start of the image's E area).  Roles
-// (14 warps): warps 0-7 read S after each chunk (thread = value row
-// 32 (warp % 4) + lane, column half warp / 4), write Sh and, after the last
-// chunk, the final state; warps 8-11 read O^T and store the outputs; warp 12
-// loads the images; warp 13 issues the products, SQ before SE, so that the
-// completion of a chunk's last product also frees Sh.  A chunk takes about
-// 2.7 K cycles whether the products have M = 128 or 64 and whether E is
-// streamed or not: an M = 64 instruction holds the tensor pipe about as long
-// as an M = 128 one, so the 24 instructions on the serial path, with the
-// round trip S -> Sh -> products -> commit around them, set the pace.
-// Hand-overs are mbarriers with bounded, sleeping waits; each role makes a
-// failed wait uniform before leaving.
+//   UK:    S   += U^T Kt          (state-independent; issued once S_c has been read)
+//   UP:    O^T  = U^T P^T         (state-independent; once O^T of chunk c - 1 is read)
+//   SE+SQ: [S | O^T] += Sh [E^T; Q']^T   (once Sh = S_c is in shared memory)
+// S (columns 0-127) and O^T (columns 128-191) sit side by side in tensor
+// memory and the image stores E^T and Q' as one K-major B operand of 192
+// rows, so the delta rules' S E and S Q'^T are a single N = 192 product: 8
+// instructions where they were 16, with the descriptors built once per chunk
+// and advanced per K-step.  What sets the pace, as measured: one K = 16
+// instruction costs about max(47, N / 2) cycles on its own, for M = 64 and
+// 128 alike, but in this kernel the products run at about 100 cycles per
+// N = 128 instruction while the 88 KB image of the next chunk lands in
+// shared memory and the state warps write Sh, and a chunk takes about 2.5 K
+// cycles whether S E and S Q'^T are fused or issued apart, in either order,
+// and whether M is 64 or 128.  The rules without retrieval have no E: SQ
+// alone (N = 64), and the gated rule's state warps scale S by e^{G_C} in
+// tensor memory when they read it (the prepare kernel leaves e^{G_C} at the
+// start of the image's E^T area).  Roles (14 warps): warps 0-7 read S after
+// each chunk (thread = value row 32 (warp % 4) + lane, column half warp / 4),
+// write Sh and, after the last chunk, the final state; warps 8-11 read O^T
+// and store the outputs; warp 12 loads the images; warp 13 issues the
+// products.  Hand-overs are mbarriers with bounded, sleeping waits; each role
+// makes a failed wait uniform before leaving.
 //
 // Value rows never mix (S <- S + U^T Kt + S E and O^T = U^T P^T + S Q'^T act
 // row by row), so with ROWS = 64 a chain is split over two CTAs, each with
@@ -611,7 +626,7 @@ constexpr int cS = 2 * IM_BYTES;              // 32 KB: Sh, 2 blocks [128 v][64 
 constexpr int cBar = cS + 32768;              // 11 mbarriers, TMEM address
 constexpr int CH_SMEM = cBar + 128 + 1024;
 static_assert(cS % 1024 == 0, "chain layout");
-constexpr uint32_t tS = 0, tO = 128;          // tensor-memory columns: S, two O^T buffers
+constexpr uint32_t tS = 0, tO = 128;          // tensor-memory columns: S [0, 128), O^T [128, 192)
 // what the state step of a rule needs beyond U^T Kt
 enum : int { kStepPlain = 0, kStepDecay = 1, kStepE = 2 };
 
@@ -630,8 +645,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     uint64_t *rsread = bars + 4;  // S_c read by the state warps (one phase per chunk, from c = 0)
     uint64_t *shready = bars + 5; // Sh = S_c written
     uint64_t *barS = bars + 6;    // every product of chunk c done
-    uint64_t *barO = bars + 7;    // [2] O^T of chunk c done
-    uint64_t *ofree = bars + 9;   // [2] O^T buffer read
+    uint64_t *barO = bars + 7;    // O^T of chunk c done
+    uint64_t *ofree = bars + 9;   // O^T of chunk c read by the output warps
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + cBar + 96);
     unsigned char *sS = sm + cS;
 
@@ -691,7 +706,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         const size_t kcol = tile + (size_t)(64 * hc) * 128 + 64 * vh + i;
         // e^{G_C} of chunk c, as the prepare kernel left it in the chunk's image
         auto gamma = [&](int c) {
-            return *reinterpret_cast<const float *>(img + ((size_t)(slot0 + c) * p.Hv + h) * IM_BYTES + IM_E);
+            return *reinterpret_cast<const float *>(img + ((size_t)(slot0 + c) * p.Hv + h) * IM_BYTES + IM_EQ);
         };
         {
             const float g0 = STEP == kStepDecay ? gamma(0) : 1.f;
@@ -788,16 +803,15 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         const size_t rstride = (size_t)p.Hv * 128;
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
-            const int bf = c & 1;
-            ok = ptx::named_bar_and(2, 128, ptx::mbar_wait_sleep(&barO[bf], (c >> 1) & 1));
+            ok = ptx::named_bar_and(2, 128, ptx::mbar_wait_sleep(barO, c & 1));
             if (!ok) break;
             tc::fence_after();
             float o0[32], o1[32];
-            tc::ld32(lo + 64 * bf, o0);
-            tc::ld32(lo + 64 * bf + 32, o1);
+            tc::ld32(lo, o0);
+            tc::ld32(lo + 32, o1);
             tc::fence_before();
             ptx::named_bar_sync(2, 128);
-            if (ot == 0) ptx::mbar_arrive(&ofree[bf]);
+            if (ot == 0) ptx::mbar_arrive(ofree);
             const int n = live ? min(TC_C, t1 - (t0 + TC_C * c)) : 0;
             __half *orow = static_cast<__half *>(p.o) + ((size_t)(t0 + TC_C * c) * p.Hv + h) * 128 + 64 * vh + i;
 #pragma unroll
@@ -811,7 +825,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     } else if (warp == 12) {
         // ===================== image loads, two buffers
         if (lane == 0) {
-            const uint32_t skip = STEP == kStepE ? 0u : (uint32_t)IM_Q;  // only the delta rules load E
+            const uint32_t skip = STEP == kStepE ? 0u : (uint32_t)(IM_U - 16384);  // only the delta rules load E^T
             const uint32_t ubytes = HALF ? 8192u : 16384u;               // U: this CTA's value rows
             for (int c = 0; c < nch; ++c) {
                 const int bf = c & 1;
@@ -828,7 +842,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     if (STEP == kStepE) {
                         ptx::prefetch_l2(nxt, IM_BYTES);
                     } else {
-                        ptx::prefetch_l2(nxt + IM_Q, IM_U - IM_Q);
+                        ptx::prefetch_l2(nxt + im_q(0), 8192);
+                        ptx::prefetch_l2(nxt + im_q(1), 8192);
                         ptx::prefetch_l2(nxt + IM_P, IM_BYTES - IM_P);
 #pragma unroll
                         for (int kb = 0; kb < 2; ++kb)
@@ -836,10 +851,11 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     }
                 }
                 if (STEP == kStepE) {
-                    ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);                                // E and Q'
+                    ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);                                // E^T and Q'
                     ptx::bulk_g2s(dstb + IM_U, src + IM_U + 8192 * vh, ubytes, &land[bf]);  // U (its rows)
                 } else {
-                    ptx::bulk_g2s(dstb + IM_Q, src + IM_Q, IM_U - IM_Q, &land[bf]);  // Q'
+                    ptx::bulk_g2s(dstb + im_q(0), src + im_q(0), 8192, &land[bf]);  // Q'
+                    ptx::bulk_g2s(dstb + im_q(1), src + im_q(1), 8192, &land[bf]);
                     // without retrieval U = V: its rows straight from the value input (the box
                     // lands in the image's U layout; rows past the request meet zero Kt rows and
                     // causally masked P entries only)
@@ -856,10 +872,16 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         // ===================== products
         if (lane == 0) {
             const uint32_t aS = ptx::smem_u32(sS);
+            // descriptors built once; each product advances them (desc_adv)
+            const uint64_t dSh0 = tc::desc_sw128(aS);
+            constexpr uint32_t idUK = tc::idesc_f16(ROWS, 128, true, true), idUP = tc::idesc_f16(ROWS, 64, true, false);
+            constexpr uint32_t idSQ = tc::idesc_f16(ROWS, 64), idSEQ = tc::idesc_f16(ROWS, 192);
             bool ok = true;
             for (int c = 0; c < nch; ++c) {
                 const int bf = c & 1;
                 const uint32_t base = ptx::smem_u32(sm + cImg + bf * IM_BYTES);
+                const uint64_t dU = tc::desc_sw128(base + IM_U, 8192), dKt = tc::desc_sw128(base + IM_KT, 8192);
+                const uint64_t dP = tc::desc_sw128(base + IM_P), dEQ = tc::desc_sw128(base + IM_EQ);
                 ok = ptx::mbar_wait_sleep(&land[bf], (c >> 1) & 1) && ptx::mbar_wait_sleep(rsread, c & 1);
                 if (!ok) break;
                 tc::fence_after();
@@ -881,37 +903,35 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 // UK: S += U^T Kt (M = 128 v, N = 128 j, K = 64 t; A and B M/N-major)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem + tS, tc::desc_sw128(base + IM_U + s * 2048, 8192),
-                                tc::desc_sw128(base + IM_KT + s * 2048, 8192), tc::idesc_f16(ROWS, 128, true, true), true);
+                    tc::mma_f16(tmem + tS, tc::desc_adv(dU, s * 2048), tc::desc_adv(dKt, s * 2048), idUK, true);
 
-                if (c >= 2) {
-                    ok = ptx::mbar_wait_sleep(&ofree[bf], ((c - 2) >> 1) & 1);
+                if (c >= 1) {  // the output warps have read O^T of chunk c - 1
+                    ok = ptx::mbar_wait_sleep(ofree, (c - 1) & 1);
                     if (!ok) break;
                     tc::fence_after();
                 }
                 // UP: O^T = U^T P^T (N = 64 r, K = 64 t; B K-major)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem + tO + 64 * bf, tc::desc_sw128(base + IM_U + s * 2048, 8192),
-                                tc::desc_sw128(base + IM_P + s * 32), tc::idesc_f16(ROWS, 64, true, false), s > 0);
+                    tc::mma_f16(tmem + tO, tc::desc_adv(dU, s * 2048), tc::desc_adv(dP, s * 32), idUP, s > 0);
                 ok = ptx::mbar_wait_sleep(shready, c & 1);
                 if (!ok) break;
                 tc::fence_after();
-                // SQ: O^T += Sh Q'^T (N = 64 t, K = 128 i; both K-major)
-#pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    tc::mma_f16(tmem + tO + 64 * bf, tc::desc_sw128(aS + (s >> 2) * SHB + (s & 3) * 32),
-                                tc::desc_sw128(base + IM_Q + (s >> 2) * 8192 + (s & 3) * 32), tc::idesc_f16(ROWS, 64),
-                                true);
-                tc::commit(&barO[bf]);
                 if (STEP == kStepE) {
-                    // SE: S += Sh E (N = 128 j, K = 128 i; B N-major)
+                    // SE and SQ as one product: [S | O^T] += Sh [E^T; Q']^T (N = 128 j + 64 t = 192,
+                    // K = 128 i; A and B K-major; S and O^T are adjacent in tensor memory)
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        tc::mma_f16(tmem + tS, tc::desc_sw128(aS + (s >> 2) * SHB + (s & 3) * 32),
-                                    tc::desc_sw128(base + IM_E + s * 2048, 16384), tc::idesc_f16(ROWS, 128, false, true),
-                                    true);
+                        tc::mma_f16(tmem + tS, tc::desc_adv(dSh0, (s >> 2) * SHB + (s & 3) * 32),
+                                    tc::desc_adv(dEQ, (s >> 2) * IM_EQ_BLK + (s & 3) * 32), idSEQ, true);
+                } else {
+                    // SQ: O^T += Sh Q'^T (N = 64 t, K = 128 i; both K-major)
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        tc::mma_f16(tmem + tO, tc::desc_adv(dSh0, (s >> 2) * SHB + (s & 3) * 32),
+                                    tc::desc_adv(dEQ, (s >> 2) * IM_EQ_BLK + IM_EQ_Q + (s & 3) * 32), idSQ, true);
                 }
+                tc::commit(barO);
                 // every product of chunk c is done: S_{c+1} is complete and Sh is free
                 tc::commit(barS);
                 tc::commit(&freeb[bf]);

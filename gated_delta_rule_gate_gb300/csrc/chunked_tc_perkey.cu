@@ -17,7 +17,7 @@
 //   P_rj = scale  sum_c qn_r[c]    kn_j[c] e^{Gamma_r[c] - Gamma_j[c]}  (j <= r)
 //   U  = T diag(beta) V,     Wn = -T diag(beta) (e^Gamma .* kappa)
 //   Kt = e^{Gamma_C - Gamma} .* Kn,       Qh = scale e^Gamma .* Qn
-//   Q' = Qh + P Wn,          E  = Wn^T Kt + Diag(e^{Gamma_C} - 1)
+//   Q' = Qh + P Wn,          E  = Wn^T Kt + Diag(e^{Gamma_C} - 1)   (written as E^T = Kt^T Wn + ...)
 //
 // and the chain kernel's two lines S <- S + U^T Kt + S E, O^T = U^T P^T + S Q'^T
 // are unchanged, so this kernel writes the same operand image as the scalar
@@ -313,6 +313,16 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
         const uint32_t aTb = ptx::smem_u32(sm + pTb), aTa = ptx::smem_u32(sm + pTa);
         const uint32_t aXo = ptx::smem_u32(sm + pXo), aYo = ptx::smem_u32(sm + pYo);
         const uint32_t aXp = ptx::smem_u32(sm + pXp);
+        // shared-memory descriptors built once; each product advances them (desc_adv)
+        const uint64_t d_aKQ_16384 = tc::desc_sw128(aKQ, 16384);
+        const uint64_t d_aKt_8192 = tc::desc_sw128(aKt, 8192);
+        const uint64_t d_aP = tc::desc_sw128(aP);
+        const uint64_t d_aTa = tc::desc_sw128(aTa);
+        const uint64_t d_aTb = tc::desc_sw128(aTb);
+        const uint64_t d_aV_8192 = tc::desc_sw128(aV, 8192);
+        const uint64_t d_aXo = tc::desc_sw128(aXo);
+        const uint64_t d_aXp_8192 = tc::desc_sw128(aXp, 8192);
+        const uint64_t d_aYo = tc::desc_sw128(aYo);
         float *At = reinterpret_cast<float *>(sm + pAt);
         float *Tf = reinterpret_cast<float *>(sm + pTf);
         const bool nk = (p.flags & kL2k) != 0, nq = (p.flags & kL2q) != 0;
@@ -542,7 +552,7 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t ao = (ks >> 2) * 16384 + (ks & 3) * 32;
                         const uint32_t bo = (ks >> 2) * kYBlk + ystart(s2) * 128 + (ks & 3) * 32;
-                        tc::mma_f16(tmem + (uint32_t)ystart(s2), tc::desc_sw128(aXo + ao), tc::desc_sw128(aYo + bo),
+                        tc::mma_f16(tmem + (uint32_t)ystart(s2), tc::desc_adv(d_aXo, ao), tc::desc_adv(d_aYo, bo),
                                     tc::idesc_f16(128, 16 * s2), ks > 0);
                     }
                 }
@@ -731,9 +741,9 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 // U = Tb V -> [0, 128) and Wn = Ta' X' -> [128, 256): M = 64, N = 128, K = 64
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
-                    tc::mma_f16(tmem, tc::desc_sw128(aTb + s * 32), tc::desc_sw128(aV + s * 2048, 8192),
+                    tc::mma_f16(tmem, tc::desc_adv(d_aTb, s * 32), tc::desc_adv(d_aV_8192, s * 2048),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
-                    tc::mma_f16(tmem + 128, tc::desc_sw128(aTa + s * 32), tc::desc_sw128(aXp + s * 2048, 8192),
+                    tc::mma_f16(tmem + 128, tc::desc_adv(d_aTa, s * 32), tc::desc_adv(d_aXp_8192, s * 2048),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
                 }
                 tc::commit(bar2);
@@ -764,15 +774,16 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 ptx::bulk_s2g(dst + IM_U, sm + pV, 16384);
                 ptx::bulk_commit();
                 tc::fence_after();
-                // Wn^T Kt -> [0, 128): M = 128 (i), N = 128 (j), K = 64 (t), both operands M/N-major
+                // Kt^T Wn = E^T - Diag(...) -> [0, 128): M = 128 (j), N = 128 (i), K = 64 (t), both
+                // operands M/N-major
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem, tc::desc_sw128(aKQ + s * 2048, 16384), tc::desc_sw128(aKt + s * 2048, 8192),
+                    tc::mma_f16(tmem, tc::desc_adv(d_aKt_8192, s * 2048), tc::desc_adv(d_aKQ_16384, s * 2048),
                                 tc::idesc_f16(128, 128, true, true), s > 0);
                 // P Wn -> [128, 256): M = 64 (r), N = 128 (i), K = 64 (t)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem + 128, tc::desc_sw128(aP + s * 32), tc::desc_sw128(aKQ + s * 2048, 16384),
+                    tc::mma_f16(tmem + 128, tc::desc_adv(d_aP, s * 32), tc::desc_adv(d_aKQ_16384, s * 2048),
                                 tc::idesc_f16(64, 128, false, true), s > 0);
                 tc::commit(bar3);
             }
@@ -823,8 +834,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             tc::fence_before();
             ptx::named_bar_sync(3, PK_WORK);
             if (tid == 0) {
-                ptx::bulk_s2g(dst + IM_Q, sm + pQh, 16384);
-                ptx::bulk_s2g(dst + IM_E, sm + pXo, 32768);
+                ptx::bulk_s2g(dst + im_q(0), sm + pQh, 8192);
+                ptx::bulk_s2g(dst + im_q(1), sm + pQh + 8192, 8192);
+                ptx::bulk_s2g(dst + im_e(0), sm + pXo, 16384);
+                ptx::bulk_s2g(dst + im_e(1), sm + pXo + 16384, 16384);
                 ptx::bulk_commit();
             }
             ph ^= 1u;

@@ -166,6 +166,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo = 16
     return d;
 }
 
+// A descriptor moved `bytes` further along shared memory (the start-address
+// field counts 16-byte units and stays below 2^14 for any shared address, so
+// the add never carries into the other fields).  Building descriptors once
+// and advancing them keeps the issuing thread's work per instruction small.
+__device__ __forceinline__ uint64_t desc_adv(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor, kind::f16 with fp16 operands and fp32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn = false, bool b_mn = false,
                                                  bool neg_b = false) {
