@@ -512,6 +512,63 @@ __device__ __forceinline__ void issue_pair(const Problem &p, const PipeLayout &L
 // L2 normalisation and k . q of staged tokens g0 .. g0 + TG - 1 (those below
 // L), written as the fp32 rows the consumers read.  The TG tokens' warp
 // reductions are interleaved.
+// N consecutive raw elements (fp16 or fp32) starting at element e, as floats;
+// e * element size is a multiple of N * element size (vector loads).
+template <int N>
+__device__ __forceinline__ void ld_raw_vec(const unsigned char *base, int e, int f16, float (&x)[N]) {
+    if (f16) {
+        const __half *hp = reinterpret_cast<const __half *>(base) + e;
+        if (N == 8) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(hp);
+            const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const float2 f = __half22float2(h2[i]);
+                x[2 * i] = f.x, x[2 * i + 1] = f.y;
+            }
+        } else if (N == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(hp);
+            const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const float2 f = __half22float2(h2[i]);
+                x[2 * i] = f.x, x[2 * i + 1] = f.y;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) x[i] = __half2float(hp[i]);
+        }
+    } else {
+        const float *fp = reinterpret_cast<const float *>(base) + e;
+        if (N % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < N; i += 4) {
+                const float4 f = *reinterpret_cast<const float4 *>(fp + i);
+                x[i] = f.x, x[i + 1] = f.y, x[i + 2] = f.z, x[i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) x[i] = fp[i];
+        }
+    }
+}
+
+// stores N floats at dst (16-byte aligned when N is a multiple of 4)
+template <int N>
+__device__ __forceinline__ void st_vec(float *dst, const float (&x)[N]) {
+    if (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) dst[i] = x[i];
+    }
+}
+
+// L2 normalisation and k . q of staged tokens g0 .. g0 + TG - 1 (those below
+// L), written as the fp32 rows the consumers read.  Lane l owns the DK / 32
+// consecutive channels l * DK / 32 + [0, DK / 32) (vector loads and stores);
+// the TG tokens' warp reductions are interleaved.
 template <int DK, int TG>
 __device__ __forceinline__ void stage_token_group(const Problem &p, const Stage &st, const PipeLayout &Ly,
                                                   const unsigned char *rk, const unsigned char *rq,
@@ -519,19 +576,22 @@ __device__ __forceinline__ void stage_token_group(const Problem &p, const Stage 
                                                   int L, int lane) {
     constexpr int EPL = DK / 32;
     const bool sig = (p.flags & kBetaSigmoid) != 0;
+    const int c0 = lane * EPL;
     float ssk[TG], ssq[TG], kq[TG];
 #pragma unroll
     for (int u = 0; u < TG; ++u) {
         const int tt = g0 + u;
         ssk[u] = ssq[u] = kq[u] = 0.f;
+        if (tt < L) {
+            float kx[EPL], qx[EPL];
+            ld_raw_vec<EPL>(rk, tt * DK + c0, p.act_f16, kx);
+            ld_raw_vec<EPL>(rq, tt * DK + c0, p.act_f16, qx);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int c = lane + 32 * i;
-            const float kx = tt < L ? ld_raw(rk, tt * DK + c, p.act_f16) : 0.f;
-            const float qx = tt < L ? ld_raw(rq, tt * DK + c, p.act_f16) : 0.f;
-            ssk[u] = fmaf(kx, kx, ssk[u]);
-            ssq[u] = fmaf(qx, qx, ssq[u]);
-            kq[u] = fmaf(kx, qx, kq[u]);
+            for (int i = 0; i < EPL; ++i) {
+                ssk[u] = fmaf(kx[i], kx[i], ssk[u]);
+                ssq[u] = fmaf(qx[i], qx[i], ssq[u]);
+                kq[u] = fmaf(kx[i], qx[i], kq[u]);
+            }
         }
     }
     const bool l2k = (p.flags & kL2k) != 0, l2q = (p.flags & kL2q) != 0;
@@ -549,22 +609,32 @@ __device__ __forceinline__ void stage_token_group(const Problem &p, const Stage 
         if (tt >= L) break;
         const float ik = l2k ? rsqrtf(ssk[u] + 1e-12f) : 1.f;
         const float iq = l2q ? rsqrtf(ssq[u] + 1e-12f) : 1.f;
+        float kn[EPL], qn[EPL];
+        ld_raw_vec<EPL>(rk, tt * DK + c0, p.act_f16, kn);
+        ld_raw_vec<EPL>(rq, tt * DK + c0, p.act_f16, qn);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int c = lane + 32 * i;
-            const float kn = ld_raw(rk, tt * DK + c, p.act_f16) * ik;
-            st.k[tt * DK + c] = kn;
-            st.q[tt * DK + c] = ld_raw(rq, tt * DK + c, p.act_f16) * iq;
-            if (Ly.has_a) {
-                float g = ld_raw(ra, tt * DK + c, p.decay_f16);
-                if (p.raw_gate) g = p.gate_scale[h] * softplus_f(g + p.gate_bias[(size_t)h * DK + c]);
-                st.a[tt * DK + c] = expf(g);
+        for (int i = 0; i < EPL; ++i) kn[i] *= ik, qn[i] *= iq;
+        st_vec<EPL>(st.k + tt * DK + c0, kn);
+        st_vec<EPL>(st.q + tt * DK + c0, qn);
+        if (Ly.has_a) {
+            float g[EPL];
+            ld_raw_vec<EPL>(ra, tt * DK + c0, p.decay_f16, g);
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                if (p.raw_gate) g[i] = p.gate_scale[h] * softplus_f(g[i] + p.gate_bias[(size_t)h * DK + c0 + i]);
+                g[i] = expf(g[i]);
             }
-            if (Ly.has_x) {
-                float bb = ld_raw(rx, tt * DK + c, p.erase_gate ? 0 : p.beta_f16);
-                if (sig && !p.erase_gate) bb = sigmoid_f(bb);
-                st.x[tt * DK + c] = bb * kn;
+            st_vec<EPL>(st.a + tt * DK + c0, g);
+        }
+        if (Ly.has_x) {
+            float bb[EPL];
+            ld_raw_vec<EPL>(rx, tt * DK + c0, p.erase_gate ? 0 : p.beta_f16, bb);
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                if (sig && !p.erase_gate) bb[i] = sigmoid_f(bb[i]);
+                bb[i] *= kn[i];
             }
+            st_vec<EPL>(st.x + tt * DK + c0, bb);
         }
         if (lane == 0) st.kq[tt] = kq[u] * ik * iq;
     }
@@ -963,6 +1033,18 @@ __global__ void __launch_bounds__(kThreads + 32 + 32 * (KM ? kMaxStagers : 1), K
             if (row >= 0 && L > 0 && L <= kTB) {
                 TokScalars ts;
                 issue_pair<DK>(p, Ly, raw, h, (int)((long long)h * p.Hq / p.Hv), t0, L, lane, ts);
+                // the next pair's key, query and value rows into L2 while this one lands
+                const int nL = nt1 - nt0;
+                if (pair + gstep < pairs && nrow >= 0 && nL > 0 && nL <= kTB && lane < 3 * nL) {
+                    const int nh = (pair + gstep) % p.Hv, nqh = (int)((long long)nh * p.Hq / p.Hv);
+                    const int tt = lane / 3, which = lane % 3, es = p.act_f16 ? 2 : 4;
+                    const unsigned char *src =
+                        which == 2 ? static_cast<const unsigned char *>(p.v) + (((size_t)(nt0 + tt) * p.Hv + nh) * p.dv) * es
+                                   : static_cast<const unsigned char *>(which ? p.q : p.k) +
+                                         (((size_t)(nt0 + tt) * p.Hq + nqh) * DK) * es;
+                    const int bytes = (which == 2 ? p.dv : DK) * es;
+                    if (bytes % 16 == 0) ptx::prefetch_l2(src, (uint32_t)bytes);
+                }
                 ptx::cp_async_wait_all();
                 __syncwarp();
                 finish_pair<DK>(p, st, Ly, raw, h, L, lane, ts);
