@@ -635,6 +635,11 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     chunk_chain_kernel(Problem p, const __grid_constant__ CUtensorMap tmV, const int *offs, const int *order,
                        const unsigned char *img, int cap) {
     constexpr bool HALF = ROWS == 64;
+    // Rules without E, split chains: the state S_{c+1} = S_c + U^T Kt (gated: scaled as it is
+    // read) does not wait for Sh, so S is published right after U^T Kt and the readout of
+    // chunk c runs while the state warps copy S_{c+1}; Sh then alternates between two buffers
+    // (they fit in the 32 KB area at ROWS = 64) and its hand-over between two barriers.
+    constexpr bool PIPE = HALF && STEP != kStepE;
     constexpr int SHB = ROWS * 128;  // bytes per 64-column block of Sh
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
@@ -646,6 +651,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     uint64_t *shready = bars + 5; // Sh = S_c written
     uint64_t *barS = bars + 6;    // every product of chunk c done
     uint64_t *barO = bars + 7;    // O^T of chunk c done
+    uint64_t *shready2 = bars + 8; // PIPE: Sh of the odd chunks written (shready: the even ones)
     uint64_t *ofree = bars + 9;   // O^T of chunk c read by the output warps
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + cBar + 96);
     unsigned char *sS = sm + cS;
@@ -769,15 +775,18 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             ptx::named_bar_sync(1, 256);
             if (tid == 0) ptx::mbar_arrive(rsread);
             if (c + 1 < nch) {
+                // PIPE: chunk c + 1 writes buffer (c + 1) % 2 (the readout of chunk c may still
+                // read the other) and publishes it on the barrier of its parity
+                unsigned char *shb = sS + (PIPE ? ((c + 1) & 1) * 2 * SHB : 0) + hc * SHB;
                 if (live) {
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * SHB, i, cc, v0 + 8 * cc);
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(shb, i, cc, v0 + 8 * cc);
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) st_chunk(sS + hc * SHB, i, 4 + cc, v1 + 8 * cc);
+                    for (int cc = 0; cc < 4; ++cc) st_chunk(shb, i, 4 + cc, v1 + 8 * cc);
                 }
                 tc::fence_async_smem();
                 ptx::named_bar_sync(1, 256);
-                if (tid == 0) ptx::mbar_arrive(shready);
+                if (tid == 0) ptx::mbar_arrive(PIPE && ((c + 1) & 1) ? shready2 : shready);
             } else if (live && km) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -904,6 +913,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     tc::mma_f16(tmem + tS, tc::desc_adv(dU, s * 2048), tc::desc_adv(dKt, s * 2048), idUK, true);
+                if (PIPE) tc::commit(barS);  // S_{c+1} is complete
 
                 if (c >= 1) {  // the output warps have read O^T of chunk c - 1
                     ok = ptx::mbar_wait_sleep(ofree, (c - 1) & 1);
@@ -914,6 +924,20 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     tc::mma_f16(tmem + tO, tc::desc_adv(dU, s * 2048), tc::desc_adv(dP, s * 32), idUP, s > 0);
+                if (PIPE) {
+                    ok = ptx::mbar_wait_sleep((c & 1) ? shready2 : shready, (c >> 1) & 1);
+                    if (!ok) break;
+                    tc::fence_after();
+                    const uint64_t dSh = tc::desc_adv(dSh0, (c & 1) * 2 * SHB);
+                    // SQ: O^T += Sh Q'^T (N = 64 t, K = 128 i; both K-major)
+#pragma unroll
+                    for (int s = 0; s < 8; ++s)
+                        tc::mma_f16(tmem + tO, tc::desc_adv(dSh, (s >> 2) * SHB + (s & 3) * 32),
+                                    tc::desc_adv(dEQ, (s >> 2) * IM_EQ_BLK + IM_EQ_Q + (s & 3) * 32), idSQ, true);
+                    tc::commit(barO);
+                    tc::commit(&freeb[bf]);
+                    continue;
+                }
                 ok = ptx::mbar_wait_sleep(shready, c & 1);
                 if (!ok) break;
                 tc::fence_after();
