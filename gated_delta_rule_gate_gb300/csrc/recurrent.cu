@@ -480,20 +480,43 @@ template <int DK>
 __device__ __forceinline__ void issue_pair(const Problem &p, const PipeLayout &Ly, unsigned char *raw, int h, int qh,
                                            int t0, int L, int lane, TokScalars &ts) {
     const int es = p.act_f16 ? 2 : 4;
-    const int des = p.decay_f16 ? 2 : 4;
+    const int des = p.decay_f16 ? 2 : 4, bes = Ly.xes;
     unsigned char *rk = raw;
     unsigned char *rq = rk + kTB * DK * es;
     unsigned char *rv = rq + kTB * DK * es;
     unsigned char *ra = rv + kTB * p.dv * es;
     unsigned char *rx = ra + (Ly.has_a ? kTB * DK * des : 0);
-    const size_t kv0 = (size_t)t0 * p.Hq + qh, hv0 = (size_t)t0 * p.Hv + h;
-    copy_token_rows(rk, p.k, kv0, p.Hq, DK * es, L, lane);
-    copy_token_rows(rq, p.q, kv0, p.Hq, DK * es, L, lane);
-    copy_token_rows(rv, p.v, hv0, p.Hv, p.dv * es, L, lane);
-    if (Ly.has_a) copy_token_rows(ra, p.decay, hv0, p.Hv, DK * des, L, lane);
-    // the GDN-2 erase gate (its own input, or the per-key beta) and write gate
-    if (Ly.has_x) copy_token_rows(rx, p.erase_gate ? (const void *)p.erase_gate : p.beta, hv0, p.Hv, DK * Ly.xes, L, lane);
-    if (Ly.has_w) copy_token_rows(rx + kTB * DK * Ly.xes, p.write_gate, hv0, p.Hv, p.dv * 4, L, lane);
+    const int kch = DK * es / 16, vch = p.dv * es / 16;
+    for (int idx = lane; idx < L * kch; idx += 32) {
+        const int tt = idx / kch, c = idx % kch;
+        const size_t off = (((size_t)(t0 + tt) * p.Hq + qh) * DK) * es + 16 * c;
+        ptx::cp_async16(rk + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.k) + off, 16);
+        ptx::cp_async16(rq + tt * DK * es + 16 * c, static_cast<const unsigned char *>(p.q) + off, 16);
+    }
+    for (int idx = lane; idx < L * vch; idx += 32) {
+        const int tt = idx / vch, c = idx % vch;
+        const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * p.dv) * es + 16 * c;
+        ptx::cp_async16(rv + tt * p.dv * es + 16 * c, static_cast<const unsigned char *>(p.v) + off, 16);
+    }
+    if (Ly.has_a) {
+        const int ach = DK * des / 16;
+        for (int idx = lane; idx < L * ach; idx += 32) {
+            const int tt = idx / ach, c = idx % ach;
+            const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * DK) * des + 16 * c;
+            ptx::cp_async16(ra + tt * DK * des + 16 * c, static_cast<const unsigned char *>(p.decay) + off, 16);
+        }
+    }
+    // the GDN-2 write gate rows (fp32)
+    if (Ly.has_w) copy_token_rows(rx + kTB * DK * Ly.xes, p.write_gate, (size_t)t0 * p.Hv + h, p.Hv, p.dv * 4, L, lane);
+    if (Ly.has_x) {  // the GDN-2 erase gate: its own input, or the per-key beta
+        const unsigned char *xsrc = static_cast<const unsigned char *>(p.erase_gate ? (const void *)p.erase_gate : p.beta);
+        const int xch = DK * bes / 16;
+        for (int idx = lane; idx < L * xch; idx += 32) {
+            const int tt = idx / xch, c = idx % xch;
+            const size_t off = (((size_t)(t0 + tt) * p.Hv + h) * DK) * bes + 16 * c;
+            ptx::cp_async16(rx + tt * DK * bes + 16 * c, xsrc + off, 16);
+        }
+    }
     ts.g = ts.b = 0u;
     ts.gs = ts.gb = 0.f;
     if (lane < L) {
@@ -1033,9 +1056,10 @@ __global__ void __launch_bounds__(kThreads + 32 + 32 * (KM ? kMaxStagers : 1), K
             if (row >= 0 && L > 0 && L <= kTB) {
                 TokScalars ts;
                 issue_pair<DK>(p, Ly, raw, h, (int)((long long)h * p.Hq / p.Hv), t0, L, lane, ts);
-                // the next pair's key, query and value rows into L2 while this one lands
+                // key-major: the next pair's key, query and value rows into L2 while this one
+                // lands (measured: helps the one-CTA-per-SM key-major kernel, not the other)
                 const int nL = nt1 - nt0;
-                if (pair + gstep < pairs && nrow >= 0 && nL > 0 && nL <= kTB && lane < 3 * nL) {
+                if (KM && pair + gstep < pairs && nrow >= 0 && nL > 0 && nL <= kTB && lane < 3 * nL) {
                     const int nh = (pair + gstep) % p.Hv, nqh = (int)((long long)nh * p.Hq / p.Hv);
                     const int tt = lane / 3, which = lane % 3, es = p.act_f16 ? 2 : 4;
                     const unsigned char *src =
