@@ -356,7 +356,7 @@ def kernel_name(p, path):
     if path == "recurrent":
         return token_serial()
     per_key = p.get("decay_per_key") and p["rule"] in ("gated", "gated_delta", "gdn2")
-    tc_shape = p["dk"] == 128 and p["dv"] == 128 and p["act_dtype"] == "f16"
+    tc_shape = p["dk"] == 128 and p["dv"] == 128  # fp32 activations go through fp16 copies
     erase = p.get("erase_gate") if p.get("erase_gate") is not None else p.get("beta")
     f32_gates = (p.get("decay") is None or p["decay"].dtype == torch.float32 or not per_key) and \
         (p["rule"] != "gdn2" or erase.dtype == torch.float32)
@@ -376,7 +376,9 @@ def launches_per_call(p, path):
     chunk-offset scan and the per-chunk operand pass (with the triangular
     solves for the delta rules) before the chain."""
     k = kernel_name(p, path)
-    return 3 if "chunk_chain_kernel" in k else 1
+    if "chunk_chain_kernel" not in k:
+        return 1
+    return 3 + (3 if p["act_dtype"] == "f32" else 0)  # + the fp16 copies of q, k, v
 
 
 def kernel_source_digest(path, kernel=""):

@@ -822,13 +822,24 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             ptx::named_bar_sync(2, 128);
             if (ot == 0) ptx::mbar_arrive(ofree);
             const int n = live ? min(TC_C, t1 - (t0 + TC_C * c)) : 0;
-            __half *orow = static_cast<__half *>(p.o) + ((size_t)(t0 + TC_C * c) * p.Hv + h) * 128 + 64 * vh + i;
+            const size_t obase = ((size_t)(t0 + TC_C * c) * p.Hv + h) * 128 + 64 * vh + i;
+            if (p.o_f32) {  // fp32 activations (the products ran on fp16 copies)
+                float *orow = static_cast<float *>(p.o) + obase;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                if (jj < n) orow[jj * rstride] = __float2half_rn(o0[jj]);
+                for (int jj = 0; jj < 32; ++jj)
+                    if (jj < n) orow[jj * rstride] = o0[jj];
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                if (32 + jj < n) orow[(32 + jj) * rstride] = __float2half_rn(o1[jj]);
+                for (int jj = 0; jj < 32; ++jj)
+                    if (32 + jj < n) orow[(32 + jj) * rstride] = o1[jj];
+            } else {
+                __half *orow = static_cast<__half *>(p.o) + obase;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    if (jj < n) orow[jj * rstride] = __float2half_rn(o0[jj]);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    if (32 + jj < n) orow[(32 + jj) * rstride] = __float2half_rn(o1[jj]);
+            }
         }
         if (!ok && p.err && ot == 0) atomicOr(p.err, 2);
     } else if (warp == 12) {
@@ -971,6 +982,20 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 
 bool al16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// fp32 -> fp16 copy of n elements (n a multiple of 4, both pointers 16-byte aligned): the
+// tensor-core prefill takes fp32 activations through fp16 copies in its workspace (its
+// products round their operands to fp16 anyway).
+__global__ void __launch_bounds__(256) f32_to_f16_kernel(const float4 *src, uint2 *dst, size_t n4) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 f = src[i];
+        dst[i] = make_uint2(ptx::pack_h2(f.x, f.y), ptx::pack_h2(f.z, f.w));
+    }
+}
+
+// bytes of each fp16 copy (256-byte aligned) for fp32 activations: q, k [T, Hq, 128], v [T, Hv, 128]
+size_t copy_bytes(const Problem &p, int heads) { return (((size_t)p.T * heads * 128 * 2) + 255) & ~(size_t)255; }
+size_t copies_bytes(const Problem &p) { return p.act_f16 ? 0 : 2 * copy_bytes(p, p.Hq) + copy_bytes(p, p.Hv); }
+
 // slots for every chunk of pairwise disjoint requests: sum ceil(len / C) <= T / C + B
 int slot_capacity(const Problem &p) { return (int)((long long)p.T / TC_C + p.B + 1); }
 // workspace head: chunk offsets (B + 1 ints), the slot -> request table (one int
@@ -986,14 +1011,15 @@ bool chunked_tc_eligible(const Problem &p) {
     // GDN-2: the per-key prepare kernel.  Both feed the same chain kernel.
     const bool rule_ok = p.rule == kLinear || p.rule == kGated || p.rule == kDelta || p.rule == kGatedDelta;
     const bool scalar_ok = rule_ok && !((p.flags & kPerKey) && rule_has_decay(p.rule));
-    return (scalar_ok || chunk_prepare_perkey_eligible(p)) && p.dk == 128 && p.dv == 128 && p.act_f16 &&
+    // fp32 activations run on fp16 copies made in the workspace
+    return (scalar_ok || chunk_prepare_perkey_eligible(p)) && p.dk == 128 && p.dv == 128 &&
            al16(p.q) && al16(p.k) && al16(p.v) && al16(p.fin) && (p.init == nullptr || al16(p.init));
 }
 
 // workspace: [offsets | slot table | order] [one operand image per (slot, head)]
 size_t chunked_tc_workspace_bytes(const Problem &p) {
     if (p.B == 0) return 0;
-    return head_bytes(p) + (size_t)slot_capacity(p) * p.Hv * IM_BYTES;
+    return head_bytes(p) + (size_t)slot_capacity(p) * p.Hv * IM_BYTES + copies_bytes(p);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1025,6 +1051,8 @@ bool make_kqv_map(CUtensorMap *m, const void *base, int heads, int tokens) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream);
+
 cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream) {
     const void *fns[8] = {(const void *)chunk_prepare_kernel<true>,
                           (const void *)chunk_prepare_kernel<false>,
@@ -1039,6 +1067,36 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         e = smem_attr(fns[f], f < 2 ? PR_SMEM : CH_SMEM);
         if (e != cudaSuccess) return e;
     }
+    if (!p.act_f16) {
+        // fp32 activations: fp16 copies of q, k and v at the end of the workspace, then the
+        // same kernels on them, the chain writing o in fp32
+        if (p.B == 0 || ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
+        unsigned char *cp = static_cast<unsigned char *>(ws) + (chunked_tc_workspace_bytes(p) - copies_bytes(p));
+        Problem pc = p;
+        const void *src[3] = {p.q, p.k, p.v};
+        const int heads[3] = {p.Hq, p.Hq, p.Hv};
+        const void **dstp[3] = {&pc.q, &pc.k, &pc.v};
+        for (int t = 0; t < 3; ++t) {
+            const size_t n4 = (size_t)p.T * heads[t] * 128 / 4;
+            const long long blocks = std::min<long long>((long long)(n4 + 255) / 256, 8LL * sm_count());
+            if (blocks > 0)
+                f32_to_f16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float4 *>(src[t]),
+                                                                       reinterpret_cast<uint2 *>(cp), n4);
+            *dstp[t] = cp;
+            cp += copy_bytes(p, heads[t]);
+        }
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        pc.act_f16 = 1;
+        pc.o_f32 = 1;
+        return launch_tc_f16(pc, ws, ws_bytes - copies_bytes(p), stream);
+    }
+    return launch_tc_f16(p, ws, ws_bytes, stream);
+}
+
+// the tensor-core prefill proper, on fp16 activations (its workspace: offsets, tables, images)
+static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    cudaError_t e;
     CUtensorMap tk, tq, tv;
     if (!make_kqv_map(&tk, p.k, p.Hq, p.T) || !make_kqv_map(&tq, p.q, p.Hq, p.T) ||
         !make_kqv_map(&tv, p.v, p.Hv, p.T))

@@ -862,7 +862,7 @@ bool chunk_prepare_perkey_eligible(const Problem &p) {
     auto al = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
     // GDN-2's erase-gate rows land by 512-byte bulk copies: fp32, 16-byte aligned
     const bool erase_ok = p.erase_gate ? al(p.erase_gate) : (!p.beta_f16 && al(p.beta));
-    return rule_ok && p.dk == 128 && p.dv == 128 && p.act_f16 && (!perkey || (!p.decay_f16 && al(p.decay))) &&
+    return rule_ok && p.dk == 128 && p.dv == 128 && (!perkey || (!p.decay_f16 && al(p.decay))) &&
            (!perkey || !p.raw_gate || al(p.gate_bias)) && (p.rule != kGdn2 || erase_ok) &&
            (p.write_gate == nullptr || al(p.write_gate));
 }

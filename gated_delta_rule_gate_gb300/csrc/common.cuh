@@ -42,6 +42,7 @@ struct Problem {
     int32_t *err;
     const float *erase_gate;  // GDN-2 erase gate as its own input [T, Hv, dk], or null
     const float *write_gate;  // GDN-2 write gate [T, Hv, dv], or null
+    int o_f32;                // tensor-core prefill on fp16 copies of fp32 inputs: o is fp32
 };
 
 // GDN-2 with the erase gate in its own input: beta is then a scalar per

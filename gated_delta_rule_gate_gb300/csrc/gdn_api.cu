@@ -187,6 +187,7 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
     d.err = p->error_word;
     d.erase_gate = p->erase_gate;
     d.write_gate = p->write_gate;
+    d.o_f32 = 0;
     return GDN_OK;
 }
 

@@ -245,10 +245,11 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  * accepted and none changes the result beyond rounding; <= 0 selects 64.)
  * Extra constraints (GDN_ERR_UNSUPPORTED otherwise): dk in {16, 32, 64, 128},
  * dv a multiple of 16 (<= 256), q, k, v, o and the state 16-byte aligned.
- * fp32 activations are rounded to fp16 for the products.  Per-key decay
- * (gated_delta) and GDN2 run on the tensor cores when dk = dv = 128, the
- * activations are fp16 and the per-key gates (log decay, erase gate) are fp32
- * and 16-byte aligned; per-key log decays are expected <= 0 there (decays in
+ * fp32 activations are rounded to fp16 for the products (at dk = dv = 128
+ * through fp16 copies of q, k and v that the library writes into the
+ * workspace; o is still written in fp32).  Per-key decay (gated_delta) and
+ * GDN2 run on the tensor cores when dk = dv = 128 and the per-key gates (log
+ * decay, erase gate) are fp32 and 16-byte aligned; per-key log decays are expected <= 0 there (decays in
  * (0, 1], as the raw-gate arm always gives).  Other per-key problems (the
  * gated rule, fp16 per-key gates, other head sizes) run the token-serial
  * form (same result).
@@ -256,11 +257,13 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  * Workspace: owned by the caller, device memory of at least
  * gdn_chunked_prefill_workspace_size() bytes, 256-byte aligned (NULL allowed
  * when that is 0); GDN_ERR_WORKSPACE otherwise.  It is non-zero whenever the
- * tensor-core path runs (every rule with dk = dv = 128 and fp16 activations,
- * per-key problems as above), and 0 otherwise.  Layout, for T / 64 + B + 1 chunk slots:
+ * tensor-core path runs (every rule with dk = dv = 128, per-key problems as
+ * above), and 0 otherwise.  Layout, for T / 64 + B + 1 chunk slots:
  * per-request chunk offsets, a chunk-slot -> request table and the requests
  * ordered by length (rounded up to 1 KB); then one 88 KB image per (chunk
- * slot, value head) of the chunk's state-independent operands (fp16).
+ * slot, value head) of the chunk's state-independent operands (fp16); with
+ * fp32 activations, last, the fp16 copies of q, k and v (each rounded up to
+ * 256 bytes).
  * Its contents are scratch, rewritten by every call on the stream; two calls
  * in flight at once need two workspaces.  Requests that share tokens can need
  * more slots than that; the ones past the capacity are skipped and

@@ -140,6 +140,11 @@ def test_chunked_workspace_size():
     p.rule, p.decay = N.RULES["gated"], FAKE
     assert size(p) == head + images
     assert size(_problem()) == 0  # dk = dv = 16 runs without a workspace
+    # fp32 activations take the same path through fp16 copies of q, k, v kept in the workspace
+    p = _problem(batch=B, total_tokens=T, num_heads_q=16, num_heads_v=hv, head_dim_k=128, head_dim_v=128,
+                 act_dtype=N.DTYPE_F32)
+    copy = lambda heads: -(-(T * heads * 128 * 2) // 256) * 256
+    assert size(p) == head + images + 2 * copy(16) + copy(hv)
 
 
 def test_chunked_rejects_a_small_workspace():

@@ -86,6 +86,9 @@ def test_kernel_names_mirror_the_dispatch():
         p = workloads.make(**kw)
         assert b.kernel_name(p, "chunked") == name, (over, b.kernel_name(p, "chunked"))
         assert b.launches_per_call(p, "chunked") == (3 if "chain" in name else 1)
+    p = workloads.make(**dict(base, rule="gated_delta", act="f32"))
+    assert b.kernel_name(p, "chunked") == "chunk_prepare_kernel<1>+chunk_chain_kernel<2>"
+    assert b.launches_per_call(p, "chunked") == 6
     p = workloads.decode(1, B=4, num_slots=8)
     assert b.kernel_name(p, "recurrent") == "recurrent_pipe_kernel<128,false>"
     p = dict(p, state_kmajor=True)
