@@ -360,7 +360,7 @@ def kernel_name(p, path):
     erase = p.get("erase_gate") if p.get("erase_gate") is not None else p.get("beta")
     f32_gates = (p.get("decay") is None or p["decay"].dtype == torch.float32 or not per_key) and \
         (p["rule"] != "gdn2" or erase.dtype == torch.float32)
-    if tc_shape and f32_gates and (p["rule"] == "gdn2" or (per_key and p["rule"] == "gated_delta")):
+    if tc_shape and f32_gates and (p["rule"] == "gdn2" or (per_key and p["rule"] in ("gated", "gated_delta"))):
         return "chunk_prepare_perkey_kernel<%d>+chunk_chain_kernel<2>" % int(p["rule"] == "gdn2")
     if per_key:
         return token_serial()

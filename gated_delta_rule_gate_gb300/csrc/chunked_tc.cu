@@ -1116,7 +1116,8 @@ static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, cu
     // persistent prepare CTAs: two per SM (shared and tensor memory), at most one per task
     const long long tasks = (long long)cap * p.Hv;
     const long long pgrid = std::min<long long>(tasks, 2LL * sm_count());
-    if (chunk_prepare_perkey_eligible(p)) {
+    const bool perkey_prep = chunk_prepare_perkey_eligible(p);
+    if (perkey_prep) {
         e = launch_chunk_prepare_perkey(p, tk, tq, tv, offs, slot_req, img, cap, stream);
     } else {
         if (retr)
@@ -1132,14 +1133,14 @@ static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, cu
     if ((long long)grid < sm_count()) {
         if (p.rule == kLinear)
             chunk_chain_kernel<kStepPlain, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
-        else if (p.rule == kGated)
+        else if (p.rule == kGated && !perkey_prep)  // (per-key decay: E carries it)
             chunk_chain_kernel<kStepDecay, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
         else
             chunk_chain_kernel<kStepE, 64><<<2 * grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
     } else {
         if (p.rule == kLinear)
             chunk_chain_kernel<kStepPlain, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
-        else if (p.rule == kGated)
+        else if (p.rule == kGated && !perkey_prep)
             chunk_chain_kernel<kStepDecay, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);
         else
             chunk_chain_kernel<kStepE, 128><<<grid, CH_THREADS, CH_SMEM, stream>>>(p, tv, offs, order, img, cap);

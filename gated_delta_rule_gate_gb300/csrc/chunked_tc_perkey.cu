@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                     }
                     if (GDN2 && !p.erase_gate) {
                         bt = 1.f;
+                    } else if (!GDN2 && p.rule == kGated) {
+                        bt = 0.f;  // no retrieval: no beta, and the A parts come out zero
                     } else {
                         bt = ld_any(p.beta, beta_at(p, x.c0 + tt, x.h), p.beta_f16);
                         if (p.flags & kBetaSigmoid) bt = sigmoid_f(bt);
@@ -709,6 +711,38 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 ptx::bulk_s2g(dst + IM_KT, sm + pKt, 16384);
                 ptx::bulk_commit();
             }
+            if (!GDN2 && p.rule == kGated) {
+                // no retrieval (W = 0): U = V, Q' = Qh and E = Diag(e^{Gamma_C} - 1), so the
+                // chain's S E scales the state per key channel.  E^T is staged over the solve
+                // area (row j = 32 q + lane, columns [64 hh, 64 hh + 64)).
+                const int ii = 32 * q + lane;
+                float v[64];
+#pragma unroll
+                for (int e = 0; e < 64; ++e) v[e] = 0.f;
+                if (hh == (q >> 1)) {
+                    const float gm1 = expm1f(F[fGC + ii]);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e)
+                        if (e == ii - 64 * hh) v[e] = gm1;
+                }
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) st_chunk(sm + pXo + hh * 16384, ii, cc, v + 8 * cc);
+                tc::fence_async_smem();
+                ptx::named_bar_sync(3, PK_WORK);
+                if (tid == 0) {
+                    ptx::bulk_s2g(dst + IM_U, sm + pV, 16384);
+                    ptx::bulk_s2g(dst + im_q(0), sm + pQh, 8192);
+                    ptx::bulk_s2g(dst + im_q(1), sm + pQh + 8192, 8192);
+                    ptx::bulk_s2g(dst + im_e(0), sm + pXo, 16384);
+                    ptx::bulk_s2g(dst + im_e(1), sm + pXo + 16384, 16384);
+                    ptx::bulk_commit();
+                    // the copies have read the value tile: the next task's tiles may land
+                    ptx::bulk_wait_read();
+                    ptx::mbar_arrive(tfree);
+                }
+                ph ^= 1u;
+                continue;
+            }
 
             // ---- 4. T = (I + A)^-1; Tb = T diag(beta) and Ta' = -T diag(beta) (j <= r), fp16,
             // K-major, over the solve area (At is no longer read); thread = (row, 16 columns)
@@ -858,7 +892,7 @@ namespace gdn {
 
 bool chunk_prepare_perkey_eligible(const Problem &p) {
     const bool perkey = (p.flags & kPerKey) != 0;
-    const bool rule_ok = p.rule == kGdn2 || (p.rule == kGatedDelta && perkey);
+    const bool rule_ok = p.rule == kGdn2 || ((p.rule == kGatedDelta || p.rule == kGated) && perkey);
     auto al = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
     // GDN-2's erase-gate rows land by 512-byte bulk copies: fp32, 16-byte aligned
     const bool erase_ok = p.erase_gate ? al(p.erase_gate) : (!p.beta_f16 && al(p.beta));

@@ -75,7 +75,9 @@ def test_kernel_names_mirror_the_dispatch():
         (dict(rule="gated_delta", decay_per_key=True, gate_dtype="f32"),
          "chunk_prepare_perkey_kernel<0>+chunk_chain_kernel<2>"),
         (dict(rule="gated_delta", decay_per_key=True, lengths=[200]), "recurrent_long_kernel<128>"),
-        (dict(rule="gated", decay_per_key=True, gate_dtype="f32"), "recurrent_pipe_kernel<128,false>"),
+        (dict(rule="gated", decay_per_key=True, gate_dtype="f32"),
+         "chunk_prepare_perkey_kernel<0>+chunk_chain_kernel<2>"),
+        (dict(rule="gated", decay_per_key=True), "recurrent_pipe_kernel<128,false>"),
         (dict(rule="gdn2", decay_per_key=True, gate_dtype="f32", erase="input", write_gate="input"),
          "chunk_prepare_perkey_kernel<1>+chunk_chain_kernel<2>"),
         (dict(rule="gated_delta", dk=64, dv=64), "chunked_mma_kernel<64,false>"),

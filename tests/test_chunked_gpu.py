@@ -55,9 +55,14 @@ CASES += [
          logdecay_range=(-6.0, 0.0), beta_mode="direct", l2norm_q=True),
     dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=2, decay_per_key=True, gate="log",
          logdecay_range=(-3.0, 0.0), l2norm_q=True),
-    # per-key decay in fp16 and the gated rule with per-key decay take the token-serial kernel
-    dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True),
+    # the gated rule with per-key decay (no retrieval) on the per-key prepare pass
     dict(rule="gated", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True, gate_dtype="f32"),
+    dict(rule="gated", act="f16", dk=128, dv=128, hq=2, hv=4, decay_per_key=True, gate="log",
+         logdecay_range=(-6.0, 0.0), l2norm_q=True),
+    dict(rule="gated", act="f32", dk=128, dv=128, hq=1, hv=2, decay_per_key=True, gate_dtype="f32"),
+    # per-key gates in fp16 take the token-serial kernel
+    dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True),
+    dict(rule="gated", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True),
 ]
 
 
@@ -228,8 +233,18 @@ def test_gdn2_full_size_gates_as_inputs():
     _full(workloads.gdn2(erase="input", write_gate="input"))
 
 
+def test_gated_per_key_long():
+    """The gated rule with decay per key channel (no retrieval) on the per-key
+    prepare pass: B = 2, S = 4096, H = 16 with the GDN-2 workload's gate
+    distribution, random incoming state; both sequences."""
+    p = workloads.make(seed=6, B=2, seq_len=4096, hq=16, hv=16, dk=128, dv=128, act="f16", rule="gated",
+                       gate="raw", decay_per_key=True, gate_dtype="f32", a_log_range=(0.0, 0.0),
+                       dt_bias_range=(0.0, 0.0), state="random", state_std=0.02)
+    _full(p)
+
+
 @pytest.mark.parametrize("rule,per_key", [("linear", False), ("gated", False), ("delta", False),
-                                          ("gated_delta", False), ("gdn2", True)])
+                                          ("gated_delta", False), ("gdn2", True), ("gated", True)])
 def test_chunked_many_chains(rule, per_key):
     """160 (request, head) chains, more than the GPU has SMs: the chain kernel
     keeps one CTA per chain (fewer chains are split over two CTAs by value
@@ -237,7 +252,7 @@ def test_chunked_many_chains(rule, per_key):
     kw = dict(seed=31, B=10, lengths=[70, 1, 64, 130, 5, 65, 0, 127, 33, 64], hq=8, hv=16, dk=128, dv=128,
               act="f16", rule=rule, state="random", state_std=0.3)
     if per_key:
-        kw.update(decay_per_key=True, gate_dtype="f32", write_gate=True)
+        kw.update(decay_per_key=True, gate_dtype="f32", write_gate=rule == "gdn2")
     p = workloads.make(**kw)
     ref_o, ref_fin, err = oracle.run_problem(p)
     assert err == 0
@@ -251,7 +266,8 @@ def test_chunked_many_chains(rule, per_key):
     dict(rule="gdn2", decay_per_key=True, gate_dtype="f32", write_gate=True),
     dict(rule="gated_delta", dk=64, dv=64),
     dict(rule="gated", decay_per_key=True, gate_dtype="f32"),
-], ids=["tc-gated_delta", "tc-linear", "tc-perkey-gdn2", "mma", "token-serial"])
+    dict(rule="gated", decay_per_key=True),
+], ids=["tc-gated_delta", "tc-linear", "tc-perkey-gdn2", "mma", "tc-perkey-gated", "token-serial"])
 def test_chunked_seq_lens_padded_rows(case):
     """Rank-4 batch whose rows are bounded by seq_lens ("gatedDeltaUpdate"):
     request b takes the first clamp(seq_lens[b], 0, S) tokens of its row, over

@@ -87,7 +87,8 @@ KM_CHUNKED = [
     dict(rule="delta", hq=8, hv=32, lengths=[70, 0, 130, 1, 64]),         # tcgen05, one CTA per chain
     dict(rule="gdn2", decay_per_key=True, gate_dtype="f32"),               # per-key prepare + chain
     dict(rule="gated_delta", dk=64, dv=64),                                # warp-level MMA kernel
-    dict(rule="gated", decay_per_key=True, gate_dtype="f32"),              # token-serial fallback
+    dict(rule="gated", decay_per_key=True, gate_dtype="f32"),              # per-key prepare, no retrieval
+    dict(rule="gated", decay_per_key=True),                                # token-serial fallback
 ]
 
 
