@@ -356,11 +356,9 @@ def kernel_name(p, path):
     if path == "recurrent":
         return token_serial()
     per_key = p.get("decay_per_key") and p["rule"] in ("gated", "gated_delta", "gdn2")
-    tc_shape = p["dk"] == 128 and p["dv"] == 128  # fp32 activations go through fp16 copies
-    erase = p.get("erase_gate") if p.get("erase_gate") is not None else p.get("beta")
-    f32_gates = (p.get("decay") is None or p["decay"].dtype == torch.float32 or not per_key) and \
-        (p["rule"] != "gdn2" or erase.dtype == torch.float32)
-    if tc_shape and f32_gates and (p["rule"] == "gdn2" or (per_key and p["rule"] in ("gated", "gated_delta"))):
+    # fp32 activations go through fp16 copies, fp16 per-key gate rows through fp32 copies
+    tc_shape = p["dk"] == 128 and p["dv"] == 128
+    if tc_shape and (p["rule"] == "gdn2" or (per_key and p["rule"] in ("gated", "gated_delta"))):
         return "chunk_prepare_perkey_kernel<%d>+chunk_chain_kernel<2>" % int(p["rule"] == "gdn2")
     if per_key:
         return token_serial()
@@ -378,7 +376,13 @@ def launches_per_call(p, path):
     k = kernel_name(p, path)
     if "chunk_chain_kernel" not in k:
         return 1
-    return 3 + (3 if p["act_dtype"] == "f32" else 0)  # + the fp16 copies of q, k, v
+    n = 3 + (3 if p["act_dtype"] == "f32" else 0)  # + the fp16 copies of q, k, v
+    if "perkey" in k:  # + the fp32 copies of fp16 per-key gate rows
+        if p.get("decay_per_key") and p["decay"].dtype == torch.float16:
+            n += 1
+        if p["rule"] == "gdn2" and p.get("erase_gate") is None and p["beta"].dtype == torch.float16:
+            n += 1
+    return n
 
 
 def kernel_source_digest(path, kernel=""):

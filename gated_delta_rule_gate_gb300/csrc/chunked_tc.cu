@@ -985,6 +985,11 @@ bool al16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 
 // fp32 -> fp16 copy of n elements (n a multiple of 4, both pointers 16-byte aligned): the
 // tensor-core prefill takes fp32 activations through fp16 copies in its workspace (its
 // products round their operands to fp16 anyway).
+__global__ void __launch_bounds__(256) f16_to_f32_kernel(const __half *src, float *dst, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = __half2float(src[i]);
+}
+
 __global__ void __launch_bounds__(256) f32_to_f16_kernel(const float4 *src, uint2 *dst, size_t n4) {
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 f = src[i];
@@ -994,7 +999,15 @@ __global__ void __launch_bounds__(256) f32_to_f16_kernel(const float4 *src, uint
 
 // bytes of each fp16 copy (256-byte aligned) for fp32 activations: q, k [T, Hq, 128], v [T, Hv, 128]
 size_t copy_bytes(const Problem &p, int heads) { return (((size_t)p.T * heads * 128 * 2) + 255) & ~(size_t)255; }
-size_t copies_bytes(const Problem &p) { return p.act_f16 ? 0 : 2 * copy_bytes(p, p.Hq) + copy_bytes(p, p.Hv); }
+// fp16 per-key gate rows that the per-key prepare pass lands by bulk copies get fp32 copies:
+// the log decay (or raw gate) and GDN-2's per-key beta (its erase gate)
+bool decay_copy(const Problem &p) { return (p.flags & kPerKey) && rule_has_decay(p.rule) && p.decay_f16; }
+bool erase_copy(const Problem &p) { return p.rule == kGdn2 && p.erase_gate == nullptr && p.beta_f16; }
+size_t gate_copy_bytes(const Problem &p) { return (((size_t)p.T * p.Hv * 128 * 4) + 255) & ~(size_t)255; }
+size_t copies_bytes(const Problem &p) {
+    return (p.act_f16 ? 0 : 2 * copy_bytes(p, p.Hq) + copy_bytes(p, p.Hv)) +
+           (decay_copy(p) ? gate_copy_bytes(p) : 0) + (erase_copy(p) ? gate_copy_bytes(p) : 0);
+}
 
 // slots for every chunk of pairwise disjoint requests: sum ceil(len / C) <= T / C + B
 int slot_capacity(const Problem &p) { return (int)((long long)p.T / TC_C + p.B + 1); }
@@ -1011,8 +1024,12 @@ bool chunked_tc_eligible(const Problem &p) {
     // GDN-2: the per-key prepare kernel.  Both feed the same chain kernel.
     const bool rule_ok = p.rule == kLinear || p.rule == kGated || p.rule == kDelta || p.rule == kGatedDelta;
     const bool scalar_ok = rule_ok && !((p.flags & kPerKey) && rule_has_decay(p.rule));
-    // fp32 activations run on fp16 copies made in the workspace
-    return (scalar_ok || chunk_prepare_perkey_eligible(p)) && p.dk == 128 && p.dv == 128 &&
+    // fp32 activations run on fp16 copies made in the workspace, fp16 per-key gate rows on
+    // fp32 copies
+    Problem pg = p;
+    if (decay_copy(p)) pg.decay_f16 = 0, pg.decay = p.q;  // (a 16-byte aligned stand-in for the copy)
+    if (erase_copy(p)) pg.beta_f16 = 0, pg.beta = p.q;
+    return (scalar_ok || chunk_prepare_perkey_eligible(pg)) && p.dk == 128 && p.dv == 128 &&
            al16(p.q) && al16(p.k) && al16(p.v) && al16(p.fin) && (p.init == nullptr || al16(p.init));
 }
 
@@ -1067,12 +1084,14 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         e = smem_attr(fns[f], f < 2 ? PR_SMEM : CH_SMEM);
         if (e != cudaSuccess) return e;
     }
+    const size_t cb = copies_bytes(p);
+    if (cb == 0) return launch_tc_f16(p, ws, ws_bytes, stream);
+    // fp32 activations: fp16 copies of q, k and v at the end of the workspace, the chain writing o
+    // in fp32; fp16 per-key gate rows: fp32 copies after them.  Then the same kernels on them.
+    if (p.B == 0 || ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
+    unsigned char *cp = static_cast<unsigned char *>(ws) + (chunked_tc_workspace_bytes(p) - cb);
+    Problem pc = p;
     if (!p.act_f16) {
-        // fp32 activations: fp16 copies of q, k and v at the end of the workspace, then the
-        // same kernels on them, the chain writing o in fp32
-        if (p.B == 0 || ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
-        unsigned char *cp = static_cast<unsigned char *>(ws) + (chunked_tc_workspace_bytes(p) - copies_bytes(p));
-        Problem pc = p;
         const void *src[3] = {p.q, p.k, p.v};
         const int heads[3] = {p.Hq, p.Hq, p.Hv};
         const void **dstp[3] = {&pc.q, &pc.k, &pc.v};
@@ -1085,13 +1104,26 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
             *dstp[t] = cp;
             cp += copy_bytes(p, heads[t]);
         }
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
         pc.act_f16 = 1;
         pc.o_f32 = 1;
-        return launch_tc_f16(pc, ws, ws_bytes - copies_bytes(p), stream);
     }
-    return launch_tc_f16(p, ws, ws_bytes, stream);
+    const bool cdec = decay_copy(p), cera = erase_copy(p);
+    for (int t = 0; t < 2; ++t) {
+        if (!(t == 0 ? cdec : cera)) continue;
+        const size_t n = (size_t)p.T * p.Hv * 128;
+        const long long blocks = std::min<long long>((long long)(n + 255) / 256, 8LL * sm_count());
+        if (blocks > 0)
+            f16_to_f32_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+                static_cast<const __half *>(t == 0 ? p.decay : p.beta), reinterpret_cast<float *>(cp), n);
+        if (t == 0)
+            pc.decay = cp, pc.decay_f16 = 0;
+        else
+            pc.beta = cp, pc.beta_f16 = 0;
+        cp += gate_copy_bytes(p);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_tc_f16(pc, ws, ws_bytes - cb, stream);
 }
 
 // the tensor-core prefill proper, on fp16 activations (its workspace: offsets, tables, images)

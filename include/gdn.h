@@ -247,12 +247,13 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  * dv a multiple of 16 (<= 256), q, k, v, o and the state 16-byte aligned.
  * fp32 activations are rounded to fp16 for the products (at dk = dv = 128
  * through fp16 copies of q, k and v that the library writes into the
- * workspace; o is still written in fp32).  Per-key decay (gated_delta) and
- * GDN2 run on the tensor cores when dk = dv = 128 and the per-key gates (log
- * decay, erase gate) are fp32 and 16-byte aligned; per-key log decays are expected <= 0 there (decays in
- * (0, 1], as the raw-gate arm always gives).  Other per-key problems (the
- * gated rule, fp16 per-key gates, other head sizes) run the token-serial
- * form (same result).
+ * workspace; o is still written in fp32).  Per-key decay (gated, gated_delta)
+ * and GDN2 run on the tensor cores when dk = dv = 128 and the per-key gate
+ * rows are 16-byte aligned (fp16 per-key log decays, and GDN2's fp16 per-key
+ * beta, through fp32 copies that the library writes into the workspace);
+ * per-key log decays are expected <= 0 there (decays in (0, 1], as the
+ * raw-gate arm always gives).  Per-key problems at other head sizes run the
+ * token-serial form (same result).
  *
  * Workspace: owned by the caller, device memory of at least
  * gdn_chunked_prefill_workspace_size() bytes, 256-byte aligned (NULL allowed
@@ -262,8 +263,9 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  * per-request chunk offsets, a chunk-slot -> request table and the requests
  * ordered by length (rounded up to 1 KB); then one 88 KB image per (chunk
  * slot, value head) of the chunk's state-independent operands (fp16); with
- * fp32 activations, last, the fp16 copies of q, k and v (each rounded up to
- * 256 bytes).
+ * fp32 activations, the fp16 copies of q, k and v (each rounded up to 256
+ * bytes); last, fp32 copies [total_tokens, Hv, 128] of fp16 per-key gate rows
+ * (the log decay; GDN2's per-key beta), each rounded up to 256 bytes.
  * Its contents are scratch, rewritten by every call on the stream; two calls
  * in flight at once need two workspaces.  Requests that share tokens can need
  * more slots than that; the ones past the capacity are skipped and

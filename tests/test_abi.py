@@ -145,6 +145,13 @@ def test_chunked_workspace_size():
                  act_dtype=N.DTYPE_F32)
     copy = lambda heads: -(-(T * heads * 128 * 2) // 256) * 256
     assert size(p) == head + images + 2 * copy(16) + copy(hv)
+    # fp16 per-key gate rows (log decay; GDN-2's per-key beta) take fp32 copies [T, Hv, 128]
+    gcopy = -(-(T * hv * 128 * 4) // 256) * 256
+    p = _problem(batch=B, total_tokens=T, num_heads_q=16, num_heads_v=hv, head_dim_k=128, head_dim_v=128,
+                 flags=N.FLAG_DECAY_PER_KEY, decay_dtype=N.DTYPE_F16, beta_dtype=N.DTYPE_F16)
+    assert size(p) == head + images + gcopy
+    p.rule = N.RULES["gdn2"]
+    assert size(p) == head + images + 2 * gcopy
 
 
 def test_chunked_rejects_a_small_workspace():

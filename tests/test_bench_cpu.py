@@ -74,10 +74,13 @@ def test_kernel_names_mirror_the_dispatch():
          "chunk_prepare_perkey_kernel<1>+chunk_chain_kernel<2>"),
         (dict(rule="gated_delta", decay_per_key=True, gate_dtype="f32"),
          "chunk_prepare_perkey_kernel<0>+chunk_chain_kernel<2>"),
-        (dict(rule="gated_delta", decay_per_key=True, lengths=[200]), "recurrent_long_kernel<128>"),
+        (dict(rule="gated_delta", decay_per_key=True, lengths=[200]),
+         "chunk_prepare_perkey_kernel<0>+chunk_chain_kernel<2>"),
+        (dict(rule="gated_delta", decay_per_key=True, lengths=[200], dk=64, dv=64), "recurrent_long_kernel<64>"),
         (dict(rule="gated", decay_per_key=True, gate_dtype="f32"),
          "chunk_prepare_perkey_kernel<0>+chunk_chain_kernel<2>"),
-        (dict(rule="gated", decay_per_key=True), "recurrent_pipe_kernel<128,false>"),
+        (dict(rule="gated", decay_per_key=True), "chunk_prepare_perkey_kernel<0>+chunk_chain_kernel<2>"),
+        (dict(rule="gated", decay_per_key=True, dk=64, dv=64), "recurrent_pipe_kernel<64,false>"),
         (dict(rule="gdn2", decay_per_key=True, gate_dtype="f32", erase="input", write_gate="input"),
          "chunk_prepare_perkey_kernel<1>+chunk_chain_kernel<2>"),
         (dict(rule="gated_delta", dk=64, dv=64), "chunked_mma_kernel<64,false>"),
@@ -87,7 +90,8 @@ def test_kernel_names_mirror_the_dispatch():
         kw.update(over)
         p = workloads.make(**kw)
         assert b.kernel_name(p, "chunked") == name, (over, b.kernel_name(p, "chunked"))
-        assert b.launches_per_call(p, "chunked") == (3 if "chain" in name else 1)
+        gate16 = over.get("decay_per_key") and "gate_dtype" not in over and "chain" in name
+        assert b.launches_per_call(p, "chunked") == ((4 if gate16 else 3) if "chain" in name else 1)
     p = workloads.make(**dict(base, rule="gated_delta", act="f32"))
     assert b.kernel_name(p, "chunked") == "chunk_prepare_kernel<1>+chunk_chain_kernel<2>"
     assert b.launches_per_call(p, "chunked") == 6

@@ -60,9 +60,12 @@ CASES += [
     dict(rule="gated", act="f16", dk=128, dv=128, hq=2, hv=4, decay_per_key=True, gate="log",
          logdecay_range=(-6.0, 0.0), l2norm_q=True),
     dict(rule="gated", act="f32", dk=128, dv=128, hq=1, hv=2, decay_per_key=True, gate_dtype="f32"),
-    # per-key gates in fp16 take the token-serial kernel
+    # per-key gates in fp16: the same path on fp32 copies of the gate rows
     dict(rule="gated_delta", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True),
     dict(rule="gated", act="f16", dk=128, dv=128, hq=1, hv=1, decay_per_key=True),
+    dict(rule="gdn2", act="f16", dk=128, dv=128, hq=1, hv=2, decay_per_key=True, write_gate=True),
+    # per-key decay at other head sizes: the token-serial kernel
+    dict(rule="gated", act="f16", dk=64, dv=64, hq=1, hv=1, decay_per_key=True),
 ]
 
 
@@ -267,7 +270,9 @@ def test_chunked_many_chains(rule, per_key):
     dict(rule="gated_delta", dk=64, dv=64),
     dict(rule="gated", decay_per_key=True, gate_dtype="f32"),
     dict(rule="gated", decay_per_key=True),
-], ids=["tc-gated_delta", "tc-linear", "tc-perkey-gdn2", "mma", "tc-perkey-gated", "token-serial"])
+    dict(rule="gated", decay_per_key=True, dk=64, dv=64),
+], ids=["tc-gated_delta", "tc-linear", "tc-perkey-gdn2", "mma", "tc-perkey-gated", "tc-perkey-f16-gates",
+        "token-serial"])
 def test_chunked_seq_lens_padded_rows(case):
     """Rank-4 batch whose rows are bounded by seq_lens ("gatedDeltaUpdate"):
     request b takes the first clamp(seq_lens[b], 0, S) tokens of its row, over

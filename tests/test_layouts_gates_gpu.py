@@ -88,7 +88,8 @@ KM_CHUNKED = [
     dict(rule="gdn2", decay_per_key=True, gate_dtype="f32"),               # per-key prepare + chain
     dict(rule="gated_delta", dk=64, dv=64),                                # warp-level MMA kernel
     dict(rule="gated", decay_per_key=True, gate_dtype="f32"),              # per-key prepare, no retrieval
-    dict(rule="gated", decay_per_key=True),                                # token-serial fallback
+    dict(rule="gated", decay_per_key=True),                                # per-key, fp16 gate copies
+    dict(rule="gated", decay_per_key=True, dk=64, dv=64),                  # token-serial fallback
 ]
 
 
@@ -158,7 +159,8 @@ GATES_CHUNKED = [
     dict(decay_per_key=False),                                             # scalar decay, same kernels
     dict(hq=8, hv=32, lengths=[70, 0, 130, 1, 64]),                        # one CTA per chain
     dict(dk=64, dv=64, decay_per_key=False),                               # warp-level MMA kernel
-    dict(gate_dtype="f16"),                                                # token-serial fallback
+    dict(gate_dtype="f16"),                                                # per-key, fp16 gate copies
+    dict(dk=64, dv=64, gate_dtype="f16"),                                  # token-serial fallback
 ]
 
 
