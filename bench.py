@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
                     [--workload decode-L1|decode-L4|decode-L1-kmajor|decode-L4-kmajor|
-                                ragged-prefill|long-prefill-<rule>|gdn2|gdn2-gates]
+                                ragged-prefill|long-prefill-<rule>|gdn2|gdn2-gates|gated-perkey]
                     [--no-extra]
 
 A step is one call of the library on one batch of the workload (the decode
@@ -63,6 +63,8 @@ def make_workload(name, seed_offset=0, shrink=1):
                                       S=8192 // shrink), "chunked"
     if name == "gdn2":
         return workloads.gdn2(seed=5 + seed_offset, S=4096 // shrink), "chunked"
+    if name == "gated-perkey":  # the gated rule with per-key decay (GLA-style gating)
+        return workloads.gated_perkey(seed=6 + seed_offset, S=4096 // shrink), "chunked"
     if name == "gdn2-gates":  # erase gate as its own input beside a scalar beta, write gate passed in
         return workloads.gdn2(seed=5 + seed_offset, S=4096 // shrink, erase="input", write_gate="input"), "chunked"
     raise SystemExit("unknown workload " + name)
@@ -655,7 +657,8 @@ def main():
         if not args.no_extra and world == 1:
             names = [n for n in ("decode-L1", "decode-L4", "decode-L1-kmajor", "decode-L4-kmajor",
                                  "ragged-prefill", "long-prefill-linear", "long-prefill-gated",
-                                 "long-prefill-delta", "long-prefill-gated_delta", "gdn2", "gdn2-gates")
+                                 "long-prefill-delta", "long-prefill-gated_delta", "gdn2", "gdn2-gates",
+                                 "gated-perkey")
                      if n != args.workload]
             del d, o, fin, prob
             torch.cuda.empty_cache()

@@ -240,10 +240,7 @@ def test_gated_per_key_long():
     """The gated rule with decay per key channel (no retrieval) on the per-key
     prepare pass: B = 2, S = 4096, H = 16 with the GDN-2 workload's gate
     distribution, random incoming state; both sequences."""
-    p = workloads.make(seed=6, B=2, seq_len=4096, hq=16, hv=16, dk=128, dv=128, act="f16", rule="gated",
-                       gate="raw", decay_per_key=True, gate_dtype="f32", a_log_range=(0.0, 0.0),
-                       dt_bias_range=(0.0, 0.0), state="random", state_std=0.02)
-    _full(p)
+    _full(workloads.gated_perkey(state="random"))
 
 
 @pytest.mark.parametrize("rule,per_key", [("linear", False), ("gated", False), ("delta", False),

@@ -185,6 +185,15 @@ def long_prefill(rule, seed=4, B=4, S=8192, h=16, dk=128, dv=128):
                 gate="raw", beta_dtype="f16")
 
 
+def gated_perkey(seed=6, B=2, S=4096, h=16, dk=128, dv=128, state="zero"):
+    """The gated rule (no retrieval) with decay per key channel, GLA-style:
+    the GDN-2 workload's per-key log decay -softplus(N(0,1)) (raw arm,
+    gate_scale = -1, gate_bias = 0), B = 2, S = 4096, H = 16, fp16, fp32 gates."""
+    return make(seed=seed, B=B, seq_len=S, hq=h, hv=h, dk=dk, dv=dv, act="f16", rule="gated", gate="raw",
+                decay_per_key=True, gate_dtype="f32", a_log_range=(0.0, 0.0), dt_bias_range=(0.0, 0.0),
+                state=state, state_std=0.02)
+
+
 def gdn2(seed=5, B=2, S=4096, h=16, dk=128, dv=128, erase="beta", write_gate="fold"):
     """GDN-2: per-key log decay -softplus(N(0,1)) (raw arm, gate_scale = -1,
     gate_bias = 0), erase gate sigmoid(N(0,1)) per key channel, write gate
