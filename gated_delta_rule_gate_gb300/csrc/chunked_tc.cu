@@ -623,10 +623,12 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
 constexpr int CH_THREADS = 448;
 constexpr int cImg = 0;                       // 2 x IM_BYTES
 constexpr int cS = 2 * IM_BYTES;              // 32 KB: Sh, 2 blocks [128 v][64 i]
-constexpr int cBar = cS + 32768;              // 11 mbarriers, TMEM address
+constexpr int cBar = cS + 32768;              // 12 mbarriers, TMEM address
 constexpr int CH_SMEM = cBar + 128 + 1024;
 static_assert(cS % 1024 == 0, "chain layout");
-constexpr uint32_t tS = 0, tO = 128;          // tensor-memory columns: S [0, 128), O^T [128, 192)
+// tensor-memory columns: S [0, 128), O^T [128, 192) (and [192, 256): the second O^T buffer of the
+// rules without E)
+constexpr uint32_t tS = 0, tO = 128;
 // what the state step of a rule needs beyond U^T Kt
 enum : int { kStepPlain = 0, kStepDecay = 1, kStepE = 2 };
 
@@ -640,6 +642,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     // chunk c runs while the state warps copy S_{c+1}; Sh then alternates between two buffers
     // (they fit in the 32 KB area at ROWS = 64) and its hand-over between two barriers.
     constexpr bool PIPE = HALF && STEP != kStepE;
+    // Rules without E: O^T alternates between two tensor-memory buffers, so the readout product
+    // of chunk c + 1 does not wait for the output warps to read chunk c (the delta rules' fused
+    // product needs O^T beside S: one buffer)
+    constexpr bool O2 = STEP != kStepE;
     constexpr int SHB = ROWS * 128;  // bytes per 64-column block of Sh
     extern __shared__ unsigned char smraw[];
     const uint32_t sb0 = ptx::smem_u32(smraw);
@@ -652,7 +658,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     uint64_t *barS = bars + 6;    // every product of chunk c done
     uint64_t *barO = bars + 7;    // O^T of chunk c done
     uint64_t *shready2 = bars + 8; // PIPE: Sh of the odd chunks written (shready: the even ones)
-    uint64_t *ofree = bars + 9;   // O^T of chunk c read by the output warps
+    uint64_t *ofree = bars + 9;   // O^T of chunk c read by the output warps (O2: the even chunks)
+    uint64_t *ofree2 = bars + 10; // O2: O^T of the odd chunks read
+    uint64_t *barO2 = bars + 11;  // O2: O^T of the odd chunks done (barO: the even ones)
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + cBar + 96);
     unsigned char *sS = sm + cS;
 
@@ -693,7 +701,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     }
 
     if (tid == 0) {
-        for (int i = 0; i < 11; ++i) ptx::mbar_init(&bars[i], 1);
+        for (int i = 0; i < 12; ++i) ptx::mbar_init(&bars[i], 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(tslot, 256);
@@ -808,11 +816,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         // ===================== outputs (128 threads): O^T[i][t] -> O[t][h][i]
         const int q4 = warp & 3, i = (HALF ? 16 : 32) * q4 + lane, ot = tid - 256;
         const bool live = !HALF || lane < 16;
-        const uint32_t lo = tmem + ((uint32_t)(32 * q4) << 16) + tO;
         const size_t rstride = (size_t)p.Hv * 128;
         bool ok = true;
         for (int c = 0; c < nch; ++c) {
-            ok = ptx::named_bar_and(2, 128, ptx::mbar_wait_sleep(barO, c & 1));
+            const bool odd = O2 && (c & 1);
+            const uint32_t lo = tmem + ((uint32_t)(32 * q4) << 16) + tO + (odd ? 64u : 0u);
+            ok = ptx::named_bar_and(2, 128, ptx::mbar_wait_sleep(odd ? barO2 : barO, O2 ? (c >> 1) & 1 : c & 1));
             if (!ok) break;
             tc::fence_after();
             float o0[32], o1[32];
@@ -820,7 +829,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             tc::ld32(lo + 32, o1);
             tc::fence_before();
             ptx::named_bar_sync(2, 128);
-            if (ot == 0) ptx::mbar_arrive(ofree);
+            if (ot == 0) ptx::mbar_arrive(odd ? ofree2 : ofree);
             const int n = live ? min(TC_C, t1 - (t0 + TC_C * c)) : 0;
             const size_t obase = ((size_t)(t0 + TC_C * c) * p.Hv + h) * 128 + 64 * vh + i;
             if (p.o_f32) {  // fp32 activations (the products ran on fp16 copies)
@@ -926,15 +935,20 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     tc::mma_f16(tmem + tS, tc::desc_adv(dU, s * 2048), tc::desc_adv(dKt, s * 2048), idUK, true);
                 if (PIPE) tc::commit(barS);  // S_{c+1} is complete
 
-                if (c >= 1) {  // the output warps have read O^T of chunk c - 1
-                    ok = ptx::mbar_wait_sleep(ofree, (c - 1) & 1);
+                // the output warps have read the O^T buffer of this chunk: of chunk c - 1 (one
+                // buffer) or c - 2 (O2)
+                const bool odd = O2 && (c & 1);
+                const uint32_t tOc = tO + (odd ? 64u : 0u);
+                if (c >= (O2 ? 2 : 1)) {
+                    ok = O2 ? ptx::mbar_wait_sleep(odd ? ofree2 : ofree, ((c - 2) >> 1) & 1)
+                            : ptx::mbar_wait_sleep(ofree, (c - 1) & 1);
                     if (!ok) break;
                     tc::fence_after();
                 }
                 // UP: O^T = U^T P^T (N = 64 r, K = 64 t; B K-major)
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
-                    tc::mma_f16(tmem + tO, tc::desc_adv(dU, s * 2048), tc::desc_adv(dP, s * 32), idUP, s > 0);
+                    tc::mma_f16(tmem + tOc, tc::desc_adv(dU, s * 2048), tc::desc_adv(dP, s * 32), idUP, s > 0);
                 if (PIPE) {
                     ok = ptx::mbar_wait_sleep((c & 1) ? shready2 : shready, (c >> 1) & 1);
                     if (!ok) break;
@@ -943,9 +957,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     // SQ: O^T += Sh Q'^T (N = 64 t, K = 128 i; both K-major)
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        tc::mma_f16(tmem + tO, tc::desc_adv(dSh, (s >> 2) * SHB + (s & 3) * 32),
+                        tc::mma_f16(tmem + tOc, tc::desc_adv(dSh, (s >> 2) * SHB + (s & 3) * 32),
                                     tc::desc_adv(dEQ, (s >> 2) * IM_EQ_BLK + IM_EQ_Q + (s & 3) * 32), idSQ, true);
-                    tc::commit(barO);
+                    tc::commit(odd ? barO2 : barO);
                     tc::commit(&freeb[bf]);
                     continue;
                 }
@@ -963,10 +977,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     // SQ: O^T += Sh Q'^T (N = 64 t, K = 128 i; both K-major)
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        tc::mma_f16(tmem + tO, tc::desc_adv(dSh0, (s >> 2) * SHB + (s & 3) * 32),
+                        tc::mma_f16(tmem + tOc, tc::desc_adv(dSh0, (s >> 2) * SHB + (s & 3) * 32),
                                     tc::desc_adv(dEQ, (s >> 2) * IM_EQ_BLK + IM_EQ_Q + (s & 3) * 32), idSQ, true);
                 }
-                tc::commit(barO);
+                tc::commit(odd ? barO2 : barO);
                 // every product of chunk c is done: S_{c+1} is complete and Sh is free
                 tc::commit(barS);
                 tc::commit(&freeb[bf]);
