@@ -637,9 +637,9 @@ cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_byte
     (void)chunk;
     if (chunked_tc_eligible(p)) return launch_chunked_tc(p, ws, ws_bytes, stream);
     if ((p.flags & kPerKey) && rule_has_decay(p.rule)) {
-        // Per-key decay outside the tcgen05 path's shapes and rules (the gated
-        // rule, other head sizes, fp32 activations) runs through the
-        // token-serial kernel (same result).
+        // Per-key decay outside the tcgen05 path's shapes (head sizes other
+        // than dk = dv = 128, unaligned rows) runs through the token-serial
+        // kernel (same result).
         return launch_recurrent(p, stream);
     }
     const bool g2 = p.rule == kGdn2;

@@ -1,9 +1,10 @@
 // chunked_tc.cu -- chunk-parallel prefill on the 5th-generation tensor cores
-// (tcgen05, accumulators in tensor memory), for dk = dv = 128, fp16
-// activations: the offsets kernel, the prepare pass for scalar decay (rules
-// linear / gated / delta / gated_delta), the chain kernel for every rule
-// (chunked_tc_perkey.cu holds the prepare pass for per-key decay and GDN-2)
-// and the launcher.
+// (tcgen05, accumulators in tensor memory), for dk = dv = 128: the offsets
+// kernel, the prepare pass for scalar decay (rules linear / gated / delta /
+// gated_delta), the chain kernel for every rule (chunked_tc_perkey.cu holds
+// the prepare pass for per-key decay and GDN-2) and the launcher, which first
+// writes fp16 copies of fp32 activations and fp32 copies of fp16 per-key gate
+// rows into the workspace when the problem has them.
 //
 // Same per-chunk algebra as chunked.cu (derived from the token recurrence;
 // see the comment there).  For one chunk of C = 64 tokens, with normalised

@@ -34,6 +34,10 @@
 // cores with the factor carried as a running product of per-token decays
 // (e^{Gamma_r - Gamma_{j-1}} = e^{Gamma_r - Gamma_j} alpha_j), so nothing
 // overflows or loses range however strong the decay.
+//
+// The gated rule with per-key decay (no retrieval: W = 0) takes the same pass
+// without the solve: U = V, Q' = Qh and E = Diag(e^{Gamma_C} - 1), so the
+// chain's S E applies the per-channel decay of the chunk.
 #include <algorithm>
 
 #include "chunk_image.cuh"
