@@ -21,6 +21,7 @@ is) on the host cores on bounded samples of the same workload.
 """
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -398,8 +399,12 @@ def kernel_source_digest(path, kernel=""):
         names = ["chunked.cu"]
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "gated_delta_rule_gate_gb300", "csrc", name)) as fh:
+            text = fh.read()
+        # the code only: comments and blank lines do not change a kernel
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 
