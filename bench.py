@@ -433,10 +433,11 @@ def peaks():
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_rate(p, budget_s, threads, max_requests=None):
+def oracle_rate(p, budget_s, threads, max_requests=None, real="f64"):
     """Oracle tokens/s on a bounded sample of the workload's requests (all
     value heads of each sampled request).  Grows the sample until one timed
-    pass takes >= budget_s seconds (or covers every request)."""
+    pass takes >= budget_s seconds (or covers every request).  ``real``: the
+    double build (the definition) or its float instantiation."""
     import oracle
     ranges = workloads.token_ranges(p)
     order = [b for b in range(p["batch"]) if ranges[b][1] > ranges[b][0]]
@@ -444,7 +445,7 @@ def oracle_rate(p, budget_s, threads, max_requests=None):
     while True:
         sample = order[:n]
         t = time.perf_counter()
-        oracle.run_problem(p, requests=sample, threads=threads)
+        oracle.run_problem(p, requests=sample, threads=threads, real=real)
         dt = time.perf_counter() - t
         toks = sum(ranges[b][1] - ranges[b][0] for b in sample)
         if dt >= budget_s or n >= len(order) or (max_requests and n >= max_requests):
@@ -531,16 +532,25 @@ def roofline(p, path, workload, kern_ms):
 
 
 def cpu_baseline(p, budget_s, single_thread_budget=None):
+    """The oracle on the host cores: the double build on every core; with
+    ``single_thread_budget`` also on one core, and its float instantiation on
+    every core and on one."""
     cores = cpu_cores()
     rate, sample, stoks, sdt = oracle_rate(p, budget_s, cores)
+    fmt = "%d of %d requests, all %d value heads (%d tokens, %.1f s), %s"
     out = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-           "sample": "%d of %d requests, all %d value heads (%d tokens, %.1f s), fp64"
-                     % (len(sample), p["batch"], p["hv"], stoks, sdt)}
+           "sample": fmt % (len(sample), p["batch"], p["hv"], stoks, sdt, "fp64")}
     if single_thread_budget:
         r1, s1, t1, d1 = oracle_rate(p, single_thread_budget, 1)
         out["single_thread"] = {"value": r1, "unit": "tokens/s", "cores": 1,
-                                "sample": "%d of %d requests, all %d value heads (%d tokens, %.1f s), fp64"
-                                          % (len(s1), p["batch"], p["hv"], t1, d1)}
+                                "sample": fmt % (len(s1), p["batch"], p["hv"], t1, d1, "fp64")}
+        rf, sf, tf, df = oracle_rate(p, single_thread_budget, cores, real="f32")
+        rf1, sf1, tf1, df1 = oracle_rate(p, single_thread_budget, 1, real="f32")
+        out["float32"] = {"value": rf, "unit": "tokens/s", "cores": cores,
+                          "sample": fmt % (len(sf), p["batch"], p["hv"], tf, df, "fp32 instantiation")}
+        out["float32_single_thread"] = {"value": rf1, "unit": "tokens/s", "cores": 1,
+                                        "sample": fmt % (len(sf1), p["batch"], p["hv"], tf1, df1,
+                                                         "fp32 instantiation")}
     return out
 
 

@@ -9,7 +9,10 @@ calls it.
 Inputs may be numpy arrays or CPU torch tensors of any float dtype; they are
 converted exactly to float64 (fp16 and fp32 embed exactly).  Outputs come back
 as float64 numpy arrays, unrounded; ``round_to`` rounds once (round to
-nearest even) to an activation dtype.
+nearest even) to an activation dtype.  ``real="f32"`` runs the float
+instantiation of the same source instead (inputs rounded to float32): only the
+benchmark's CPU-baseline leg uses it, to time it; every parity check uses the
+double build.
 """
 import ctypes
 import os
@@ -22,11 +25,12 @@ RULES = {"linear": 0, "gated": 1, "delta": 2, "gated_delta": 3, "gdn2": 4}
 ERR_BAD_SLOT = 1
 
 _dp = ctypes.POINTER(ctypes.c_double)
+_fp = ctypes.POINTER(ctypes.c_float)
 _ip = ctypes.POINTER(ctypes.c_int32)
 
 
-class _Problem(ctypes.Structure):
-    _fields_ = [
+def _problem_fields(creal, rp):
+    return [
         ("batch", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
         ("hq", ctypes.c_int32), ("hv", ctypes.c_int32),
         ("dk", ctypes.c_int32), ("dv", ctypes.c_int32),
@@ -35,30 +39,39 @@ class _Problem(ctypes.Structure):
         ("beta_sigmoid", ctypes.c_int32), ("decay_per_key", ctypes.c_int32),
         ("raw_gate", ctypes.c_int32), ("num_state_rows", ctypes.c_int32),
         ("threads", ctypes.c_int32),
-        ("scale", ctypes.c_double),
-        ("q", _dp), ("k", _dp), ("v", _dp),
-        ("decay", _dp), ("gate_bias", _dp), ("gate_scale", _dp), ("beta", _dp),
+        ("scale", creal),
+        ("q", rp), ("k", rp), ("v", rp),
+        ("decay", rp), ("gate_bias", rp), ("gate_scale", rp), ("beta", rp),
         ("cu_seqlens", _ip), ("slot_ids", _ip),
-        ("initial_state", _dp), ("final_state", _dp), ("o", _dp),
+        ("initial_state", rp), ("final_state", rp), ("o", rp),
         ("error_word", _ip), ("seq_lens", _ip), ("beta_shared", ctypes.c_int32),
-        ("state_kmajor", ctypes.c_int32), ("erase_gate", _dp), ("write_gate", _dp),
+        ("state_kmajor", ctypes.c_int32), ("erase_gate", rp), ("write_gate", rp),
     ]
 
 
-_lib = None
+class _Problem(ctypes.Structure):
+    _fields_ = _problem_fields(ctypes.c_double, _dp)
 
 
-def _load():
-    global _lib
-    if _lib is None:
-        path = _build.build()
-        lib = ctypes.CDLL(path)
-        lib.oracle_gdn.argtypes = [ctypes.POINTER(_Problem)]
+class _ProblemF32(ctypes.Structure):
+    _fields_ = _problem_fields(ctypes.c_float, _fp)
+
+
+# per arithmetic type: (numpy dtype, pointer type, problem struct)
+_REAL = {"f64": (np.float64, _dp, _Problem), "f32": (np.float32, _fp, _ProblemF32)}
+_libs = {}
+
+
+def _load(real="f64"):
+    if real not in _libs:
+        _, rp, prob = _REAL[real]
+        lib = ctypes.CDLL(_build.build(real=real))
+        lib.oracle_gdn.argtypes = [ctypes.POINTER(prob)]
         lib.oracle_gdn.restype = ctypes.c_int
-        lib.oracle_gate.argtypes = [ctypes.c_int64, ctypes.c_int32, _dp, _dp, _dp, _dp, _dp, _dp]
+        lib.oracle_gate.argtypes = [ctypes.c_int64, ctypes.c_int32, rp, rp, rp, rp, rp, rp]
         lib.oracle_gate.restype = ctypes.c_int
-        _lib = lib
-    return _lib
+        _libs[real] = lib
+    return _libs[real]
 
 
 def _f64(x):
@@ -112,7 +125,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         initial_state=None, final_state=None, num_state_rows=None, scale=0.0,
         l2norm_q=False, l2norm_k=False, beta_sigmoid=False, decay_per_key=False,
         threads=1, seq_lens=None, beta_shared=False, state_kmajor=False, erase_gate=None,
-        write_gate=None):
+        write_gate=None, real="f64"):
     """Runs the recurrence token by token in float64.
 
     q, k: [T, Hq, dk]; v: [T, Hv, dv] (rank-4 callers flatten [B, S] to T and
@@ -126,10 +139,16 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
     [rows, Hv, dk, dv] ("gatedDeltaUpdate") instead of [rows, Hv, dv, dk].
     ``erase_gate`` ([T, Hv, dk], rule gdn2): the GDN-2 erase gate as its own
     input, beta then being the scalar write rate; ``write_gate`` ([T, Hv, dv],
-    rule gdn2): the GDN-2 write gate, applied to v here.
+    rule gdn2): the GDN-2 write gate, applied to v here.  ``real``: "f64" (the
+    definition) or "f32" (the float instantiation, for timing only).
     """
-    lib = _load()
-    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    lib = _load(real)
+    dt, rp, Prob = _REAL[real]
+
+    def cv(x):
+        x = _f64(x)
+        return x if x is None or real == "f64" else np.ascontiguousarray(x.astype(dt))
+    q64, k64, v64 = cv(q), cv(k), cv(v)
     T, hq, dk = q64.shape
     hv, dv = v64.shape[1], v64.shape[2]
     cu = _i32(cu_seqlens)
@@ -137,7 +156,7 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
     sl = _i32(seq_lens)
     if batch is None:
         batch = (len(cu) - 1) if cu is not None else 1
-    init = _f64(initial_state)
+    init = cv(initial_state)
     if num_state_rows is None:
         if final_state is not None:
             num_state_rows = int(np.asarray(final_state.shape)[0])
@@ -146,36 +165,37 @@ def gdn(q, k, v, *, rule="gated_delta", decay=None, beta=None, gate_bias=None,
         else:
             num_state_rows = batch
     if final_state is not None:
-        fin = _f64(final_state).copy()
+        fin = cv(final_state).copy()
     elif init is not None:
         fin = init.copy()
     else:
-        fin = np.zeros((num_state_rows, hv, dk, dv) if state_kmajor else (num_state_rows, hv, dv, dk),
-                       np.float64)
-    o = np.full((T, hv, dv), np.nan, np.float64)
+        fin = np.zeros((num_state_rows, hv, dk, dv) if state_kmajor else (num_state_rows, hv, dv, dk), dt)
+    o = np.full((T, hv, dv), np.nan, dt)
     err = np.zeros(1, np.int32)
-    dec = _f64(decay)
-    bet = _f64(beta)
-    gb = _f64(gate_bias)
-    gs = _f64(gate_scale)
-    eg = _f64(erase_gate)
-    wg = _f64(write_gate)
+    dec = cv(decay)
+    bet = cv(beta)
+    gb = cv(gate_bias)
+    gs = cv(gate_scale)
+    eg = cv(erase_gate)
+    wg = cv(write_gate)
     raw = gb is not None or gs is not None
-    prob = _Problem(
+    prob = Prob(
         batch=batch, total_tokens=T, hq=hq, hv=hv, dk=dk, dv=dv, rule=RULES[rule],
         l2norm_q=int(l2norm_q), l2norm_k=int(l2norm_k), beta_sigmoid=int(beta_sigmoid),
         decay_per_key=int(decay_per_key), raw_gate=int(raw), num_state_rows=num_state_rows,
         threads=int(threads), scale=float(scale),
-        q=_ptr(q64, _dp), k=_ptr(k64, _dp), v=_ptr(v64, _dp),
-        decay=_ptr(dec, _dp), gate_bias=_ptr(gb, _dp), gate_scale=_ptr(gs, _dp),
-        beta=_ptr(bet, _dp), cu_seqlens=_ptr(cu, _ip), slot_ids=_ptr(slots, _ip),
-        initial_state=_ptr(init, _dp), final_state=_ptr(fin, _dp), o=_ptr(o, _dp),
+        q=_ptr(q64, rp), k=_ptr(k64, rp), v=_ptr(v64, rp),
+        decay=_ptr(dec, rp), gate_bias=_ptr(gb, rp), gate_scale=_ptr(gs, rp),
+        beta=_ptr(bet, rp), cu_seqlens=_ptr(cu, _ip), slot_ids=_ptr(slots, _ip),
+        initial_state=_ptr(init, rp), final_state=_ptr(fin, rp), o=_ptr(o, rp),
         error_word=_ptr(err, _ip), seq_lens=_ptr(sl, _ip), beta_shared=int(beta_shared),
-        state_kmajor=int(bool(state_kmajor)), erase_gate=_ptr(eg, _dp), write_gate=_ptr(wg, _dp),
+        state_kmajor=int(bool(state_kmajor)), erase_gate=_ptr(eg, rp), write_gate=_ptr(wg, rp),
     )
     rc = lib.oracle_gdn(ctypes.byref(prob))
     if rc != 0:
         raise ValueError("oracle_gdn rejected its arguments (rc=%d)" % rc)
+    if real != "f64":
+        o, fin = o.astype(np.float64), fin.astype(np.float64)
     return o, fin, int(err[0])
 
 
@@ -198,12 +218,12 @@ __all__ = ["gate", "gdn", "run_problem", "round_to", "RULES", "ERR_BAD_SLOT", "l
 os.environ.setdefault("OMP_WAIT_POLICY", "PASSIVE")
 
 
-def run_problem(p, threads=1, requests=None):
+def run_problem(p, threads=1, requests=None, real="f64"):
     """Runs the oracle on a problem dict (the layout ``workloads.make`` draws).
 
     ``requests`` optionally restricts the run to a subset of request indices
     (their tokens and state rows only); the other outputs stay NaN and the
-    other state rows keep their initial values.
+    other state rows keep their initial values.  ``real`` as for ``gdn``.
     """
     q, k, v = p["q"], p["k"], p["v"]
     T = p["total_tokens"]
@@ -266,7 +286,8 @@ def run_problem(p, threads=1, requests=None):
                             decay_per_key=p.get("decay_per_key", False), threads=threads,
                             beta_shared=p.get("beta_shared", False),
                             state_kmajor=p.get("state_kmajor", False),
-                            erase_gate=take(p.get("erase_gate")), write_gate=take(p.get("write_gate")))
+                            erase_gate=take(p.get("erase_gate")), write_gate=take(p.get("write_gate")),
+                            real=real)
         o = np.full((T, p["hv"], p["dv"]), np.nan)
         if len(idx):
             o[idx] = o_s
@@ -280,4 +301,4 @@ def run_problem(p, threads=1, requests=None):
                beta_sigmoid=p.get("beta_sigmoid", False),
                decay_per_key=p.get("decay_per_key", False), threads=threads, seq_lens=sl,
                beta_shared=p.get("beta_shared", False), state_kmajor=p.get("state_kmajor", False),
-               erase_gate=p.get("erase_gate"), write_gate=p.get("write_gate"))
+               erase_gate=p.get("erase_gate"), write_gate=p.get("write_gate"), real=real)

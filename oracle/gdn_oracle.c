@@ -67,7 +67,7 @@
  * delta = beta (w .* v) - u, with beta == 1 when the erase gate rides in
  * beta (proposal A) and w == 1 when no write gate is passed.
  */
-#include <math.h>
+#include <tgmath.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -75,6 +75,15 @@
 #ifdef _OPENMP
 #include <omp.h>
 #endif
+
+/* The arithmetic type.  The definition is the double build (parity); the same
+ * source compiled with -DORACLE_REAL=float is a float instantiation that the
+ * benchmark times beside it (tgmath.h sends exp, log1p and sqrt to the
+ * function of the argument's type). */
+#ifndef ORACLE_REAL
+#define ORACLE_REAL double
+#endif
+typedef ORACLE_REAL real;
 
 #define ORACLE_RULE_LINEAR 0
 #define ORACLE_RULE_GATED 1
@@ -95,38 +104,38 @@ typedef struct {
     int32_t raw_gate;      /* decay holds the raw gate; gate_bias/gate_scale set */
     int32_t num_state_rows;
     int32_t threads;
-    double scale;                /* 0 selects 1/sqrt(dk) */
-    const double *q, *k, *v;     /* [T,Hq,dk], [T,Hq,dk], [T,Hv,dv] */
-    const double *decay;         /* [T,Hv] or [T,Hv,dk] */
-    const double *gate_bias;     /* [Hv] or [Hv,dk] (raw arm) */
-    const double *gate_scale;    /* [Hv] (raw arm) */
-    const double *beta;          /* [T,Hv]; GDN-2: [T,Hv,dk] */
+    real scale;                /* 0 selects 1/sqrt(dk) */
+    const real *q, *k, *v;     /* [T,Hq,dk], [T,Hq,dk], [T,Hv,dv] */
+    const real *decay;         /* [T,Hv] or [T,Hv,dk] */
+    const real *gate_bias;     /* [Hv] or [Hv,dk] (raw arm) */
+    const real *gate_scale;    /* [Hv] (raw arm) */
+    const real *beta;          /* [T,Hv]; GDN-2: [T,Hv,dk] */
     const int32_t *cu_seqlens;   /* [B+1] or NULL */
     const int32_t *slot_ids;     /* [B] or NULL */
-    const double *initial_state; /* [rows,Hv,dv,dk] or NULL */
-    double *final_state;         /* [rows,Hv,dv,dk] */
-    double *o;                   /* [T,Hv,dv] */
+    const real *initial_state; /* [rows,Hv,dv,dk] or NULL */
+    real *final_state;         /* [rows,Hv,dv,dk] */
+    real *o;                   /* [T,Hv,dv] */
     int32_t *error_word;         /* may be NULL */
     const int32_t *seq_lens;     /* [B] or NULL: rows of the uniform layout shortened */
     int32_t beta_shared;         /* scalar beta is [T]: one per token for every value head */
     int32_t state_kmajor;        /* states are [rows,Hv,dk,dv] (key-major) instead of [rows,Hv,dv,dk] */
-    const double *erase_gate;    /* GDN-2 proposal (B): [T,Hv,dk]; beta is then scalar */
-    const double *write_gate;    /* GDN-2: [T,Hv,dv] or NULL (w == 1) */
+    const real *erase_gate;    /* GDN-2 proposal (B): [T,Hv,dk]; beta is then scalar */
+    const real *write_gate;    /* GDN-2: [T,Hv,dv] or NULL (w == 1) */
 } oracle_problem;
 
 /* softplus(x) = ln(1 + e^x), evaluated without overflow. */
-static double softplus(double x) {
+static real softplus(real x) {
     return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));
 }
 
-static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+static real sigmoid(real x) { return 1.0 / (1.0 + exp(-x)); }
 
 /* "com.microsoft.LinearAttentionGate", Description:
  * decay = decay_scale * softplus(a + dt_bias); beta = sigmoid(b) when asked.
  * a and b are [n, h] with the head axis last. */
-int oracle_gate(int64_t n, int32_t h, const double *a, const double *dt_bias,
-                const double *decay_scale, const double *b, double *decay_out,
-                double *beta_out) {
+int oracle_gate(int64_t n, int32_t h, const real *a, const real *dt_bias,
+                const real *decay_scale, const real *b, real *decay_out,
+                real *beta_out) {
     if (n < 0 || h <= 0 || !a || !dt_bias || !decay_scale || !decay_out) return 1;
     if (beta_out && !b) return 1;
     for (int64_t i = 0; i < n; ++i) {
@@ -157,10 +166,10 @@ static void request_range(const oracle_problem *p, int32_t b, int32_t *t0, int32
     }
 }
 
-static void l2_normalise(double *x, int32_t n) {
-    double ss = 0.0;
+static void l2_normalise(real *x, int32_t n) {
+    real ss = 0.0;
     for (int32_t i = 0; i < n; ++i) ss += x[i] * x[i];
-    double inv = 1.0 / sqrt(ss + 1e-12);
+    real inv = 1.0 / sqrt(ss + 1e-12);
     for (int32_t i = 0; i < n; ++i) x[i] *= inv;
 }
 
@@ -172,7 +181,7 @@ static int rule_has_retrieval(int32_t r) {
 }
 
 /* One (request, value head) pair, token by token. */
-static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work) {
+static void run_pair(const oracle_problem *p, int32_t b, int32_t h, real *work) {
     const int32_t dk = p->dk, dv = p->dv, hq = p->hq, hv = p->hv;
     const int32_t qh = (int32_t)((int64_t)h * hq / hv); /* grouped heads */
     const int32_t row = p->slot_ids ? p->slot_ids[b] : b;
@@ -183,46 +192,46 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
         }
         return;
     }
-    double *M = work;                 /* dv * dk */
-    double *kv = M + (size_t)dv * dk; /* dk */
-    double *qv = kv + dk;             /* dk */
-    double *alpha = qv + dk;          /* dk */
-    double *kappa = alpha + dk;       /* dk */
-    double *u = kappa + dk;           /* dv */
-    double *delta = u + dv;           /* dv */
+    real *M = work;                 /* dv * dk */
+    real *kv = M + (size_t)dv * dk; /* dk */
+    real *qv = kv + dk;             /* dk */
+    real *alpha = qv + dk;          /* dk */
+    real *kappa = alpha + dk;       /* dk */
+    real *u = kappa + dk;           /* dv */
+    real *delta = u + dv;           /* dv */
 
     const size_t state_off = (((size_t)row * hv) + h) * (size_t)dv * dk;
     if (!p->initial_state)
-        memset(M, 0, sizeof(double) * (size_t)dv * dk);
+        memset(M, 0, sizeof(real) * (size_t)dv * dk);
     else if (p->state_kmajor) /* stored [dk][dv]: element (i, c) of M at c * dv + i */
         for (int32_t i = 0; i < dv; ++i)
             for (int32_t c = 0; c < dk; ++c) M[(size_t)i * dk + c] = p->initial_state[state_off + (size_t)c * dv + i];
     else
-        memcpy(M, p->initial_state + state_off, sizeof(double) * (size_t)dv * dk);
+        memcpy(M, p->initial_state + state_off, sizeof(real) * (size_t)dv * dk);
 
-    const double scale = p->scale != 0.0 ? p->scale : 1.0 / sqrt((double)dk);
+    const real scale = p->scale != 0.0 ? p->scale : 1.0 / sqrt((real)dk);
     int32_t t0, t1;
     request_range(p, b, &t0, &t1);
 
     for (int32_t t = t0; t < t1; ++t) {
-        const double *kin = p->k + ((size_t)t * hq + qh) * dk;
-        const double *qin = p->q + ((size_t)t * hq + qh) * dk;
-        const double *vin = p->v + ((size_t)t * hv + h) * dv;
-        memcpy(kv, kin, sizeof(double) * dk);
-        memcpy(qv, qin, sizeof(double) * dk);
+        const real *kin = p->k + ((size_t)t * hq + qh) * dk;
+        const real *qin = p->q + ((size_t)t * hq + qh) * dk;
+        const real *vin = p->v + ((size_t)t * hv + h) * dv;
+        memcpy(kv, kin, sizeof(real) * dk);
+        memcpy(qv, qin, sizeof(real) * dk);
         if (p->l2norm_k) l2_normalise(kv, dk);
         if (p->l2norm_q) l2_normalise(qv, dk);
 
         /* decay: alpha_c = exp(g_c); scalar decay broadcasts over c */
         if (rule_has_decay(p->rule)) {
             for (int32_t c = 0; c < dk; ++c) {
-                double g;
+                real g;
                 if (p->decay_per_key) {
-                    double raw = p->decay[((size_t)t * hv + h) * dk + c];
+                    real raw = p->decay[((size_t)t * hv + h) * dk + c];
                     g = p->raw_gate ? p->gate_scale[h] * softplus(raw + p->gate_bias[(size_t)h * dk + c])
                                     : raw;
                 } else {
-                    double raw = p->decay[(size_t)t * hv + h];
+                    real raw = p->decay[(size_t)t * hv + h];
                     g = p->raw_gate ? p->gate_scale[h] * softplus(raw + p->gate_bias[h]) : raw;
                 }
                 alpha[c] = exp(g);
@@ -235,7 +244,7 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
             /* erase gate b: its own input (proposal B, taken as given) or the
              * per-key beta (proposal A, through the sigmoid when asked) */
             for (int32_t c = 0; c < dk; ++c) {
-                double bc;
+                real bc;
                 if (p->erase_gate) {
                     bc = p->erase_gate[((size_t)t * hv + h) * dk + c];
                 } else {
@@ -245,40 +254,40 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
                 kappa[c] = bc * kv[c];
             }
             /* the write's scalar: beta under proposal B, 1 under proposal A */
-            double beta = 1.0;
+            real beta = 1.0;
             if (p->erase_gate) {
                 beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];
                 if (p->beta_sigmoid) beta = sigmoid(beta);
             }
             for (int32_t i = 0; i < dv; ++i) {
-                double s = 0.0;
+                real s = 0.0;
                 for (int32_t c = 0; c < dk; ++c) s += M[(size_t)i * dk + c] * kappa[c];
                 u[i] = s;
             }
             for (int32_t i = 0; i < dv; ++i) {
-                const double w = p->write_gate ? p->write_gate[((size_t)t * hv + h) * dv + i] : 1.0;
+                const real w = p->write_gate ? p->write_gate[((size_t)t * hv + h) * dv + i] : 1.0;
                 delta[i] = beta * (w * vin[i]) - u[i];
             }
         } else if (rule_has_retrieval(p->rule)) {
-            double beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];
+            real beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];
             if (p->beta_sigmoid) beta = sigmoid(beta);
-            memcpy(kappa, kv, sizeof(double) * dk);
+            memcpy(kappa, kv, sizeof(real) * dk);
             for (int32_t i = 0; i < dv; ++i) {
-                double s = 0.0;
+                real s = 0.0;
                 for (int32_t c = 0; c < dk; ++c) s += M[(size_t)i * dk + c] * kappa[c];
                 u[i] = s;
             }
             for (int32_t i = 0; i < dv; ++i) delta[i] = beta * (vin[i] - u[i]);
         } else {
-            memcpy(delta, vin, sizeof(double) * dv);
+            memcpy(delta, vin, sizeof(real) * dv);
         }
 
         for (int32_t i = 0; i < dv; ++i)
             for (int32_t c = 0; c < dk; ++c) M[(size_t)i * dk + c] += delta[i] * kv[c];
 
-        double *out = p->o + ((size_t)t * hv + h) * dv;
+        real *out = p->o + ((size_t)t * hv + h) * dv;
         for (int32_t i = 0; i < dv; ++i) {
-            double s = 0.0;
+            real s = 0.0;
             for (int32_t c = 0; c < dk; ++c) s += M[(size_t)i * dk + c] * qv[c];
             out[i] = scale * s;
         }
@@ -287,7 +296,7 @@ static void run_pair(const oracle_problem *p, int32_t b, int32_t h, double *work
         for (int32_t i = 0; i < dv; ++i)
             for (int32_t c = 0; c < dk; ++c) p->final_state[state_off + (size_t)c * dv + i] = M[(size_t)i * dk + c];
     else
-        memcpy(p->final_state + state_off, M, sizeof(double) * (size_t)dv * dk);
+        memcpy(p->final_state + state_off, M, sizeof(real) * (size_t)dv * dk);
 }
 
 /* Runs every (request, value head) pair.  Returns 0, or 1 on bad arguments. */
@@ -309,7 +318,7 @@ int oracle_gdn(const oracle_problem *p) {
     const int64_t pairs = (int64_t)p->batch * p->hv;
     const size_t per = (size_t)p->dv * p->dk + 4 * (size_t)p->dk + 2 * (size_t)p->dv;
     int nthreads = p->threads > 0 ? p->threads : 1;
-    double *work = (double *)malloc(sizeof(double) * per * (size_t)nthreads);
+    real *work = (real *)malloc(sizeof(real) * per * (size_t)nthreads);
     if (!work) return 2;
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
     for (int64_t i = 0; i < pairs; ++i) {

@@ -652,3 +652,22 @@ def test_gdn2_write_gate_input_equals_folded():
                            initial_state=S0, decay_per_key=True)
     np.testing.assert_allclose(o3, o1, rtol=1e-14, atol=1e-15)
     np.testing.assert_allclose(f3, f1, rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("rule", ["linear", "gated_delta", "gdn2"])
+def test_float_instantiation_tracks_the_double_build(rule):
+    """The float instantiation of the oracle source (timed as a CPU baseline,
+    never used for parity) computes the same recurrence: within fp32 rounding
+    of the double build on a small random problem."""
+    kw = dict(seed=7, B=3, lengths=[9, 0, 17], hq=2, hv=4, dk=16, dv=8, act="f32", rule=rule,
+              state="random", state_std=0.3)
+    if rule == "gdn2":
+        kw.update(decay_per_key=True, gate_dtype="f32")
+    p = workloads.make(**kw)
+    o64, f64, e64 = oracle.run_problem(p)
+    o32, f32, e32 = oracle.run_problem(p, real="f32")
+    assert e64 == e32 == 0
+    m = ~np.isnan(o64)
+    assert np.array_equal(m, ~np.isnan(o32))
+    assert np.abs(o32[m] - o64[m]).max() <= 1e-5 * np.abs(o64[m]).max()
+    assert np.abs(f32 - f64).max() <= 1e-5 * np.abs(f64).max()
