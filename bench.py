@@ -318,31 +318,67 @@ def time_device(api, prob, path, steps, warmup, stream, barrier):
 
 def time_e2e(api, p, d, prob, path, steps, warmup, stream, dev):
     """Every step: pinned host -> device copies of the step's inputs, the call,
-    and a device -> host copy of the output."""
+    and a device -> host copy of the output.  Steps run through two sets of
+    device input and output buffers, with the copies on their own streams, so
+    the input copies of one step overlap the call of the step before and its
+    output copy (the other direction) the input copies of the step after; the
+    state (slab or final state) and the workspace are shared and the calls run
+    in order on ``stream``.  The timed region spans the first input copy to the
+    last output copy."""
     names = [k for k in ("q", "k", "v", "decay", "beta", "erase_gate", "write_gate", "cu_seqlens", "slot_ids")
              if p.get(k) is not None]
     host = {k: p[k].contiguous().pin_memory() for k in names}
-    o_host = torch.empty(p["v"].shape, dtype=p["v"].dtype).pin_memory()
     o_dev = prob._keep[3]
+    fin = prob._keep[4]
+    d2 = dict(d)
+    for k in names:
+        d2[k] = torch.empty_like(d[k])
+    o2 = torch.empty_like(o_dev)
+    prob2 = build_problem(api, p, d2, o2, fin)
+    prob2._ws_buf = prob._ws_buf
+    sets = [(d, prob, o_dev), (d2, prob2, o2)]
+    o_host = [torch.empty(p["v"].shape, dtype=p["v"].dtype).pin_memory() for _ in range(2)]
     h2d = sum(_nbytes(host[k]) for k in names)
-    d2h = _nbytes(o_host)
+    d2h = _nbytes(o_host[0])
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        with torch.cuda.stream(stream):
+    def one(i):
+        b = i & 1
+        dd, pr, od = sets[b]
+        if i >= 2:
+            cin.wait_event(ev_done[b])  # the call of step i - 2 has read this input set
+        with torch.cuda.stream(cin):
             for k in names:
-                d[k].copy_(host[k], non_blocking=True)
-            launch(api, prob, path, stream)
-            o_host.copy_(o_dev.view(o_host.shape), non_blocking=True)
+                dd[k].copy_(host[k], non_blocking=True)
+        ev_in[b].record(cin)
+        stream.wait_event(ev_in[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])  # the output of step i - 2 has been copied out
+        launch(api, pr, path, stream)
+        ev_done[b].record(stream)
+        cout.wait_event(ev_done[b])
+        with torch.cuda.stream(cout):
+            o_host[b].copy_(od.view(o_host[b].shape), non_blocking=True)
+        ev_out[b].record(cout)
 
-    for _ in range(warmup):
-        one()
+    def run(n):
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        cin.wait_event(start)
+        for i in range(n):
+            one(i)
+        for b in range(min(n, 2)):
+            stream.wait_event(ev_out[b])
+        end = torch.cuda.Event(enable_timing=True)
+        end.record(stream)
+        return start, end
+
+    run(warmup)
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        one()
-    t1.record(stream)
+    t0, t1 = run(steps)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1), h2d, d2h
 
