@@ -321,3 +321,29 @@ def test_chunked_ignores_uncovered_tokens(case):
     assert err == 0
     o, fin, _ = run(p, path="chunked")
     _check(p, o, fin, ref_o, ref_fin)
+
+
+@pytest.mark.parametrize("dk", [16, 128])
+def test_chunked_widest_value_heads(dk):
+    """dv = 256, the widest value head the chunked entry point takes (the
+    warp-level MMA kernel), over several chunks and a ragged tail."""
+    p = workloads.make(seed=51 + dk, B=3, lengths=[130, 0, 67], hq=1, hv=2, dk=dk, dv=256, act="f16",
+                       rule="gated_delta", state="random", state_std=0.3)
+    ref_o, ref_fin, err = oracle.run_problem(p, threads=THREADS)
+    assert err == 0
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
+
+
+def test_chunked_more_requests_than_the_order_sort_takes():
+    """2100 requests, past the 2048 the offsets kernel sorts longest first (it
+    keeps index order above that): lengths 0..96 tokens, so the workspace holds
+    T / 64 + B + 1 slots and every chain runs on its own CTA."""
+    g = torch.Generator().manual_seed(52)
+    lengths = torch.randint(0, 97, (2100,), generator=g).tolist()
+    p = workloads.make(seed=52, B=len(lengths), lengths=lengths, hq=1, hv=1, dk=128, dv=128, act="f16",
+                       rule="gated_delta", state="random", state_std=0.3)
+    ref_o, ref_fin, err = oracle.run_problem(p, threads=THREADS)
+    assert err == 0
+    o, fin, _ = run(p, path="chunked")
+    _check(p, o, fin, ref_o, ref_fin)
