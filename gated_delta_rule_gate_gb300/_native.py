@@ -19,8 +19,8 @@ FLAG_STATE_KMAJOR = 0x20
 DEVERR_BAD_SLOT, DEVERR_TIMEOUT, DEVERR_OVERLAP, DEVERR_DECAY_RANGE = 0x1, 0x2, 0x4, 0x8
 
 EXPORTS = ("gdn_gate", "gdn_recurrent_step", "gdn_chunked_prefill_workspace_size",
-           "gdn_chunked_prefill", "gdn_chunked_prefill_noalloc", "gdn_status_string",
-           "gdn_last_error_message")
+           "gdn_chunked_prefill_workspace_size_min", "gdn_chunked_prefill", "gdn_chunked_prefill_noalloc",
+           "gdn_status_string", "gdn_last_error_message")
 
 _vp = ctypes.c_void_p
 
@@ -87,6 +87,8 @@ def load():
         lib.gdn_recurrent_step.restype = ctypes.c_int
         lib.gdn_chunked_prefill_workspace_size.argtypes = [ctypes.POINTER(GdnProblem), ctypes.c_int32]
         lib.gdn_chunked_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.gdn_chunked_prefill_workspace_size_min.argtypes = [ctypes.POINTER(GdnProblem), ctypes.c_int32]
+        lib.gdn_chunked_prefill_workspace_size_min.restype = ctypes.c_size_t
         lib.gdn_chunked_prefill.argtypes = [ctypes.POINTER(GdnProblem), ctypes.c_int32, _vp,
                                             ctypes.c_size_t, _vp]
         lib.gdn_chunked_prefill.restype = ctypes.c_int

@@ -148,6 +148,13 @@ def gdn_chunked_prefill_workspace_size(problem, chunk_size=64):
     return n
 
 
+def gdn_chunked_prefill_workspace_size_min(problem, chunk_size=64):
+    n = N.load().gdn_chunked_prefill_workspace_size_min(ctypes.byref(problem), int(chunk_size))
+    if n == ctypes.c_size_t(-1).value:
+        raise N.GdnError(N.GDN_ERR_UNSUPPORTED, N.last_error_message())
+    return n
+
+
 def gdn_chunked_prefill(problem=None, chunk_size=64, workspace=None, *, stream=None, **kw):
     """Chunk-parallel recurrence (same result within the tensor-core
     tolerance).  Allocates the workspace with torch when none is given."""

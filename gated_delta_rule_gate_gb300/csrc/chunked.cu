@@ -617,6 +617,10 @@ size_t chunked_workspace_bytes(const Problem &p, int) {
     return chunked_tc_eligible(p) ? chunked_tc_workspace_bytes(p) : 0;
 }
 
+size_t chunked_workspace_min_bytes(const Problem &p, int) {
+    return chunked_tc_eligible(p) ? chunked_tc_workspace_min_bytes(p) : 0;
+}
+
 bool chunked_supported(const Problem &p, int, const char **why) {
     if (!(p.dk == 16 || p.dk == 32 || p.dk == 64 || p.dk == 128)) {
         *why = "head_dim_k must be 16, 32, 64 or 128";

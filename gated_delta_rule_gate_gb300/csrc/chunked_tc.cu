@@ -1028,8 +1028,26 @@ size_t copies_bytes(const Problem &p) {
 int slot_capacity(const Problem &p) { return (int)((long long)p.T / TC_C + p.B + 1); }
 // workspace head: chunk offsets (B + 1 ints), the slot -> request table (one int
 // per slot) and the request order (B ints), rounded up to 1 KB
-size_t head_bytes(const Problem &p) {
-    return (((size_t)2 * p.B + 1 + (size_t)slot_capacity(p)) * sizeof(int) + 1023) & ~(size_t)1023;
+// offsets [B + 1], slot -> request [cap], order [B], rounded to 1 KB
+size_t head_bytes(const Problem &p, int cap) {
+    return (((size_t)2 * p.B + 1 + (size_t)cap) * sizeof(int) + 1023) & ~(size_t)1023;
+}
+size_t head_bytes(const Problem &p) { return head_bytes(p, slot_capacity(p)); }
+// the windowed call: the per-request window ranges [B][2] (rounded to 256 bytes), then a head
+// and images for W chunks of every request: at most window_fixed + W * window_per_chunk bytes
+size_t window_bytes(const Problem &p) { return ((size_t)2 * p.B * sizeof(int) + 255) & ~(size_t)255; }
+size_t window_fixed(const Problem &p) { return window_bytes(p) + ((size_t)2 * p.B + 1) * sizeof(int) + 1023; }
+size_t window_per_chunk(const Problem &p) { return (size_t)p.B * ((size_t)p.Hv * IM_BYTES + sizeof(int)); }
+
+// The windowed call: window w holds chunks [w W, (w + 1) W) of every request.
+__global__ void __launch_bounds__(256) window_ranges_kernel(Problem p, int w, int W, int32_t *win) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= p.B) return;
+    int t0, t1;
+    request_range(p, b, t0, t1);  // (p.win is null here: the request's own range)
+    const long long a = (long long)t0 + (long long)w * W * TC_C, c = a + (long long)W * TC_C;
+    win[2 * b] = (int)(a < t1 ? a : t1);
+    win[2 * b + 1] = (int)(c < t1 ? c : t1);
 }
 
 }  // namespace
@@ -1052,6 +1070,14 @@ bool chunked_tc_eligible(const Problem &p) {
 size_t chunked_tc_workspace_bytes(const Problem &p) {
     if (p.B == 0) return 0;
     return head_bytes(p) + (size_t)slot_capacity(p) * p.Hv * IM_BYTES + copies_bytes(p);
+}
+
+// one chunk per request at a time (the windowed call with W = 1)
+size_t chunked_tc_workspace_min_bytes(const Problem &p) {
+    if (p.B == 0) return 0;
+    const size_t full = chunked_tc_workspace_bytes(p);
+    const size_t one = ((window_fixed(p) + window_per_chunk(p) + 255) & ~(size_t)255) + copies_bytes(p);
+    return one < full ? one : full;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1083,7 +1109,7 @@ bool make_kqv_map(CUtensorMap *m, const void *base, int heads, int tokens) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream);
+static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, int cap, cudaStream_t stream);
 
 cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream) {
     const void *fns[8] = {(const void *)chunk_prepare_kernel<true>,
@@ -1100,11 +1126,12 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
         if (e != cudaSuccess) return e;
     }
     const size_t cb = copies_bytes(p);
-    if (cb == 0) return launch_tc_f16(p, ws, ws_bytes, stream);
+    if (p.B == 0) return cudaSuccess;
     // fp32 activations: fp16 copies of q, k and v at the end of the workspace, the chain writing o
     // in fp32; fp16 per-key gate rows: fp32 copies after them.  Then the same kernels on them.
-    if (p.B == 0 || ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
-    unsigned char *cp = static_cast<unsigned char *>(ws) + (chunked_tc_workspace_bytes(p) - cb);
+    if (ws == nullptr || ws_bytes < chunked_tc_workspace_min_bytes(p)) return cudaErrorInvalidValue;
+    const size_t avail = (ws_bytes - cb) & ~(size_t)255;  // the copies sit above it, 256-byte aligned
+    unsigned char *cp = static_cast<unsigned char *>(ws) + avail;
     Problem pc = p;
     if (!p.act_f16) {
         const void *src[3] = {p.q, p.k, p.v};
@@ -1138,11 +1165,35 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_tc_f16(pc, ws, ws_bytes - cb, stream);
+    const int full_cap = slot_capacity(p);
+    if (avail >= head_bytes(p, full_cap) + (size_t)full_cap * p.Hv * IM_BYTES)
+        return launch_tc_f16(pc, ws, avail, full_cap, stream);
+    // Windowed: W chunks of every request at a time, as many as the workspace holds.  Window w
+    // reads the state window w - 1 left in final_state (fp32, so the carry is exact) and writes
+    // its outputs in place; a request past its end is empty in a window and keeps its state.
+    const size_t wb = window_bytes(p), fixed = window_fixed(p);
+    const long long W = avail > fixed ? (long long)((avail - fixed) / window_per_chunk(p)) : 0;
+    if (W < 1) return cudaErrorInvalidValue;
+    // the longest a request can be: the uniform length, else every token
+    const long long L = p.cu ? p.T : (p.seq_len ? p.seq_len : (long long)p.T / p.B);
+    const long long nwin = ((L + TC_C - 1) / TC_C + W - 1) / W;
+    int32_t *win = static_cast<int32_t *>(ws);
+    unsigned char *rest = static_cast<unsigned char *>(ws) + wb;
+    for (long long w = 0; w < nwin; ++w) {
+        window_ranges_kernel<<<(unsigned)((p.B + 255) / 256), 256, 0, stream>>>(pc, (int)w, (int)W, win);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        Problem pw = pc;
+        pw.win = win;
+        if (w > 0) pw.init = pc.fin;
+        e = launch_tc_f16(pw, rest, avail - wb, (int)(p.B * W), stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // the tensor-core prefill proper, on fp16 activations (its workspace: offsets, tables, images)
-static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream) {
+static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, int cap, cudaStream_t stream) {
     cudaError_t e;
     CUtensorMap tk, tq, tv;
     if (!make_kqv_map(&tk, p.k, p.Hq, p.T) || !make_kqv_map(&tq, p.q, p.Hq, p.T) ||
@@ -1150,13 +1201,12 @@ static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, cu
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)((long long)p.B * p.Hv);
     if (grid == 0) return cudaSuccess;
-    if (ws == nullptr || ws_bytes < chunked_tc_workspace_bytes(p)) return cudaErrorInvalidValue;
+    if (ws == nullptr || ws_bytes < head_bytes(p, cap) + (size_t)cap * p.Hv * IM_BYTES) return cudaErrorInvalidValue;
     const bool retr = rule_has_retrieval(p.rule);
-    const int cap = slot_capacity(p);
     int *offs = static_cast<int *>(ws);
     int *slot_req = offs + p.B + 1;
     int *order = slot_req + cap;
-    unsigned char *img = static_cast<unsigned char *>(ws) + head_bytes(p);
+    unsigned char *img = static_cast<unsigned char *>(ws) + head_bytes(p, cap);
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(p, offs, slot_req, order, cap);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

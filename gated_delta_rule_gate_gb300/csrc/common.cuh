@@ -43,6 +43,9 @@ struct Problem {
     const float *erase_gate;  // GDN-2 erase gate as its own input [T, Hv, dk], or null
     const float *write_gate;  // GDN-2 write gate [T, Hv, dv], or null
     int o_f32;                // tensor-core prefill on fp16 copies of fp32 inputs: o is fp32
+    // windowed tensor-core prefill: per request the [t0, t1) of the current window (device,
+    // 2 B ints), which then replaces the request's own range; null otherwise
+    const int32_t *win;
 };
 
 // GDN-2 with the erase gate in its own input: beta is then a scalar per
@@ -76,6 +79,11 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-
 // decreasing pair gives an empty request), or uniform packing, whose rows
 // seq_lens (clamped to [0, seq_len]) can shorten.
 __device__ __forceinline__ void request_range(const Problem &p, int b, int &t0, int &t1) {
+    if (p.win) {
+        t0 = p.win[2 * b];
+        t1 = p.win[2 * b + 1];
+        return;
+    }
     if (p.cu) {
         int a = p.cu[b], c = p.cu[b + 1];
         a = a < 0 ? 0 : (a > p.T ? p.T : a);

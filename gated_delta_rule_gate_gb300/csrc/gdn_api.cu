@@ -188,6 +188,7 @@ gdn_status validate(const gdn_problem *p, gdn::Problem *out) {
     d.erase_gate = p->erase_gate;
     d.write_gate = p->write_gate;
     d.o_f32 = 0;
+    d.win = nullptr;
     return GDN_OK;
 }
 
@@ -311,6 +312,18 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
     return gdn::chunked_workspace_bytes(d, chunk_size);
 }
 
+size_t gdn_chunked_prefill_workspace_size_min(const gdn_problem *p, int32_t chunk_size) {
+    gdn::Problem d;
+    if (validate(p, &d) != GDN_OK) return (size_t)-1;
+    const char *why = nullptr;
+    if (!gdn::chunked_supported(d, chunk_size, &why)) {
+        fail(GDN_ERR_UNSUPPORTED, "chunked prefill: %s", why);
+        return (size_t)-1;
+    }
+    ok();
+    return gdn::chunked_workspace_min_bytes(d, chunk_size);
+}
+
 gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *ws, size_t ws_bytes,
                                gdn_stream stream) {
     gdn::Problem d;
@@ -319,8 +332,11 @@ gdn_status gdn_chunked_prefill(const gdn_problem *p, int32_t chunk_size, void *w
     const char *why = nullptr;
     if (!gdn::chunked_supported(d, chunk_size, &why)) return fail(GDN_ERR_UNSUPPORTED, "chunked prefill: %s", why);
     const size_t need = gdn::chunked_workspace_bytes(d, chunk_size);
-    if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256)))
-        return fail(GDN_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+    const size_t least = gdn::chunked_workspace_min_bytes(d, chunk_size);
+    if (need > 0 && (ws == nullptr || ws_bytes < least || !aligned(ws, 256)))
+        return fail(GDN_ERR_WORKSPACE,
+                    "workspace needs at least %zu bytes (%zu for a single pass), 256-byte aligned (got %zu)", least,
+                    need, ws_bytes);
     if (d.B == 0) return ok();
     return cuda_status(gdn::launch_chunked(d, chunk_size, ws, ws_bytes, (cudaStream_t)stream));
 }

@@ -35,14 +35,17 @@ cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream);
 // falls outside what the kernel supports (the launcher then returns
 // cudaErrorNotSupported without launching).
 size_t chunked_workspace_bytes(const Problem &p, int chunk);
+size_t chunked_workspace_min_bytes(const Problem &p, int chunk);
 bool chunked_supported(const Problem &p, int chunk, const char **why);
 cudaError_t launch_chunked(const Problem &p, int chunk, void *ws, size_t ws_bytes, cudaStream_t stream);
 
-// tcgen05 chunked kernels (dk = dv = 128, fp16, scalar decay, v1 rules).  The
-// delta rules take a workspace of chunked_tc_workspace_bytes() for the
-// per-chunk triangular solves.
+// tcgen05 chunked kernels (dk = dv = 128, every rule).  They take a workspace
+// of chunked_tc_workspace_bytes() (every chunk's operand image at once), or
+// down to chunked_tc_workspace_min_bytes() (one chunk per request at a time:
+// the call then runs in windows of chunks, the state carried in final_state).
 bool chunked_tc_eligible(const Problem &p);
 size_t chunked_tc_workspace_bytes(const Problem &p);
+size_t chunked_tc_workspace_min_bytes(const Problem &p);
 cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace gdn

@@ -236,6 +236,21 @@ gdn_status gdn_recurrent_step(const gdn_problem *p, gdn_stream stream);
 size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_size);
 
 /*
+ * gdn_chunked_prefill_workspace_size_min -- the least workspace
+ * gdn_chunked_prefill accepts for this problem (0, (size_t)-1 as above).  It
+ * holds one chunk of every request at a time, so it does not grow with the
+ * request lengths (the fp32-activation and fp16-gate copies aside).  With any
+ * workspace from this size up to gdn_chunked_prefill_workspace_size() the call
+ * runs in windows of as many chunks per request as fit, one after another on
+ * the stream: each window reads the state the previous one left in
+ * final_state (fp32, so the result is the same, bit for bit, as a single pass)
+ * and writes its tokens' outputs.  Not an operation of the pages: a bound on
+ * the library's own scratch ("aclnnRecurrentGatedDeltaRule" asks for its
+ * workspace in a first phase; this is the least of it).
+ */
+size_t gdn_chunked_prefill_workspace_size_min(const gdn_problem *p, int32_t chunk_size);
+
+/*
  * gdn_chunked_prefill -- the same result as gdn_recurrent_step, computed
  * chunk-parallel: within a chunk the delta rule becomes a unit-lower-
  * triangular system solved once per chunk, and the intra-chunk attention and
@@ -256,8 +271,10 @@ size_t gdn_chunked_prefill_workspace_size(const gdn_problem *p, int32_t chunk_si
  * token-serial form (same result).
  *
  * Workspace: owned by the caller, device memory of at least
- * gdn_chunked_prefill_workspace_size() bytes, 256-byte aligned (NULL allowed
- * when that is 0); GDN_ERR_WORKSPACE otherwise.  It is non-zero whenever the
+ * gdn_chunked_prefill_workspace_size_min() bytes, 256-byte aligned (NULL
+ * allowed when that is 0); GDN_ERR_WORKSPACE otherwise.  Below
+ * gdn_chunked_prefill_workspace_size() the call runs in windows (see
+ * gdn_chunked_prefill_workspace_size_min).  It is non-zero whenever the
  * tensor-core path runs (every rule with dk = dv = 128, per-key problems as
  * above), and 0 otherwise.  Layout, for T / 64 + B + 1 chunk slots:
  * per-request chunk offsets, a chunk-slot -> request table and the requests

@@ -61,11 +61,13 @@ def shape_qkv(p, d):
 
 
 def run(p, path="recurrent", chunk=64, in_place=None, sentinel=float("nan"), error_word=None,
-        stream=None, d=None):
+        stream=None, d=None, workspace_extra=None):
     """Runs the problem on the GPU.  Returns (o, final_state, d) with o and
     final_state on the device.  Output tokens not covered stay ``sentinel``.
     ``in_place``: final_state is the same tensor as initial_state (default: when
-    slot_ids are present).  Otherwise final_state starts as ``sentinel``."""
+    slot_ids are present).  Otherwise final_state starts as ``sentinel``.
+    ``workspace_extra`` (chunked path): the workspace is the least the call
+    accepts plus this many bytes, instead of the single-pass size."""
     if d is None:
         d = to_dev(p)
     q, k, v = shape_qkv(p, d)
@@ -94,6 +96,10 @@ def run(p, path="recurrent", chunk=64, in_place=None, sentinel=float("nan"), err
     prob = api.make_problem(**kw)
     if path == "recurrent":
         api.gdn_recurrent_step(prob, stream=stream)
+    elif workspace_extra is not None:
+        n = api.gdn_chunked_prefill_workspace_size_min(prob, chunk) + workspace_extra
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=DEV)
+        api.gdn_chunked_prefill(prob, chunk_size=chunk, workspace=ws, stream=stream)
     else:
         api.gdn_chunked_prefill(prob, chunk_size=chunk, stream=stream)
     return o, fin, d

@@ -158,8 +158,9 @@ def test_chunked_rejects_a_small_workspace():
     p = _problem(batch=1, total_tokens=64, num_heads_q=1, num_heads_v=1, head_dim_k=128,
                  head_dim_v=128)
     need = N.load().gdn_chunked_prefill_workspace_size(ctypes.byref(p), 64)
-    assert need > 0
-    st = N.load().gdn_chunked_prefill(ctypes.byref(p), 64, ctypes.c_void_p(FAKE), need - 1, None)
+    least = N.load().gdn_chunked_prefill_workspace_size_min(ctypes.byref(p), 64)
+    assert need >= least > 0
+    st = N.load().gdn_chunked_prefill(ctypes.byref(p), 64, ctypes.c_void_p(FAKE), least - 1, None)
     assert st == N.GDN_ERR_WORKSPACE
     st = N.load().gdn_chunked_prefill(ctypes.byref(p), 64, None, need, None)
     assert st == N.GDN_ERR_WORKSPACE
@@ -190,3 +191,27 @@ def test_zero_batch_is_a_noop():
     p = _problem(batch=0, total_tokens=0)
     assert _call(p) == N.GDN_OK
     assert N.load().gdn_recurrent_step(None, None) == N.GDN_ERR_INVALID
+
+
+def test_chunked_workspace_minimum():
+    """The least workspace holds one chunk of every request (window ranges, a
+    head and B * Hv images, plus any copies), whatever the request lengths;
+    it never exceeds the single-pass size.  Below it the call is rejected with
+    GDN_ERR_WORKSPACE."""
+    lib = N.load()
+    least = lambda p: lib.gdn_chunked_prefill_workspace_size_min(ctypes.byref(p), 64)
+    full = lambda p: lib.gdn_chunked_prefill_workspace_size(ctypes.byref(p), 64)
+    B, hv = 4, 16
+    img = 88 * 1024
+    for T in (4 * 8192, 4 * 65536):
+        p = _problem(batch=B, total_tokens=T, num_heads_q=16, num_heads_v=hv, head_dim_k=128, head_dim_v=128)
+        m = least(p)
+        fixed = -(-(2 * B * 4) // 256) * 256 + (2 * B + 1) * 4 + 1023
+        assert m == -(-(fixed + B * (hv * img + 4)) // 256) * 256
+        assert m < full(p)
+    p = _problem(batch=1, total_tokens=64, num_heads_q=1, num_heads_v=1, head_dim_k=128, head_dim_v=128)
+    assert 0 < least(p) <= full(p)
+    assert least(_problem()) == 0  # dk = dv = 16 runs without a workspace
+    p = _problem(batch=B, total_tokens=4 * 8192, num_heads_q=16, num_heads_v=hv, head_dim_k=128, head_dim_v=128)
+    st = lib.gdn_chunked_prefill(ctypes.byref(p), 64, ctypes.c_void_p(FAKE), least(p) - 256, None)
+    assert st == N.GDN_ERR_WORKSPACE

@@ -347,3 +347,51 @@ def test_chunked_more_requests_than_the_order_sort_takes():
     assert err == 0
     o, fin, _ = run(p, path="chunked")
     _check(p, o, fin, ref_o, ref_fin)
+
+
+WINDOWED = [
+    dict(rule="gated_delta"),
+    dict(rule="linear"),
+    dict(rule="gated"),
+    dict(rule="delta", beta_shared=True),
+    dict(rule="gdn2", decay_per_key=True, gate_dtype="f32", write_gate=True),
+    dict(rule="gated", decay_per_key=True, gate_dtype="f32"),
+    dict(rule="gated_delta", act="f32"),
+    dict(rule="gated_delta", state_kmajor=True, num_slots=8, slot_mode="perm"),
+]
+
+
+@pytest.mark.parametrize("chunks", [1, 2])
+@pytest.mark.parametrize("case", WINDOWED, ids=[_cid(c) for c in WINDOWED])
+def test_chunked_windowed_workspace(case, chunks):
+    """A workspace that holds ``chunks`` chunks of every request: the call runs
+    in windows, each reading the fp32 state the last one left in final_state,
+    so outputs and final state equal the single pass bit for bit (and the
+    oracle within the tolerance).  Requests of 0, 1, 70, 130 and 200 tokens:
+    some end in an early window and sit out the later ones."""
+    kw = dict(seed=61, B=5, lengths=[70, 0, 130, 1, 200], hq=1, hv=2, dk=128, dv=128, act="f16",
+              rule="gated_delta", state="random", state_std=0.3)
+    kw.update(case)
+    p = workloads.make(**kw)
+    o1, f1, _ = run(p, path="chunked")
+    per_chunk = p["batch"] * (p["hv"] * 88 * 1024 + 4)
+    o2, f2, _ = run(p, path="chunked", workspace_extra=(chunks - 1) * per_chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.nan_to_num(o1, nan=7.0), torch.nan_to_num(o2, nan=7.0))
+    assert torch.equal(torch.nan_to_num(f1, nan=7.0), torch.nan_to_num(f2, nan=7.0))
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    _check(p, o2, f2, ref_o, ref_fin)
+
+
+def test_ragged_prefill_full_size_windowed():
+    """Config 3 (8 requests, 16384 tokens, Hv = 32) with a workspace of 16
+    chunks per request (about 365 MB instead of 765 MB): four windows for the
+    longest request; every request checked against the oracle."""
+    p = workloads.ragged_prefill()
+    per_chunk = p["batch"] * (p["hv"] * 88 * 1024 + 4)
+    o, fin, _ = run(p, path="chunked", workspace_extra=15 * per_chunk)
+    torch.cuda.synchronize()
+    ref_o, ref_fin, err = oracle.run_problem(p, threads=THREADS)
+    assert err == 0
+    _check(p, o, fin, ref_o, ref_fin)
