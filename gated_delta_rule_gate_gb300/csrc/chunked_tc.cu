@@ -59,10 +59,25 @@ __device__ __forceinline__ int request_chunks(const Problem &p, int b) {
 // decreasing chunk count (ties by index) when B <= kSortMax, else in index
 // order: the chain kernel starts the longest chains first.  One CTA.
 constexpr int kSortMax = 2048;
-__global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *offs, int *slot_req, int *order, int cap) {
+__global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *offs, int *slot_req, int *order, int cap,
+                                                             int win_w, int win_W) {
     __shared__ int wsum[32];
     __shared__ int snch[kSortMax];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (p.win) {
+        // windowed call: first the window's range of every request, chunks [w W, (w + 1) W) of
+        // it, for this kernel and the ones after it (p.win is the output here)
+        Problem po = p;
+        po.win = nullptr;
+        for (int b = tid; b < p.B; b += 1024) {
+            int t0, t1;
+            request_range(po, b, t0, t1);
+            const long long a = (long long)t0 + (long long)win_w * win_W * TC_C, c = a + (long long)win_W * TC_C;
+            const_cast<int32_t *>(p.win)[2 * b] = (int)(a < t1 ? a : t1);
+            const_cast<int32_t *>(p.win)[2 * b + 1] = (int)(c < t1 ? c : t1);
+        }
+        __syncthreads();
+    }
     const int per = (p.B + 1023) / 1024;
     const int b0 = min(p.B, tid * per), b1 = min(p.B, b0 + per);
     int s = 0;
@@ -1039,16 +1054,7 @@ size_t window_bytes(const Problem &p) { return ((size_t)2 * p.B * sizeof(int) + 
 size_t window_fixed(const Problem &p) { return window_bytes(p) + ((size_t)2 * p.B + 1) * sizeof(int) + 1023; }
 size_t window_per_chunk(const Problem &p) { return (size_t)p.B * ((size_t)p.Hv * IM_BYTES + sizeof(int)); }
 
-// The windowed call: window w holds chunks [w W, (w + 1) W) of every request.
-__global__ void __launch_bounds__(256) window_ranges_kernel(Problem p, int w, int W, int32_t *win) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= p.B) return;
-    int t0, t1;
-    request_range(p, b, t0, t1);  // (p.win is null here: the request's own range)
-    const long long a = (long long)t0 + (long long)w * W * TC_C, c = a + (long long)W * TC_C;
-    win[2 * b] = (int)(a < t1 ? a : t1);
-    win[2 * b + 1] = (int)(c < t1 ? c : t1);
-}
+
 
 }  // namespace
 
@@ -1109,7 +1115,8 @@ bool make_kqv_map(CUtensorMap *m, const void *base, int heads, int tokens) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, int cap, cudaStream_t stream);
+static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, int cap, cudaStream_t stream,
+                                 int win_w = 0, int win_W = 0);
 
 cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaStream_t stream) {
     const void *fns[8] = {(const void *)chunk_prepare_kernel<true>,
@@ -1180,20 +1187,19 @@ cudaError_t launch_chunked_tc(const Problem &p, void *ws, size_t ws_bytes, cudaS
     int32_t *win = static_cast<int32_t *>(ws);
     unsigned char *rest = static_cast<unsigned char *>(ws) + wb;
     for (long long w = 0; w < nwin; ++w) {
-        window_ranges_kernel<<<(unsigned)((p.B + 255) / 256), 256, 0, stream>>>(pc, (int)w, (int)W, win);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        // (the offsets kernel of each window first writes the window's request ranges)
         Problem pw = pc;
         pw.win = win;
         if (w > 0) pw.init = pc.fin;
-        e = launch_tc_f16(pw, rest, avail - wb, (int)(p.B * W), stream);
+        e = launch_tc_f16(pw, rest, avail - wb, (int)(p.B * W), stream, (int)w, (int)W);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
 // the tensor-core prefill proper, on fp16 activations (its workspace: offsets, tables, images)
-static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, int cap, cudaStream_t stream) {
+static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, int cap, cudaStream_t stream,
+                                 int win_w, int win_W) {
     cudaError_t e;
     CUtensorMap tk, tq, tv;
     if (!make_kqv_map(&tk, p.k, p.Hq, p.T) || !make_kqv_map(&tq, p.q, p.Hq, p.T) ||
@@ -1207,7 +1213,7 @@ static cudaError_t launch_tc_f16(const Problem &p, void *ws, size_t ws_bytes, in
     int *slot_req = offs + p.B + 1;
     int *order = slot_req + cap;
     unsigned char *img = static_cast<unsigned char *>(ws) + head_bytes(p, cap);
-    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(p, offs, slot_req, order, cap);
+    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(p, offs, slot_req, order, cap, win_w, win_W);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // persistent prepare CTAs: two per SM (shared and tensor memory), at most one per task
