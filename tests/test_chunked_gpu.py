@@ -395,3 +395,19 @@ def test_ragged_prefill_full_size_windowed():
     ref_o, ref_fin, err = oracle.run_problem(p, threads=THREADS)
     assert err == 0
     _check(p, o, fin, ref_o, ref_fin)
+
+
+def test_chunked_windowed_seq_lens_rows():
+    """Windows over the rank-4 layout with padded seq_lens rows (padding tokens
+    NaN): bit-identical to the single pass, padding outputs untouched."""
+    kw = dict(seed=62, B=4, seq_len=300, seq_lens=[300, 0, 37, 999], hq=1, hv=2, dk=128, dv=128,
+              act="f16", rule="gated_delta", state="random", state_std=0.3)
+    p = poison_uncovered(workloads.make(**kw))
+    o1, f1, _ = run(p, path="chunked")
+    o2, f2, _ = run(p, path="chunked", workspace_extra=0)  # one chunk per request per window
+    torch.cuda.synchronize()
+    assert torch.equal(torch.nan_to_num(o1, nan=7.0), torch.nan_to_num(o2, nan=7.0))
+    assert torch.equal(f1, f2)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    _check(p, o2, f2, ref_o, ref_fin)
