@@ -83,7 +83,7 @@ def test_chunk_form_equals_token_loop(rule, C):
     np.testing.assert_allclose(M, ref_f[0, 0], rtol=1e-10, atol=1e-12)
 
 
-def _chunked_perkey(q, k, v, g, beta, kappa, M0, scale, C, blk=16):
+def _chunked_perkey(q, k, v, g, beta, kappa, M0, scale, C, blk=16, retrieval=True):
     """The per-key-decay chunk step in the form the tensor-core prepare pass and
     the chain kernel compute it.  g is [T, dk] (one log decay per key channel),
     Gamma its in-chunk cumulants.  A and P: entries whose column lies in an
@@ -92,7 +92,8 @@ def _chunked_perkey(q, k, v, g, beta, kappa, M0, scale, C, blk=16):
     most 1; entries inside a block come from a running product of per-token
     decays.  Then the affine chunk map
         S <- S + U^T Kt + S E,   O^T = U^T P^T + S Q'^T,
-        E = Diag(e^{Gamma_C}) - I + Wn^T Kt,   Q' = Qh + P Wn,   Wn = -W."""
+        E = Diag(e^{Gamma_C}) - I + Wn^T Kt,   Q' = Qh + P Wn,   Wn = -W.
+    Without retrieval (the gated rule) there is no system: U = V and Wn = 0."""
     T, dk = k.shape
     S = M0.copy()
     out = np.zeros((T, v.shape[1]))
@@ -120,9 +121,12 @@ def _chunked_perkey(q, k, v, g, beta, kappa, M0, scale, C, blk=16):
                     A[r, j] = bt[r] * np.sum(X[r] * K[j] * e)
                 P[r, j] = np.sum(Q[r] * K[j] * e)
                 e = e * alpha[j]
-        Tm = np.linalg.inv(np.eye(n) + A)
-        U = Tm @ (bt[:, None] * V)
-        Wn = -Tm @ (bt[:, None] * (np.exp(G) * X))
+        if retrieval:
+            Tm = np.linalg.inv(np.eye(n) + A)
+            U = Tm @ (bt[:, None] * V)
+            Wn = -Tm @ (bt[:, None] * (np.exp(G) * X))
+        else:
+            U, Wn = V, np.zeros((n, dk))
         Kt = np.exp(G[-1] - G) * K
         Qh = scale * np.exp(G) * Q
         E = np.diag(np.exp(G[-1])) - np.eye(dk) + Wn.T @ Kt
@@ -132,7 +136,7 @@ def _chunked_perkey(q, k, v, g, beta, kappa, M0, scale, C, blk=16):
     return out, S
 
 
-@pytest.mark.parametrize("rule", ["gated_delta", "gdn2"])
+@pytest.mark.parametrize("rule", ["gated_delta", "gdn2", "gated"])
 @pytest.mark.parametrize("C", [16, 64])
 @pytest.mark.parametrize("lo", [-1.0, -6.0])
 def test_per_key_chunk_form_equals_token_loop(rule, C, lo):
@@ -152,11 +156,13 @@ def test_per_key_chunk_form_equals_token_loop(rule, C, lo):
     g = p["decay"].double().numpy()[:, 0]  # [T, dk]
     if rule == "gdn2":
         kappa, beta = p["beta"].double().numpy()[:, 0] * k, np.ones(T)
+    elif rule == "gated":
+        kappa, beta = k, np.zeros(T)
     else:
         kappa, beta = k, p["beta"].double().numpy()[:, 0]
     M0 = p["initial_state"].double().numpy()[0, 0]
     ref_o, ref_f, _ = oracle.run_problem(p)
-    o, M = _chunked_perkey(q, k, v, g, beta, kappa, M0, 1 / np.sqrt(dk), C)
+    o, M = _chunked_perkey(q, k, v, g, beta, kappa, M0, 1 / np.sqrt(dk), C, retrieval=rule != "gated")
     np.testing.assert_allclose(o, ref_o[:, 0], rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(M, ref_f[0, 0], rtol=1e-9, atol=1e-11)
 
