@@ -781,9 +781,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             ok = ptx::named_bar_and(1, 256, ptx::mbar_wait_sleep(barS, c & 1));
             if (!ok) break;
             tc::fence_after();
-            float v0[32], v1[32];
-            tc::ld32(lo, v0);
-            tc::ld32(lo + 32, v1);
+            float sv[64];  // both column blocks in one load (one wait)
+            tc::ld64(lo, sv);
+            const float *v0 = sv, *v1 = sv + 32;
             if (STEP == kStepDecay && c + 1 < nch) {
                 // S <- e^{G_C} S of the next chunk before its U^T Kt lands
                 float w[32];
@@ -840,9 +840,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             ok = ptx::named_bar_and(2, 128, ptx::mbar_wait_sleep(odd ? barO2 : barO, O2 ? (c >> 1) & 1 : c & 1));
             if (!ok) break;
             tc::fence_after();
-            float o0[32], o1[32];
-            tc::ld32(lo, o0);
-            tc::ld32(lo + 32, o1);
+            float ov[64];  // both column blocks in one load (one wait)
+            tc::ld64(lo, ov);
+            const float *o0 = ov, *o1 = ov + 32;
             tc::fence_before();
             ptx::named_bar_sync(2, 128);
             if (ot == 0) ptx::mbar_arrive(odd ? ofree2 : ofree);
