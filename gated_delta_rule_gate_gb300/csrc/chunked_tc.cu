@@ -717,7 +717,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     }
 
     if (tid == 0) {
-        for (int i = 0; i < 12; ++i) ptx::mbar_init(&bars[i], 1);
+        // rsread, shready and shready2 take one arrival from each of the eight state warps
+        for (int i = 0; i < 12; ++i) ptx::mbar_init(&bars[i], (i == 4 || i == 5 || i == 8) ? 8 : 1);
         ptx::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(tslot, 256);
@@ -768,10 +769,11 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             }
             tc::wait_st();
         }
+        // each warp hands over its rows itself (the barriers count the eight warps)
         tc::fence_async_smem();
         tc::fence_before();
-        ptx::named_bar_sync(1, 256);
-        if (tid == 0) {
+        __syncwarp();
+        if (lane == 0) {
             ptx::mbar_arrive(rsread);
             ptx::mbar_arrive(shready);
         }
@@ -796,8 +798,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 tc::wait_st();
             }
             tc::fence_before();
-            ptx::named_bar_sync(1, 256);
-            if (tid == 0) ptx::mbar_arrive(rsread);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(rsread);
             if (c + 1 < nch) {
                 // PIPE: chunk c + 1 writes buffer (c + 1) % 2 (the readout of chunk c may still
                 // read the other) and publishes it on the barrier of its parity
@@ -809,8 +811,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     for (int cc = 0; cc < 4; ++cc) st_chunk(shb, i, 4 + cc, v1 + 8 * cc);
                 }
                 tc::fence_async_smem();
-                ptx::named_bar_sync(1, 256);
-                if (tid == 0) ptx::mbar_arrive(PIPE && ((c + 1) & 1) ? shready2 : shready);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(PIPE && ((c + 1) & 1) ? shready2 : shready);
             } else if (live && km) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
