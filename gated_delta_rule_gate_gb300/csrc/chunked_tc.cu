@@ -929,7 +929,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 const uint32_t base = ptx::smem_u32(sm + cImg + bf * IM_BYTES);
                 const uint64_t dU = tc::desc_sw128(base + IM_U, 8192), dKt = tc::desc_sw128(base + IM_KT, 8192);
                 const uint64_t dP = tc::desc_sw128(base + IM_P), dEQ = tc::desc_sw128(base + IM_EQ);
-                ok = ptx::mbar_wait_sleep(&land[bf], (c >> 1) & 1) && ptx::mbar_wait_sleep(rsread, c & 1);
+                // (the issuing thread polls its waits on the chain's serial path: one lane, and
+                // a poll wakes sooner than a suspended wait)
+                ok = ptx::mbar_wait_spin(&land[bf], (c >> 1) & 1) && ptx::mbar_wait_spin(rsread, c & 1);
                 if (!ok) break;
                 tc::fence_after();
                 if (STEP != kStepE && c == nch - 1) {
@@ -968,7 +970,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 for (int s = 0; s < 4; ++s)
                     tc::mma_f16(tmem + tOc, tc::desc_adv(dU, s * 2048), tc::desc_adv(dP, s * 32), idUP, s > 0);
                 if (PIPE) {
-                    ok = ptx::mbar_wait_sleep((c & 1) ? shready2 : shready, (c >> 1) & 1);
+                    ok = ptx::mbar_wait_spin((c & 1) ? shready2 : shready, (c >> 1) & 1);
                     if (!ok) break;
                     tc::fence_after();
                     const uint64_t dSh = tc::desc_adv(dSh0, (c & 1) * 2 * SHB);
@@ -981,7 +983,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     tc::commit(&freeb[bf]);
                     continue;
                 }
-                ok = ptx::mbar_wait_sleep(shready, c & 1);
+                ok = ptx::mbar_wait_spin(shready, c & 1);
                 if (!ok) break;
                 tc::fence_after();
                 if (STEP == kStepE) {
