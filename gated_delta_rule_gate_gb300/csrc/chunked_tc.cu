@@ -783,6 +783,55 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             ok = ptx::named_bar_and(1, 256, ptx::mbar_wait_sleep(barS, c & 1));
             if (!ok) break;
             tc::fence_after();
+            if (HALF) {
+                // M = 64: the 16 rows of this warp's lane quarter over all 32 lanes (16x256b
+                // shape): rows ra and ra + 8, columns 8 k + cq and + 1 of this warp's half
+                const int ra = 16 * q4 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+                float hv[32];
+                tc::ld16x256<8>(lo, hv);
+                if (STEP == kStepDecay && c + 1 < nch) {
+                    // S <- e^{G_C} S of the next chunk before its U^T Kt lands
+                    float w[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = hv[e] * gn;
+                    tc::st16x256_8(lo, w);
+                    tc::wait_st();
+                }
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(rsread);
+                if (c + 1 < nch) {
+                    unsigned char *shb = sS + (PIPE ? ((c + 1) & 1) * 2 * SHB : 0) + hc * SHB;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        *reinterpret_cast<uint32_t *>(shb + sw(ra, k) + 2 * cq) = ptx::pack_h2(hv[4 * k], hv[4 * k + 1]);
+                        *reinterpret_cast<uint32_t *>(shb + sw(rb, k) + 2 * cq) =
+                            ptx::pack_h2(hv[4 * k + 2], hv[4 * k + 3]);
+                    }
+                    tc::fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(PIPE && ((c + 1) & 1) ? shready2 : shready);
+                } else if (km) {
+                    const size_t kc = tile + (size_t)(64 * hc) * 128 + 64 * vh;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const size_t c0 = kc + (size_t)(8 * k + cq) * 128;
+                        p.fin[c0 + ra] = hv[4 * k];
+                        p.fin[c0 + 128 + ra] = hv[4 * k + 1];
+                        p.fin[c0 + rb] = hv[4 * k + 2];
+                        p.fin[c0 + 128 + rb] = hv[4 * k + 3];
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const size_t c0 = sbase + 64 * hc + 8 * k + cq;
+                        *reinterpret_cast<float2 *>(p.fin + c0 + (size_t)ra * 128) = make_float2(hv[4 * k], hv[4 * k + 1]);
+                        *reinterpret_cast<float2 *>(p.fin + c0 + (size_t)rb * 128) =
+                            make_float2(hv[4 * k + 2], hv[4 * k + 3]);
+                    }
+                }
+                continue;
+            }
             float sv[64];  // both column blocks in one load (one wait)
             tc::ld64(lo, sv);
             const float *v0 = sv, *v1 = sv + 32;
