@@ -891,6 +891,35 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             ok = ptx::named_bar_and(2, 128, ptx::mbar_wait_sleep(odd ? barO2 : barO, O2 ? (c >> 1) & 1 : c & 1));
             if (!ok) break;
             tc::fence_after();
+            if (HALF) {
+                // M = 64: the 16 rows of this quarter over all 32 lanes (16x256b shape): value
+                // rows ra and ra + 8, tokens 8 k + cq and + 1
+                const int ra = 16 * q4 + (lane >> 2), rb = ra + 8, cq = 2 * (lane & 3);
+                float hv[32];
+                tc::ld16x256<8>(lo, hv);
+                tc::fence_before();
+                ptx::named_bar_sync(2, 128);
+                if (ot == 0) ptx::mbar_arrive(odd ? ofree2 : ofree);
+                const int n = min(TC_C, t1 - (t0 + TC_C * c));
+                const size_t ob = ((size_t)(t0 + TC_C * c) * p.Hv + h) * 128 + 64 * vh;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = 8 * k + cq + e;
+                        if (t < n) {
+                            const size_t o_t = ob + (size_t)t * rstride;
+                            if (p.o_f32) {
+                                static_cast<float *>(p.o)[o_t + ra] = hv[4 * k + e];
+                                static_cast<float *>(p.o)[o_t + rb] = hv[4 * k + 2 + e];
+                            } else {
+                                static_cast<__half *>(p.o)[o_t + ra] = __float2half_rn(hv[4 * k + e]);
+                                static_cast<__half *>(p.o)[o_t + rb] = __float2half_rn(hv[4 * k + 2 + e]);
+                            }
+                        }
+                    }
+                continue;
+            }
             float ov[64];  // both column blocks in one load (one wait)
             tc::ld64(lo, ov);
             const float *o0 = ov, *o1 = ov + 32;
