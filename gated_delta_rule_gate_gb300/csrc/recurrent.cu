@@ -385,7 +385,6 @@ struct PipeLayout {
     int stage_floats; // floats per staging buffer
     int raw_bytes;    // cp.async landing area of the stager
     int ring_bytes;
-    int red_bytes;    // key-major consumers: per-warp partial sums, two buffers
     int stages;       // state slices in flight
     int nbuf;         // staging buffers
     int nstg;         // stager warps (each with its own landing area)
@@ -394,8 +393,9 @@ struct PipeLayout {
     bool has_a, has_x, has_w;
 };
 
-// Key-major state in the decode kernel: one CTA per SM with twice the ring
-// (when the staging area leaves room for it), two stager warps taking
+// Key-major state in the decode kernel: its consumers hold a whole 128 x 128
+// tile (each warp 16 columns of all key rows), so one CTA per SM, with twice
+// the ring (when the staging area leaves room for it), two stager warps taking
 // alternate pairs and three staging buffers, so that one CTA stages pairs as
 // fast as the two CTAs per SM of the value-major kernel.
 constexpr int kStagesKM = 8;
@@ -418,11 +418,10 @@ __host__ __device__ inline PipeLayout pipe_layout(const Problem &p) {
     L.raw_bytes = (L.raw_bytes + 15) & ~15;
     L.nbuf = km ? kMaxStageBufs : 2;
     L.nstg = km ? kMaxStagers : 1;
-    L.red_bytes = km ? 2 * (kThreads / 32) * 32 * 32 : 0;
     // a slice is 32 stored rows: value rows of dk floats, or key rows of dv floats (key-major)
     const int slice_bytes = kFastRows * (km ? p.dv : p.dk) * 4;
     auto total = [&](int stages) {
-        return stages * slice_bytes + L.nbuf * L.stage_floats * 4 + L.nstg * L.raw_bytes + L.red_bytes +
+        return stages * slice_bytes + L.nbuf * L.stage_floats * 4 + L.nstg * L.raw_bytes +
                (2 * stages + 2 * L.nbuf) * 8;
     };
     L.stages = km && total(kStagesKM) <= 200 * 1024 ? kStagesKM : kStages;
@@ -840,16 +839,24 @@ __device__ __forceinline__ float4 f4_scale(float a, const float4 &x) {
     return make_float4(a * x.x, a * x.y, a * x.z, a * x.w);
 }
 
-// `tok` counts the tokens this thread has applied (it picks the buffer of red).
-__device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s, float4 (&S)[4][4], float4 *red,
-                                                int nt, int tb, int h, int warp, int lane, int &tok) {
+// Key-major consumers.  Warp w holds the state columns 16 w + [0, 16) of
+// all 128 key rows, so every sum over key rows stays inside the warp: lane
+// (rg = lane / 4, cq = lane % 4) keeps the float4 of columns 16 w + 4 cq of key
+// rows 32 s + 4 rg + e (S[s][e]: slice s, e < 4).  The staged key / query
+// entries a thread needs are one float4 per slice and vector (the four lanes
+// of a row group read the same one), and the sums are the thread's 16 rows and
+// then three shuffle levels over the eight row groups.
+
+__device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s, float4 (&S)[4][4], int nt, int tb,
+                                                int h, int warp, int lane) {
     constexpr int DK = 128;
     const bool perkey = (p.flags & kPerKey) != 0 && rule_has_decay(p.rule);
     const bool retrieval = rule_has_retrieval(p.rule);
     const float *kap = p.rule == kGdn2 ? s.x : s.k;
+    const int rg = lane >> 2, col = 16 * warp + 4 * (lane & 3);
     float c = 1.f;
-    for (int tt = 0; tt < nt; ++tt, ++tok) {
-        const int ro = tt * DK + 4 * warp;  // staged entry of key row 4 warp (+ 32 s + m)
+    for (int tt = 0; tt < nt; ++tt) {
+        const int ro = tt * DK + 4 * rg;  // staged entry of key row 4 rg (+ 32 s + e)
         if (perkey) {
 #pragma unroll
             for (int sl = 0; sl < 4; ++sl) {
@@ -869,20 +876,18 @@ __device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s
             wa = f4_fma(q4.x, S[sl][0], wa), wb = f4_fma(q4.y, S[sl][1], wb);
             wa = f4_fma(q4.z, S[sl][2], wa), wb = f4_fma(q4.w, S[sl][3], wb);
         }
-        // [u partials of the 8 warps][w partials]: a warp's loads are 512 contiguous bytes
-        float4 *rb = red + (tok & 1) * (2 * kThreads);
-        rb[warp * 32 + lane] = f4_add(ua, ub);
-        rb[kThreads + warp * 32 + lane] = f4_add(wa, wb);
-        ptx::named_bar_sync(2, kThreads);
-        float4 U = rb[lane], W = rb[kThreads + lane];
+        float4 U = f4_add(ua, ub), W = f4_add(wa, wb);
+        // over the eight row groups: every lane of a column quad ends with the same sums
 #pragma unroll
-        for (int w2 = 1; w2 < kThreads / 32; ++w2) {
-            U = f4_add(U, rb[w2 * 32 + lane]);
-            W = f4_add(W, rb[kThreads + w2 * 32 + lane]);
+        for (int o = 4; o < 32; o <<= 1) {
+            U.x += __shfl_xor_sync(0xffffffffu, U.x, o), U.y += __shfl_xor_sync(0xffffffffu, U.y, o);
+            U.z += __shfl_xor_sync(0xffffffffu, U.z, o), U.w += __shfl_xor_sync(0xffffffffu, U.w, o);
+            W.x += __shfl_xor_sync(0xffffffffu, W.x, o), W.y += __shfl_xor_sync(0xffffffffu, W.y, o);
+            W.z += __shfl_xor_sync(0xffffffffu, W.z, o), W.w += __shfl_xor_sync(0xffffffffu, W.w, o);
         }
         float cn = c * s.alpha[tt];  // alpha is 1 without scalar decay
         const float bt = s.beta[tt], kq = s.kq[tt];
-        const float4 v4 = lds_f4(s.v + tt * s.vrows + 4 * lane);
+        const float4 v4 = lds_f4(s.v + tt * s.vrows + col);
         float4 d;
         if (retrieval) {
             d.x = bt * (v4.x - cn * U.x), d.y = bt * (v4.y - cn * U.y);
@@ -890,10 +895,10 @@ __device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s
         } else {
             d = v4;
         }
-        if (warp == 0) {
+        if (rg == 0) {
             const float4 ov = make_float4(p.scale * fmaf(cn, W.x, d.x * kq), p.scale * fmaf(cn, W.y, d.y * kq),
                                           p.scale * fmaf(cn, W.z, d.z * kq), p.scale * fmaf(cn, W.w, d.w * kq));
-            const size_t oi = ((size_t)(tb + tt) * p.Hv + h) * p.dv + 4 * lane;
+            const size_t oi = ((size_t)(tb + tt) * p.Hv + h) * p.dv + col;
             if (p.act_f16) {
                 __half2 *o2 = reinterpret_cast<__half2 *>(static_cast<__half *>(p.o) + oi);
                 o2[0] = __floats2half2_rn(ov.x, ov.y);
@@ -906,18 +911,18 @@ __device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s
 #pragma unroll
             for (int sl = 0; sl < 4; ++sl)
 #pragma unroll
-                for (int m = 0; m < 4; ++m) S[sl][m] = f4_scale(cn, S[sl][m]);
+                for (int e = 0; e < 4; ++e) S[sl][e] = f4_scale(cn, S[sl][e]);
             cn = 1.f;
         }
         const float rc = __frcp_rn(cn);
-        const float4 e = f4_scale(rc, d);
+        const float4 ev = f4_scale(rc, d);
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl) {
             const float4 k4 = lds_f4(s.k + ro + 32 * sl);
-            S[sl][0] = f4_fma(k4.x, e, S[sl][0]);
-            S[sl][1] = f4_fma(k4.y, e, S[sl][1]);
-            S[sl][2] = f4_fma(k4.z, e, S[sl][2]);
-            S[sl][3] = f4_fma(k4.w, e, S[sl][3]);
+            S[sl][0] = f4_fma(k4.x, ev, S[sl][0]);
+            S[sl][1] = f4_fma(k4.y, ev, S[sl][1]);
+            S[sl][2] = f4_fma(k4.z, ev, S[sl][2]);
+            S[sl][3] = f4_fma(k4.w, ev, S[sl][3]);
         }
         c = cn;
     }
@@ -925,16 +930,17 @@ __device__ __forceinline__ void apply_tokens_km(const Problem &p, const Stage &s
 #pragma unroll
         for (int sl = 0; sl < 4; ++sl)
 #pragma unroll
-            for (int m = 0; m < 4; ++m) S[sl][m] = f4_scale(c, S[sl][m]);
+            for (int e = 0; e < 4; ++e) S[sl][e] = f4_scale(c, S[sl][e]);
     }
 }
 
 // The key-major consumer side of one (request, head) pair.  `j` counts ring
-// uses (set to -1 if a wait runs out); `tok` as in apply_tokens_km.
+// uses (set to -1 if a wait runs out).
 __device__ __forceinline__ void consume_tile_km(const Problem &p, const Stage &st, const float *ring, uint64_t *full,
-                                                uint64_t *empty, float4 *red, int &j, int &tok, int row, int h,
+                                                uint64_t *empty, int &j, int row, int h,
                                                 int qh, int t0, int t1, int tid, int warp, int lane, int NST) {
     constexpr int kSlice = kFastRows * 128;
+    const int rg = lane >> 2, col = 16 * warp + 4 * (lane & 3);
     float4 S[4][4];
 #pragma unroll
     for (int sl = 0; sl < 4; ++sl) {
@@ -946,9 +952,9 @@ __device__ __forceinline__ void consume_tile_km(const Problem &p, const Stage &s
         }
         ++j;
         const bool have = row >= 0 && p.init != nullptr;
-        const float *src = ring + slot * kSlice + 4 * warp * 128 + 4 * lane;
+        const float *src = ring + slot * kSlice + 4 * rg * 128 + col;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) S[sl][m] = have ? lds_f4(src + m * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < 4; ++e) S[sl][e] = have ? lds_f4(src + e * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&empty[slot]);
     }
@@ -962,16 +968,16 @@ __device__ __forceinline__ void consume_tile_km(const Problem &p, const Stage &s
                 stage_tokens(p, st, h, qh, tb, nt, 0, tid, kThreads);
                 ptx::named_bar_sync(1, kThreads);
             }
-            apply_tokens_km(p, st, S, red, nt, tb, h, warp, lane, tok);
+            apply_tokens_km(p, st, S, nt, tb, h, warp, lane);
         }
     } else if (p.fin == p.init) {
         return;  // empty request, in place: nothing changes
     }
-    float *dst = p.fin + ((size_t)row * p.Hv + h) * 128 * 128 + 4 * warp * 128 + 4 * lane;
+    float *dst = p.fin + ((size_t)row * p.Hv + h) * 128 * 128 + 4 * rg * 128 + col;
 #pragma unroll
     for (int sl = 0; sl < 4; ++sl)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) __stcs(reinterpret_cast<float4 *>(dst + (32 * sl + m) * 128), S[sl][m]);
+        for (int e = 0; e < 4; ++e) __stcs(reinterpret_cast<float4 *>(dst + (32 * sl + e) * 128), S[sl][e]);
 }
 
 template <int DK, bool KM>
@@ -987,8 +993,7 @@ __global__ void __launch_bounds__(kThreads + 32 + 32 * (KM ? kMaxStagers : 1), K
     float *ring = reinterpret_cast<float *>(smem_raw);
     float *stage_base = reinterpret_cast<float *>(smem_raw + Ly.ring_bytes);
     unsigned char *raw0 = smem_raw + Ly.ring_bytes + NBUF * Ly.stage_floats * 4;
-    float4 *red = reinterpret_cast<float4 *>(raw0 + NSTG * Ly.raw_bytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(raw0 + NSTG * Ly.raw_bytes + Ly.red_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw0 + NSTG * Ly.raw_bytes);
     uint64_t *empty = full + NST;
     uint64_t *tok_full = empty + NST;
     uint64_t *tok_empty = tok_full + NBUF;
@@ -1096,7 +1101,7 @@ __global__ void __launch_bounds__(kThreads + 32 + 32 * (KM ? kMaxStagers : 1), K
     // ---- consumer warps
     const int cg = lane & 7;
     const int rloc = warp * 4 + (lane >> 3);
-    int j = 0, k = 0, tok = 0;
+    int j = 0, k = 0;
     for (int pair = blockIdx.x; pair < pairs; pair += gridDim.x, ++k) {
         const int buf = k % NBUF;
         if (!ptx::mbar_wait(&tok_full[buf], (k / NBUF) & 1)) {
@@ -1113,7 +1118,7 @@ __global__ void __launch_bounds__(kThreads + 32 + 32 * (KM ? kMaxStagers : 1), K
         // R state slices per pass (2 when the slice count is even): the staged
         // key/query loads are shared and the rows' reduction chains interleave
         if (KM)
-            consume_tile_km(p, st, ring, full, empty, red, j, tok, row, h, qh, t0, t1, tid, warp, lane, NST);
+            consume_tile_km(p, st, ring, full, empty, j, row, h, qh, t0, t1, tid, warp, lane, NST);
         else if ((slices & 1) == 0)
             consume_slices<DK, 2>(p, st, ring, full, empty, j, slices, row, h, qh, t0, t1, tid, lane, cg, rloc);
         else
