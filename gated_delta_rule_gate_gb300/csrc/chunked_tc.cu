@@ -265,12 +265,13 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             __syncwarp();
             if (lane == 0) {
                 const int qh = (int)((long long)nx.h * p.Hq / p.Hv);
-                ptx::mbar_arrive_expect_tx(land, 3 * 16384);
+                // the rules without retrieval never read the value tile here (U = V)
+                ptx::mbar_arrive_expect_tx(land, (RETR ? 3 : 2) * 16384);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     ptx::tma_load_3d(sm + rKQ + kb * 16384, &tmK, 64 * kb, qh, nx.c0, land);
                     ptx::tma_load_3d(sm + rKQ + kb * 16384 + 8192, &tmQ, 64 * kb, qh, nx.c0, land);
-                    ptx::tma_load_3d(sm + rV + kb * 8192, &tmV, 64 * kb, nx.h, nx.c0, land);
+                    if (RETR) ptx::tma_load_3d(sm + rV + kb * 8192, &tmV, 64 * kb, nx.h, nx.c0, land);
                 }
             }
             if (t + G < ntasks) {
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                     for (int kb = 0; kb < 2; ++kb) {
                         ptx::prefetch_tile_3d(&tmK, 64 * kb, qh, nx.c0);
                         ptx::prefetch_tile_3d(&tmQ, 64 * kb, qh, nx.c0);
-                        ptx::prefetch_tile_3d(&tmV, 64 * kb, nx.h, nx.c0);
+                        if (RETR) ptx::prefetch_tile_3d(&tmV, 64 * kb, nx.h, nx.c0);
                     }
                 }
             }
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
             unsigned char *dst = img + ((size_t)slot * p.Hv + h) * IM_BYTES;
             if (n < TC_C) {  // the boxes run past this request: clear the rows beyond it
                 const int nz = (TC_C - n) * 16;
-                for (int idx = tid; idx < 3 * nz; idx += PR_WORK) {
+                for (int idx = tid; idx < (RETR ? 3 : 2) * nz; idx += PR_WORK) {
                     const int which = idx / nz, rem = idx % nz, r = n + (rem >> 4), ch = rem & 15;
                     const int off = which == 2 ? rV + (ch >> 3) * 8192 + sw(r, ch & 7) : kq_off(r, ch, which == 1);
                     *reinterpret_cast<uint4 *>(sm + off) = make_uint4(0, 0, 0, 0);
