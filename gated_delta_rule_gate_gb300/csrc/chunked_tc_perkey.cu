@@ -39,6 +39,7 @@
 // without the solve: U = V, Q' = Qh and E = Diag(e^{Gamma_C} - 1), so the
 // chain's S E applies the per-channel decay of the chunk.
 #include <algorithm>
+#include <type_traits>
 
 #include "chunk_image.cuh"
 #include "common.cuh"
@@ -583,7 +584,10 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             const int ds = warp >> 1, drp = 4 * (warp & 1) + (lane >> 3), dcg = lane & 7;
             const int dR1 = 16 * ds + drp, dR2 = dR1 + 8;
             float2 A1[8], P1[8], A2[16], P2[16];
-            {
+            // the gated rule has no retrieval: its A parts are zero, so its loop sums P alone
+            const bool with_a = GDN2 || p.rule != kGated;
+            auto diag = [&](auto wa_tag) {
+                constexpr bool WA = decltype(wa_tag)::value;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) A1[e] = P1[e] = make_float2(0.f, 0.f);
 #pragma unroll
@@ -594,7 +598,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                     const int ic = 2 * m + (dcg >> 2);  // the 16-byte chunk of channels 16 m + 2 cg, + 1
                     const int xo1 = GDN2 ? pKap + t64(dR1, ic) : pKQ + kq_at(dR1, ic, false);
                     const int xo2 = GDN2 ? pKap + t64(dR2, ic) : pKQ + kq_at(dR2, ic, false);
-                    const float2 xk1 = h2f(sm + xo1 + bo), xk2 = h2f(sm + xo2 + bo);
+                    const float2 xk1 = WA ? h2f(sm + xo1 + bo) : make_float2(0.f, 0.f);
+                    const float2 xk2 = WA ? h2f(sm + xo2 + bo) : make_float2(0.f, 0.f);
                     const float2 xq1 = h2f(sm + pKQ + kq_at(dR1, ic, true) + bo);
                     const float2 xq2 = h2f(sm + pKQ + kq_at(dR2, ic, true) + bo);
                     // e = 0 above the row's diagonal, 1 on it, then the running product: no branches,
@@ -608,19 +613,23 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                         const float2 a2 = *reinterpret_cast<const float2 *>(G + J * 128 + 16 * m + 2 * dcg);
                         e2 = jl == drp + 8 ? one : e2;
                         const float2 t2 = __fmul2_rn(kk, e2);
-                        A2[jl] = __ffma2_rn(xk2, t2, A2[jl]);
+                        if (WA) A2[jl] = __ffma2_rn(xk2, t2, A2[jl]);
                         P2[jl] = __ffma2_rn(xq2, t2, P2[jl]);
                         e2 = __fmul2_rn(e2, a2);
                         if (jl < 8) {
                             e1 = jl == drp ? one : e1;
                             const float2 t1 = __fmul2_rn(kk, e1);
-                            A1[jl & 7] = __ffma2_rn(xk1, t1, A1[jl & 7]);
+                            if (WA) A1[jl & 7] = __ffma2_rn(xk1, t1, A1[jl & 7]);
                             P1[jl & 7] = __ffma2_rn(xq1, t1, P1[jl & 7]);
                             e1 = __fmul2_rn(e1, a2);
                         }
                     }
                 }
-            }
+            };
+            if (with_a)
+                diag(std::true_type{});
+            else
+                diag(std::false_type{});
             // sums over the channel pair and the eight channel groups
             float a1[8], p1[8], a2s[16], p2s[16];
 #pragma unroll
@@ -631,12 +640,12 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             for (int o = 1; o < 8; o <<= 1) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    a1[e] += __shfl_xor_sync(0xffffffffu, a1[e], o);
+                    if (with_a) a1[e] += __shfl_xor_sync(0xffffffffu, a1[e], o);
                     p1[e] += __shfl_xor_sync(0xffffffffu, p1[e], o);
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    a2s[e] += __shfl_xor_sync(0xffffffffu, a2s[e], o);
+                    if (with_a) a2s[e] += __shfl_xor_sync(0xffffffffu, a2s[e], o);
                     p2s[e] += __shfl_xor_sync(0xffffffffu, p2s[e], o);
                 }
             }
