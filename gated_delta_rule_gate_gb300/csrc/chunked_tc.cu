@@ -953,6 +953,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         if (lane == 0) {
             const uint32_t skip = STEP == kStepE ? 0u : (uint32_t)(IM_U - 16384);  // only the delta rules load E^T
             const uint32_t ubytes = HALF ? 8192u : 16384u;               // U: this CTA's value rows
+            // U = V, from the value input: the rules without retrieval (the per-key gated rule's
+            // image carries E^T but no U)
+            const bool u_from_v = STEP != kStepE || p.rule == kGated;
             for (int c = 0; c < nch; ++c) {
                 const int bf = c & 1;
                 if (c >= 2 && !ptx::mbar_wait_sleep(&freeb[bf], ((c - 2) >> 1) & 1)) {
@@ -965,8 +968,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 // the image two chunks ahead into L2, so that its load from there is short
                 if (c + 2 < nch) {
                     const unsigned char *nxt = src + 2 * (size_t)p.Hv * IM_BYTES;
-                    if (STEP == kStepE) {
+                    if (STEP == kStepE && !u_from_v) {
                         ptx::prefetch_l2(nxt, IM_BYTES);
+                    } else if (STEP == kStepE) {
+                        ptx::prefetch_l2(nxt, IM_U);
+                        ptx::prefetch_l2(nxt + IM_P, IM_BYTES - IM_P);
+#pragma unroll
+                        for (int kb = 0; kb < 2; ++kb)
+                            if (!HALF || kb == vh) ptx::prefetch_tile_3d(&tmV, 64 * kb, h, t0 + TC_C * (c + 2));
                     } else {
                         ptx::prefetch_l2(nxt + im_q(0), 8192);
                         ptx::prefetch_l2(nxt + im_q(1), 8192);
@@ -977,11 +986,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                     }
                 }
                 if (STEP == kStepE) {
-                    ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);                                // E^T and Q'
-                    ptx::bulk_g2s(dstb + IM_U, src + IM_U + 8192 * vh, ubytes, &land[bf]);  // U (its rows)
+                    ptx::bulk_g2s(dstb, src, IM_U, &land[bf]);  // E^T and Q'
+                    if (!u_from_v) ptx::bulk_g2s(dstb + IM_U, src + IM_U + 8192 * vh, ubytes, &land[bf]);  // U (its rows)
                 } else {
                     ptx::bulk_g2s(dstb + im_q(0), src + im_q(0), 8192, &land[bf]);  // Q'
                     ptx::bulk_g2s(dstb + im_q(1), src + im_q(1), 8192, &land[bf]);
+                }
+                if (u_from_v) {
                     // without retrieval U = V: its rows straight from the value input (the box
                     // lands in the image's U layout; rows past the request meet zero Kt rows and
                     // causally masked P entries only)
@@ -1013,7 +1024,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 ok = ptx::mbar_wait_spin(&land[bf], (c >> 1) & 1) && ptx::mbar_wait_spin(rsread, c & 1);
                 if (!ok) break;
                 tc::fence_after();
-                if (STEP != kStepE && c == nch - 1) {
+                if ((STEP != kStepE || p.rule == kGated) && c == nch - 1) {
                     // U came straight from the value input: in a short last chunk its rows past the
                     // request hold other tokens (or whatever the caller keeps there) and are cleared
                     const int n = t1 - (t0 + TC_C * c);

@@ -276,12 +276,14 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
             }
             if (lane == 0) {
                 const int qh = (int)((long long)nx.h * p.Hq / p.Hv);
-                ptx::mbar_arrive_expect_tx(land, 3 * 16384 + (GDN2 ? (uint32_t)nx.n * 512u : 0u));
+                // the gated rule's chain loads U = V from the value input itself
+                const bool needv = GDN2 || p.rule != kGated;
+                ptx::mbar_arrive_expect_tx(land, (needv ? 3 : 2) * 16384 + (GDN2 ? (uint32_t)nx.n * 512u : 0u));
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     ptx::tma_load_3d(sm + pKQ + kb * 16384, &tmK, 64 * kb, qh, nx.c0, land);
                     ptx::tma_load_3d(sm + pKQ + kb * 16384 + 8192, &tmQ, 64 * kb, qh, nx.c0, land);
-                    ptx::tma_load_3d(sm + pV + kb * 8192, &tmV, 64 * kb, nx.h, nx.c0, land);
+                    if (needv) ptx::tma_load_3d(sm + pV + kb * 8192, &tmV, 64 * kb, nx.h, nx.c0, land);
                 }
             }
             __syncwarp();
@@ -725,8 +727,8 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 ptx::bulk_commit();
             }
             if (!GDN2 && p.rule == kGated) {
-                // no retrieval (W = 0): U = V, Q' = Qh and E = Diag(e^{Gamma_C} - 1), so the
-                // chain's S E scales the state per key channel.  E^T is staged over the solve
+                // no retrieval (W = 0): U = V (which the chain loads from the value input), Q' = Qh
+                // and E = Diag(e^{Gamma_C} - 1), so the chain's S E scales the state per key channel.  E^T is staged over the solve
                 // area (row j = 32 q + lane, columns [64 hh, 64 hh + 64)).
                 const int ii = 32 * q + lane;
                 float v[64];
@@ -743,13 +745,12 @@ __global__ void __launch_bounds__(PK_THREADS, 1)
                 tc::fence_async_smem();
                 ptx::named_bar_sync(3, PK_WORK);
                 if (tid == 0) {
-                    ptx::bulk_s2g(dst + IM_U, sm + pV, 16384);
                     ptx::bulk_s2g(dst + im_q(0), sm + pQh, 8192);
                     ptx::bulk_s2g(dst + im_q(1), sm + pQh + 8192, 8192);
                     ptx::bulk_s2g(dst + im_e(0), sm + pXo, 16384);
                     ptx::bulk_s2g(dst + im_e(1), sm + pXo + 16384, 16384);
                     ptx::bulk_commit();
-                    // the copies have read the value tile: the next task's tiles may land
+                    // the copies have read their staging areas: the next task's tiles may land
                     ptx::bulk_wait_read();
                     ptx::mbar_arrive(tfree);
                 }
