@@ -306,9 +306,10 @@ def test_chunked_shared_beta(case, rule):
 @pytest.mark.parametrize("case", [dict(rule="linear"), dict(rule="gated"), dict(rule="gated_delta"),
                                   dict(rule="gdn2", decay_per_key=True, gate_dtype="f32", write_gate=True),
                                   dict(rule="gated", dk=64, dv=64), dict(rule="gated_delta", act="f32"),
-                                  dict(rule="gdn2", act="f32", decay_per_key=True, gate_dtype="f32")],
+                                  dict(rule="gdn2", act="f32", decay_per_key=True, gate_dtype="f32"),
+                                  dict(rule="gated", decay_per_key=True, gate_dtype="f32")],
                          ids=["tc-linear", "tc-gated", "tc-gated_delta", "tc-perkey-gdn2", "mma-gated",
-                              "tc-f32-gated_delta", "tc-f32-perkey-gdn2"])
+                              "tc-f32-gated_delta", "tc-f32-perkey-gdn2", "tc-perkey-gated"])
 def test_chunked_ignores_uncovered_tokens(case):
     """Tokens outside every request (before the first, between clamped
     requests, after the last) hold NaN in q, k, v and the gates: outputs and
