@@ -821,12 +821,8 @@ __device__ __forceinline__ void consume_slices(const Problem &p, const Stage &st
 // Key-major state ("gatedDeltaUpdate": [rows, Hv, dk, dv]; dk = dv = 128).
 // The stored rows are key rows, so a slice is 32 key rows of 128 value
 // columns, and the dot products S^T kappa and S^T q of a value column run
-// over all four slices.  The consumers hold the whole tile in registers:
-// thread (warp w, lane l) keeps key rows 32 s + 4 w + m (s, m = 0..3) of the
-// value columns 4 l .. 4 l + 3 (every ring load is a 512-byte row per warp).
-// Per token each warp's partial sums go through shared memory (two buffers,
-// one barrier of the consumer warps per token) and every thread adds the
-// eight partials of its four columns.  The scalar decay is kept as a lazy
+// over all four slices.  The consumers hold the whole tile in registers (the
+// layout is described at apply_tokens_km).  The scalar decay is kept as a lazy
 // factor as in apply_tokens_multi.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float4 f4_fma(float a, const float4 &x, const float4 &y) {
