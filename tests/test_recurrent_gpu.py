@@ -120,6 +120,27 @@ def test_decode_blocks_of_one_to_four_tokens(case):
     assert rel_err(fg, ref_fin[slots]) <= TOL_STATE
 
 
+@pytest.mark.parametrize("kmajor", [False, True], ids=["vmajor", "kmajor"])
+@pytest.mark.parametrize("rule", ["gated", "gated_delta"])
+def test_decode_strong_decay_folds_the_lazy_factor(rule, kmajor):
+    """Per-token log decays in [-7, -5]: within a block of staged tokens the
+    decode kernels' lazy decay factor (the state kept as c * S~) falls below
+    1e-20 and is folded into the state mid-block.  Requests of 8 tokens (one
+    block) and 20 (restaged in blocks of 8) match the oracle in both state
+    layouts."""
+    kw = dict(seed=71 + 2 * int(kmajor) + int(rule == "gated"), B=4, lengths=[8, 20, 3, 1], hq=1, hv=2,
+              dk=128, dv=128, act="f16", rule=rule, gate="log", logdecay_range=(-7.0, -5.0),
+              state="random", state_std=0.5, num_slots=6, slot_mode="perm", state_kmajor=kmajor)
+    p = workloads.make(**kw)
+    ref_o, ref_fin, err = oracle.run_problem(p)
+    assert err == 0
+    o, fin, _ = run(p, in_place=True)
+    assert rel_err(o_flat(o, p), ref_o) <= TOL_O["f16"]
+    slots = [int(s) for s in p["slot_ids"]]
+    fg = fin[torch.tensor(slots, device=DEV)].double().cpu().numpy()
+    assert rel_err(fg, ref_fin[slots]) <= TOL_STATE
+
+
 @pytest.mark.parametrize("in_place", [False, True])
 def test_slots_routing_and_untouched_rows(in_place):
     p = workloads.make(seed=51, B=5, lengths=[2, 1, 0, 4, 3], hq=4, hv=8, dk=128, dv=128,
