@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(Problem p, int *off
 //
 // Persistent CTAs, two per SM: a producer warp (task lookup and gates in fp32
 // one task ahead, the key / query / value tiles by TMA as soon as the
-// previous task releases them) and eight worker warps.  Waits are bounded.
+// previous task releases them; the rules without retrieval take no value tile)
+// and eight worker warps.  Waits are bounded.
 constexpr int PR_WORK = 256;
 constexpr int PR_THREADS = PR_WORK + 32;
 constexpr int FA = 68;  // fp32 row stride of At (16-byte rows; lanes = consecutive r, conflict-free)
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(PR_THREADS, 2)
                 if (tid == 0) {
                     ptx::bulk_s2g(dst + IM_KT, sm + rKt, 16384);
                     ptx::bulk_commit();
-                    // without retrieval nothing reads the key, query and value tiles any more
+                    // without retrieval nothing reads the key and query tiles any more
                     ptx::mbar_arrive(tfree);
                 }
             }

@@ -126,7 +126,8 @@ __device__ __forceinline__ void unpack8(uint4 u, float *x) {
 // The producer looks up the next task and loads its scalar gates one task
 // ahead.  It lands the per-key log-decay rows and the head's gate bias as soon
 // as the previous task has finished its diagonal blocks (gfree).  The key,
-// query and value tiles (TMA) and the erase-gate rows follow once that task's
+// query and value tiles (TMA; the gated rule takes no value tile, its chain
+// reads v itself) and the erase-gate rows follow once that task's
 // last products have read their buffers (tfree), and the task after that is
 // prefetched into L2.  So the next task's loads overlap the solve and the
 // epilogues of the current one.  Per task the workers
