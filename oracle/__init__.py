@@ -65,7 +65,10 @@ _libs = {}
 def _load(real="f64"):
     if real not in _libs:
         _, rp, prob = _REAL[real]
-        lib = ctypes.CDLL(_build.build(real=real))
+        # GDN_ORACLE_LIB names a double build of a deliberately altered copy of
+        # gdn_oracle.c: the planted-mistake test runs the pins against it
+        alt = os.environ.get("GDN_ORACLE_LIB") if real == "f64" else None
+        lib = ctypes.CDLL(alt or _build.build(real=real))
         lib.oracle_gdn.argtypes = [ctypes.POINTER(prob)]
         lib.oracle_gdn.restype = ctypes.c_int
         lib.oracle_gate.argtypes = [ctypes.c_int64, ctypes.c_int32, rp, rp, rp, rp, rp, rp]
