@@ -48,6 +48,16 @@ MUTANTS = [
     ("softplus-sign", "x + log1p(exp(-x))", "x - log1p(exp(-x))"),
     ("sigmoid-sign", "1.0 / (1.0 + exp(-x))", "1.0 / (1.0 + exp(x))"),
     ("gate-op-bias-sign", "softplus(a[e] + dt_bias[j])", "softplus(a[e] - dt_bias[j])"),
+    ("beta-head-ignored",
+     "real beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];\n"
+     "            if (p->beta_sigmoid) beta = sigmoid(beta);\n            memcpy",
+     "real beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv];\n"
+     "            if (p->beta_sigmoid) beta = sigmoid(beta);\n            memcpy"),
+    ("default-scale-no-sqrt", "1.0 / sqrt((real)dk)", "1.0 / (real)dk"),
+    ("query-norm-ignored", "if (p->l2norm_q) l2_normalise(qv, dk);", ""),
+    ("per-key-decay-one-channel", "real raw = p->decay[((size_t)t * hv + h) * dk + c];",
+     "real raw = p->decay[((size_t)t * hv + h) * dk];"),
+    ("bad-slot-not-flagged", "*p->error_word |= ORACLE_ERR_BAD_SLOT;", "*p->error_word |= 0;"),
     ("beta-no-sigmoid",
      "real beta = p->beta[p->beta_shared ? (size_t)t : (size_t)t * hv + h];\n"
      "            if (p->beta_sigmoid) beta = sigmoid(beta);\n            memcpy",
@@ -112,7 +122,7 @@ def test_every_planted_mistake_fails_a_pin(tmp_path):
             assert altered.count(old) == 1, "the text to alter must occur exactly once: " + name
             altered = altered.replace(old, new)
         libs[name] = _build(altered, str(tmp_path), name.replace("-", "_"))
-    with ThreadPoolExecutor(max_workers=4) as ex:
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         results = dict(zip(libs, ex.map(_run_pins, libs.values())))
     rc, out = results.pop("control")
     assert rc == 0, "the unaltered copy must pass every pin:\n" + out
